@@ -1,0 +1,19 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    config.addinivalue_line("markers", "slow: takes more than a few seconds on CPU")
+
+
+def pytest_collection_modifyitems(config, items):
+    # GPU tests fail loudly (never skip) when selected on a machine without a GPU; the CPU
+    # suite deselects them with -m "not gpu".
+    pass
