@@ -1,0 +1,491 @@
+"""Benchmark of the MoE expert layer on GB300: one JSON line on rank 0.
+
+A step is one pass of the whole layer over one batch: route, dispatch, gate_up GEMM + SwiGLU,
+down GEMM (and the shared expert's two GEMMs when the workload has one), combine - the same
+C-ABI calls moe_forward makes, issued one by one so CUDA events between them time each kernel
+family on the stream it runs on. Inputs are seeded synthetic tensors resident in HBM before the
+timed region; the weights alone (GBs) exceed the 129 MB L2, so no flush is inserted.
+
+e2e: the same metric through moe_forward with host buffers: every step copies x and the logits
+from pinned host memory, runs the layer, and copies the output back.
+
+--impl reference: the CPU oracle (float64 numpy, the test reference) timed on the host cores
+on a bounded token sample of the same workload.
+
+Multi-GPU (torchrun): every rank runs the same per-GPU workload on its own GPU (weak scaling, no
+collective on the data path); the time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("MoE layer tokens/s & expert-GEMM TFLOP/s on 1 GB300; decode µs/layer vs HBM "
+          "GB/s")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="mixtral_8x7b")
+    ap.add_argument("--T", type=int, default=None, help="override the token count")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=None, help="tokens in the CPU sample")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    """Samples the SM clock and the clock-event (throttle) reasons while the timed region runs.
+    Read-only NVML queries every 2 ms (libnvidia-ml through ctypes); nvidia-smi as a fallback."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int, period_s: float = 0.002):
+        self.index = index
+        self.period = period_s
+        self.samples = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._nvml = None
+        self._proc = None
+
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(self.index, ctypes.byref(h)) != 0:
+            return None
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return lib, h, reasons_fn
+
+    def _loop_nvml(self):
+        import ctypes
+        lib, h, reasons_fn = self._nvml
+        c, m = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(c)) == 0 and \
+                    reasons_fn(h, ctypes.byref(m)) == 0:
+                self.samples.append((float(c.value), int(m.value)))
+            time.sleep(self.period)
+
+    def _loop_smi(self):
+        for line in self._proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            try:
+                self.max_mhz = float(parts[1])
+                mask = int(parts[2], 16)
+                self.samples.append((float(parts[0]), mask))
+            except (ValueError, IndexError):
+                continue
+
+    def __enter__(self):
+        try:
+            self._nvml = self._nvml_open()
+        except OSError:
+            self._nvml = None
+        if self._nvml is not None:
+            self._t = threading.Thread(target=self._loop_nvml, daemon=True)
+        else:
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index),
+                     "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self._t = threading.Thread(target=self._loop_smi, daemon=True)
+            except OSError:
+                self._t = None
+        if self._t is not None:
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+        if self._t is not None:
+            self._t.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return None
+        reasons = set()
+        for _, mask in self.samples:
+            for bit, name in self.REASONS.items():
+                if mask & bit:
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(v for v, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": sorted(reasons),
+                "samples": len(self.samples),
+                "source": "nvml" if self._nvml is not None else "nvidia-smi"}
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU oracle on a token sample (the baseline and the reference arm)
+# ------------------------------------------------------------------------------------------------
+def cpu_oracle_run(cfg, inp_host, tokens):
+    """The oracle's whole layer on the first `tokens` tokens; returns wall seconds."""
+    import numpy as np
+
+    from oracle import moe_oracle as o
+
+    class Widen:
+        def __init__(self, t):
+            self.t = t
+
+        def __len__(self):
+            return self.t.shape[0]
+
+        def __getitem__(self, e):
+            return self.t[e].double().numpy()
+
+    x = inp_host["x"][:tokens].double().numpy()
+    logits = inp_host["logits"][:tokens].numpy()
+    sh = inp_host.get("w_shared_gate_up")
+    t0 = time.perf_counter()
+    o.forward(x, logits, Widen(inp_host["w_gate_up"]), Widen(inp_host["w_down"]), cfg.k,
+              cfg.score_fn, cfg.renormalize, cfg.scale_input, True,
+              None if sh is None else sh.double().numpy(),
+              None if sh is None else inp_host["w_shared_down"].double().numpy())
+    return time.perf_counter() - t0
+
+
+def blas_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        v = os.environ.get(var)
+        if v and v.isdigit():
+            return int(v)
+    return os.cpu_count()
+
+
+def default_sample(cfg):
+    # about 10-30 s of the oracle on a 16-core host: it sustains roughly 300 GFLOP/s of float64
+    # matrix products there, plus the per-expert widening of the weights
+    per_token = 6.0 * cfg.d * cfg.I * cfg.k + 6.0 * cfg.d * cfg.I_shared
+    return int(max(8, min(cfg.T, 3e12 / per_token)))
+
+
+def host_inputs(cfg, dev_inputs):
+    out = {}
+    for k_, v in dev_inputs.items():
+        out[k_] = None if v is None else v.cpu()
+    return out
+
+
+# ------------------------------------------------------------------------------------------------
+def traffic_for(kernel_file: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    source of the kernel (matching sha256), else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    src = os.path.join(ROOT, "routing_dispatch_grouped_gb300", "csrc", kernel_file)
+    if not os.path.exists(p) or not os.path.exists(src):
+        return None, None
+    with open(p) as f:
+        d = json.load(f)
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()
+    ent = d.get(kernel_file)
+    if not ent or ent.get("sha256") != h:
+        return None, None
+    return ent.get("bytes_per_launch"), ent
+
+
+def reduce_max(x: float, device) -> float:
+    """Maximum of a per-rank float over all ranks (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def shard_tokens(T: int, rank: int, world: int):
+    """Token range [a, b) of one rank when a batch is split across ranks."""
+    per = (T + world - 1) // world
+    a = min(T, rank * per)
+    return a, min(T, a + per)
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    from routing_dispatch_grouped_gb300 import moe, synth
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    cfg = synth.CONFIGS[args.config]
+    if args.T is not None:
+        cfg = cfg.with_T(args.T)
+    moe.lib()
+    inp = synth.make_inputs(cfg, dev)
+    T, d, E, k, I, Is = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.I_shared
+    R = T * k
+    flags = (moe.RENORMALIZE if cfg.renormalize else 0) | (moe.SCALE_INPUT if cfg.scale_input
+                                                           else 0)
+    dt = cfg.dtype
+    stream = torch.cuda.current_stream(dev)
+
+    # buffers (outside the timed region)
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    out = torch.empty(T, d, dtype=dt, device=dev)
+    ws = torch.empty(moe.moe_forward_workspace_size(T, d, E, k, I, Is, dt), dtype=torch.uint8,
+                     device=dev)
+    v = moe.forward_workspace_views(ws, T, d, E, k, I, Is, dt)
+    dws = torch.empty(moe.moe_dispatch_workspace_size(T, E, k), dtype=torch.uint8, device=dev)
+    gws = torch.empty(256, dtype=torch.uint8, device=dev)
+    disp_out = {n: v[n] for n in ("counts", "offsets", "sorted_to_slot", "slot_to_sorted",
+                                  "x_sorted")}
+
+    stages = ["route", "dispatch", "gate_up", "down"] + (["shared_gate_up", "shared_down"]
+                                                         if Is else []) + ["combine"]
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        moe.moe_route(inp["logits"], k, cfg.score_fn, cfg.renormalize, ids, w, stream)
+        mark(1)
+        moe.moe_dispatch(ids, E, x=inp["x"], workspace=dws, out=disp_out, stream=stream)
+        mark(2)
+        moe.moe_gate_up(v["x_sorted"], v["offsets"], inp["w_gate_up"], v["sorted_to_slot"], w,
+                        cfg.scale_input, h=v["h"], workspace=gws, stream=stream)
+        mark(3)
+        moe.moe_down(v["h"], v["offsets"], inp["w_down"], y_sorted=v["y_sorted"],
+                     workspace=gws, stream=stream)
+        mark(4)
+        i = 5
+        if Is:
+            moe.moe_gate_up(inp["x"], None, inp["w_shared_gate_up"].unsqueeze(0),
+                            h=v["h_shared"], workspace=gws, stream=stream)
+            mark(i)
+            moe.moe_down(v["h_shared"], None, inp["w_shared_down"].unsqueeze(0),
+                         y_sorted=v["y_shared"], workspace=gws, stream=stream)
+            mark(i + 1)
+            i += 2
+        moe.moe_combine(v["y_sorted"], v["slot_to_sorted"], k, dt,
+                        topk_weights=None if cfg.scale_input else w,
+                        y_shared=v["y_shared"] if Is else None, out=out, stream=stream)
+        mark(i)
+
+    nev = len(stages) + 1
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(gws) == 0 and moe.moe_read_device_status(dws) == 0
+
+    import torch.distributed as dist
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+              for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        for s in range(args.steps):
+            step(events[s])
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    per_stage = {name: [] for name in stages}
+    step_ms = []
+    for ev in events:
+        for i, name in enumerate(stages):
+            per_stage[name].append(ev[i].elapsed_time(ev[i + 1]))
+        step_ms.append(ev[0].elapsed_time(ev[-1]))
+    total_ms = events[0][0].elapsed_time(events[-1][-1])
+    ms_per_step = total_ms / args.steps
+    if world > 1:
+        ms_per_step = reduce_max(ms_per_step, dev)
+
+    # the product call alone, for the record
+    for _ in range(3):
+        moe.moe_forward(inp["x"], inp["logits"], inp["w_gate_up"], inp["w_down"], k,
+                        cfg.score_fn, flags, inp["w_shared_gate_up"], inp["w_shared_down"],
+                        out=out, topk_ids=ids, topk_weights=w, workspace=ws, stream=stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        moe.moe_forward(inp["x"], inp["logits"], inp["w_gate_up"], inp["w_down"], k,
+                        cfg.score_fn, flags, inp["w_shared_gate_up"], inp["w_shared_down"],
+                        out=out, topk_ids=ids, topk_weights=w, workspace=ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    forward_ms = e0.elapsed_time(e1) / args.steps
+
+    # end to end through moe_forward with host buffers
+    x_h = inp["x"].cpu().pin_memory()
+    lg_h = inp["logits"].cpu().pin_memory()
+    out_h = torch.empty(T, d, dtype=dt).pin_memory()
+    x_d = torch.empty_like(inp["x"])
+    lg_d = torch.empty_like(inp["logits"])
+
+    def e2e_step():
+        x_d.copy_(x_h, non_blocking=True)
+        lg_d.copy_(lg_h, non_blocking=True)
+        moe.moe_forward(x_d, lg_d, inp["w_gate_up"], inp["w_down"], k, cfg.score_fn, flags,
+                        inp["w_shared_gate_up"], inp["w_shared_down"], out=out, topk_ids=ids,
+                        topk_weights=w, workspace=ws, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        e2e_ms = reduce_max(e2e_ms, dev)
+
+    # roofline of the dominant kernel (the gate_up grouped GEMM: 2/3 of the expert FLOPs)
+    pk, pk_src = peaks()
+    gu_ms = statistics.mean(per_stage["gate_up"])
+    dn_ms = statistics.mean(per_stage["down"])
+    gu_flops = 4.0 * d * I * R
+    dn_flops = 2.0 * d * I * R
+    sh_flops, sh_ms = 0.0, 0.0
+    if Is:
+        sh_flops = 6.0 * d * Is * T
+        sh_ms = statistics.mean(per_stage["shared_gate_up"]) + statistics.mean(
+            per_stage["shared_down"])
+    ach = gu_flops / (gu_ms * 1e-3) / 1e12
+    traffic, _ = traffic_for("gemm_tc.cu")
+    roof = {"bound": "tensor", "kernel": "tc_grouped_gemm<gate_up>", "achieved": round(ach, 1),
+            "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(ach / pk["bf16_tflops"], 4), "traffic": traffic,
+            "peak_source": f"{pk_src} bf16_tflops (burst)",
+            "frac_of_sustained": round(ach / pk.get("bf16_tflops_sustained",
+                                                    pk["bf16_tflops"]), 4)}
+    expert_tflops = (gu_flops + dn_flops + sh_flops) / ((gu_ms + dn_ms + sh_ms) * 1e-3) / 1e12
+
+    tokens_per_s = T * world / (ms_per_step * 1e-3)
+    res = {
+        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if dt == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded counter-based generator; shapes of the workload)",
+        "config": {"workload": cfg.name, "T": T, "d": d, "E": E, "k": k, "I": I,
+                   "I_shared": Is, "seed": cfg.seed,
+                   "l2": "no flush: weights alone exceed the 129 MB L2"},
+        "roofline": roof,
+        "expert_gemm_tflops": round(expert_tflops, 1),
+        "stages_ms": {n: round(statistics.mean(vv), 4) for n, vv in per_stage.items()},
+        "forward_call_ms": round(forward_ms, 4),
+        "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": x_h.numel() * x_h.element_size()
+                + lg_h.numel() * lg_h.element_size(),
+                "d2h_bytes_per_step": out_h.numel() * out_h.element_size()},
+        "gpu_launches": args.steps * moe.moe_forward_kernel_count(T, Is),
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = args.cpu_sample or default_sample(cfg)
+        hi = host_inputs(cfg, inp)
+        secs = cpu_oracle_run(cfg, hi, n)
+        res["cpu_baseline"] = {"value": round(n / secs, 2), "unit": "tokens/s",
+                               "cores": blas_threads(), "kind": "oracle",
+                               "sample": f"first {n} of {T} tokens, whole layer, float64 numpy "
+                                         f"({secs:.1f} s)"}
+    return res
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is the whole layer on a token sample."""
+    import torch
+
+    from routing_dispatch_grouped_gb300 import synth
+
+    cfg = synth.CONFIGS[args.config]
+    if args.T is not None:
+        cfg = cfg.with_T(args.T)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = host_inputs(cfg, synth.make_inputs(cfg, dev))
+    n = args.cpu_sample or max(8, default_sample(cfg) // max(1, args.steps + args.warmup) * 2)
+    for _ in range(args.warmup):
+        cpu_oracle_run(cfg, inp, n)
+    secs = [cpu_oracle_run(cfg, inp, n) for _ in range(args.steps)]
+    ms = 1e3 * sum(secs) / len(secs)
+    val = n / (ms * 1e-3)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(val, 2), "unit": "tokens/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": cfg.name, "T": cfg.T, "d": cfg.d,
+                                        "E": cfg.E, "k": cfg.k, "I": cfg.I,
+                                        "I_shared": cfg.I_shared},
+        "cpu_baseline": {"value": round(val, 2), "unit": "tokens/s", "cores": blas_threads(),
+                         "kind": "oracle",
+                         "sample": f"first {n} of {cfg.T} tokens per step, whole layer"},
+        "e2e": {"value": round(val, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,235 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) MoE expert-layer library (libmoe.so).
+ *
+ * The layer: router top-k gating over per-token expert logits, dispatch of every (token, expert)
+ * pair to its expert, the per-expert gated feed-forward (gate/up projection, SwiGLU, down
+ * projection) as a grouped GEMM, and the router-weighted combine back to token order.
+ *
+ * Sources (Transformers documentation):
+ *   [EP-intro]     "Expert parallelism", introduction: a router sends tokens to the matching
+ *                  experts and gathers the results; Llama-4 experts get every token already
+ *                  scaled by the router score.
+ *   [EP-add]       "Expert parallelism", "Adding an implementation": __call__(hidden_states,
+ *                  top_k_index, top_k_weights) returns the weighted expert output for each token
+ *                  of the batch; experts_forward runs on the rows, expert ids and weights routed
+ *                  to the experts; an implementation may keep state such as buffers.
+ *   [EP-choose]    "Expert parallelism", "Choosing an implementation": all_to_all needs a host
+ *                  synchronisation per layer and so cannot be captured in a CUDA graph;
+ *                  all_reduce moves no tokens, needs no host sync and is captured at decode.
+ *   [EP-dispatch]  "Expert parallelism", "Token dispatch": each (token, expert) pair is sent to
+ *                  the owner of that expert, the local experts run on what arrived, the results
+ *                  come back and are combined with the routing weights.
+ *   [EP-tp]        "Expert parallelism", "With tensor parallelism": token slices may be uneven
+ *                  or empty, including single-token decoding.
+ *   [EP-override]  "Expert parallelism", "Overriding the plans": a bad key raises ValueError
+ *                  before anything is sharded (errors are reported before any work).
+ *   [TP-packed]    "Tensor parallelism for inference", "Packed strategies": gate_up_proj is
+ *                  [num_experts, hidden, 2 * expert_dim]; bmm(hidden_states, gate_up_proj) then
+ *                  chunk(2, dim=-1) gives gate (first half) and up (second half).
+ *
+ * On one GPU the all-to-all of [EP-dispatch] becomes a local permutation (moe_dispatch) and the
+ * return all-to-all plus weighted sum becomes moe_combine; no call here crosses GPUs.
+ *
+ * Conventions for every entry point
+ *   - All device pointers are caller-owned device memory. The library never allocates, frees or
+ *     synchronises inside these calls; work is enqueued on `stream` (NULL = legacy default
+ *     stream) and the call returns at once. Nothing here needs a host sync, so a sequence of
+ *     calls with fixed pointers can be captured in a CUDA graph (the property [EP-choose] asks
+ *     of decode).
+ *   - Every argument is checked before any launch ([EP-override] convention). A bad argument
+ *     returns MOE_ERR_INVALID_ARG, a shape or dtype the kernels do not cover returns
+ *     MOE_ERR_UNSUPPORTED, a short workspace returns MOE_ERR_WORKSPACE; in all three cases
+ *     nothing is enqueued. A failed launch returns MOE_ERR_CUDA.
+ *   - Faults only the device can see (an expert id outside [0, E) handed to moe_dispatch, a
+ *     device-side wait that ran out of time) are written to a status word at the start of the
+ *     call's workspace; the kernels stay memory-safe and finish. moe_read_device_status()
+ *     reports the word (it synchronises the stream: diagnostics only).
+ *   - Pointers must be 16-byte aligned. Row lengths must give 16-byte rows: d and I multiples
+ *     of 8 for MOE_BF16, of 4 for MOE_F32.
+ *   - Ranges: 1 <= E <= 256, 1 <= k <= min(E, 32), T >= 0, T * k < 2^31. T == 0 is a no-op
+ *     returning MOE_OK ([EP-tp]: slices may be empty).
+ *   - Calls are stateless and re-entrant; calls on different streams must not share outputs or
+ *     workspace.
+ *
+ * Layouts (row-major, C order)
+ *   logits         float  [T, E]
+ *   topk_ids       int32  [T, k]   slot j = 0 is the best expert; slot index s = t*k + j
+ *   topk_weights   float  [T, k]
+ *   x              dtype  [T, d]
+ *   w_gate_up      dtype  [E, d, 2I]  gate = columns [0, I), up = columns [I, 2I) ([TP-packed])
+ *   w_down         dtype  [E, I, d]
+ *   counts         int32  [E]
+ *   offsets        int32  [E + 1]  exclusive prefix of counts; expert e owns sorted rows
+ *                                  [offsets[e], offsets[e+1])
+ *   sorted_to_slot int32  [R]      sorted row p came from slot sorted_to_slot[p]   (R = T*k)
+ *   slot_to_sorted int32  [R]      inverse permutation (-1 for a slot whose id was invalid)
+ *   x_sorted       dtype  [R, d]   x_sorted[p] = x[sorted_to_slot[p] / k]
+ *   h              dtype  [R, I]   SiLU(gate) * up; stored in the layer dtype
+ *   y_sorted       float  [R, d]   expert outputs in sorted order, fp32
+ *   out            dtype  [T, d]
+ *
+ * Precision: MOE_BF16 layers take bf16 inputs and weights, accumulate in fp32 on the tensor
+ * cores (tcgen05), store h as bf16 (round to nearest even), keep y_sorted in fp32 and round the
+ * combined output once. MOE_F32 layers run in fp32 throughout (FFMA, no TF32).
+ */
+#ifndef RDG_MOE_H
+#define RDG_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so the header needs no CUDA include. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad size or flag, misaligned pointer */
+    MOE_ERR_UNSUPPORTED = 2,   /* valid request outside what the kernels cover (e.g. E > 256) */
+    MOE_ERR_WORKSPACE = 3,     /* workspace null or smaller than the matching *_workspace_size */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call or a launch failed */
+    MOE_ERR_DEVICE_BOUNDS = 5, /* device saw an expert id outside [0, E); those slots skipped */
+    MOE_ERR_TIMEOUT = 6        /* a device-side wait passed its time limit; kernel gave up */
+} moe_status;
+
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum moe_score_fn { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_fn;
+
+/* flags (bitwise or) */
+enum {
+    MOE_RENORMALIZE = 1u,         /* divide the k selected weights by their sum */
+    MOE_SCALE_INPUT = 2u,         /* router weight multiplies the expert input; combine weight 1 */
+    MOE_FUSE_COMBINE_WEIGHT = 4u  /* down-projection epilogue multiplies rows by their weight */
+};
+
+/*
+ * moe_route - router top-k gating ([EP-add]: top_k_index, top_k_weights; [EP-intro]).
+ *   logits        device float [T, E], read only.
+ *   topk_ids      device int32 [T, k], written: the k experts with the largest logits, in
+ *                 descending logit order; equal logits go to the lower expert index; -0.0 equals
+ *                 +0.0; NaN ranks below -inf. Selection compares the fp32 logits directly, so the
+ *                 ids do not depend on how exp is evaluated.
+ *   topk_weights  device float [T, k], written.
+ *                 MOE_SCORE_SOFTMAX: exp(l_j - max) / sum over all E of exp(l_i - max); with
+ *                 MOE_RENORMALIZE this is a softmax over the k selected logits.
+ *                 MOE_SCORE_SIGMOID: 1 / (1 + exp(-l_j)); divided by the sum of the k selected
+ *                 when MOE_RENORMALIZE is set.
+ *   flags         MOE_RENORMALIZE only; other bits are MOE_ERR_INVALID_ARG.
+ * Weights from a row holding NaN logits are unspecified.
+ */
+moe_status moe_route(const float* logits, int T, int E, int k, moe_score_fn score_fn,
+                     unsigned flags, int32_t* topk_ids, float* topk_weights, moe_stream_t stream);
+
+/*
+ * moe_dispatch - group the T*k routed slots by expert ([EP-dispatch]: every (token, expert)
+ * pair goes to that expert; on one GPU this is a local permutation).
+ *   topk_ids       device int32 [T, k], read. An id outside [0, E) sets MOE_ERR_DEVICE_BOUNDS in
+ *                  the status word; that slot is left out of counts and rows and its
+ *                  slot_to_sorted entry is -1.
+ *   x, x_sorted    device [T, d] and [R, d] of dtype dt; both NULL = indices only.
+ *   counts, offsets, sorted_to_slot, slot_to_sorted: device int32 outputs (layouts above).
+ *                  Inside an expert rows keep ascending slot order, so the permutation is
+ *                  deterministic (no atomics decide it).
+ *   workspace      device scratch of at least moe_dispatch_workspace_size(T, E, k) bytes,
+ *                  256-byte aligned; its first 4 bytes are the status word, cleared by the call.
+ */
+moe_status moe_dispatch(const int32_t* topk_ids, const void* x, moe_dtype dt, int T, int d, int E,
+                        int k, int32_t* counts, int32_t* offsets, int32_t* sorted_to_slot,
+                        int32_t* slot_to_sorted, void* x_sorted, void* workspace,
+                        size_t ws_bytes, moe_stream_t stream);
+size_t moe_dispatch_workspace_size(int T, int E, int k);
+
+/*
+ * moe_gate_up - grouped gate/up projection with SwiGLU ([TP-packed]; [EP-add] experts_forward):
+ *   for each expert e and each row p in [offsets[e], offsets[e+1]):
+ *     g = x_rows[p] . w_gate_up[e][:, 0:I],  u = x_rows[p] . w_gate_up[e][:, I:2I]
+ *     if MOE_SCALE_INPUT: g, u *= s_p with s_p = topk_weights[sorted_to_slot[p]] (the router
+ *       score applied to the expert input, [EP-intro]; applied to the fp32 accumulators, which
+ *       equals scaling the input by linearity)
+ *     h[p] = SiLU(g) * u, SiLU(z) = z / (1 + exp(-z)), stored in dt.
+ *   x_rows     device dtype [R, d] (x_sorted, or x itself for an always-on expert).
+ *   offsets    device int32 [E + 1] with offsets[0] == 0 and offsets[E] <= R, or NULL meaning one
+ *              expert (E must be 1) owning all R rows. Read on the device: no host sync.
+ *   sorted_to_slot, topk_weights: read only with MOE_SCALE_INPUT, else may be NULL.
+ *   w_gate_up  device dtype [E, d, 2I].   h: device dtype [R, I], written for owned rows only.
+ *   flags      MOE_SCALE_INPUT or 0.
+ *   workspace  at least moe_experts_workspace_size() bytes (status word), 256-byte aligned.
+ */
+moe_status moe_gate_up(const void* x_rows, const int32_t* offsets, const int32_t* sorted_to_slot,
+                       const float* topk_weights, moe_dtype dt, int R, int d, int E, int I,
+                       const void* w_gate_up, unsigned flags, void* h, void* workspace,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_down - grouped down projection: y_sorted[p] = h[p] . w_down[e] (fp32), for p owned by e;
+ *   with MOE_FUSE_COMBINE_WEIGHT the row is multiplied by topk_weights[sorted_to_slot[p]].
+ *   h device dtype [R, I]; w_down device dtype [E, I, d]; y_sorted device float [R, d].
+ *   offsets, sorted_to_slot, topk_weights, workspace: as for moe_gate_up.
+ */
+moe_status moe_down(const void* h, const int32_t* offsets, const int32_t* sorted_to_slot,
+                    const float* topk_weights, moe_dtype dt, int R, int d, int E, int I,
+                    const void* w_down, unsigned flags, float* y_sorted, void* workspace,
+                    size_t ws_bytes, moe_stream_t stream);
+
+/* moe_experts - moe_gate_up followed by moe_down ([EP-add] experts_forward). */
+moe_status moe_experts(const void* x_sorted, const int32_t* offsets, const int32_t* sorted_to_slot,
+                       const float* topk_weights, moe_dtype dt, int R, int d, int E, int I,
+                       const void* w_gate_up, const void* w_down, unsigned flags, void* h,
+                       float* y_sorted, void* workspace, size_t ws_bytes, moe_stream_t stream);
+size_t moe_experts_workspace_size(void);
+
+/*
+ * moe_combine - weighted return to token order ([EP-dispatch]: results combined with the
+ * routing weights; [EP-add]: the weighted expert output for each token):
+ *   out[t] = sum_{j<k} w[t, j] * y_sorted[slot_to_sorted[t*k + j]]  (+ y_shared[t])
+ *   summed in fp32 in slot order, the shared row added last, rounded once to out_dt.
+ *   topk_weights NULL means weight 1 (router score already applied to the input, or fused into
+ *   the down projection). y_shared (device float [T, d]) may be NULL. Slots whose
+ *   slot_to_sorted entry is negative contribute nothing.
+ */
+moe_status moe_combine(const float* y_sorted, const int32_t* slot_to_sorted,
+                       const float* topk_weights, const float* y_shared, int T, int d, int k,
+                       moe_dtype out_dt, void* out, moe_stream_t stream);
+
+/*
+ * moe_forward - the whole layer ([EP-add] __call__): route, dispatch, experts, combine.
+ *   x, logits, weights as above; topk_ids/topk_weights/out are caller outputs.
+ *   w_shared_gate_up [d, 2*Is] and w_shared_down [Is, d] (dtype dt): an always-on SwiGLU expert
+ *   run on the unscaled x and added to every token before the one output rounding; both NULL
+ *   (and Is == 0) for none.
+ *   flags: MOE_RENORMALIZE | MOE_SCALE_INPUT | MOE_FUSE_COMBINE_WEIGHT (the last two exclude
+ *   each other).
+ *   workspace: at least moe_forward_workspace_size(...) bytes, 256-byte aligned. Holds counts,
+ *   offsets, both permutations, x_sorted, h, y_sorted and the shared expert's h and y.
+ */
+moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, int d, int E,
+                       int k, int I, moe_score_fn score_fn, unsigned flags, const void* w_gate_up,
+                       const void* w_down, const void* w_shared_gate_up,
+                       const void* w_shared_down, int Is, int32_t* topk_ids, float* topk_weights,
+                       void* out, void* workspace, size_t ws_bytes, moe_stream_t stream);
+size_t moe_forward_workspace_size(int T, int d, int E, int k, int I, int Is, moe_dtype dt);
+
+/*
+ * Number of kernels moe_forward enqueues for these sizes (dispatch, experts and combine
+ * kernels included; the status-word clear is a memset, not counted). 0 for T == 0.
+ */
+int moe_forward_kernel_count(int T, int Is);
+
+/*
+ * moe_read_device_status - synchronise `stream`, then return the status word the kernels of
+ * the last call that used `workspace` left there (MOE_OK if none). Diagnostics only.
+ */
+moe_status moe_read_device_status(const void* workspace, moe_stream_t stream);
+
+/* Static text for a status code. */
+const char* moe_status_string(moe_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RDG_MOE_H */

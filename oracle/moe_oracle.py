@@ -149,14 +149,16 @@ def swiglu_ffn(xrows, w_gate_up, w_down, round_h: bool):
 def experts(x_sorted, offsets, w_gate_up, w_down, round_h: bool, row_scale=None):
     """Run expert e on its rows [offsets[e], offsets[e+1]); returns y_sorted float64 [R, d].
 
+    w_gate_up[e] / w_down[e] are read one expert at a time, so any indexable of per-expert
+    arrays works (e.g. one that widens bf16 blocks to float64 on access).
+
     row_scale (optional, [R]): the router score that multiplies each row's expert input (the
     Llama-4 form, "experts receive each token already scaled by the router score").
     """
     xs = np.asarray(x_sorted, dtype=np.float64)
     if row_scale is not None:
         xs = xs * np.asarray(row_scale, dtype=np.float64)[:, None]
-    R = xs.shape[0]
-    d = np.asarray(w_down).shape[-1]
+    R, d = xs.shape   # the layer maps hidden size d back to d
     y = np.zeros((R, d), dtype=np.float64)
     E = len(offsets) - 1
     for e in range(E):
@@ -202,7 +204,7 @@ def forward(x, logits, w_gate_up, w_down, k: int, score_fn: int = SOFTMAX,
     routed sum.
     """
     x = np.asarray(x, dtype=np.float64)
-    E = np.asarray(w_gate_up).shape[0]
+    E = len(w_gate_up)   # per-expert blocks are only ever indexed one expert at a time
     ids, w = route(logits, k, score_fn, renormalize)
     counts, offsets, s2p, p2s = dispatch(ids, E)
     xs = permute_rows(x, s2p, k)

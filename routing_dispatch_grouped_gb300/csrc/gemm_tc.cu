@@ -1,0 +1,437 @@
+// Grouped expert GEMM on the sm_103a tensor cores (tcgen05 + TMEM + TMA), bf16 in, fp32 accumulate.
+//
+// Tensor parallelism page, "Packed strategies": the experts' gate and up projections are one
+// packed weight [E, hidden, 2*expert_dim] applied with a batched matmul and split in two along
+// the last dimension (gate first). Expert parallelism page, "Adding an implementation":
+// experts_forward runs each expert on the rows routed to it. Here both become one persistent
+// grouped GEMM over ragged per-expert row ranges read from the device offsets (no host sync):
+//
+//   gate_up: for rows of expert e, accumulate [gate | up] = x_rows . W_gu[e][:, n0:n0+128 | I+n0:..]
+//            in one 128 x 256 fp32 TMEM accumulator (one N=256 MMA covers both halves), then the
+//            epilogue applies the optional row scale and SiLU(gate) * up and stores bf16 h.
+//   down:    y = h . W_down[e][:, n0:n0+256] into a 128 x 256 accumulator; the epilogue applies
+//            the optional row weight and stores fp32.
+//
+// Structure (one CTA per SM, 192 threads):
+//   warp 0        TMA producer: A tile 128 x 64 (K-major, 128B swizzle) and four 64 x 64 weight
+//                 blocks (MN-major, 128B swizzle) per stage, 4 stages in shared memory.
+//   warp 1        allocates 512 TMEM columns (two 256-column accumulators), one lane issues
+//                 tcgen05.mma (M=128, N=256, K=16) and commits stage/accumulator barriers.
+//   warps 2..5    epilogue: tcgen05.ld of their 32 TMEM lanes, math, 16-byte global stores,
+//                 while the MMA warp fills the other accumulator.
+// Tiles are ordered expert-major, then by N block, then by M block, so the CTAs working at
+// the same time share weight blocks through L2. Every mbarrier wait is bounded in time; on
+// expiry the kernel records MOE_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and
+// returns.
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+namespace rdg {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kABytes = kTileM * kTileK * 2;       // 16 KB
+constexpr int kBBlockBytes = 64 * kTileK * 2;      // 8 KB: 64 columns x 64 k-rows
+constexpr int kBBytes = 4 * kBBlockBytes;          // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;     // 48 KB
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s for any single wait
+
+struct TcParams {
+    const int32_t* offsets;  // [E+1] or nullptr
+    const int32_t* sorted_to_slot;
+    const float* topk_weights;
+    void* out;
+    int* status;
+    int R, K, N, E;
+    int n_tile;      // output columns per tile: 128 (gate_up) or 256 (down)
+    int n_tiles;     // ceil(N / n_tile)
+    int k_blocks;    // ceil(K / 64)
+    int row_scale;   // gate_up: scale accumulators; down: weight rows
+};
+
+struct __align__(8) SmemTail {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    int total_tiles;
+    int prefix[kMaxE + 1];  // first tile index of each expert
+    int off[kMaxE + 1];     // row offsets
+    int mt[kMaxE];          // M blocks of each expert
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(SmemTail);
+
+struct TileInfo {
+    int e, row0, row_end, n0;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(const SmemTail& st, int E, int n_tiles,
+                                                int n_tile, int tile) {
+    int lo = 0, hi = E - 1;  // largest e with prefix[e] <= tile
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (st.prefix[mid] <= tile)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int e = lo;
+    const int local = tile - st.prefix[e];
+    const int m = st.mt[e];
+    const int nb = local / m, mb = local - nb * m;
+    TileInfo ti;
+    ti.e = e;
+    ti.row0 = st.off[e] + mb * kTileM;
+    ti.row_end = st.off[e + 1];
+    ti.n0 = nb * n_tile;
+    return ti;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float silu(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const TcParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + (size_t)kStages * kStageBytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = p.E;
+
+    // ---- set-up: barriers, TMEM, tile table ----
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&st.full[s], 1);
+            mbar_init(&st.empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&st.tfull[a], 1);
+            mbar_init(&st.tempty[a], 4);
+        }
+        mbar_init(&st.drain, 1);
+        st.abort = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) tmem_alloc(&st.tmem_base, kTmemCols);
+    if (warp == 2) {
+        for (int e = lane; e <= E; e += 32)
+            st.off[e] = p.offsets ? __ldg(p.offsets + e) : (e == 0 ? 0 : p.R);
+        __syncwarp();
+        if (lane == 0) {
+            int acc = 0;
+            for (int e = 0; e < E; ++e) {
+                int rows = st.off[e + 1] - st.off[e];
+                if (rows < 0) rows = 0;
+                const int m = (rows + kTileM - 1) / kTileM;
+                st.mt[e] = m > 0 ? m : 1;  // avoid division by zero; such experts own no tiles
+                st.prefix[e] = acc;
+                acc += m * p.n_tiles;
+            }
+            st.prefix[E] = acc;
+            st.total_tiles = acc;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = st.tmem_base;
+    const int total = st.total_tiles;
+    volatile int* abort_flag = &st.abort;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            uint32_t stage = 0, phase = 0;
+            uint32_t armed_phase[kStages];
+            bool armed[kStages];
+#pragma unroll
+            for (int s = 0; s < kStages; ++s) {
+                armed[s] = false;
+                armed_phase[s] = 0;
+            }
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const TileInfo ti = decode_tile(st, E, p.n_tiles, p.n_tile, tile);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&st.empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&st.full[stage], kStageBytes);
+                    armed[stage] = true;
+                    armed_phase[stage] = phase;
+                    const uint32_t a_dst = smem_u32(smem + (size_t)stage * kStageBytes);
+                    const uint32_t b_dst = a_dst + kABytes;
+                    const int kc = kb * kTileK;
+                    tma_load_2d(a_dst, &tmA, &st.full[stage], kc, ti.row0);
+                    if (KIND == kGateUp) {
+                        tma_load_3d(b_dst, &tmB, &st.full[stage], ti.n0, kc, ti.e);
+                        tma_load_3d(b_dst + kBBlockBytes, &tmB, &st.full[stage], ti.n0 + 64, kc,
+                                    ti.e);
+                        tma_load_3d(b_dst + 2 * kBBlockBytes, &tmB, &st.full[stage], p.N + ti.n0,
+                                    kc, ti.e);
+                        tma_load_3d(b_dst + 3 * kBBlockBytes, &tmB, &st.full[stage],
+                                    p.N + ti.n0 + 64, kc, ti.e);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            tma_load_3d(b_dst + j * kBBlockBytes, &tmB, &st.full[stage],
+                                        ti.n0 + 64 * j, kc, ti.e);
+                    }
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                st.abort = 1;
+                set_status(p.status, MOE_ERR_TIMEOUT);
+            }
+            if (*abort_flag) {
+                // let every copy this thread started land before shared memory is released
+                for (int s = 0; s < kStages; ++s)
+                    if (armed[s]) mbar_wait(&st.full[s], armed_phase[s], nullptr, kWaitLimitNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, true);
+            uint32_t stage = 0, phase = 0, it = 0;
+            bool ok = true, issued = false;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+                const uint32_t acc = it & 1u;
+                if (!mbar_wait(&st.tempty[acc], ((it >> 1) & 1u) ^ 1u, abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * kTileN;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&st.full[stage], phase, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + (size_t)stage * kStageBytes);
+                    const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTileK / 16; ++kk) {
+                        // A: K-major, +32 bytes per K=16 step inside the 128-byte swizzle row.
+                        // B: MN-major, 64-column blocks 8 KB apart (LBO), 8-row groups 1 KB apart
+                        //    (SBO), +2 KB per K=16 step.
+                        const uint64_t adesc = smem_desc(a_addr + kk * 32, 16, 1024);
+                        const uint64_t bdesc = smem_desc(b_addr + kk * 2048, kBBlockBytes, 1024);
+                        umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    umma_commit(&st.empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) umma_commit(&st.tfull[acc]);
+            }
+            if (!ok) {
+                st.abort = 1;
+                set_status(p.status, MOE_ERR_TIMEOUT);
+            }
+            if (*abort_flag && issued) {
+                umma_commit(&st.drain);  // completes once every MMA issued above is done
+                mbar_wait(&st.drain, 0, nullptr, kWaitLimitNs);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================= epilogue (warps 2..5) =================
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        uint32_t it = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+            const TileInfo ti = decode_tile(st, E, p.n_tiles, p.n_tile, tile);
+            const uint32_t acc = it & 1u;
+            if (!mbar_wait(&st.tfull[acc], (it >> 1) & 1u, abort_flag, kWaitLimitNs)) {
+                if (lane == 0) {
+                    st.abort = 1;
+                    set_status(p.status, MOE_ERR_TIMEOUT);
+                }
+                break;
+            }
+            tc_fence_after();
+            const int row = ti.row0 + q * 32 + lane;
+            const bool row_ok = row < ti.row_end;
+            float s = 1.0f;
+            if (p.row_scale && row_ok) s = __ldg(p.topk_weights + __ldg(p.sorted_to_slot + row));
+            const uint32_t tbase = tmem_base + acc * kTileN + ((uint32_t)(q * 32) << 16);
+            if (KIND == kGateUp) {
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t g[32], u[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, g);
+                    tmem_ld_32x32b_x32(tbase + 128 + c * 32, u);
+                    tmem_ld_wait();
+                    const int col0 = ti.n0 + c * 32;
+                    if (row_ok) {
+                        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * p.N + col0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            if (col0 + v * 8 < p.N) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int h2 = 0; h2 < 4; ++h2) {
+                                    const int i = v * 8 + h2 * 2;
+                                    const float g0 = __uint_as_float(g[i]) * s;
+                                    const float g1 = __uint_as_float(g[i + 1]) * s;
+                                    const float u0 = __uint_as_float(u[i]) * s;
+                                    const float u1 = __uint_as_float(u[i + 1]) * s;
+                                    w[h2] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
+                                }
+                                dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                            }
+                        }
+                    }
+                }
+            } else {
+                float* out = static_cast<float*>(p.out);
+#pragma unroll 1
+                for (int c = 0; c < kTileN / 32; ++c) {
+                    uint32_t y[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, y);
+                    tmem_ld_wait();
+                    const int col0 = ti.n0 + c * 32;
+                    if (row_ok) {
+                        float4* dst = reinterpret_cast<float4*>(out + (size_t)row * p.N + col0);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            if (col0 + v * 4 < p.N) {
+                                dst[v] = make_float4(__uint_as_float(y[v * 4]) * s,
+                                                     __uint_as_float(y[v * 4 + 1]) * s,
+                                                     __uint_as_float(y[v * 4 + 2]) * s,
+                                                     __uint_as_float(y[v * 4 + 3]) * s);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&st.tempty[acc]);
+        }
+    }
+
+    // ---- teardown ----
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------------------------
+// host side: tensor maps and launch
+// ---------------------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+            const cuuint64_t* strides, const cuuint32_t* box) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint32_t elem[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims,
+              strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KIND>
+cudaError_t launch_kind(const GroupedGemmArgs& a, cudaStream_t s) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(tc_grouped_gemm<KIND>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    CUtensorMap tmA, tmB;
+    const cuuint64_t a_dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.R};
+    const cuuint64_t a_str[1] = {(cuuint64_t)a.K * 2};
+    const cuuint32_t a_box[2] = {kTileK, kTileM};
+    const int groups = a.offsets ? a.E : 1;
+    const cuuint64_t bn = (KIND == kGateUp) ? 2 * (cuuint64_t)a.N : (cuuint64_t)a.N;
+    const cuuint64_t b_dims[3] = {bn, (cuuint64_t)a.K, (cuuint64_t)groups};
+    const cuuint64_t b_str[2] = {bn * 2, bn * 2 * (cuuint64_t)a.K};
+    const cuuint32_t b_box[3] = {64, kTileK, 1};
+    if (!encode(&tmA, a.a, 2, a_dims, a_str, a_box) || !encode(&tmB, a.b, 3, b_dims, b_str, b_box))
+        return cudaErrorInvalidValue;
+
+    TcParams p;
+    p.offsets = a.offsets;
+    p.sorted_to_slot = a.sorted_to_slot;
+    p.topk_weights = a.topk_weights;
+    p.out = a.out;
+    p.status = a.status;
+    p.R = a.R;
+    p.K = a.K;
+    p.N = a.N;
+    p.E = groups;
+    p.n_tile = (KIND == kGateUp) ? 128 : 256;
+    p.n_tiles = (a.N + p.n_tile - 1) / p.n_tile;
+    p.k_blocks = (a.K + kTileK - 1) / kTileK;
+    p.row_scale = (KIND == kGateUp) ? (a.scale_rows ? 1 : 0) : (a.weight_rows ? 1 : 0);
+
+    // upper bound on tiles: sum_e ceil(n_e / 128) <= R / 128 + groups
+    const long long m_ub = (long long)(a.R + kTileM - 1) / kTileM + groups;
+    const long long tiles_ub = m_ub * p.n_tiles;
+    int grid = device_sm_count();
+    if (tiles_ub < grid) grid = (int)tiles_ub;
+    if (grid < 1) grid = 1;
+    tc_grouped_gemm<KIND><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
+    return a.kind == kGateUp ? launch_kind<kGateUp>(a, s) : launch_kind<kDown>(a, s);
+}
+
+}  // namespace rdg

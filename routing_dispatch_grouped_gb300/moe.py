@@ -1,0 +1,278 @@
+"""Python binding of libmoe (ctypes). Argument marshalling only: every step runs in the library's
+CUDA kernels. Tensors are PyTorch CUDA tensors (PyTorch provides device memory and streams);
+outputs and workspaces not passed in are allocated here with torch.
+
+The functions keep the C names: moe_route, moe_dispatch, moe_gate_up, moe_down, moe_experts,
+moe_combine, moe_forward. A non-zero status raises MoEError. There is no CPU fallback: if the
+library is missing, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe.so")
+
+SOFTMAX, SIGMOID = 0, 1
+RENORMALIZE, SCALE_INPUT, FUSE_COMBINE_WEIGHT = 1, 2, 4
+F32, BF16 = 0, 1
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+          3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_BOUNDS",
+          6: "MOE_ERR_TIMEOUT"}
+
+# name -> (restype, argtypes)
+_P, _I, _U, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
+SIGNATURES = {
+    "moe_route": (_I, [_P, _I, _I, _I, _I, _U, _P, _P, _P]),
+    "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_dispatch_workspace_size": (_S, [_I, _I, _I]),
+    "moe_gate_up": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _U, _P, _P, _S, _P]),
+    "moe_down": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _U, _P, _P, _S, _P]),
+    "moe_experts": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _U, _P, _P, _P, _S, _P]),
+    "moe_experts_workspace_size": (_S, []),
+    "moe_combine": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "moe_forward": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P, _P,
+                         _P, _P, _S, _P]),
+    "moe_forward_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
+    "moe_forward_kernel_count": (_I, [_I, _I]),
+    "moe_read_device_status": (_I, [_P, _P]),
+    "moe_status_string": (ctypes.c_char_p, [_I]),
+}
+
+_lib = None
+
+
+class MoEError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe.so (built in-tree by routing_dispatch_grouped_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -m routing_dispatch_grouped_gb300.build`")
+        cdll = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(cdll, name)
+            f.restype, f.argtypes = res, args
+        _lib = cdll
+    return _lib
+
+
+def _check(fn: str, st: int):
+    if st != 0:
+        raise MoEError(fn, st)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _need(t: torch.Tensor, name: str):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    return t
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    # torch's caching allocator returns blocks aligned to at least 512 bytes
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+# ------------------------------------------------------------------------------------------------
+def moe_route(logits, k, score_fn=SOFTMAX, renormalize=True, topk_ids=None, topk_weights=None,
+              stream=None):
+    _need(logits, "logits")
+    T, E = logits.shape
+    dev = logits.device
+    ids = topk_ids if topk_ids is not None else torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = topk_weights if topk_weights is not None else torch.empty(T, k, dtype=torch.float32,
+                                                                  device=dev)
+    _check("moe_route", lib().moe_route(_p(logits), T, E, k, score_fn,
+                                        RENORMALIZE if renormalize else 0, _p(ids), _p(w),
+                                        _stream(stream)))
+    return ids, w
+
+
+def moe_dispatch_workspace_size(T, E, k) -> int:
+    return lib().moe_dispatch_workspace_size(T, E, k)
+
+
+def moe_dispatch(topk_ids, E, x=None, workspace=None, out=None, stream=None):
+    """Returns dict(counts, offsets, sorted_to_slot, slot_to_sorted, x_sorted, workspace)."""
+    _need(topk_ids, "topk_ids")
+    T, k = topk_ids.shape
+    R = T * k
+    dev = topk_ids.device
+    o = dict(out or {})
+    o.setdefault("counts", torch.empty(E, dtype=torch.int32, device=dev))
+    o.setdefault("offsets", torch.empty(E + 1, dtype=torch.int32, device=dev))
+    o.setdefault("sorted_to_slot", torch.empty(R, dtype=torch.int32, device=dev))
+    o.setdefault("slot_to_sorted", torch.empty(R, dtype=torch.int32, device=dev))
+    d, dt = 0, BF16
+    if x is not None:
+        _need(x, "x")
+        d, dt = x.shape[1], _dt(x)
+        o.setdefault("x_sorted", torch.empty(R, d, dtype=x.dtype, device=dev))
+    else:
+        o["x_sorted"] = None
+    ws = workspace if workspace is not None else _workspace(moe_dispatch_workspace_size(T, E, k),
+                                                            dev)
+    _check("moe_dispatch", lib().moe_dispatch(
+        _p(topk_ids), _p(x), dt, T, d, E, k, _p(o["counts"]), _p(o["offsets"]),
+        _p(o["sorted_to_slot"]), _p(o["slot_to_sorted"]), _p(o["x_sorted"]), _p(ws),
+        ws.numel(), _stream(stream)))
+    o["workspace"] = ws
+    return o
+
+
+def moe_experts_workspace_size() -> int:
+    return lib().moe_experts_workspace_size()
+
+
+def moe_gate_up(x_rows, offsets, w_gate_up, sorted_to_slot=None, topk_weights=None,
+                scale_input=False, h=None, workspace=None, stream=None):
+    _need(x_rows, "x_rows")
+    R, d = x_rows.shape
+    E, _, two_i = w_gate_up.shape
+    I = two_i // 2
+    dev = x_rows.device
+    h = h if h is not None else torch.empty(R, I, dtype=x_rows.dtype, device=dev)
+    ws = workspace if workspace is not None else _workspace(moe_experts_workspace_size(), dev)
+    _check("moe_gate_up", lib().moe_gate_up(
+        _p(x_rows), _p(offsets), _p(sorted_to_slot), _p(topk_weights), _dt(x_rows), R, d, E, I,
+        _p(w_gate_up), SCALE_INPUT if scale_input else 0, _p(h), _p(ws), ws.numel(),
+        _stream(stream)))
+    return h
+
+
+def moe_down(h, offsets, w_down, sorted_to_slot=None, topk_weights=None, fuse_weight=False,
+             y_sorted=None, workspace=None, stream=None):
+    _need(h, "h")
+    R, I = h.shape
+    E, _, d = w_down.shape
+    dev = h.device
+    y = y_sorted if y_sorted is not None else torch.empty(R, d, dtype=torch.float32, device=dev)
+    ws = workspace if workspace is not None else _workspace(moe_experts_workspace_size(), dev)
+    _check("moe_down", lib().moe_down(
+        _p(h), _p(offsets), _p(sorted_to_slot), _p(topk_weights), _dt(h), R, d, E, I,
+        _p(w_down), FUSE_COMBINE_WEIGHT if fuse_weight else 0, _p(y), _p(ws), ws.numel(),
+        _stream(stream)))
+    return y
+
+
+def moe_experts(x_sorted, offsets, w_gate_up, w_down, sorted_to_slot=None, topk_weights=None,
+                flags=0, h=None, y_sorted=None, workspace=None, stream=None):
+    _need(x_sorted, "x_sorted")
+    R, d = x_sorted.shape
+    E, _, two_i = w_gate_up.shape
+    I = two_i // 2
+    dev = x_sorted.device
+    h = h if h is not None else torch.empty(R, I, dtype=x_sorted.dtype, device=dev)
+    y = y_sorted if y_sorted is not None else torch.empty(R, d, dtype=torch.float32, device=dev)
+    ws = workspace if workspace is not None else _workspace(moe_experts_workspace_size(), dev)
+    _check("moe_experts", lib().moe_experts(
+        _p(x_sorted), _p(offsets), _p(sorted_to_slot), _p(topk_weights), _dt(x_sorted), R, d, E,
+        I, _p(w_gate_up), _p(w_down), flags, _p(h), _p(y), _p(ws), ws.numel(), _stream(stream)))
+    return h, y
+
+
+def moe_combine(y_sorted, slot_to_sorted, k, out_dtype, topk_weights=None, y_shared=None,
+                out=None, stream=None):
+    _need(y_sorted, "y_sorted")
+    R, d = y_sorted.shape
+    T = slot_to_sorted.numel() // k
+    out = out if out is not None else torch.empty(T, d, dtype=out_dtype, device=y_sorted.device)
+    _check("moe_combine", lib().moe_combine(
+        _p(y_sorted), _p(slot_to_sorted), _p(topk_weights), _p(y_shared), T, d, k, _dt(out),
+        _p(out), _stream(stream)))
+    return out
+
+
+def moe_forward_workspace_size(T, d, E, k, I, Is, dtype) -> int:
+    return lib().moe_forward_workspace_size(T, d, E, k, I, Is, BF16 if dtype == torch.bfloat16
+                                            else F32)
+
+
+def moe_forward_kernel_count(T, Is) -> int:
+    return lib().moe_forward_kernel_count(T, Is)
+
+
+def moe_forward(x, logits, w_gate_up, w_down, k, score_fn=SOFTMAX, flags=RENORMALIZE,
+                w_shared_gate_up=None, w_shared_down=None, out=None, topk_ids=None,
+                topk_weights=None, workspace=None, stream=None):
+    """The whole layer. Returns (out, topk_ids, topk_weights, workspace)."""
+    _need(x, "x")
+    _need(logits, "logits")
+    T, d = x.shape
+    E, _, two_i = w_gate_up.shape
+    I = two_i // 2
+    Is = 0 if w_shared_gate_up is None else w_shared_gate_up.shape[1] // 2
+    dev = x.device
+    out = out if out is not None else torch.empty(T, d, dtype=x.dtype, device=dev)
+    ids = topk_ids if topk_ids is not None else torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = topk_weights if topk_weights is not None else torch.empty(T, k, dtype=torch.float32,
+                                                                  device=dev)
+    ws = workspace if workspace is not None else _workspace(
+        moe_forward_workspace_size(T, d, E, k, I, Is, x.dtype), dev)
+    _check("moe_forward", lib().moe_forward(
+        _p(x), _p(logits), _dt(x), T, d, E, k, I, score_fn, flags, _p(w_gate_up), _p(w_down),
+        _p(w_shared_gate_up), _p(w_shared_down), Is, _p(ids), _p(w), _p(out), _p(ws), ws.numel(),
+        _stream(stream)))
+    return out, ids, w, ws
+
+
+def moe_read_device_status(workspace, stream=None) -> int:
+    return lib().moe_read_device_status(_p(workspace), _stream(stream))
+
+
+def forward_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is, dtype):
+    """Views of the intermediates moe_forward leaves in its workspace (for tests and tools);
+    the offsets follow the library's layout rule: 256-byte status word, then counts, offsets,
+    dispatch scratch, sorted_to_slot, slot_to_sorted, x_sorted, h, y_sorted, shared h, shared y,
+    each rounded up to 256 bytes."""
+    R = T * k
+    b = 2 if dtype == torch.bfloat16 else 4
+    nchunks = (R + 255) // 256
+    sizes = [("counts", E * 4), ("offsets", (E + 1) * 4), ("chunk", nchunks * E * 4),
+             ("sorted_to_slot", R * 4), ("slot_to_sorted", R * 4), ("x_sorted", R * d * b),
+             ("h", R * I * b), ("y_sorted", R * d * 4), ("h_shared", T * Is * b),
+             ("y_shared", T * d * 4 if Is else 0)]
+    views, o = {}, 256
+    for name, nbytes in sizes:
+        views[name] = ws[o:o + nbytes]
+        o = (o + nbytes + 255) // 256 * 256
+    v = views
+    out = {
+        "counts": v["counts"].view(torch.int32),
+        "offsets": v["offsets"].view(torch.int32),
+        "sorted_to_slot": v["sorted_to_slot"].view(torch.int32),
+        "slot_to_sorted": v["slot_to_sorted"].view(torch.int32),
+        "x_sorted": v["x_sorted"].view(dtype).view(R, d),
+        "h": v["h"].view(dtype).view(R, I),
+        "y_sorted": v["y_sorted"].view(torch.float32).view(R, d),
+    }
+    if Is:
+        out["h_shared"] = v["h_shared"].view(dtype).view(T, Is)
+        out["y_shared"] = v["y_shared"].view(torch.float32).view(T, d)
+    return out

@@ -1,0 +1,143 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every entry point the header
+declares, and rejects bad arguments before enqueueing anything (no CUDA call is reached)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from routing_dispatch_grouped_gb300 import moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(moe.LIB_PATH):
+        from routing_dispatch_grouped_gb300 import build
+        build.build()
+    return moe.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_five_steps():
+    names = declared_functions()
+    for n in ("moe_route", "moe_dispatch", "moe_experts", "moe_combine", "moe_forward"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(moe.SIGNATURES), "binding and header disagree"
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails validation first
+MIS = 0x10004   # misaligned
+NULL = None
+
+
+def test_route_validation(L):
+    r = L.moe_route
+    assert r(FAKE, 4, 8, 9, 0, 1, FAKE, FAKE, NULL) == 1          # k > E
+    assert r(FAKE, 4, 300, 2, 0, 1, FAKE, FAKE, NULL) == 2        # E > 256
+    assert r(FAKE, 4, 8, 0, 0, 1, FAKE, FAKE, NULL) == 1          # k = 0
+    assert r(FAKE, -1, 8, 2, 0, 1, FAKE, FAKE, NULL) == 1         # T < 0
+    assert r(FAKE, 4, 8, 2, 7, 1, FAKE, FAKE, NULL) == 1          # bad score fn
+    assert r(FAKE, 4, 8, 2, 0, 8, FAKE, FAKE, NULL) == 1          # unknown flag
+    assert r(NULL, 4, 8, 2, 0, 1, FAKE, FAKE, NULL) == 1          # null logits
+    assert r(MIS, 4, 8, 2, 0, 1, FAKE, FAKE, NULL) == 1           # misaligned
+    assert r(NULL, 0, 8, 2, 0, 1, NULL, NULL, NULL) == 0          # T = 0: no-op
+    assert r(FAKE, 1 << 28, 8, 8, 0, 1, FAKE, FAKE, NULL) == 2    # T*k >= 2^31
+
+
+def test_dispatch_validation(L):
+    d = L.moe_dispatch
+    ws_need = L.moe_dispatch_workspace_size(100, 8, 2)
+    assert ws_need >= 256 and ws_need % 256 == 0
+    ok = dict(ids=FAKE, x=FAKE, dt=1, T=100, d=64, E=8, k=2)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return d(a["ids"], a["x"], a["dt"], a["T"], a["d"], a["E"], a["k"], FAKE, FAKE, FAKE,
+                 FAKE, FAKE if a["x"] else None, a.get("ws", 0x100000), a.get("wsb", ws_need),
+                 NULL)
+    assert call(d=60) == 1                    # bf16 rows must be a multiple of 8 elements
+    assert call(dt=5) == 1
+    assert call(wsb=ws_need - 1) == 3         # short workspace
+    assert call(ws=0x100010) == 3             # workspace not 256-byte aligned
+    assert call(k=9) == 1
+    assert d(FAKE, FAKE, 1, 100, 64, 8, 2, FAKE, FAKE, FAKE, FAKE, None, 0x100000, ws_need,
+             NULL) == 1                       # x without x_sorted
+
+
+def test_experts_validation(L):
+    g = L.moe_gate_up
+    ws = 0x100000
+    # offsets NULL needs E == 1
+    assert g(FAKE, None, None, None, 1, 128, 64, 4, 64, FAKE, 0, FAKE, ws, 256, NULL) == 1
+    # scale needs sorted_to_slot and weights
+    assert g(FAKE, FAKE, None, None, 1, 128, 64, 4, 64, FAKE, 2, FAKE, ws, 256, NULL) == 1
+    # bad flag for gate_up
+    assert g(FAKE, FAKE, FAKE, FAKE, 1, 128, 64, 4, 64, FAKE, 4, FAKE, ws, 256, NULL) == 1
+    # I not a multiple of 8
+    assert g(FAKE, FAKE, None, None, 1, 128, 64, 4, 60, FAKE, 0, FAKE, ws, 256, NULL) == 1
+    # workspace too small
+    assert g(FAKE, FAKE, None, None, 1, 128, 64, 4, 64, FAKE, 0, FAKE, ws, 16, NULL) == 3
+    # R == 0 is a no-op
+    assert g(FAKE, FAKE, None, None, 1, 0, 64, 4, 64, FAKE, 0, FAKE, ws, 256, NULL) == 0
+    e = L.moe_experts
+    assert e(FAKE, FAKE, FAKE, FAKE, 1, 128, 64, 4, 64, FAKE, FAKE, 6, FAKE, FAKE, ws, 256,
+             NULL) == 1                         # scale + fused weight exclude each other
+    assert L.moe_experts_workspace_size() == 256
+
+
+def test_combine_and_forward_validation(L):
+    c = L.moe_combine
+    assert c(FAKE, FAKE, None, None, 10, 64, 33, 1, FAKE, NULL) == 2   # k > 32
+    assert c(FAKE, FAKE, None, None, 10, 60, 2, 1, FAKE, NULL) == 1    # bf16 d % 8
+    assert c(MIS, FAKE, None, None, 10, 64, 2, 1, FAKE, NULL) == 1
+    assert c(None, None, None, None, 0, 64, 2, 1, None, NULL) == 0
+    f = L.moe_forward
+    sz = L.moe_forward_workspace_size(64, 128, 8, 2, 256, 0, 1)
+    args = [FAKE, FAKE, 1, 64, 128, 8, 2, 256, 0, 1, FAKE, FAKE, None, None, 0, FAKE, FAKE, FAKE,
+            0x100000, sz, NULL]
+    bad = list(args); bad[9] = 1 | 2 | 4
+    assert f(*bad) == 1                                            # scale + fuse
+    bad = list(args); bad[12] = FAKE
+    assert f(*bad) == 1                                            # shared weights without Is
+    bad = list(args); bad[19] = sz - 256
+    assert f(*bad) == 3
+    bad = list(args); bad[3] = 0
+    assert f(*bad) == 0
+
+
+def test_workspace_size_matches_binding_layout(L):
+    import torch
+    for (T, d, E, k, I, Is, dt) in [(256, 128, 8, 2, 256, 0, torch.float32),
+                                    (4096, 4096, 8, 2, 14336, 0, torch.bfloat16),
+                                    (16384, 5120, 16, 1, 8192, 8192, torch.bfloat16),
+                                    (1, 2048, 128, 8, 768, 0, torch.bfloat16)]:
+        sz = moe.moe_forward_workspace_size(T, d, E, k, I, Is, dt)
+        ws = torch.empty(sz, dtype=torch.uint8)
+        v = moe.forward_workspace_views(ws, T, d, E, k, I, Is, dt)
+        assert v["y_sorted"].numel() == T * k * d
+        last = v["y_shared"] if Is else v["y_sorted"]
+        end = last.untyped_storage().data_ptr()
+        assert sz >= (last.data_ptr() - ws.data_ptr()) + last.numel() * last.element_size()
+
+
+def test_kernel_count_and_strings(L):
+    assert L.moe_forward_kernel_count(0, 0) == 0
+    assert L.moe_forward_kernel_count(10, 0) == 8
+    assert L.moe_forward_kernel_count(10, 128) == 10
+    for code in range(7):
+        assert L.moe_status_string(code).decode().startswith(moe.STATUS[code])
