@@ -190,12 +190,15 @@ cudaError_t launch_dispatch(const int32_t* ids, const void* x, size_t row_bytes,
     const int R = T * k;
     const int nchunks = (R + kDispatchChunk - 1) / kDispatchChunk;
     const int blocks = (nchunks + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    dispatch_hist_kernel<<<blocks, 32 * kWarpsPerBlock, 0, s>>>(ids, R, E, nchunks,
-                                                                chunk_scratch, status);
+    // With no slots only the scan runs: it writes zero counts and offsets.
+    if (blocks > 0)
+        dispatch_hist_kernel<<<blocks, 32 * kWarpsPerBlock, 0, s>>>(ids, R, E, nchunks,
+                                                                    chunk_scratch, status);
     dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_scratch, nchunks, E, counts, offsets);
-    dispatch_rank_kernel<<<blocks, 32 * kWarpsPerBlock, 0, s>>>(ids, R, E, nchunks, chunk_scratch,
-                                                                sorted_to_slot, slot_to_sorted);
-    if (x != nullptr && x_sorted != nullptr) {
+    if (blocks > 0)
+        dispatch_rank_kernel<<<blocks, 32 * kWarpsPerBlock, 0, s>>>(
+            ids, R, E, nchunks, chunk_scratch, sorted_to_slot, slot_to_sorted);
+    if (T > 0 && x != nullptr && x_sorted != nullptr) {
         const int vec = (int)(row_bytes / 16);
         const int max_blocks = device_sm_count() * 8;
         int cblocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;

@@ -107,7 +107,7 @@ def test_dispatch_matches_oracle(name, T):
 
 
 @pytest.mark.parametrize("case", ["all_experts", "one_expert", "sparse", "ragged", "single",
-                                  "E1", "big_ragged"])
+                                  "E1", "big_ragged", "empty"])
 def test_dispatch_edge_cases(case):
     rng = np.random.default_rng(0)
     if case == "all_experts":
@@ -122,6 +122,8 @@ def test_dispatch_edge_cases(case):
         E, ids = 128, rng.permutation(128)[:8][None, :]
     elif case == "E1":
         E, ids = 1, np.zeros((77, 1), int)
+    elif case == "empty":      # T = 0: counts and offsets are all zero
+        E, ids = 12, np.zeros((0, 3), int)
     else:
         E, ids = 64, np.stack([rng.permutation(64)[:6] for _ in range(10007)])
     x = synth.normal((ids.shape[0], 40), torch.bfloat16, 1, "xd", 1.0, device=DEV)
