@@ -33,9 +33,9 @@
  * Conventions for every entry point
  *   - All device pointers are caller-owned device memory. The library never allocates, frees or
  *     synchronises inside these calls; work is enqueued on `stream` (NULL = legacy default
- *     stream) and the call returns at once. Nothing here needs a host sync, so a sequence of
- *     calls with fixed pointers can be captured in a CUDA graph (the property [EP-choose] asks
- *     of decode).
+ *     stream) and the call returns at once. moe_route, moe_dispatch, moe_gate_up, moe_down,
+ *     moe_experts, moe_combine and moe_forward need no host sync, so a sequence of them with
+ *     fixed pointers can be captured in a CUDA graph (the property [EP-choose] asks of decode).
  *   - Every argument is checked before any launch ([EP-override] convention). A bad argument
  *     returns MOE_ERR_INVALID_ARG, a shape or dtype the kernels do not cover returns
  *     MOE_ERR_UNSUPPORTED, a short workspace returns MOE_ERR_WORKSPACE; in all three cases
@@ -142,6 +142,31 @@ moe_status moe_dispatch(const int32_t* topk_ids, const void* x, moe_dtype dt, in
                         int32_t* slot_to_sorted, void* x_sorted, void* workspace,
                         size_t ws_bytes, moe_stream_t stream);
 size_t moe_dispatch_workspace_size(int T, int E, int k);
+
+/*
+ * moe_dispatch_noalloc - moe_dispatch without a workspace, for callers that cannot allocate
+ * device memory where they call it (a plugin inside a host application that owns every device
+ * allocation and hands it no allocator, or a service that forbids device allocation after
+ * start-up). The pages have no counterpart to this entry point: it exists for those callers.
+ *   Arguments and outputs as for moe_dispatch, minus workspace and ws_bytes. The scratch
+ *   (one int32 count per (256-slot chunk, expert)) lives in a fixed device array of
+ *   MOE_DISPATCH_NOALLOC_MAX_SCRATCH_INTS int32 (1 MiB) inside the library, which every GPU
+ *   that loads the library holds until the process exits. Requests needing more,
+ *   ceil(T*k / 256) * E > MOE_DISPATCH_NOALLOC_MAX_SCRATCH_INTS, return MOE_ERR_UNSUPPORTED
+ *   before anything is enqueued; use moe_dispatch for those.
+ *   No cudaMalloc, cudaFree or other allocating call is made.
+ *   The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ *   with that device current) and caches it; make that first call before any stream capture.
+ *   All calls share the array and it keeps the last call's contents (the kernels overwrite
+ *   every entry before reading it). Calls whose kernels overlap on the GPU, e.g. on two
+ *   streams, race on it: serialise them. There is no status word: an expert id outside [0, E)
+ *   is skipped as in moe_dispatch and shows only as slot_to_sorted == -1.
+ */
+#define MOE_DISPATCH_NOALLOC_MAX_SCRATCH_INTS 262144
+moe_status moe_dispatch_noalloc(const int32_t* topk_ids, const void* x, moe_dtype dt, int T,
+                                int d, int E, int k, int32_t* counts, int32_t* offsets,
+                                int32_t* sorted_to_slot, int32_t* slot_to_sorted, void* x_sorted,
+                                moe_stream_t stream);
 
 /*
  * moe_gate_up - grouped gate/up projection with SwiGLU ([TP-packed]; [EP-add] experts_forward):

@@ -29,6 +29,7 @@ SIGNATURES = {
     "moe_route": (_I, [_P, _I, _I, _I, _I, _U, _P, _P, _P]),
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_dispatch_workspace_size": (_S, [_I, _I, _I]),
+    "moe_dispatch_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_gate_up": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _U, _P, _P, _S, _P]),
     "moe_down": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _U, _P, _P, _S, _P]),
     "moe_experts": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _U, _P, _P, _P, _S, _P]),
