@@ -18,6 +18,7 @@ collective on the data path); the time is the maximum over ranks.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -43,6 +44,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="mixtral_8x7b")
     ap.add_argument("--T", type=int, default=None, help="override the token count")
+    ap.add_argument("--E", type=int, default=None,
+                    help="override the expert count (smaller cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=None, help="tokens in the CPU sample")
     return ap.parse_args()
@@ -253,6 +256,8 @@ def run_ours(args, rank, world):
     cfg = synth.CONFIGS[args.config]
     if args.T is not None:
         cfg = cfg.with_T(args.T)
+    if args.E is not None:
+        cfg = dataclasses.replace(cfg, E=args.E, name=f"{cfg.name}@E{args.E}")
     moe.lib()
     inp = synth.make_inputs(cfg, dev)
     T, d, E, k, I, Is = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.I_shared

@@ -347,9 +347,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
+}  // namespace
+
 // ---------------------------------------------------------------------------------------------
-// host side: tensor maps and launch
+// host side: tensor maps (shared with the swapped-operand kernel) and launch
 // ---------------------------------------------------------------------------------------------
+namespace {
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
@@ -368,9 +371,10 @@ EncodeTiledFn encode_fn() {
     });
     return fn;
 }
+}  // namespace
 
-bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
-            const cuuint64_t* strides, const cuuint32_t* box) {
+bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                            const cuuint64_t* strides, const cuuint32_t* box) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint32_t elem[3] = {1, 1, 1};
@@ -379,6 +383,8 @@ bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <int KIND>
 cudaError_t launch_kind(const GroupedGemmArgs& a, cudaStream_t s) {
@@ -400,7 +406,8 @@ cudaError_t launch_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     const cuuint64_t b_dims[3] = {bn, (cuuint64_t)a.K, (cuuint64_t)groups};
     const cuuint64_t b_str[2] = {bn * 2, bn * 2 * (cuuint64_t)a.K};
     const cuuint32_t b_box[3] = {64, kTileK, 1};
-    if (!encode(&tmA, a.a, 2, a_dims, a_str, a_box) || !encode(&tmB, a.b, 3, b_dims, b_str, b_box))
+    if (!encode_tensor_map_bf16(&tmA, a.a, 2, a_dims, a_str, a_box) ||
+        !encode_tensor_map_bf16(&tmB, a.b, 3, b_dims, b_str, b_box))
         return cudaErrorInvalidValue;
 
     TcParams p;
@@ -430,7 +437,7 @@ cudaError_t launch_kind(const GroupedGemmArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
+cudaError_t launch_grouped_gemm_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s) {
     return a.kind == kGateUp ? launch_kind<kGateUp>(a, s) : launch_kind<kDown>(a, s);
 }
 

@@ -1,0 +1,435 @@
+// Grouped expert GEMM on the sm_103a tensor cores with the weights as the MMA M operand.
+//
+// Same computation as gemm_tc.cu (Tensor parallelism page, "Packed strategies": packed
+// [E, hidden, 2*expert_dim] gate|up weight, gate first; Expert parallelism page, "Adding an
+// implementation": each expert runs on the rows routed to it), with the roles of the operands
+// swapped so that ragged expert row counts cost at most 15 padded rows instead of 127:
+//
+//   D^T[w_cols, tokens] = W^T[w_cols, K] . X^T[K, tokens]
+//
+// - A = 128 weight rows of the MMA x 64 K, read by TMA straight from the pages' [K, N]-contiguous
+//   weight layout as an MN-major operand (two 64-column blocks, 128-byte swizzle). For gate_up
+//   the two blocks are 64 gate columns and the 64 up columns of the same h columns; for down
+//   they are 128 consecutive output columns.
+// - B = up to 256 token rows x 64 K of x_sorted / h, K-major.
+// - MMA: M = 128, N = the tile's token count rounded up to 16 (at most 256), K = 16: one MMA
+//   per K step reads 12 KB of shared memory per 128 cycles, inside its bandwidth.
+// - TMEM: two tile buffers of 256 columns (512 total): the epilogue of one tile overlaps the
+//   MMAs of the next.
+// - Epilogue: thread = one accumulator row (weight column), loop over the tile's tokens. In
+//   gate_up, TMEM lanes 64..127 (up) are read by two warps that pass their values through a
+//   double-buffered 16 KB shared-memory exchange to the two warps holding lanes 0..63 (gate),
+//   which compute SiLU(gate) * up. Each warp store covers 32 consecutive columns of one token
+//   row (64 B for bf16 h, 128 B for fp32 y).
+// Tiles are enumerated on the device from the offsets: expert, then weight-column block, then
+// token block, so CTAs running together share weight blocks through L2. Waits are bounded as
+// in gemm_tc.cu.
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+namespace rdg {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kWM = 128;                 // MMA M: weight rows of the accumulator
+constexpr int kTok = 256;                // tokens per tile (MMA N at most)
+constexpr int kWBlock = 64 * kTileK * 2; // one 64-column x 64-k MN-major block: 8 KB
+constexpr int kABytes = 2 * kWBlock;     // 16 KB
+constexpr int kBBytes = kTok * kTileK * 2;  // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
+constexpr int kXchFloats = 32 * 64;      // one exchange buffer: 32 tokens x 64 columns fp32
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Output columns covered by one tile: 64 h columns (gate_up) or 128 y columns (down).
+template <int KIND>
+struct Shape {
+    static constexpr int kCols = (KIND == kGateUp) ? 64 : 128;
+};
+
+struct SwapParams {
+    const int32_t* offsets;
+    const int32_t* sorted_to_slot;
+    const float* topk_weights;
+    void* out;
+    int* status;
+    int R, K, N, E;
+    int n_tiles;   // ceil(N / 128) weight-column blocks
+    int k_blocks;  // ceil(K / 64)
+    int row_scale;
+};
+
+struct __align__(8) SmemTail {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    int total_tiles;
+    int prefix[kMaxE + 1];
+    int off[kMaxE + 1];
+    int mt[kMaxE];
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 2 * kXchFloats * 4 +
+                              sizeof(SmemTail);
+
+struct Tile {
+    int e, row0, row_end, n0;
+};
+
+template <int KIND>
+__device__ __forceinline__ Tile decode(const SmemTail& st, int E, int tile) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (st.prefix[mid] <= tile)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int local = tile - st.prefix[lo];
+    const int m = st.mt[lo];
+    const int nb = local / m, mb = local - nb * m;
+    Tile t;
+    t.e = lo;
+    t.row0 = st.off[lo] + mb * kTok;
+    t.row_end = st.off[lo + 1];
+    t.n0 = nb * Shape<KIND>::kCols;
+    return t;
+}
+
+__device__ __forceinline__ uint32_t idesc_swap(int n_tok) {
+    // fp32 accumulator, bf16 A and B, A MN-major (bit 15), B K-major, N >> 3, M = 128 >> 4
+    return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | ((uint32_t)(n_tok >> 3) << 17) |
+           ((uint32_t)(kWM >> 4) << 24);
+}
+
+__device__ __forceinline__ float silu(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
+
+// Barrier among the 128 epilogue threads only (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void epilogue_sync() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+// Same barrier, returning to every epilogue thread whether any of them passed `v` true, so all
+// four epilogue warps take the same branch.
+__device__ __forceinline__ bool epilogue_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, 1, 128, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_grouped_gemm_swap(const __grid_constant__ CUtensorMap tmW,
+                         const __grid_constant__ CUtensorMap tmX, const SwapParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float* xch = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);
+    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + (size_t)kStages * kStageBytes +
+                                                2 * kXchFloats * 4);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = p.E;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&st.full[s], 1);
+            mbar_init(&st.empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&st.tfull[a], 1);
+            mbar_init(&st.tempty[a], 4);
+        }
+        mbar_init(&st.drain, 1);
+        st.abort = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) tmem_alloc(&st.tmem_base, kTmemCols);
+    if (warp == 2) {
+        for (int e = lane; e <= E; e += 32)
+            st.off[e] = p.offsets ? __ldg(p.offsets + e) : (e == 0 ? 0 : p.R);
+        __syncwarp();
+        if (lane == 0) {
+            int acc = 0;
+            for (int e = 0; e < E; ++e) {
+                int rows = st.off[e + 1] - st.off[e];
+                if (rows < 0) rows = 0;
+                const int m = (rows + kTok - 1) / kTok;
+                st.mt[e] = m > 0 ? m : 1;
+                st.prefix[e] = acc;
+                acc += m * p.n_tiles;
+            }
+            st.prefix[E] = acc;
+            st.total_tiles = acc;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = st.tmem_base;
+    const int total = st.total_tiles;
+    volatile int* abort_flag = &st.abort;
+
+    if (warp == 0) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmW);
+            tma_prefetch_desc(&tmX);
+            uint32_t stage = 0, phase = 0;
+            uint32_t armed_phase[kStages];
+            bool armed[kStages];
+#pragma unroll
+            for (int s = 0; s < kStages; ++s) {
+                armed[s] = false;
+                armed_phase[s] = 0;
+            }
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const Tile t = decode<KIND>(st, E, tile);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&st.empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&st.full[stage], kStageBytes);
+                    armed[stage] = true;
+                    armed_phase[stage] = phase;
+                    const uint32_t a_dst = smem_u32(smem + (size_t)stage * kStageBytes);
+                    const int kc = kb * kTileK;
+                    tma_load_3d(a_dst, &tmW, &st.full[stage], t.n0, kc, t.e);
+                    // gate_up: the up columns of the same h columns; down: the next 64 columns
+                    tma_load_3d(a_dst + kWBlock, &tmW, &st.full[stage],
+                                (KIND == kGateUp) ? p.N + t.n0 : t.n0 + 64, kc, t.e);
+                    tma_load_2d(a_dst + kABytes, &tmX, &st.full[stage], kc, t.row0);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                st.abort = 1;
+                set_status(p.status, MOE_ERR_TIMEOUT);
+            }
+            if (*abort_flag) {
+                for (int s = 0; s < kStages; ++s)
+                    if (armed[s]) mbar_wait(&st.full[s], armed_phase[s], nullptr, kWaitLimitNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, it = 0;
+            bool ok = true, issued = false;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+                const Tile t = decode<KIND>(st, E, tile);
+                int n_tok = t.row_end - t.row0;
+                if (n_tok > kTok) n_tok = kTok;
+                n_tok = (n_tok + 15) & ~15;
+                const uint32_t idesc = idesc_swap(n_tok);
+                const uint32_t acc = it & 1u;
+                if (!mbar_wait(&st.tempty[acc], ((it >> 1) & 1u) ^ 1u, abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d0 = tmem_base + acc * 256u;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&st.full[stage], phase, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + (size_t)stage * kStageBytes);
+                    const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTileK / 16; ++kk) {
+                        // A: MN-major weight blocks (64 columns, 8 KB apart), 8-row K groups 1 KB
+                        //    apart, +2 KB per K=16 step. B: K-major tokens, +32 B per K=16 step.
+                        umma_bf16(d0, smem_desc(a_addr + kk * 2048, kWBlock, 1024),
+                                  smem_desc(b_addr + kk * 32, 16, 1024), idesc,
+                                  (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    umma_commit(&st.empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) umma_commit(&st.tfull[acc]);
+            }
+            if (!ok) {
+                st.abort = 1;
+                set_status(p.status, MOE_ERR_TIMEOUT);
+            }
+            if (*abort_flag && issued) {
+                umma_commit(&st.drain);
+                mbar_wait(&st.drain, 0, nullptr, kWaitLimitNs);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================= epilogue (warps 2..5) =================
+        const int q = warp & 3;  // TMEM lane quarter: rows 32q .. 32q+31 of the accumulator
+        uint32_t it = 0, xbuf = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+            const Tile t = decode<KIND>(st, E, tile);
+            const uint32_t acc = it & 1u;
+            const bool ok = mbar_wait(&st.tfull[acc], (it >> 1) & 1u, abort_flag, kWaitLimitNs);
+            if (!ok && lane == 0) {
+                st.abort = 1;
+                set_status(p.status, MOE_ERR_TIMEOUT);
+            }
+            // the four epilogue warps leave together, so none is left at a named barrier
+            if (epilogue_any(!ok || *abort_flag != 0)) break;
+            tc_fence_after();
+            int n_valid = t.row_end - t.row0;
+            if (n_valid > kTok) n_valid = kTok;
+            const int chunks = (n_valid + 31) >> 5;
+            const uint32_t tbase = tmem_base + acc * 256u + ((uint32_t)(q * 32) << 16);
+            if (KIND == kGateUp) {
+                // lanes 0..63: gate of h columns n0 .. n0+63; lanes 64..127: up of the same
+                const bool is_gate = q < 2;
+                const int hc = (q & 1) * 32 + lane;  // h column within the tile
+                const int col = t.n0 + hc;
+                const bool col_ok = col < p.N;
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 1
+                for (int c = 0; c < chunks; ++c, xbuf ^= 1u) {
+                    const int tok0 = t.row0 + c * 32;
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, v);
+                    tmem_ld_wait();
+                    float* xb = xch + xbuf * kXchFloats;
+                    if (!is_gate) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) xb[j * 64 + hc] = __uint_as_float(v[j]);
+                    }
+                    float my_s = 1.0f;
+                    if (p.row_scale && tok0 + lane < t.row_end)
+                        my_s = __ldg(p.topk_weights + __ldg(p.sorted_to_slot + tok0 + lane));
+                    epilogue_sync();
+                    if (is_gate) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float s = __shfl_sync(0xFFFFFFFFu, my_s, j);
+                            const float g = __uint_as_float(v[j]) * s;
+                            const float u = xb[j * 64 + hc] * s;
+                            if (tok0 + j < t.row_end && col_ok)
+                                out[(size_t)(tok0 + j) * p.N + col] =
+                                    __float2bfloat16_rn(silu(g) * u);
+                        }
+                    }
+                }
+            } else {
+                const int col = t.n0 + q * 32 + lane;
+                const bool col_ok = col < p.N;
+                float* out = static_cast<float*>(p.out);
+#pragma unroll 1
+                for (int c = 0; c < chunks; ++c) {
+                    const int tok0 = t.row0 + c * 32;
+                    float my_s = 1.0f;
+                    if (p.row_scale && tok0 + lane < t.row_end)
+                        my_s = __ldg(p.topk_weights + __ldg(p.sorted_to_slot + tok0 + lane));
+                    uint32_t y[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, y);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const float s = __shfl_sync(0xFFFFFFFFu, my_s, j);
+                        if (tok0 + j < t.row_end && col_ok)
+                            out[(size_t)(tok0 + j) * p.N + col] = __uint_as_float(y[j]) * s;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&st.tempty[acc]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+}
+
+template <int KIND>
+cudaError_t launch_swap_kind(const GroupedGemmArgs& a, cudaStream_t s) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(tc_grouped_gemm_swap<KIND>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    const int groups = a.offsets ? a.E : 1;
+    CUtensorMap tmW, tmX;
+    const cuuint64_t wn = (KIND == kGateUp) ? 2 * (cuuint64_t)a.N : (cuuint64_t)a.N;
+    const cuuint64_t w_dims[3] = {wn, (cuuint64_t)a.K, (cuuint64_t)groups};
+    const cuuint64_t w_str[2] = {wn * 2, wn * 2 * (cuuint64_t)a.K};
+    const cuuint32_t w_box[3] = {64, kTileK, 1};
+    const cuuint64_t x_dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.R};
+    const cuuint64_t x_str[1] = {(cuuint64_t)a.K * 2};
+    const cuuint32_t x_box[2] = {kTileK, kTok};
+    if (!encode_tensor_map_bf16(&tmW, a.b, 3, w_dims, w_str, w_box) ||
+        !encode_tensor_map_bf16(&tmX, a.a, 2, x_dims, x_str, x_box))
+        return cudaErrorInvalidValue;
+
+    SwapParams p;
+    p.offsets = a.offsets;
+    p.sorted_to_slot = a.sorted_to_slot;
+    p.topk_weights = a.topk_weights;
+    p.out = a.out;
+    p.status = a.status;
+    p.R = a.R;
+    p.K = a.K;
+    p.N = a.N;
+    p.E = groups;
+    p.n_tiles = (a.N + Shape<KIND>::kCols - 1) / Shape<KIND>::kCols;
+    p.k_blocks = (a.K + kTileK - 1) / kTileK;
+    p.row_scale = (KIND == kGateUp) ? (a.scale_rows ? 1 : 0) : (a.weight_rows ? 1 : 0);
+
+    const long long m_ub = (long long)(a.R + kTok - 1) / kTok + groups;
+    const long long tiles_ub = m_ub * p.n_tiles;
+    int grid = device_sm_count();
+    if (tiles_ub < grid) grid = (int)tiles_ub;
+    if (grid < 1) grid = 1;
+    tc_grouped_gemm_swap<KIND><<<grid, kThreads, kSmemBytes, s>>>(tmW, tmX, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s) {
+    return a.kind == kGateUp ? launch_swap_kind<kGateUp>(a, s) : launch_swap_kind<kDown>(a, s);
+}
+
+// gate_up runs on the 128-row kernel: there each epilogue thread holds gate and up of its h
+// columns, while this kernel's gate_up has to pass the up half between warps and leaves the
+// SiLU work to two of the four epilogue warps, which measured slower on every workload. down
+// runs here: it pads each expert to 16 rows instead of 128 and measured faster everywhere.
+cudaError_t launch_grouped_gemm_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
+    return a.kind == kGateUp ? launch_grouped_gemm_bf16_rows(a, s)
+                             : launch_grouped_gemm_bf16_swap(a, s);
+}
+
+}  // namespace rdg

@@ -210,7 +210,15 @@ struct GroupedGemmArgs {
     void* out;                // h [R, I] (layer dtype) or y_sorted [R, d] fp32
     int* status;
 };
+// bf16 tensor-core path; picks one of the two kernels below.
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmArgs& a, cudaStream_t s);
+// tokens as the MMA M side (128-row tiles; gemm_tc.cu)
+cudaError_t launch_grouped_gemm_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
+// weights as the MMA M side, tokens as N (tiles padded to 16 tokens; gemm_tc_swap.cu)
+cudaError_t launch_grouped_gemm_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s);
+// 2D/3D bf16 tensor map with 128-byte swizzle and zero fill outside the tensor.
+bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                            const cuuint64_t* strides, const cuuint32_t* box);
 cudaError_t launch_grouped_gemm_f32(const GroupedGemmArgs& a, cudaStream_t s);
 
 int device_sm_count();
