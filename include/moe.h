@@ -240,9 +240,10 @@ size_t moe_forward_workspace_size(int T, int d, int E, int k, int I, int Is, moe
 
 /*
  * Number of kernels moe_forward enqueues for these sizes (dispatch, experts and combine
- * kernels included; the status-word clear is a memset, not counted). 0 for T == 0.
+ * kernels included; the status-word clear is a memset, not counted). 0 for T == 0. Batches
+ * with T*k <= 1024 route and build the dispatch indices in one fused launch.
  */
-int moe_forward_kernel_count(int T, int Is);
+int moe_forward_kernel_count(int T, int k, int Is);
 
 /*
  * moe_read_device_status - synchronise `stream`, then return the status word the kernels of

@@ -8,6 +8,13 @@
 
 namespace rdg {
 
+namespace {
+thread_local bool t_pdl = false;
+}
+bool pdl_enabled() { return t_pdl; }
+PdlScope::PdlScope(bool on) : prev(t_pdl) { t_pdl = on; }
+PdlScope::~PdlScope() { t_pdl = prev; }
+
 int device_sm_count() {
     static int cache[64] = {0};
     int dev = 0;
@@ -270,9 +277,11 @@ size_t moe_forward_workspace_size(int T, int d, int E, int k, int I, int Is, moe
     return forward_layout(T, d, E, k, I, Is, dt).total;
 }
 
-int moe_forward_kernel_count(int T, int Is) {
-    if (T <= 0) return 0;
-    return 1 + dispatch_kernel_count(true) + 2 + (Is > 0 ? 2 : 0) + 1;
+int moe_forward_kernel_count(int T, int k, int Is) {
+    if (T <= 0 || k <= 0) return 0;
+    const bool small = (long long)T * k <= kSmallDispatchMaxSlots;
+    const int front = small ? 2 : 1 + dispatch_kernel_count(true);
+    return front + 2 + (Is > 0 ? 2 : 0) + 1;
 }
 
 moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, int d, int E,
@@ -322,14 +331,32 @@ moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, 
     const int R = T * k;
 
     if ((st = clear_status(workspace, s)) != MOE_OK) return st;
-    if ((st = launch_status(launch_route(logits, T, E, k, (int)score_fn,
-                                         (flags & MOE_RENORMALIZE) != 0, topk_ids, topk_weights,
-                                         s))) != MOE_OK)
-        return st;
-    if ((st = launch_status(launch_dispatch(topk_ids, x, (size_t)d * dtype_bytes(dt), T, E, k,
-                                            counts, offsets, s2p, p2s, xs, chunk, status, s))) !=
-        MOE_OK)
-        return st;
+    const bool renorm = (flags & MOE_RENORMALIZE) != 0;
+    // The first kernel follows the caller's work in plain stream order; every later kernel of
+    // the chain may start early and waits for its predecessor itself (griddep_wait).
+    if (R <= kSmallDispatchMaxSlots) {
+        // few tokens: route and the dispatch indices in one launch, then the row copy
+        if ((st = launch_status(launch_route_dispatch_small(logits, T, E, k, (int)score_fn,
+                                                            renorm, topk_ids, topk_weights,
+                                                            counts, offsets, s2p, p2s, s))) !=
+            MOE_OK)
+            return st;
+    } else {
+        if ((st = launch_status(launch_route(logits, T, E, k, (int)score_fn, renorm, topk_ids,
+                                             topk_weights, s))) != MOE_OK)
+            return st;
+    }
+    PdlScope pdl(true);
+    if (R <= kSmallDispatchMaxSlots) {
+        if ((st = launch_status(launch_dispatch_copy(x, (size_t)d * dtype_bytes(dt), T, k, p2s,
+                                                     xs, s))) != MOE_OK)
+            return st;
+    } else {
+        if ((st = launch_status(launch_dispatch(topk_ids, x, (size_t)d * dtype_bytes(dt), T, E,
+                                                k, counts, offsets, s2p, p2s, xs, chunk, status,
+                                                s))) != MOE_OK)
+            return st;
+    }
     if ((st = run_gemm(kGateUp, xs, w_gate_up, offsets, s2p, topk_weights, scale, dt, R, d, I, E,
                        h, status, s)) != MOE_OK)
         return st;

@@ -12,8 +12,8 @@
 //   3. rank   - one warp per chunk: walks its slots in order, 32 at a time; a slot's position
 //               is the chunk base for its expert plus the number of earlier slots of the chunk
 //               routed to the same expert.
-//   4. copy   - one warp per token: reads the token's row once (16-byte vectors) and writes it
-//               to the k sorted positions.
+//   4. copy   - one thread per 16-byte vector of a token's row: reads it once and writes it to
+//               the token's k sorted positions.
 #include "moe_internal.cuh"
 
 namespace rdg {
@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(256) dispatch_hist_kernel(const int32_t* __res
                                                             int32_t* __restrict__ chunk_counts,
                                                             int* status) {
     __shared__ int cnt[kWarpsPerBlock][kMaxE];
+    griddep_wait();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int c = blockIdx.x * kWarpsPerBlock + w;
     if (c >= nchunks) return;
@@ -62,6 +63,7 @@ __global__ void __launch_bounds__(1024) dispatch_scan_kernel(int32_t* __restrict
     __shared__ int part[1024];
     __shared__ int tot[kMaxE];
     __shared__ int off[kMaxE + 1];
+    griddep_wait();
     const int tid = threadIdx.x;
     const int G = blockDim.x / E;
     const int L = (nchunks + G - 1) / G;
@@ -124,6 +126,7 @@ __global__ void __launch_bounds__(256) dispatch_rank_kernel(const int32_t* __res
                                                             int32_t* __restrict__ sorted_to_slot,
                                                             int32_t* __restrict__ slot_to_sorted) {
     __shared__ int run[kWarpsPerBlock][kMaxE];
+    griddep_wait();
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int c = blockIdx.x * kWarpsPerBlock + w;
     if (c >= nchunks) return;
@@ -151,25 +154,24 @@ __global__ void __launch_bounds__(256) dispatch_rank_kernel(const int32_t* __res
     }
 }
 
-// One warp per token (grid-stride). Rows are moved as 16-byte vectors.
+// Grid: x over 16-byte vectors of the row (256 per block), y over tokens (grid-stride). Each
+// thread reads its vector of x once and writes it to the token's k sorted rows.
 __global__ void __launch_bounds__(256) dispatch_copy_kernel(const uint4* __restrict__ x,
                                                             int T, int k, int vec_per_row,
                                                             const int32_t* __restrict__ slot_to_sorted,
                                                             uint4* __restrict__ x_sorted) {
-    const int lane = threadIdx.x & 31;
-    const int warps_total = gridDim.x * (blockDim.x >> 5);
-    for (int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps_total) {
-        const int my_pos = (lane < k) ? __ldg(slot_to_sorted + (size_t)t * k + lane) : -1;
-        const uint4* src = x + (size_t)t * vec_per_row;
-        // uniform trip count: every lane takes part in each shuffle
-        for (int base = 0; base < vec_per_row; base += 32) {
-            const int v = base + lane;
-            const bool in = v < vec_per_row;
-            const uint4 val = in ? __ldg(src + v) : make_uint4(0u, 0u, 0u, 0u);
-            for (int j = 0; j < k; ++j) {
-                const int p = __shfl_sync(0xFFFFFFFFu, my_pos, j);
-                if (in && p >= 0) x_sorted[(size_t)p * vec_per_row + v] = val;
-            }
+    __shared__ int pos_s[kMaxK];
+    griddep_wait();
+    const int v = blockIdx.x * blockDim.x + threadIdx.x;
+    for (int t = blockIdx.y; t < T; t += gridDim.y) {
+        __syncthreads();
+        if (threadIdx.x < k) pos_s[threadIdx.x] = __ldg(slot_to_sorted + (size_t)t * k + threadIdx.x);
+        __syncthreads();
+        if (v >= vec_per_row) continue;
+        const uint4 val = __ldg(x + (size_t)t * vec_per_row + v);
+        for (int j = 0; j < k; ++j) {
+            const int p = pos_s[j];
+            if (p >= 0) x_sorted[(size_t)p * vec_per_row + v] = val;
         }
     }
 }
@@ -191,22 +193,31 @@ cudaError_t launch_dispatch(const int32_t* ids, const void* x, size_t row_bytes,
     const int nchunks = (R + kDispatchChunk - 1) / kDispatchChunk;
     const int blocks = (nchunks + kWarpsPerBlock - 1) / kWarpsPerBlock;
     // With no slots only the scan runs: it writes zero counts and offsets.
-    if (blocks > 0)
-        dispatch_hist_kernel<<<blocks, 32 * kWarpsPerBlock, 0, s>>>(ids, R, E, nchunks,
-                                                                    chunk_scratch, status);
-    dispatch_scan_kernel<<<1, 1024, 0, s>>>(chunk_scratch, nchunks, E, counts, offsets);
-    if (blocks > 0)
-        dispatch_rank_kernel<<<blocks, 32 * kWarpsPerBlock, 0, s>>>(
-            ids, R, E, nchunks, chunk_scratch, sorted_to_slot, slot_to_sorted);
-    if (T > 0 && x != nullptr && x_sorted != nullptr) {
-        const int vec = (int)(row_bytes / 16);
-        const int max_blocks = device_sm_count() * 8;
-        int cblocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-        if (cblocks > max_blocks) cblocks = max_blocks;
-        dispatch_copy_kernel<<<cblocks, 32 * kWarpsPerBlock, 0, s>>>(
-            static_cast<const uint4*>(x), T, k, vec, slot_to_sorted, static_cast<uint4*>(x_sorted));
-    }
+    cudaError_t e = cudaSuccess;
+    if (blocks > 0 &&
+        (e = launch_kernel(dispatch_hist_kernel, dim3(blocks), dim3(32 * kWarpsPerBlock), 0, s,
+                           ids, R, E, nchunks, chunk_scratch, status)) != cudaSuccess)
+        return e;
+    if ((e = launch_kernel(dispatch_scan_kernel, dim3(1), dim3(1024), 0, s, chunk_scratch,
+                           nchunks, E, counts, offsets)) != cudaSuccess)
+        return e;
+    if (blocks > 0 &&
+        (e = launch_kernel(dispatch_rank_kernel, dim3(blocks), dim3(32 * kWarpsPerBlock), 0, s,
+                           ids, R, E, nchunks, (const int32_t*)chunk_scratch, sorted_to_slot,
+                           slot_to_sorted)) != cudaSuccess)
+        return e;
+    if (T > 0 && x != nullptr && x_sorted != nullptr)
+        return launch_dispatch_copy(x, row_bytes, T, k, slot_to_sorted, x_sorted, s);
     return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_copy(const void* x, size_t row_bytes, int T, int k,
+                                 const int32_t* slot_to_sorted, void* x_sorted, cudaStream_t s) {
+    const int vec = (int)(row_bytes / 16);
+    const dim3 grid((vec + 255) / 256, T < 65535 ? T : 65535);
+    return launch_kernel(dispatch_copy_kernel, grid, dim3(256), 0, s,
+                         static_cast<const uint4*>(x), T, k, vec, slot_to_sorted,
+                         static_cast<uint4*>(x_sorted));
 }
 
 }  // namespace rdg

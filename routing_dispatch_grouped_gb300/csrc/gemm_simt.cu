@@ -17,6 +17,7 @@ __global__ void __launch_bounds__(256) simt_grouped_gemm(GroupedGemmArgs p) {
     __shared__ float As[BM][BK + 1];
     __shared__ float Bs[2][BK][BN + 1];
     __shared__ int s_e, s_m0, s_end;
+    griddep_wait();
     const int tid = threadIdx.x;
     if (tid == 0) {
         int e_found = -1, m0 = 0, end = 0;
@@ -104,11 +105,8 @@ __global__ void __launch_bounds__(256) simt_grouped_gemm(GroupedGemmArgs p) {
 cudaError_t launch_grouped_gemm_f32(const GroupedGemmArgs& a, cudaStream_t s) {
     const int groups = a.offsets ? a.E : 1;
     const dim3 grid((a.N + BN - 1) / BN, (a.R + BM - 1) / BM + groups);
-    if (a.kind == kGateUp)
-        simt_grouped_gemm<true><<<grid, 256, 0, s>>>(a);
-    else
-        simt_grouped_gemm<false><<<grid, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_kernel(a.kind == kGateUp ? simt_grouped_gemm<true> : simt_grouped_gemm<false>,
+                         grid, dim3(256), 0, s, a);
 }
 
 }  // namespace rdg

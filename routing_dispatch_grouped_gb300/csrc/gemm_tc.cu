@@ -129,6 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
     }
     if (warp == 1) tmem_alloc(&st.tmem_base, kTmemCols);
+    // everything above is independent of the previous kernel; its outputs are read from here on
+    griddep_wait();
     if (warp == 2) {
         for (int e = lane; e <= E; e += 32)
             st.off[e] = p.offsets ? __ldg(p.offsets + e) : (e == 0 ? 0 : p.R);
@@ -431,8 +433,7 @@ cudaError_t launch_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     int grid = device_sm_count();
     if (tiles_ub < grid) grid = (int)tiles_ub;
     if (grid < 1) grid = 1;
-    tc_grouped_gemm<KIND><<<grid, kThreads, kSmemBytes, s>>>(tmA, tmB, p);
-    return cudaGetLastError();
+    return launch_kernel(tc_grouped_gemm<KIND>, dim3(grid), dim3(kThreads), kSmemBytes, s, tmA, tmB, p);
 }
 
 }  // namespace

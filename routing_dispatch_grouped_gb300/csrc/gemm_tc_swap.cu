@@ -31,17 +31,28 @@
 namespace rdg {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 512;
 constexpr int kWM = 128;                 // MMA M: weight rows of the accumulator
-constexpr int kTok = 256;                // tokens per tile (MMA N at most)
 constexpr int kWBlock = 64 * kTileK * 2; // one 64-column x 64-k MN-major block: 8 KB
-constexpr int kABytes = 2 * kWBlock;     // 16 KB
-constexpr int kBBytes = kTok * kTileK * 2;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;  // 48 KB
+constexpr int kABytes = 2 * kWBlock;     // 16 KB of weights per stage
 constexpr int kXchFloats = 32 * 64;      // one exchange buffer: 32 tokens x 64 columns fp32
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Token-tile size and pipeline depth. Large batches: 256-token tiles, 4 stages of 48 KB. Small
+// batches (decode): 32-token tiles, 10 stages of 20 KB, so more weight bytes are in flight and no
+// 256-row token box is fetched for a handful of tokens.
+template <int TOK, int STAGES>
+struct Cfg {
+    static constexpr int kTok = TOK;
+    static constexpr int kStages = STAGES;
+    static constexpr int kBBytes = TOK * kTileK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr uint32_t kAccCols = TOK;                 // one accumulator: TOK fp32 columns
+    static constexpr uint32_t kTmemCols = 2 * TOK < 32 ? 32 : 2 * TOK;  // two buffers, pow2
+    static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
+};
+using CfgLarge = Cfg<256, 4>;
+using CfgSmall = Cfg<32, 10>;
 
 // Output columns covered by one tile: 64 h columns (gate_up) or 128 y columns (down).
 template <int KIND>
@@ -61,9 +72,10 @@ struct SwapParams {
     int row_scale;
 };
 
+template <int STAGES>
 struct __align__(8) SmemTail {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -75,15 +87,18 @@ struct __align__(8) SmemTail {
     int mt[kMaxE];
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + 2 * kXchFloats * 4 +
-                              sizeof(SmemTail);
+template <class C>
+constexpr size_t smem_bytes() {
+    return 1024 + (size_t)C::kStages * C::kStageBytes + 2 * kXchFloats * 4 +
+           sizeof(SmemTail<C::kStages>);
+}
 
 struct Tile {
     int e, row0, row_end, n0;
 };
 
-template <int KIND>
-__device__ __forceinline__ Tile decode(const SmemTail& st, int E, int tile) {
+template <int KIND, int TOK, class ST>
+__device__ __forceinline__ Tile decode(const ST& st, int E, int tile) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -97,7 +112,7 @@ __device__ __forceinline__ Tile decode(const SmemTail& st, int E, int tile) {
     const int nb = local / m, mb = local - nb * m;
     Tile t;
     t.e = lo;
-    t.row0 = st.off[lo] + mb * kTok;
+    t.row0 = st.off[lo] + mb * TOK;
     t.row_end = st.off[lo + 1];
     t.n0 = nb * Shape<KIND>::kCols;
     return t;
@@ -131,16 +146,21 @@ __device__ __forceinline__ bool epilogue_any(bool v) {
     return r != 0;
 }
 
-template <int KIND>
+template <int KIND, class C>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm_swap(const __grid_constant__ CUtensorMap tmW,
                          const __grid_constant__ CUtensorMap tmX, const SwapParams p) {
+    constexpr int kStages = C::kStages;
+    constexpr int kStageBytes = C::kStageBytes;
+    constexpr int kTok = C::kTok;
+    constexpr uint32_t kTmemCols = C::kTmemCols;
+    constexpr uint32_t kAcc = C::kAccCols;
+    using ST = SmemTail<kStages>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     float* xch = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);
-    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + (size_t)kStages * kStageBytes +
-                                                2 * kXchFloats * 4);
+    ST& st = *reinterpret_cast<ST*>(smem + (size_t)kStages * kStageBytes + 2 * kXchFloats * 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
 
@@ -159,6 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
     }
     if (warp == 1) tmem_alloc(&st.tmem_base, kTmemCols);
+    // everything above is independent of the previous kernel; its outputs are read from here on
+    griddep_wait();
     if (warp == 2) {
         for (int e = lane; e <= E; e += 32)
             st.off[e] = p.offsets ? __ldg(p.offsets + e) : (e == 0 ? 0 : p.R);
@@ -199,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const Tile t = decode<KIND>(st, E, tile);
+                const Tile t = decode<KIND, kTok>(st, E, tile);
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(&st.empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
                         ok = false;
@@ -237,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0, it = 0;
             bool ok = true, issued = false;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-                const Tile t = decode<KIND>(st, E, tile);
+                const Tile t = decode<KIND, kTok>(st, E, tile);
                 int n_tok = t.row_end - t.row0;
                 if (n_tok > kTok) n_tok = kTok;
                 n_tok = (n_tok + 15) & ~15;
@@ -248,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d0 = tmem_base + acc * 256u;
+                const uint32_t d0 = tmem_base + acc * kAcc;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(&st.full[stage], phase, abort_flag, kWaitLimitNs)) {
                         ok = false;
@@ -289,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;  // TMEM lane quarter: rows 32q .. 32q+31 of the accumulator
         uint32_t it = 0, xbuf = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-            const Tile t = decode<KIND>(st, E, tile);
+            const Tile t = decode<KIND, kTok>(st, E, tile);
             const uint32_t acc = it & 1u;
             const bool ok = mbar_wait(&st.tfull[acc], (it >> 1) & 1u, abort_flag, kWaitLimitNs);
             if (!ok && lane == 0) {
@@ -302,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int n_valid = t.row_end - t.row0;
             if (n_valid > kTok) n_valid = kTok;
             const int chunks = (n_valid + 31) >> 5;
-            const uint32_t tbase = tmem_base + acc * 256u + ((uint32_t)(q * 32) << 16);
+            const uint32_t tbase = tmem_base + acc * kAcc + ((uint32_t)(q * 32) << 16);
             if (KIND == kGateUp) {
                 // lanes 0..63: gate of h columns n0 .. n0+63; lanes 64..127: up of the same
                 const bool is_gate = q < 2;
@@ -370,12 +392,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-template <int KIND>
+template <int KIND, class C>
 cudaError_t launch_swap_kind(const GroupedGemmArgs& a, cudaStream_t s) {
+    constexpr int kTok = C::kTok;
+    constexpr size_t kSmemBytes = smem_bytes<C>();
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_grouped_gemm_swap<KIND>,
+        attr_err = cudaFuncSetAttribute(tc_grouped_gemm_swap<KIND, C>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kSmemBytes);
     });
@@ -413,23 +437,28 @@ cudaError_t launch_swap_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     int grid = device_sm_count();
     if (tiles_ub < grid) grid = (int)tiles_ub;
     if (grid < 1) grid = 1;
-    tc_grouped_gemm_swap<KIND><<<grid, kThreads, kSmemBytes, s>>>(tmW, tmX, p);
-    return cudaGetLastError();
+    return launch_kernel(tc_grouped_gemm_swap<KIND, C>, dim3(grid), dim3(kThreads), kSmemBytes, s, tmW, tmX, p);
 }
 
 }  // namespace
 
 cudaError_t launch_grouped_gemm_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s) {
-    return a.kind == kGateUp ? launch_swap_kind<kGateUp>(a, s) : launch_swap_kind<kDown>(a, s);
+    if (a.R <= kSmallBatchRows)
+        return a.kind == kGateUp ? launch_swap_kind<kGateUp, CfgSmall>(a, s)
+                                 : launch_swap_kind<kDown, CfgSmall>(a, s);
+    return a.kind == kGateUp ? launch_swap_kind<kGateUp, CfgLarge>(a, s)
+                             : launch_swap_kind<kDown, CfgLarge>(a, s);
 }
 
-// gate_up runs on the 128-row kernel: there each epilogue thread holds gate and up of its h
-// columns, while this kernel's gate_up has to pass the up half between warps and leaves the
-// SiLU work to two of the four epilogue warps, which measured slower on every workload. down
-// runs here: it pads each expert to 16 rows instead of 128 and measured faster everywhere.
+// Large batches: gate_up runs on the 128-row kernel, where each epilogue thread holds gate and
+// up of its h columns (this kernel's gate_up passes the up half between warps and leaves the
+// SiLU work to two of the four epilogue warps, which measured slower on every prefill
+// workload); down runs here, padding each expert to 16 rows instead of 128 (measured faster
+// everywhere). Small batches (at most kSmallBatchRows routed rows): both run here with 32-token
+// tiles, which stream weights without fetching 128- or 256-row token tiles.
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
-    return a.kind == kGateUp ? launch_grouped_gemm_bf16_rows(a, s)
-                             : launch_grouped_gemm_bf16_swap(a, s);
+    if (a.kind == kGateUp && a.R > kSmallBatchRows) return launch_grouped_gemm_bf16_rows(a, s);
+    return launch_grouped_gemm_bf16_swap(a, s);
 }
 
 }  // namespace rdg

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "moe.h"
 
 namespace rdg {
@@ -176,7 +178,42 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
 }
 
 // ---------------------------------------------------------------------------------------------
-// launchers (one per kernel family); each returns cudaGetLastError() of its launch
+// programmatic dependent launch
+// ---------------------------------------------------------------------------------------------
+// Every kernel calls griddep_wait() before it reads data written by the kernel launched before
+// it on the stream. Launched normally this returns at once; launched with programmatic stream
+// serialization (inside moe_forward's chain) it lets the kernel start, run its prologue
+// (barrier set-up, TMEM allocation, descriptor prefetch) while the previous kernel drains, and
+// only then wait for that kernel's results.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launches issued while a PdlScope(true) is alive on this host thread may overlap the previous
+// kernel on the stream as described above.
+bool pdl_enabled();
+struct PdlScope {
+    explicit PdlScope(bool on);
+    ~PdlScope();
+    bool prev;
+};
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// ---------------------------------------------------------------------------------------------
+// launchers (one per kernel family); each returns the error of its launch
 // ---------------------------------------------------------------------------------------------
 cudaError_t launch_route(const float* logits, int T, int E, int k, int score_fn, bool renorm,
                          int32_t* ids, float* weights, cudaStream_t s);
@@ -190,6 +227,18 @@ cudaError_t launch_dispatch(const int32_t* ids, const void* x, size_t row_bytes,
                             int* status, cudaStream_t s);
 // Number of kernels launch_dispatch enqueues.
 int dispatch_kernel_count(bool copy_rows);
+
+// Row copy of dispatch alone: x_sorted[slot_to_sorted[t*k+j]] = x[t] (grid-wide).
+cudaError_t launch_dispatch_copy(const void* x, size_t row_bytes, int T, int k,
+                                 const int32_t* slot_to_sorted, void* x_sorted, cudaStream_t s);
+
+// Route and dispatch indices in one single-block kernel, for T*k <= kSmallDispatchMaxSlots.
+constexpr int kSmallDispatchMaxSlots = 1024;
+cudaError_t launch_route_dispatch_small(const float* logits, int T, int E, int k, int score_fn,
+                                        bool renorm, int32_t* ids, float* weights,
+                                        int32_t* counts, int32_t* offsets,
+                                        int32_t* sorted_to_slot, int32_t* slot_to_sorted,
+                                        cudaStream_t s);
 
 cudaError_t launch_combine(const float* y_sorted, const int32_t* slot_to_sorted,
                            const float* weights, const float* y_shared, int T, int d, int k,
@@ -210,6 +259,8 @@ struct GroupedGemmArgs {
     void* out;                // h [R, I] (layer dtype) or y_sorted [R, d] fp32
     int* status;
 };
+// Batches with at most this many routed rows use the small-batch (decode) GEMM configuration.
+constexpr int kSmallBatchRows = 512;
 // bf16 tensor-core path; picks one of the two kernels below.
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmArgs& a, cudaStream_t s);
 // tokens as the MMA M side (128-row tiles; gemm_tc.cu)

@@ -38,7 +38,7 @@ SIGNATURES = {
     "moe_forward": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P, _P,
                          _P, _P, _S, _P]),
     "moe_forward_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
-    "moe_forward_kernel_count": (_I, [_I, _I]),
+    "moe_forward_kernel_count": (_I, [_I, _I, _I]),
     "moe_read_device_status": (_I, [_P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -215,8 +215,8 @@ def moe_forward_workspace_size(T, d, E, k, I, Is, dtype) -> int:
                                             else F32)
 
 
-def moe_forward_kernel_count(T, Is) -> int:
-    return lib().moe_forward_kernel_count(T, Is)
+def moe_forward_kernel_count(T, k, Is) -> int:
+    return lib().moe_forward_kernel_count(T, k, Is)
 
 
 def moe_forward(x, logits, w_gate_up, w_down, k, score_fn=SOFTMAX, flags=RENORMALIZE,

@@ -136,8 +136,10 @@ def test_workspace_size_matches_binding_layout(L):
 
 
 def test_kernel_count_and_strings(L):
-    assert L.moe_forward_kernel_count(0, 0) == 0
-    assert L.moe_forward_kernel_count(10, 0) == 8
-    assert L.moe_forward_kernel_count(10, 128) == 10
+    assert L.moe_forward_kernel_count(0, 2, 0) == 0
+    assert L.moe_forward_kernel_count(10, 2, 0) == 5        # fused small-batch front end
+    assert L.moe_forward_kernel_count(10, 2, 128) == 7
+    assert L.moe_forward_kernel_count(4096, 2, 0) == 8
+    assert L.moe_forward_kernel_count(16384, 1, 8192) == 10
     for code in range(7):
         assert L.moe_status_string(code).decode().startswith(moe.STATUS[code])

@@ -296,8 +296,11 @@ def _oracle_forward(cfg, inp):
                      None if sh is None else f64(inp["w_shared_down"]))
 
 
+# T*k <= 1024 runs the fused small-batch router/dispatch; decode at T=128 (1024 slots) and
+# T=129 (1032 slots) sit on either side of that boundary.
 FORWARD_CASES = [("tiny_fp32", None), ("mixtral_8x7b", 600), ("gpt_oss_120b", 700),
-                 ("decode", 1), ("decode", 8), ("decode", 64), ("llama4_scout", 700)]
+                 ("decode", 1), ("decode", 8), ("decode", 64), ("decode", 128), ("decode", 129),
+                 ("llama4_scout", 700)]
 
 
 @pytest.mark.parametrize("name,T", FORWARD_CASES)
