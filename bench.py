@@ -261,6 +261,15 @@ def run_ours(args, rank, world):
     moe.lib()
     inp = synth.make_inputs(cfg, dev)
     T, d, E, k, I, Is = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.I_shared
+    # expert weights are repacked once, as at model load (moe_pack_weights); bf16 layers only
+    packed = cfg.dtype == torch.bfloat16
+    wts = {}
+    for n_ in ("w_gate_up", "w_down", "w_shared_gate_up", "w_shared_down"):
+        w_ = inp[n_]
+        if w_ is not None and packed:
+            w_ = moe.pack_weights(w_, moe.W_GATE_UP if "gate_up" in n_ else moe.W_DOWN)
+        wts[n_] = w_
+    torch.cuda.synchronize()
     R = T * k
     flags = (moe.RENORMALIZE if cfg.renormalize else 0) | (moe.SCALE_INPUT if cfg.scale_input
                                                            else 0)
@@ -291,18 +300,19 @@ def run_ours(args, rank, world):
         mark(1)
         moe.moe_dispatch(ids, E, x=inp["x"], workspace=dws, out=disp_out, stream=stream)
         mark(2)
-        moe.moe_gate_up(v["x_sorted"], v["offsets"], inp["w_gate_up"], v["sorted_to_slot"], w,
+        moe.moe_gate_up(v["x_sorted"], v["offsets"], wts["w_gate_up"], v["sorted_to_slot"], w,
                         cfg.scale_input, h=v["h"], workspace=gws, stream=stream)
         mark(3)
-        moe.moe_down(v["h"], v["offsets"], inp["w_down"], y_sorted=v["y_sorted"],
+        moe.moe_down(v["h"], v["offsets"], wts["w_down"], y_sorted=v["y_sorted"],
                      workspace=gws, stream=stream)
         mark(4)
         i = 5
         if Is:
-            moe.moe_gate_up(inp["x"], None, inp["w_shared_gate_up"].unsqueeze(0),
+            sgu, sdn = wts["w_shared_gate_up"], wts["w_shared_down"]
+            moe.moe_gate_up(inp["x"], None, sgu if packed else sgu.unsqueeze(0),
                             h=v["h_shared"], workspace=gws, stream=stream)
             mark(i)
-            moe.moe_down(v["h_shared"], None, inp["w_shared_down"].unsqueeze(0),
+            moe.moe_down(v["h_shared"], None, sdn if packed else sdn.unsqueeze(0),
                          y_sorted=v["y_shared"], workspace=gws, stream=stream)
             mark(i + 1)
             i += 2
@@ -342,8 +352,8 @@ def run_ours(args, rank, world):
 
     # the product call: moe_forward issued from the host every step ...
     def fwd(st_):
-        moe.moe_forward(inp["x"], inp["logits"], inp["w_gate_up"], inp["w_down"], k,
-                        cfg.score_fn, flags, inp["w_shared_gate_up"], inp["w_shared_down"],
+        moe.moe_forward(inp["x"], inp["logits"], wts["w_gate_up"], wts["w_down"], k,
+                        cfg.score_fn, flags, wts["w_shared_gate_up"], wts["w_shared_down"],
                         out=out, topk_ids=ids, topk_weights=w, workspace=ws, stream=st_)
 
     for _ in range(3):
@@ -394,8 +404,8 @@ def run_ours(args, rank, world):
     def e2e_step():
         x_d.copy_(x_h, non_blocking=True)
         lg_d.copy_(lg_h, non_blocking=True)
-        moe.moe_forward(x_d, lg_d, inp["w_gate_up"], inp["w_down"], k, cfg.score_fn, flags,
-                        inp["w_shared_gate_up"], inp["w_shared_down"], out=out, topk_ids=ids,
+        moe.moe_forward(x_d, lg_d, wts["w_gate_up"], wts["w_down"], k, cfg.score_fn, flags,
+                        wts["w_shared_gate_up"], wts["w_shared_down"], out=out, topk_ids=ids,
                         topk_weights=w, workspace=ws, stream=stream)
         out_h.copy_(out, non_blocking=True)
 
@@ -445,6 +455,8 @@ def run_ours(args, rank, world):
         "data": "synthetic (seeded counter-based generator; shapes of the workload)",
         "config": {"workload": cfg.name, "T": T, "d": d, "E": E, "k": k, "I": I,
                    "I_shared": Is, "seed": cfg.seed,
+                   "weights": "repacked once at load (moe_pack_weights)" if packed
+                   else "layout of the pages",
                    "l2": "no flush: weights alone exceed the 129 MB L2"},
         "roofline": roof,
         "expert_gemm_tflops": round(expert_tflops, 1),

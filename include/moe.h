@@ -101,10 +101,14 @@ typedef enum moe_score_fn { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_s
 
 /* flags (bitwise or) */
 enum {
-    MOE_RENORMALIZE = 1u,         /* divide the k selected weights by their sum */
-    MOE_SCALE_INPUT = 2u,         /* router weight multiplies the expert input; combine weight 1 */
-    MOE_FUSE_COMBINE_WEIGHT = 4u  /* down-projection epilogue multiplies rows by their weight */
+    MOE_RENORMALIZE = 1u,          /* divide the k selected weights by their sum */
+    MOE_SCALE_INPUT = 2u,          /* router weight multiplies the expert input; combine weight 1 */
+    MOE_FUSE_COMBINE_WEIGHT = 4u,  /* down-projection epilogue multiplies rows by their weight */
+    MOE_WEIGHTS_PACKED = 8u        /* expert weights were repacked by moe_pack_weights */
 };
+
+/* Which expert weight a packed buffer holds. */
+typedef enum moe_weight_kind { MOE_W_GATE_UP = 0, MOE_W_DOWN = 1 } moe_weight_kind;
 
 /*
  * moe_route - router top-k gating ([EP-add]: top_k_index, top_k_weights; [EP-intro]).
@@ -180,8 +184,9 @@ moe_status moe_dispatch_noalloc(const int32_t* topk_ids, const void* x, moe_dtyp
  *   offsets    device int32 [E + 1] with offsets[0] == 0 and offsets[E] <= R, or NULL meaning one
  *              expert (E must be 1) owning all R rows. Read on the device: no host sync.
  *   sorted_to_slot, topk_weights: read only with MOE_SCALE_INPUT, else may be NULL.
- *   w_gate_up  device dtype [E, d, 2I].   h: device dtype [R, I], written for owned rows only.
- *   flags      MOE_SCALE_INPUT or 0.
+ *   w_gate_up  device dtype [E, d, 2I], or packed by moe_pack_weights with MOE_WEIGHTS_PACKED.
+ *   h          device dtype [R, I], written for owned rows only.
+ *   flags      MOE_SCALE_INPUT, MOE_WEIGHTS_PACKED or 0.
  *   workspace  at least moe_experts_workspace_size() bytes (status word), 256-byte aligned.
  */
 moe_status moe_gate_up(const void* x_rows, const int32_t* offsets, const int32_t* sorted_to_slot,
@@ -192,7 +197,8 @@ moe_status moe_gate_up(const void* x_rows, const int32_t* offsets, const int32_t
 /*
  * moe_down - grouped down projection: y_sorted[p] = h[p] . w_down[e] (fp32), for p owned by e;
  *   with MOE_FUSE_COMBINE_WEIGHT the row is multiplied by topk_weights[sorted_to_slot[p]].
- *   h device dtype [R, I]; w_down device dtype [E, I, d]; y_sorted device float [R, d].
+ *   h device dtype [R, I]; w_down device dtype [E, I, d] (or packed, with MOE_WEIGHTS_PACKED);
+ *   y_sorted device float [R, d].
  *   offsets, sorted_to_slot, topk_weights, workspace: as for moe_gate_up.
  */
 moe_status moe_down(const void* h, const int32_t* offsets, const int32_t* sorted_to_slot,
@@ -206,6 +212,27 @@ moe_status moe_experts(const void* x_sorted, const int32_t* offsets, const int32
                        const void* w_gate_up, const void* w_down, unsigned flags, void* h,
                        float* y_sorted, void* workspace, size_t ws_bytes, moe_stream_t stream);
 size_t moe_experts_workspace_size(void);
+
+/*
+ * moe_pack_weights - one-time repacking of expert weights for faster streaming (bf16 only).
+ *   The pages' layout ([TP-packed]: gate_up [E, d, 2I] gate first, down [E, I, d]) makes each
+ *   64 x 64 weight tile the GEMMs read a set of 64 rows of 128 bytes a full weight row apart.
+ *   The packed layout stores every such tile as one contiguous 8 KB block, so the kernels read
+ *   expert weights sequentially. It is a storage layout of this library, not of the pages.
+ *   kind MOE_W_GATE_UP: w = [E, K=d, 2I] in the pages' layout, N = I; the gate and up halves are
+ *   blocked separately. kind MOE_W_DOWN: w = [E, K=I, N=d].
+ *   Layout: block (e, nb, kb) = rows [64 kb, 64 kb + 64) of the 64 columns of block nb, at rows
+ *   ((e * NB + nb) * Kpad + 64 kb) of a [E * NB * Kpad, 64] bf16 matrix; Kpad = K rounded up to
+ *   64; NB = ceil(N / 64) for down, 2 * ceil(I / 64) for gate_up (gate blocks first). Padding
+ *   is zero. packed: device buffer of moe_packed_weights_size() bytes, 16-byte aligned.
+ *   Pass MOE_WEIGHTS_PACKED to moe_gate_up / moe_down / moe_experts / moe_forward to use it
+ *   (for moe_forward the shared expert's weights, if any, must be packed too, with E = 1).
+ *   Results are the same as with the unpacked weights. Returns MOE_ERR_UNSUPPORTED for
+ *   MOE_F32.
+ */
+size_t moe_packed_weights_size(moe_weight_kind kind, int E, int K, int N, moe_dtype dt);
+moe_status moe_pack_weights(moe_weight_kind kind, const void* w, void* packed, moe_dtype dt,
+                            int E, int K, int N, moe_stream_t stream);
 
 /*
  * moe_combine - weighted return to token order ([EP-dispatch]: results combined with the
@@ -226,8 +253,8 @@ moe_status moe_combine(const float* y_sorted, const int32_t* slot_to_sorted,
  *   w_shared_gate_up [d, 2*Is] and w_shared_down [Is, d] (dtype dt): an always-on SwiGLU expert
  *   run on the unscaled x and added to every token before the one output rounding; both NULL
  *   (and Is == 0) for none.
- *   flags: MOE_RENORMALIZE | MOE_SCALE_INPUT | MOE_FUSE_COMBINE_WEIGHT (the last two exclude
- *   each other).
+ *   flags: MOE_RENORMALIZE | MOE_SCALE_INPUT | MOE_FUSE_COMBINE_WEIGHT (these two exclude
+ *   each other) | MOE_WEIGHTS_PACKED (all expert weights, shared ones included, packed).
  *   workspace: at least moe_forward_workspace_size(...) bytes, 256-byte aligned. Holds counts,
  *   offsets, both permutations, x_sorted, h, y_sorted and the shared expert's h and y.
  */

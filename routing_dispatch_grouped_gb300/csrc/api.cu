@@ -86,13 +86,15 @@ moe_status clear_status(void* workspace, cudaStream_t s) {
     return launch_status(cudaMemsetAsync(workspace, 0, sizeof(int), s));
 }
 
-moe_status run_gemm(GemmKind kind, const void* a, const void* b, const int32_t* offsets,
-                    const int32_t* s2p, const float* w, bool scale, moe_dtype dt, int R, int K,
-                    int N, int E, void* out, int* status, cudaStream_t s) {
+moe_status run_gemm(GemmKind kind, const void* a, const void* b, bool packed,
+                    const int32_t* offsets, const int32_t* s2p, const float* w, bool scale,
+                    moe_dtype dt, int R, int K, int N, int E, void* out, int* status,
+                    cudaStream_t s) {
     GroupedGemmArgs g;
     g.kind = kind;
     g.a = a;
     g.b = b;
+    g.packed = packed;
     g.offsets = offsets;
     g.sorted_to_slot = s2p;
     g.topk_weights = w;
@@ -195,8 +197,10 @@ moe_status moe_gate_up(const void* x_rows, const int32_t* offsets, const int32_t
                        const float* topk_weights, moe_dtype dt, int R, int d, int E, int I,
                        const void* w_gate_up, unsigned flags, void* h, void* workspace,
                        size_t ws_bytes, moe_stream_t stream) {
-    if (flags & ~(unsigned)MOE_SCALE_INPUT) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)(MOE_SCALE_INPUT | MOE_WEIGHTS_PACKED)) return MOE_ERR_INVALID_ARG;
     const bool scale = (flags & MOE_SCALE_INPUT) != 0;
+    const bool packed = (flags & MOE_WEIGHTS_PACKED) != 0;
+    if (packed && dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     moe_status st = check_experts_args(offsets, sorted_to_slot, topk_weights, scale, dt, R, d, E,
                                        I, workspace, ws_bytes);
     if (st != MOE_OK) return st;
@@ -206,16 +210,19 @@ moe_status moe_gate_up(const void* x_rows, const int32_t* offsets, const int32_t
     cudaStream_t s = (cudaStream_t)stream;
     st = clear_status(workspace, s);
     if (st != MOE_OK) return st;
-    return run_gemm(kGateUp, x_rows, w_gate_up, offsets, sorted_to_slot, topk_weights, scale, dt,
-                    R, d, I, E, h, static_cast<int*>(workspace), s);
+    return run_gemm(kGateUp, x_rows, w_gate_up, packed, offsets, sorted_to_slot, topk_weights,
+                    scale, dt, R, d, I, E, h, static_cast<int*>(workspace), s);
 }
 
 moe_status moe_down(const void* h, const int32_t* offsets, const int32_t* sorted_to_slot,
                     const float* topk_weights, moe_dtype dt, int R, int d, int E, int I,
                     const void* w_down, unsigned flags, float* y_sorted, void* workspace,
                     size_t ws_bytes, moe_stream_t stream) {
-    if (flags & ~(unsigned)MOE_FUSE_COMBINE_WEIGHT) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)(MOE_FUSE_COMBINE_WEIGHT | MOE_WEIGHTS_PACKED))
+        return MOE_ERR_INVALID_ARG;
     const bool weight = (flags & MOE_FUSE_COMBINE_WEIGHT) != 0;
+    const bool packed = (flags & MOE_WEIGHTS_PACKED) != 0;
+    if (packed && dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     moe_status st = check_experts_args(offsets, sorted_to_slot, topk_weights, weight, dt, R, d, E,
                                        I, workspace, ws_bytes);
     if (st != MOE_OK) return st;
@@ -225,16 +232,19 @@ moe_status moe_down(const void* h, const int32_t* offsets, const int32_t* sorted
     cudaStream_t s = (cudaStream_t)stream;
     st = clear_status(workspace, s);
     if (st != MOE_OK) return st;
-    return run_gemm(kDown, h, w_down, offsets, sorted_to_slot, topk_weights, weight, dt, R, I, d,
-                    E, y_sorted, static_cast<int*>(workspace), s);
+    return run_gemm(kDown, h, w_down, packed, offsets, sorted_to_slot, topk_weights, weight, dt,
+                    R, I, d, E, y_sorted, static_cast<int*>(workspace), s);
 }
 
 moe_status moe_experts(const void* x_sorted, const int32_t* offsets, const int32_t* sorted_to_slot,
                        const float* topk_weights, moe_dtype dt, int R, int d, int E, int I,
                        const void* w_gate_up, const void* w_down, unsigned flags, void* h,
                        float* y_sorted, void* workspace, size_t ws_bytes, moe_stream_t stream) {
-    if (flags & ~(unsigned)(MOE_SCALE_INPUT | MOE_FUSE_COMBINE_WEIGHT)) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)(MOE_SCALE_INPUT | MOE_FUSE_COMBINE_WEIGHT | MOE_WEIGHTS_PACKED))
+        return MOE_ERR_INVALID_ARG;
     if ((flags & MOE_SCALE_INPUT) && (flags & MOE_FUSE_COMBINE_WEIGHT)) return MOE_ERR_INVALID_ARG;
+    const bool packed = (flags & MOE_WEIGHTS_PACKED) != 0;
+    if (packed && dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     const bool any_w = (flags & (MOE_SCALE_INPUT | MOE_FUSE_COMBINE_WEIGHT)) != 0;
     moe_status st = check_experts_args(offsets, sorted_to_slot, topk_weights, any_w, dt, R, d, E,
                                        I, workspace, ws_bytes);
@@ -248,11 +258,31 @@ moe_status moe_experts(const void* x_sorted, const int32_t* offsets, const int32
     st = clear_status(workspace, s);
     if (st != MOE_OK) return st;
     int* status = static_cast<int*>(workspace);
-    st = run_gemm(kGateUp, x_sorted, w_gate_up, offsets, sorted_to_slot, topk_weights,
+    st = run_gemm(kGateUp, x_sorted, w_gate_up, packed, offsets, sorted_to_slot, topk_weights,
                   (flags & MOE_SCALE_INPUT) != 0, dt, R, d, I, E, h, status, s);
     if (st != MOE_OK) return st;
-    return run_gemm(kDown, h, w_down, offsets, sorted_to_slot, topk_weights,
+    return run_gemm(kDown, h, w_down, packed, offsets, sorted_to_slot, topk_weights,
                     (flags & MOE_FUSE_COMBINE_WEIGHT) != 0, dt, R, I, d, E, y_sorted, status, s);
+}
+
+size_t moe_packed_weights_size(moe_weight_kind kind, int E, int K, int N, moe_dtype dt) {
+    if ((kind != MOE_W_GATE_UP && kind != MOE_W_DOWN) || dt != MOE_BF16) return 0;
+    if (E < 1 || K < 1 || N < 1) return 0;
+    const PackedGeom g = packed_geom(kind == MOE_W_GATE_UP ? kGateUp : kDown, K, N);
+    return (size_t)E * g.nb * g.kpad * 64 * 2;
+}
+
+moe_status moe_pack_weights(moe_weight_kind kind, const void* w, void* packed, moe_dtype dt,
+                            int E, int K, int N, moe_stream_t stream) {
+    if (kind != MOE_W_GATE_UP && kind != MOE_W_DOWN) return MOE_ERR_INVALID_ARG;
+    if (!dtype_ok(dt)) return MOE_ERR_INVALID_ARG;
+    if (dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (E < 1 || K < 1 || N < 1 || N % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (!w || !packed || !aligned16(w) || !aligned16(packed)) return MOE_ERR_INVALID_ARG;
+    if (moe_packed_weights_size(kind, E, K, N, dt) / 128 >= (1ull << 31))
+        return MOE_ERR_UNSUPPORTED;  // packed rows are addressed with 32-bit coordinates
+    return launch_status(launch_pack_weights(kind == MOE_W_GATE_UP ? kGateUp : kDown, w, packed,
+                                             E, K, N, (cudaStream_t)stream));
 }
 
 moe_status moe_combine(const float* y_sorted, const int32_t* slot_to_sorted,
@@ -293,10 +323,13 @@ moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, 
     if (st != MOE_OK) return st;
     if (!dtype_ok(dt)) return MOE_ERR_INVALID_ARG;
     if (score_fn != MOE_SCORE_SOFTMAX && score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
-    if (flags & ~(unsigned)(MOE_RENORMALIZE | MOE_SCALE_INPUT | MOE_FUSE_COMBINE_WEIGHT))
+    if (flags & ~(unsigned)(MOE_RENORMALIZE | MOE_SCALE_INPUT | MOE_FUSE_COMBINE_WEIGHT |
+                            MOE_WEIGHTS_PACKED))
         return MOE_ERR_INVALID_ARG;
     const bool scale = (flags & MOE_SCALE_INPUT) != 0;
     const bool fuse_w = (flags & MOE_FUSE_COMBINE_WEIGHT) != 0;
+    const bool packed = (flags & MOE_WEIGHTS_PACKED) != 0;
+    if (packed && dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     if (scale && fuse_w) return MOE_ERR_INVALID_ARG;
     if (d < 1 || I < 1 || Is < 0) return MOE_ERR_INVALID_ARG;
     if (d % row_multiple(dt) != 0 || I % row_multiple(dt) != 0 || Is % row_multiple(dt) != 0)
@@ -357,18 +390,18 @@ moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, 
                                                 s))) != MOE_OK)
             return st;
     }
-    if ((st = run_gemm(kGateUp, xs, w_gate_up, offsets, s2p, topk_weights, scale, dt, R, d, I, E,
-                       h, status, s)) != MOE_OK)
+    if ((st = run_gemm(kGateUp, xs, w_gate_up, packed, offsets, s2p, topk_weights, scale, dt, R,
+                       d, I, E, h, status, s)) != MOE_OK)
         return st;
-    if ((st = run_gemm(kDown, h, w_down, offsets, s2p, topk_weights, fuse_w, dt, R, I, d, E, y,
-                       status, s)) != MOE_OK)
+    if ((st = run_gemm(kDown, h, w_down, packed, offsets, s2p, topk_weights, fuse_w, dt, R, I, d,
+                       E, y, status, s)) != MOE_OK)
         return st;
     if (shared) {
-        if ((st = run_gemm(kGateUp, x, w_shared_gate_up, nullptr, nullptr, nullptr, false, dt, T,
-                           d, Is, 1, h_sh, status, s)) != MOE_OK)
+        if ((st = run_gemm(kGateUp, x, w_shared_gate_up, packed, nullptr, nullptr, nullptr, false,
+                           dt, T, d, Is, 1, h_sh, status, s)) != MOE_OK)
             return st;
-        if ((st = run_gemm(kDown, h_sh, w_shared_down, nullptr, nullptr, nullptr, false, dt, T, Is,
-                           d, 1, y_sh, status, s)) != MOE_OK)
+        if ((st = run_gemm(kDown, h_sh, w_shared_down, packed, nullptr, nullptr, nullptr, false,
+                           dt, T, Is, d, 1, y_sh, status, s)) != MOE_OK)
             return st;
     }
     const float* comb_w = (scale || fuse_w) ? nullptr : topk_weights;

@@ -50,6 +50,8 @@ struct TcParams {
     int n_tiles;     // ceil(N / n_tile)
     int k_blocks;    // ceil(K / 64)
     int row_scale;   // gate_up: scale accumulators; down: weight rows
+    int packed;      // weights in the packed layout (PackedGeom below)
+    int nb, nbh, kpad;
 };
 
 struct __align__(8) SmemTail {
@@ -184,7 +186,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t b_dst = a_dst + kABytes;
                     const int kc = kb * kTileK;
                     tma_load_2d(a_dst, &tmA, &st.full[stage], kc, ti.row0);
-                    if (KIND == kGateUp) {
+                    if (p.packed) {
+                        // packed blocks of one expert are adjacent along the third dimension:
+                        // gate_up = {gate n0, gate n0+64} + {up n0, up n0+64} (two copies of two
+                        // blocks), down = the four blocks from n0 (one copy)
+                        const int blk0 = ti.e * p.nb + (ti.n0 >> 6);
+                        tma_load_3d(b_dst, &tmB, &st.full[stage], 0, kc, blk0);
+                        if (KIND == kGateUp)
+                            tma_load_3d(b_dst + 2 * kBBlockBytes, &tmB, &st.full[stage], 0, kc,
+                                        blk0 + p.nbh);
+                    } else if (KIND == kGateUp) {
                         tma_load_3d(b_dst, &tmB, &st.full[stage], ti.n0, kc, ti.e);
                         tma_load_3d(b_dst + kBBlockBytes, &tmB, &st.full[stage], ti.n0 + 64, kc,
                                     ti.e);
@@ -408,8 +419,14 @@ cudaError_t launch_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     const cuuint64_t b_dims[3] = {bn, (cuuint64_t)a.K, (cuuint64_t)groups};
     const cuuint64_t b_str[2] = {bn * 2, bn * 2 * (cuuint64_t)a.K};
     const cuuint32_t b_box[3] = {64, kTileK, 1};
+    const PackedGeom g = packed_geom(KIND, a.K, a.N);
+    // packed: {64 columns, Kpad rows, blocks}; one copy = 2 (gate_up) or 4 (down) blocks
+    const cuuint64_t pk_dims[3] = {64, (cuuint64_t)g.kpad, (cuuint64_t)groups * g.nb};
+    const cuuint64_t pk_str[2] = {128, (cuuint64_t)g.kpad * 128};
+    const cuuint32_t pk_box[3] = {64, kTileK, (KIND == kGateUp) ? 2u : 4u};
     if (!encode_tensor_map_bf16(&tmA, a.a, 2, a_dims, a_str, a_box) ||
-        !encode_tensor_map_bf16(&tmB, a.b, 3, b_dims, b_str, b_box))
+        !(a.packed ? encode_tensor_map_bf16(&tmB, a.b, 3, pk_dims, pk_str, pk_box)
+                   : encode_tensor_map_bf16(&tmB, a.b, 3, b_dims, b_str, b_box)))
         return cudaErrorInvalidValue;
 
     TcParams p;
@@ -426,6 +443,10 @@ cudaError_t launch_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     p.n_tiles = (a.N + p.n_tile - 1) / p.n_tile;
     p.k_blocks = (a.K + kTileK - 1) / kTileK;
     p.row_scale = (KIND == kGateUp) ? (a.scale_rows ? 1 : 0) : (a.weight_rows ? 1 : 0);
+    p.packed = a.packed ? 1 : 0;
+    p.nb = g.nb;
+    p.nbh = g.nbh;
+    p.kpad = g.kpad;
 
     // upper bound on tiles: sum_e ceil(n_e / 128) <= R / 128 + groups
     const long long m_ub = (long long)(a.R + kTileM - 1) / kTileM + groups;

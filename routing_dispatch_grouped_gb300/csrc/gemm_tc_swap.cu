@@ -70,6 +70,8 @@ struct SwapParams {
     int n_tiles;   // ceil(N / 128) weight-column blocks
     int k_blocks;  // ceil(K / 64)
     int row_scale;
+    int packed;    // weights in the packed layout (pack.cu)
+    int nb, nbh, kpad;
 };
 
 template <int STAGES>
@@ -232,10 +234,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     armed_phase[stage] = phase;
                     const uint32_t a_dst = smem_u32(smem + (size_t)stage * kStageBytes);
                     const int kc = kb * kTileK;
-                    tma_load_3d(a_dst, &tmW, &st.full[stage], t.n0, kc, t.e);
-                    // gate_up: the up columns of the same h columns; down: the next 64 columns
-                    tma_load_3d(a_dst + kWBlock, &tmW, &st.full[stage],
-                                (KIND == kGateUp) ? p.N + t.n0 : t.n0 + 64, kc, t.e);
+                    if (p.packed) {
+                        // packed blocks of one expert are adjacent along the third dimension:
+                        // down reads blocks n0/64 and n0/64 + 1 in one copy; gate_up reads the
+                        // gate block and the up block of the same columns (two copies)
+                        const int b0 = t.e * p.nb + (t.n0 >> 6);
+                        tma_load_3d(a_dst, &tmW, &st.full[stage], 0, kc, b0);
+                        if (KIND == kGateUp)
+                            tma_load_3d(a_dst + kWBlock, &tmW, &st.full[stage], 0, kc, b0 + p.nbh);
+                    } else {
+                        tma_load_3d(a_dst, &tmW, &st.full[stage], t.n0, kc, t.e);
+                        // gate_up: the up columns of the same h columns; down: the next 64
+                        tma_load_3d(a_dst + kWBlock, &tmW, &st.full[stage],
+                                    (KIND == kGateUp) ? p.N + t.n0 : t.n0 + 64, kc, t.e);
+                    }
                     tma_load_2d(a_dst + kABytes, &tmX, &st.full[stage], kc, t.row0);
                     if (++stage == kStages) {
                         stage = 0;
@@ -414,7 +426,12 @@ cudaError_t launch_swap_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     const cuuint64_t x_dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.R};
     const cuuint64_t x_str[1] = {(cuuint64_t)a.K * 2};
     const cuuint32_t x_box[2] = {kTileK, kTok};
-    if (!encode_tensor_map_bf16(&tmW, a.b, 3, w_dims, w_str, w_box) ||
+    const PackedGeom g = packed_geom(KIND, a.K, a.N);
+    const cuuint64_t pk_dims[3] = {64, (cuuint64_t)g.kpad, (cuuint64_t)groups * g.nb};
+    const cuuint64_t pk_str[2] = {128, (cuuint64_t)g.kpad * 128};
+    const cuuint32_t pk_box[3] = {64, kTileK, (KIND == kGateUp) ? 1u : 2u};
+    if (!(a.packed ? encode_tensor_map_bf16(&tmW, a.b, 3, pk_dims, pk_str, pk_box)
+                   : encode_tensor_map_bf16(&tmW, a.b, 3, w_dims, w_str, w_box)) ||
         !encode_tensor_map_bf16(&tmX, a.a, 2, x_dims, x_str, x_box))
         return cudaErrorInvalidValue;
 
@@ -431,6 +448,10 @@ cudaError_t launch_swap_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     p.n_tiles = (a.N + Shape<KIND>::kCols - 1) / Shape<KIND>::kCols;
     p.k_blocks = (a.K + kTileK - 1) / kTileK;
     p.row_scale = (KIND == kGateUp) ? (a.scale_rows ? 1 : 0) : (a.weight_rows ? 1 : 0);
+    p.packed = a.packed ? 1 : 0;
+    p.nb = g.nb;
+    p.nbh = g.nbh;
+    p.kpad = g.kpad;
 
     const long long m_ub = (long long)(a.R + kTok - 1) / kTok + groups;
     const long long tiles_ub = m_ub * p.n_tiles;

@@ -196,20 +196,38 @@ struct PdlScope {
     bool prev;
 };
 
+// cluster_x > 1 launches thread-block clusters of that many CTAs along x.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                          cudaStream_t s, Args&&... args) {
+cudaError_t launch_kernel_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, int cluster_x, Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (pdl_enabled()) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, Args&&... args) {
+    return launch_kernel_ex(kernel, grid, block, smem, s, 1, std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -246,10 +264,23 @@ cudaError_t launch_combine(const float* y_sorted, const int32_t* slot_to_sorted,
 
 // Grouped GEMMs. `which` selects gate_up (+SwiGLU, output dtype of the layer) or down (fp32).
 enum GemmKind { kGateUp = 0, kDown = 1 };
+// Packed weight layout (pack.cu): 64-column x 64-row blocks stored contiguously, block
+// (e, nb, kb) at rows ((e * nb_total + nb) * kpad + 64 kb) of a [rows, 64] bf16 matrix. gate_up
+// blocks its gate and up halves separately (nbh blocks each).
+struct PackedGeom {
+    int nbh;   // 64-column blocks per half (gate_up) or in all (down)
+    int nb;    // blocks per expert: 2 nbh (gate_up) or nbh (down)
+    int kpad;  // K rounded up to 64
+};
+PackedGeom packed_geom(int kind, int K, int N);  // N = I (gate_up) or d (down)
+cudaError_t launch_pack_weights(int kind, const void* w, void* packed, int E, int K, int N,
+                                cudaStream_t s);
+
 struct GroupedGemmArgs {
     GemmKind kind;
     const void* a;            // [R, K] rows (x_sorted / x for gate_up, h for down)
-    const void* b;            // weights: [E, K, 2I] (gate_up) or [E, K, d] (down)
+    const void* b;            // weights: [E, K, 2I] (gate_up) or [E, K, d] (down), or packed
+    bool packed;              // b is in the packed layout
     const int32_t* offsets;   // [E+1] or nullptr (one group of R rows)
     const int32_t* sorted_to_slot;
     const float* topk_weights;

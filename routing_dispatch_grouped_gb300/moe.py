@@ -17,7 +17,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe.so")
 
 SOFTMAX, SIGMOID = 0, 1
-RENORMALIZE, SCALE_INPUT, FUSE_COMBINE_WEIGHT = 1, 2, 4
+RENORMALIZE, SCALE_INPUT, FUSE_COMBINE_WEIGHT, WEIGHTS_PACKED = 1, 2, 4, 8
+W_GATE_UP, W_DOWN = 0, 1
 F32, BF16 = 0, 1
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
           3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_DEVICE_BOUNDS",
@@ -35,6 +36,8 @@ SIGNATURES = {
     "moe_experts": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _U, _P, _P, _P, _S, _P]),
     "moe_experts_workspace_size": (_S, []),
     "moe_combine": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
+    "moe_packed_weights_size": (_S, [_I, _I, _I, _I, _I]),
+    "moe_pack_weights": (_I, [_I, _P, _P, _I, _I, _I, _I, _P]),
     "moe_forward": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P, _P,
                          _P, _P, _S, _P]),
     "moe_forward_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
@@ -93,6 +96,43 @@ def _need(t: torch.Tensor, name: str):
     if not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
     return t
+
+
+class PackedWeights:
+    """Expert weights repacked by moe_pack_weights (bf16): `data` is the packed buffer, kind is
+    W_GATE_UP (logical [E, K=d, 2I], N = I) or W_DOWN (logical [E, K=I, N=d])."""
+
+    def __init__(self, data: torch.Tensor, kind: int, E: int, K: int, N: int):
+        self.data, self.kind, self.E, self.K, self.N = data, kind, E, K, N
+
+    def data_ptr(self):
+        return self.data.data_ptr()
+
+
+def moe_packed_weights_size(kind, E, K, N) -> int:
+    return lib().moe_packed_weights_size(kind, E, K, N, BF16)
+
+
+def pack_weights(w: torch.Tensor, kind: int, stream=None) -> PackedWeights:
+    """Repack gate_up ([E, d, 2I] or [d, 2I]) or down ([E, I, d] or [I, d]) bf16 weights."""
+    _need(w, "w")
+    w3 = w.unsqueeze(0) if w.dim() == 2 else w
+    E, K, C = w3.shape
+    N = C // 2 if kind == W_GATE_UP else C
+    out = torch.empty(moe_packed_weights_size(kind, E, K, N), dtype=torch.uint8,
+                      device=w.device)
+    _check("moe_pack_weights", lib().moe_pack_weights(kind, _p(w3), _p(out), _dt(w3), E, K, N,
+                                                      _stream(stream)))
+    return PackedWeights(out, kind, E, K, N)
+
+
+def _w_dims(w, kind):
+    """(E, K, N, flag) of a weight argument, packed or not."""
+    if isinstance(w, PackedWeights):
+        assert w.kind == kind, "packed weights of the other kind"
+        return w.E, w.K, w.N, WEIGHTS_PACKED
+    E, K, C = w.shape
+    return E, K, (C // 2 if kind == W_GATE_UP else C), 0
 
 
 def _workspace(nbytes: int, device) -> torch.Tensor:
@@ -155,14 +195,13 @@ def moe_gate_up(x_rows, offsets, w_gate_up, sorted_to_slot=None, topk_weights=No
                 scale_input=False, h=None, workspace=None, stream=None):
     _need(x_rows, "x_rows")
     R, d = x_rows.shape
-    E, _, two_i = w_gate_up.shape
-    I = two_i // 2
+    E, _, I, pk = _w_dims(w_gate_up, W_GATE_UP)
     dev = x_rows.device
     h = h if h is not None else torch.empty(R, I, dtype=x_rows.dtype, device=dev)
     ws = workspace if workspace is not None else _workspace(moe_experts_workspace_size(), dev)
     _check("moe_gate_up", lib().moe_gate_up(
         _p(x_rows), _p(offsets), _p(sorted_to_slot), _p(topk_weights), _dt(x_rows), R, d, E, I,
-        _p(w_gate_up), SCALE_INPUT if scale_input else 0, _p(h), _p(ws), ws.numel(),
+        _p(w_gate_up), (SCALE_INPUT if scale_input else 0) | pk, _p(h), _p(ws), ws.numel(),
         _stream(stream)))
     return h
 
@@ -171,13 +210,13 @@ def moe_down(h, offsets, w_down, sorted_to_slot=None, topk_weights=None, fuse_we
              y_sorted=None, workspace=None, stream=None):
     _need(h, "h")
     R, I = h.shape
-    E, _, d = w_down.shape
+    E, _, d, pk = _w_dims(w_down, W_DOWN)
     dev = h.device
     y = y_sorted if y_sorted is not None else torch.empty(R, d, dtype=torch.float32, device=dev)
     ws = workspace if workspace is not None else _workspace(moe_experts_workspace_size(), dev)
     _check("moe_down", lib().moe_down(
         _p(h), _p(offsets), _p(sorted_to_slot), _p(topk_weights), _dt(h), R, d, E, I,
-        _p(w_down), FUSE_COMBINE_WEIGHT if fuse_weight else 0, _p(y), _p(ws), ws.numel(),
+        _p(w_down), (FUSE_COMBINE_WEIGHT if fuse_weight else 0) | pk, _p(y), _p(ws), ws.numel(),
         _stream(stream)))
     return y
 
@@ -186,8 +225,8 @@ def moe_experts(x_sorted, offsets, w_gate_up, w_down, sorted_to_slot=None, topk_
                 flags=0, h=None, y_sorted=None, workspace=None, stream=None):
     _need(x_sorted, "x_sorted")
     R, d = x_sorted.shape
-    E, _, two_i = w_gate_up.shape
-    I = two_i // 2
+    E, _, I, pk = _w_dims(w_gate_up, W_GATE_UP)
+    flags |= pk
     dev = x_sorted.device
     h = h if h is not None else torch.empty(R, I, dtype=x_sorted.dtype, device=dev)
     y = y_sorted if y_sorted is not None else torch.empty(R, d, dtype=torch.float32, device=dev)
@@ -226,9 +265,12 @@ def moe_forward(x, logits, w_gate_up, w_down, k, score_fn=SOFTMAX, flags=RENORMA
     _need(x, "x")
     _need(logits, "logits")
     T, d = x.shape
-    E, _, two_i = w_gate_up.shape
-    I = two_i // 2
-    Is = 0 if w_shared_gate_up is None else w_shared_gate_up.shape[1] // 2
+    E, _, I, pk = _w_dims(w_gate_up, W_GATE_UP)
+    flags |= pk
+    Is = 0
+    if w_shared_gate_up is not None:
+        Is = (w_shared_gate_up.N if isinstance(w_shared_gate_up, PackedWeights)
+              else w_shared_gate_up.shape[-1] // 2)
     dev = x.device
     out = out if out is not None else torch.empty(T, d, dtype=x.dtype, device=dev)
     ids = topk_ids if topk_ids is not None else torch.empty(T, k, dtype=torch.int32, device=dev)

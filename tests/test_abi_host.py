@@ -135,6 +135,26 @@ def test_workspace_size_matches_binding_layout(L):
         assert sz >= (last.data_ptr() - ws.data_ptr()) + last.numel() * last.element_size()
 
 
+def test_pack_validation_and_sizes(L):
+    P = L.moe_pack_weights
+    assert P(0, FAKE, FAKE, 0, 2, 64, 64, NULL) == 2     # fp32 packing is not supported
+    assert P(7, FAKE, FAKE, 1, 2, 64, 64, NULL) == 1     # unknown kind
+    assert P(0, FAKE, FAKE, 1, 2, 64, 60, NULL) == 1     # N not a multiple of 8
+    assert P(1, MIS, FAKE, 1, 2, 64, 64, NULL) == 1      # misaligned
+    S = L.moe_packed_weights_size
+    # gate_up [E=8, d=4096, 2I=2*14336]: 2 * 224 blocks of 64 columns, Kpad 4096
+    assert S(0, 8, 4096, 14336, 1) == 8 * 448 * 4096 * 64 * 2
+    # down [E=128, I=2880, d=2880]: 45 blocks, Kpad 2880
+    assert S(1, 128, 2880, 2880, 1) == 128 * 45 * 2880 * 128
+    # padding: K=200 -> 256, N=200 -> 4 blocks per half
+    assert S(0, 1, 200, 200, 1) == 8 * 256 * 128
+    assert S(0, 1, 200, 200, 0) == 0
+    f = L.moe_forward
+    sz = L.moe_forward_workspace_size(64, 128, 8, 2, 256, 0, 0)
+    assert f(FAKE, FAKE, 0, 64, 128, 8, 2, 256, 0, 1 | 8, FAKE, FAKE, None, None, 0, FAKE, FAKE,
+             FAKE, 0x100000, sz, NULL) == 2           # packed weights need bf16
+
+
 def test_kernel_count_and_strings(L):
     assert L.moe_forward_kernel_count(0, 2, 0) == 0
     assert L.moe_forward_kernel_count(10, 2, 0) == 5        # fused small-batch front end

@@ -34,9 +34,14 @@ def _sample_tokens(ids, E, n=40, seed=0):
 def test_forward_full_size(name):
     cfg = synth.CONFIGS[name]
     inp = synth.make_inputs(cfg, DEV)
-    out, ids, w, ws = moe.moe_forward(inp["x"], inp["logits"], inp["w_gate_up"], inp["w_down"],
-                                      cfg.k, cfg.score_fn, _flags(cfg), inp["w_shared_gate_up"],
-                                      inp["w_shared_down"])
+    # the benchmark's configuration: expert weights packed once, then the layer
+    pk = {n: moe.pack_weights(inp[n], moe.W_GATE_UP if "gate_up" in n else moe.W_DOWN)
+          if inp[n] is not None else None
+          for n in ("w_gate_up", "w_down", "w_shared_gate_up", "w_shared_down")}
+    out, ids, w, ws = moe.moe_forward(inp["x"], inp["logits"], pk["w_gate_up"], pk["w_down"],
+                                      cfg.k, cfg.score_fn, _flags(cfg), pk["w_shared_gate_up"],
+                                      pk["w_shared_down"])
+    del pk
     assert moe.moe_read_device_status(ws) == 0
     rid, rw = o.route(inp["logits"].cpu().numpy(), cfg.k, cfg.score_fn, cfg.renormalize)
     assert np.array_equal(ids.cpu().numpy(), rid)

@@ -371,3 +371,68 @@ def test_forward_in_cuda_graph():
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+
+
+# ------------------------------------------------------------------------------------------------
+# packed weights (moe_pack_weights): same results as the pages' layout
+# ------------------------------------------------------------------------------------------------
+def _ref_pack(w, kind):
+    """The packed layout by plain tensor indexing: 64 x 64 blocks (e, nb, k rows, 64 columns),
+    gate and up halves blocked separately for gate_up, zero padding."""
+    E, K, C = w.shape
+    N = C // 2 if kind == moe.W_GATE_UP else C
+    kpad = (K + 63) // 64 * 64
+    nbh = (N + 63) // 64
+    halves = [w[..., :N], w[..., N:]] if kind == moe.W_GATE_UP else [w]
+    blocks = []
+    for hw in halves:
+        padded = torch.zeros(E, kpad, nbh * 64, dtype=w.dtype, device=w.device)
+        padded[:, :K, :N] = hw
+        blocks.append(padded.view(E, kpad, nbh, 64).permute(0, 2, 1, 3))
+    return torch.cat(blocks, dim=1).contiguous()
+
+
+@pytest.mark.parametrize("E,K,N", [(3, 256, 384), (1, 200, 200), (5, 64, 8), (2, 130, 1000)])
+def test_pack_layout(E, K, N):
+    for kind in (moe.W_GATE_UP, moe.W_DOWN):
+        C = 2 * N if kind == moe.W_GATE_UP else N
+        w = synth.normal((E, K, C), torch.bfloat16, E + K, "pk", 1.0, device=DEV)
+        pw = moe.pack_weights(w, kind)
+        ref = _ref_pack(w, kind)
+        assert pw.data.numel() == ref.numel() * 2
+        assert torch.equal(pw.data.view(torch.bfloat16), ref.view(-1))
+
+
+@pytest.mark.parametrize("shape", range(len(GEMM_SHAPES)))
+def test_grouped_gemm_packed_weights(shape):
+    counts, d, I = GEMM_SHAPES[shape]
+    offsets, xs, wgu, wd = _gemm_case(counts, d, I, torch.bfloat16, seed=shape)
+    off_t = torch.from_numpy(offsets.astype(np.int32)).to(DEV)
+    h_ref = moe.moe_gate_up(xs, off_t, wgu)
+    y_ref = moe.moe_down(h_ref, off_t, wd)
+    h = moe.moe_gate_up(xs, off_t, moe.pack_weights(wgu, moe.W_GATE_UP))
+    y = moe.moe_down(h, off_t, moe.pack_weights(wd, moe.W_DOWN))
+    # the packed layout changes only where weights are read from, not the arithmetic
+    assert torch.equal(h, h_ref)
+    assert torch.equal(y, y_ref)
+
+
+@pytest.mark.parametrize("name,T", [("gpt_oss_120b", 700), ("decode", 8), ("llama4_scout", 300),
+                                    ("mixtral_8x7b", 600)])
+def test_forward_packed_weights_matches_oracle(name, T):
+    cfg = _cfg(name, T)
+    inp = synth.make_inputs(cfg, DEV)
+    pk = dict(inp)
+    pk["w_gate_up"] = moe.pack_weights(inp["w_gate_up"], moe.W_GATE_UP)
+    pk["w_down"] = moe.pack_weights(inp["w_down"], moe.W_DOWN)
+    if inp["w_shared_gate_up"] is not None:
+        pk["w_shared_gate_up"] = moe.pack_weights(inp["w_shared_gate_up"], moe.W_GATE_UP)
+        pk["w_shared_down"] = moe.pack_weights(inp["w_shared_down"], moe.W_DOWN)
+    out, ids, _, ws = _run_forward(cfg, pk)
+    assert moe.moe_read_device_status(ws) == 0
+    ref = _oracle_forward(cfg, inp)
+    assert np.array_equal(ids.cpu().numpy(), ref["topk_ids"])
+    e = err_rms(f64(out), ref["out"])
+    assert e <= TOL[cfg.dtype], e
+    out_u, _, _, _ = _run_forward(cfg, inp)
+    assert torch.equal(out, out_u)
