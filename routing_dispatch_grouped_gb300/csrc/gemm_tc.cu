@@ -35,7 +35,7 @@ constexpr int kABytes = kTileM * kTileK * 2;       // 16 KB
 constexpr int kBBlockBytes = 64 * kTileK * 2;      // 8 KB: 64 columns x 64 k-rows
 constexpr int kBBytes = 4 * kBBlockBytes;          // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;     // 48 KB
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;  // 7 warps: A loads, MMA, 4 epilogue, weight loads
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s for any single wait
 
@@ -185,7 +185,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t a_dst = smem_u32(smem + (size_t)stage * kStageBytes);
                     const uint32_t b_dst = a_dst + kABytes;
                     const int kc = kb * kTileK;
+                    (void)b_dst;
                     tma_load_2d(a_dst, &tmA, &st.full[stage], kc, ti.row0);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                st.abort = 1;
+                set_status(p.status, MOE_ERR_TIMEOUT);
+            }
+            if (*abort_flag) {
+                // let every copy this thread started land before shared memory is released
+                for (int s = 0; s < kStages; ++s)
+                    if (armed[s]) mbar_wait(&st.full[s], armed_phase[s], nullptr, kWaitLimitNs);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 6) {
+        // ================= TMA producer, weight blocks =================
+        // Same stage sequence as warp 0; warp 0 arms each stage's barrier for all 48 KB, this
+        // warp's copies complete their share of it. Two issuing threads double the rate at which
+        // copies are started.
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            uint32_t armed_phase[kStages];
+            bool armed[kStages];
+#pragma unroll
+            for (int s = 0; s < kStages; ++s) {
+                armed[s] = false;
+                armed_phase[s] = 0;
+            }
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const TileInfo ti = decode_tile(st, E, p.n_tiles, p.n_tile, tile);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&st.empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    armed[stage] = true;
+                    armed_phase[stage] = phase;
+                    const uint32_t b_dst = smem_u32(smem + (size_t)stage * kStageBytes) + kABytes;
+                    const int kc = kb * kTileK;
                     if (p.packed) {
                         // packed blocks of one expert are adjacent along the third dimension:
                         // gate_up = {gate n0, gate n0+64} + {up n0, up n0+64} (two copies of two
@@ -220,7 +264,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 set_status(p.status, MOE_ERR_TIMEOUT);
             }
             if (*abort_flag) {
-                // let every copy this thread started land before shared memory is released
                 for (int s = 0; s < kStages; ++s)
                     if (armed[s]) mbar_wait(&st.full[s], armed_phase[s], nullptr, kWaitLimitNs);
             }
