@@ -1,0 +1,503 @@
+// Grouped expert GEMM on CTA pairs: tcgen05.mma.cta_group::2 (the 2-SM form of the sm_100-family
+// tensor core instruction), bf16 in, fp32 accumulate.
+//
+// Same computation as gemm_tc.cu (Tensor parallelism page, "Packed strategies": packed
+// [E, hidden, 2*expert_dim] gate|up weight, gate first; Expert parallelism page, "Adding an
+// implementation": each expert runs on the rows routed to it), for experts with many rows. A
+// cluster of two CTAs computes one 256-row x 256-column tile:
+//   - CTA r holds rows [m0 + 128 r, m0 + 128 r + 128) of the token tile (A, 16 KB per k-block)
+//     and half of the weight tile (B, 16 KB per k-block): for gate_up CTA 0 holds the 128 gate
+//     columns and CTA 1 the 128 up columns of the same h columns; for down the two halves of the
+//     256 output columns.
+//   - The leader (rank 0) issues one M=256, N=256, K=16 MMA per step; each CTA's tensor memory
+//     receives its own 128 rows x all 256 columns, so the epilogue of each CTA is the 1-SM one.
+//   - A stage is 32 KB per CTA instead of 48 KB, so six stages fit in shared memory and the
+//     loads in flight cover about half as much again of MMA time.
+// Synchronisation: both CTAs' copies complete on the leader's stage barrier (armed by the leader
+// for the 64 KB of both), the leader's commits arrive on the stage and accumulator barriers of
+// both CTAs, and the epilogue warps of both CTAs release an accumulator on the leader's barrier.
+// Every mbarrier wait is bounded in time as in the 1-SM kernels.
+#include <mutex>
+
+#include "moe_internal.cuh"
+
+namespace rdg {
+namespace {
+
+constexpr int kStages = 6;
+constexpr int kABytes = kTileM * kTileK * 2;     // 16 KB: this CTA's 128 rows
+constexpr int kBBlockBytes = 64 * kTileK * 2;    // 8 KB
+constexpr int kBBytes = 2 * kBBlockBytes;        // 16 KB: this CTA's half of the 256 columns
+constexpr int kStageBytes = kABytes + kBBytes;   // 32 KB
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kPairRows = 2 * kTileM;            // 256 rows per pair tile
+
+// ---- cta_group::2 forms and cluster helpers ----
+__device__ __forceinline__ uint32_t cta_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_idx() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_cnt() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+// shared::cluster address of `local` (a shared::cta address) in CTA `rank` of this cluster
+__device__ __forceinline__ uint32_t mapa(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void tmem_alloc_2sm(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_2sm(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void umma_bf16_2sm(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive on the mbarrier at this shared-memory offset in both CTAs of the pair once every MMA
+// this thread issued has completed.
+__device__ __forceinline__ void umma_commit_2sm(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"((uint16_t)0x3)
+        : "memory");
+}
+// Tile loads into this CTA's shared memory that complete on the mbarrier at `bar_cluster` (a
+// shared::cluster address, here the leader's stage barrier).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(map), "r"(bar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(map), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+struct PairParams {
+    const int32_t* offsets;
+    const int32_t* sorted_to_slot;
+    const float* topk_weights;
+    void* out;
+    int* status;
+    int R, K, N, E;
+    int n_tile;    // output columns per pair tile: 128 h columns (gate_up) or 256 (down)
+    int n_tiles;
+    int k_blocks;
+    int row_scale;
+    int packed, nb, nbh, kpad;
+};
+
+struct __align__(8) SmemTail {
+    uint64_t full[kStages];   // used in the leader: both CTAs' copies complete here
+    uint64_t empty[kStages];  // in both CTAs: released by the leader's commits
+    uint64_t tfull[2];        // in both CTAs
+    uint64_t tempty[2];       // used in the leader: 4 epilogue warps of each CTA
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    int total_tiles;
+    int prefix[kMaxE + 1];
+    int off[kMaxE + 1];
+    int mt[kMaxE];  // 256-row blocks of each expert
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(SmemTail);
+
+struct PairTile {
+    int e, row0, row_end, n0;  // row0: this CTA's first row
+};
+
+__device__ __forceinline__ PairTile decode_pair(const SmemTail& st, int E, int n_tile, int tile,
+                                                uint32_t rank) {
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (st.prefix[mid] <= tile)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int local = tile - st.prefix[lo];
+    const int m = st.mt[lo];
+    const int nb = local / m, mb = local - nb * m;
+    PairTile t;
+    t.e = lo;
+    t.row0 = st.off[lo] + mb * kPairRows + (int)rank * kTileM;
+    t.row_end = st.off[lo + 1];
+    t.n0 = nb * n_tile;
+    return t;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float silu(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_grouped_gemm_2sm(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const PairParams p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + (size_t)kStages * kStageBytes);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = p.E;
+    const uint32_t rank = cta_rank();
+    const bool leader = rank == 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&st.full[s], 1);   // the leader's producer arms it for both CTAs
+            mbar_init(&st.empty[s], 1);  // one multicast commit from the leader
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&st.tfull[a], 1);
+            mbar_init(&st.tempty[a], 8);  // 4 epilogue warps in each CTA
+        }
+        mbar_init(&st.drain, 1);
+        st.abort = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+    }
+    if (warp == 1) tmem_alloc_2sm(&st.tmem_base, kTmemCols);
+    // the peer's barriers exist before any copy, commit or arrive reaches them
+    cluster_sync_all();
+    griddep_wait();
+    if (warp == 2) {
+        for (int e = lane; e <= E; e += 32)
+            st.off[e] = p.offsets ? __ldg(p.offsets + e) : (e == 0 ? 0 : p.R);
+        __syncwarp();
+        if (lane == 0) {
+            int acc = 0;
+            for (int e = 0; e < E; ++e) {
+                int rows = st.off[e + 1] - st.off[e];
+                if (rows < 0) rows = 0;
+                const int m = (rows + kPairRows - 1) / kPairRows;
+                st.mt[e] = m > 0 ? m : 1;
+                st.prefix[e] = acc;
+                acc += m * p.n_tiles;
+            }
+            st.prefix[E] = acc;
+            st.total_tiles = acc;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = st.tmem_base;
+    const int total = st.total_tiles;
+    const int pair0 = (int)cluster_idx(), npairs = (int)cluster_cnt();
+    volatile int* abort_flag = &st.abort;
+
+    if (warp == 0) {
+        // ================= TMA producer (both CTAs) =================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmA);
+            tma_prefetch_desc(&tmB);
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int tile = pair0; tile < total && ok; tile += npairs) {
+                const PairTile t = decode_pair(st, E, p.n_tile, tile, rank);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&st.empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    // the leader's stage barrier counts the bytes of both CTAs
+                    if (leader) mbar_arrive_expect_tx(&st.full[stage], 2 * kStageBytes);
+                    const uint32_t bar = mapa(smem_u32(&st.full[stage]), 0);
+                    const uint32_t a_dst = smem_u32(smem + (size_t)stage * kStageBytes);
+                    const uint32_t b_dst = a_dst + kABytes;
+                    const int kc = kb * kTileK;
+                    tma_load_2d_pair(a_dst, &tmA, bar, kc, t.row0);
+                    // this CTA's two 64-column weight blocks: gate_up = gate (rank 0) or up
+                    // (rank 1) of h columns n0 .. n0+127; down = output columns
+                    // n0 + 128 rank .. + 127
+                    if (p.packed) {
+                        const int blk = t.e * p.nb + ((KIND == kGateUp)
+                                                          ? (int)rank * p.nbh + (t.n0 >> 6)
+                                                          : (t.n0 >> 6) + 2 * (int)rank);
+                        tma_load_3d_pair(b_dst, &tmB, bar, 0, kc, blk);
+                    } else {
+                        const int c0 = (KIND == kGateUp) ? (int)rank * p.N + t.n0
+                                                         : t.n0 + 128 * (int)rank;
+                        tma_load_3d_pair(b_dst, &tmB, bar, c0, kc, t.e);
+                        tma_load_3d_pair(b_dst + kBBlockBytes, &tmB, bar, c0 + 64, kc, t.e);
+                    }
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                st.abort = 1;
+                set_status(p.status, MOE_ERR_TIMEOUT);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ================= MMA issuer (leader only) =================
+        if (lane == 0 && leader) {
+            // M = 256 across the pair, N = 256, A K-major, B MN-major
+            constexpr uint32_t idesc = idesc_bf16_f32(2 * kTileM, kTileN, true);
+            uint32_t stage = 0, phase = 0, it = 0;
+            bool ok = true, issued = false;
+            for (int tile = pair0; tile < total && ok; tile += npairs, ++it) {
+                const uint32_t acc = it & 1u;
+                if (!mbar_wait(&st.tempty[acc], ((it >> 1) & 1u) ^ 1u, abort_flag, kWaitLimitNs)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * kTileN;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait(&st.full[stage], phase, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_u32(smem + (size_t)stage * kStageBytes);
+                    const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+                    for (int kk = 0; kk < kTileK / 16; ++kk) {
+                        // each CTA's operands sit at these offsets of its own shared memory:
+                        // A 128 rows K-major (+32 B per K step), B 128 columns MN-major in two
+                        // 64-column blocks 8 KB apart (+2 KB per K step)
+                        const uint64_t adesc = smem_desc(a_addr + kk * 32, 16, 1024);
+                        const uint64_t bdesc = smem_desc(b_addr + kk * 2048, kBBlockBytes, 1024);
+                        umma_bf16_2sm(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    umma_commit_2sm(&st.empty[stage]);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) umma_commit_2sm(&st.tfull[acc]);
+            }
+            if (!ok) {
+                st.abort = 1;
+                set_status(p.status, MOE_ERR_TIMEOUT);
+            }
+            if (*abort_flag && issued) {
+                umma_commit_2sm(&st.drain);  // tracks the pair MMAs issued above
+                mbar_wait(&st.drain, 0, nullptr, kWaitLimitNs);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ================= epilogue (warps 2..5, both CTAs) =================
+        const int q = warp & 3;
+        uint32_t it = 0;
+        const uint32_t tempty_leader0 = mapa(smem_u32(&st.tempty[0]), 0);
+        const uint32_t tempty_leader1 = mapa(smem_u32(&st.tempty[1]), 0);
+        for (int tile = pair0; tile < total; tile += npairs, ++it) {
+            const PairTile t = decode_pair(st, E, p.n_tile, tile, rank);
+            const uint32_t acc = it & 1u;
+            if (!mbar_wait(&st.tfull[acc], (it >> 1) & 1u, abort_flag, kWaitLimitNs)) {
+                if (lane == 0) {
+                    st.abort = 1;
+                    set_status(p.status, MOE_ERR_TIMEOUT);
+                }
+                break;
+            }
+            tc_fence_after();
+            const int row = t.row0 + q * 32 + lane;
+            const bool row_ok = row < t.row_end;
+            float s = 1.0f;
+            if (p.row_scale && row_ok) s = __ldg(p.topk_weights + __ldg(p.sorted_to_slot + row));
+            const uint32_t tbase = tmem_base + acc * kTileN + ((uint32_t)(q * 32) << 16);
+            if (KIND == kGateUp) {
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t g[32], u[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, g);
+                    tmem_ld_32x32b_x32(tbase + 128 + c * 32, u);
+                    tmem_ld_wait();
+                    const int col0 = t.n0 + c * 32;
+                    if (row_ok) {
+                        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * p.N + col0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            if (col0 + v * 8 < p.N) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int h2 = 0; h2 < 4; ++h2) {
+                                    const int i = v * 8 + h2 * 2;
+                                    const float g0 = __uint_as_float(g[i]) * s;
+                                    const float g1 = __uint_as_float(g[i + 1]) * s;
+                                    const float u0 = __uint_as_float(u[i]) * s;
+                                    const float u1 = __uint_as_float(u[i + 1]) * s;
+                                    w[h2] = pack_bf16x2(silu(g0) * u0, silu(g1) * u1);
+                                }
+                                dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+                            }
+                        }
+                    }
+                }
+            } else {
+                float* out = static_cast<float*>(p.out);
+#pragma unroll 1
+                for (int c = 0; c < kTileN / 32; ++c) {
+                    uint32_t y[32];
+                    tmem_ld_32x32b_x32(tbase + c * 32, y);
+                    tmem_ld_wait();
+                    const int col0 = t.n0 + c * 32;
+                    if (row_ok) {
+                        float4* dst = reinterpret_cast<float4*>(out + (size_t)row * p.N + col0);
+#pragma unroll
+                        for (int v = 0; v < 8; ++v) {
+                            if (col0 + v * 4 < p.N) {
+                                dst[v] = make_float4(__uint_as_float(y[v * 4]) * s,
+                                                     __uint_as_float(y[v * 4 + 1]) * s,
+                                                     __uint_as_float(y[v * 4 + 2]) * s,
+                                                     __uint_as_float(y[v * 4 + 3]) * s);
+                            }
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+        }
+    }
+
+    // ---- teardown ----
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // nothing of the peer reaches this CTA's shared memory or tensor memory after this point
+    cluster_sync_all();
+    if (warp == 1) tmem_dealloc_2sm(tmem_base, kTmemCols);
+}
+
+template <int KIND>
+cudaError_t launch_pair_kind(const GroupedGemmArgs& a, cudaStream_t s) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(tc_grouped_gemm_2sm<KIND>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    const int groups = a.offsets ? a.E : 1;
+    CUtensorMap tmA, tmB;
+    const cuuint64_t a_dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.R};
+    const cuuint64_t a_str[1] = {(cuuint64_t)a.K * 2};
+    const cuuint32_t a_box[2] = {kTileK, kTileM};
+    const cuuint64_t bn = (KIND == kGateUp) ? 2 * (cuuint64_t)a.N : (cuuint64_t)a.N;
+    const cuuint64_t b_dims[3] = {bn, (cuuint64_t)a.K, (cuuint64_t)groups};
+    const cuuint64_t b_str[2] = {bn * 2, bn * 2 * (cuuint64_t)a.K};
+    const cuuint32_t b_box[3] = {64, kTileK, 1};
+    const PackedGeom g = packed_geom(KIND, a.K, a.N);
+    const cuuint64_t pk_dims[3] = {64, (cuuint64_t)g.kpad, (cuuint64_t)groups * g.nb};
+    const cuuint64_t pk_str[2] = {128, (cuuint64_t)g.kpad * 128};
+    const cuuint32_t pk_box[3] = {64, kTileK, 2};
+    if (!encode_tensor_map_bf16(&tmA, a.a, 2, a_dims, a_str, a_box) ||
+        !(a.packed ? encode_tensor_map_bf16(&tmB, a.b, 3, pk_dims, pk_str, pk_box)
+                   : encode_tensor_map_bf16(&tmB, a.b, 3, b_dims, b_str, b_box)))
+        return cudaErrorInvalidValue;
+
+    PairParams p;
+    p.offsets = a.offsets;
+    p.sorted_to_slot = a.sorted_to_slot;
+    p.topk_weights = a.topk_weights;
+    p.out = a.out;
+    p.status = a.status;
+    p.R = a.R;
+    p.K = a.K;
+    p.N = a.N;
+    p.E = groups;
+    p.n_tile = (KIND == kGateUp) ? 128 : 256;
+    p.n_tiles = (a.N + p.n_tile - 1) / p.n_tile;
+    p.k_blocks = (a.K + kTileK - 1) / kTileK;
+    p.row_scale = (KIND == kGateUp) ? (a.scale_rows ? 1 : 0) : (a.weight_rows ? 1 : 0);
+    p.packed = a.packed ? 1 : 0;
+    p.nb = g.nb;
+    p.nbh = g.nbh;
+    p.kpad = g.kpad;
+
+    // clusters that can be resident at once (SMs pair up within a GPC)
+    static int max_clusters[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) dev = 0;
+    if (max_clusters[dev] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(device_sm_count() & ~1);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, tc_grouped_gemm_2sm<KIND>, &cfg) != cudaSuccess ||
+            n < 1)
+            n = device_sm_count() / 2;
+        max_clusters[dev] = n;
+    }
+    const long long pair_ub = ((long long)(a.R + kPairRows - 1) / kPairRows + groups) * p.n_tiles;
+    long long clusters = max_clusters[dev];
+    if (pair_ub < clusters) clusters = pair_ub;
+    if (clusters < 1) clusters = 1;
+    return launch_kernel_ex(tc_grouped_gemm_2sm<KIND>, dim3((unsigned)(2 * clusters)),
+                            dim3(kThreads), kSmemBytes, s, 2, tmA, tmB, p);
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm_bf16_2sm(const GroupedGemmArgs& a, cudaStream_t s) {
+    return a.kind == kGateUp ? launch_pair_kind<kGateUp>(a, s) : launch_pair_kind<kDown>(a, s);
+}
+
+}  // namespace rdg

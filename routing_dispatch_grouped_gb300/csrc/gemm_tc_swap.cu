@@ -11,7 +11,9 @@
 //   weight layout as an MN-major operand (two 64-column blocks, 128-byte swizzle). For gate_up
 //   the two blocks are 64 gate columns and the 64 up columns of the same h columns; for down
 //   they are 128 consecutive output columns.
-// - B = up to 256 token rows x 64 K of x_sorted / h, K-major.
+// - B = up to 256 token rows x 64 K of x_sorted / h, K-major, fetched with the smallest of four
+//   token boxes (256/128/64/32 rows) that covers the tile's tokens, so a tile holding the last
+//   40 rows of an expert moves 4 KB of tokens per k-block instead of 32 KB.
 // - MMA: M = 128, N = the tile's token count rounded up to 16 (at most 256), K = 16: one MMA
 //   per K step reads 12 KB of shared memory per 128 cycles, inside its bandwidth.
 // - TMEM: two tile buffers of 256 columns (512 total): the epilogue of one tile overlaps the
@@ -148,10 +150,21 @@ __device__ __forceinline__ bool epilogue_any(bool v) {
     return r != 0;
 }
 
+// Token box i has max(16, TOK >> i) rows; pick the smallest that holds n_tok rows.
+template <int TOK>
+__device__ __forceinline__ int token_box(int n_tok) {
+    int i = 0;
+    while (i < 3 && (TOK >> (i + 1)) >= 16 && (TOK >> (i + 1)) >= n_tok) ++i;
+    return i;
+}
+
 template <int KIND, class C>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm_swap(const __grid_constant__ CUtensorMap tmW,
-                         const __grid_constant__ CUtensorMap tmX, const SwapParams p) {
+                         const __grid_constant__ CUtensorMap tmX0,
+                         const __grid_constant__ CUtensorMap tmX1,
+                         const __grid_constant__ CUtensorMap tmX2,
+                         const __grid_constant__ CUtensorMap tmX3, const SwapParams p) {
     constexpr int kStages = C::kStages;
     constexpr int kStageBytes = C::kStageBytes;
     constexpr int kTok = C::kTok;
@@ -212,7 +225,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= TMA producer =================
         if (lane == 0) {
             tma_prefetch_desc(&tmW);
-            tma_prefetch_desc(&tmX);
+            tma_prefetch_desc(&tmX0);
+            tma_prefetch_desc(&tmX1);
+            tma_prefetch_desc(&tmX2);
+            tma_prefetch_desc(&tmX3);
             uint32_t stage = 0, phase = 0;
             uint32_t armed_phase[kStages];
             bool armed[kStages];
@@ -224,12 +240,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const Tile t = decode<KIND, kTok>(st, E, tile);
+                int n_tok = t.row_end - t.row0;
+                if (n_tok > kTok) n_tok = kTok;
+                const int bi = token_box<kTok>((n_tok + 15) & ~15);
+                const int box_rows = (kTok >> bi) < 16 ? 16 : (kTok >> bi);
+                const CUtensorMap* tmX = bi == 0 ? &tmX0 : bi == 1 ? &tmX1 : bi == 2 ? &tmX2 : &tmX3;
+                const uint32_t stage_bytes = kABytes + (uint32_t)box_rows * kTileK * 2;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(&st.empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&st.full[stage], kStageBytes);
+                    mbar_arrive_expect_tx(&st.full[stage], stage_bytes);
                     armed[stage] = true;
                     armed_phase[stage] = phase;
                     const uint32_t a_dst = smem_u32(smem + (size_t)stage * kStageBytes);
@@ -248,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(a_dst + kWBlock, &tmW, &st.full[stage],
                                     (KIND == kGateUp) ? p.N + t.n0 : t.n0 + 64, kc, t.e);
                     }
-                    tma_load_2d(a_dst + kABytes, &tmX, &st.full[stage], kc, t.row0);
+                    tma_load_2d(a_dst + kABytes, tmX, &st.full[stage], kc, t.row0);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
@@ -425,15 +447,22 @@ cudaError_t launch_swap_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     const cuuint32_t w_box[3] = {64, kTileK, 1};
     const cuuint64_t x_dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.R};
     const cuuint64_t x_str[1] = {(cuuint64_t)a.K * 2};
-    const cuuint32_t x_box[2] = {kTileK, kTok};
+    CUtensorMap tmX1, tmX2, tmX3;
     const PackedGeom g = packed_geom(KIND, a.K, a.N);
     const cuuint64_t pk_dims[3] = {64, (cuuint64_t)g.kpad, (cuuint64_t)groups * g.nb};
     const cuuint64_t pk_str[2] = {128, (cuuint64_t)g.kpad * 128};
     const cuuint32_t pk_box[3] = {64, kTileK, (KIND == kGateUp) ? 1u : 2u};
     if (!(a.packed ? encode_tensor_map_bf16(&tmW, a.b, 3, pk_dims, pk_str, pk_box)
-                   : encode_tensor_map_bf16(&tmW, a.b, 3, w_dims, w_str, w_box)) ||
-        !encode_tensor_map_bf16(&tmX, a.a, 2, x_dims, x_str, x_box))
+                   : encode_tensor_map_bf16(&tmW, a.b, 3, w_dims, w_str, w_box)))
         return cudaErrorInvalidValue;
+    // token boxes of max(16, kTok >> i) rows (token_box picks one per tile)
+    CUtensorMap* xm[4] = {&tmX, &tmX1, &tmX2, &tmX3};
+    for (int i = 0; i < 4; ++i) {
+        const int rows = (kTok >> i) < 16 ? 16 : (kTok >> i);
+        const cuuint32_t x_box[2] = {kTileK, (cuuint32_t)rows};
+        if (!encode_tensor_map_bf16(xm[i], a.a, 2, x_dims, x_str, x_box))
+            return cudaErrorInvalidValue;
+    }
 
     SwapParams p;
     p.offsets = a.offsets;
@@ -458,7 +487,8 @@ cudaError_t launch_swap_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     int grid = device_sm_count();
     if (tiles_ub < grid) grid = (int)tiles_ub;
     if (grid < 1) grid = 1;
-    return launch_kernel(tc_grouped_gemm_swap<KIND, C>, dim3(grid), dim3(kThreads), kSmemBytes, s, tmW, tmX, p);
+    return launch_kernel(tc_grouped_gemm_swap<KIND, C>, dim3(grid), dim3(kThreads), kSmemBytes, s,
+                         tmW, tmX, tmX1, tmX2, tmX3, p);
 }
 
 }  // namespace
@@ -474,11 +504,23 @@ cudaError_t launch_grouped_gemm_bf16_swap(const GroupedGemmArgs& a, cudaStream_t
 // Large batches: gate_up runs on the 128-row kernel, where each epilogue thread holds gate and
 // up of its h columns (this kernel's gate_up passes the up half between warps and leaves the
 // SiLU work to two of the four epilogue warps, which measured slower on every prefill
-// workload); down runs here, padding each expert to 16 rows instead of 128 (measured faster
-// everywhere). Small batches (at most kSmallBatchRows routed rows): both run here with 32-token
+// workload). Small batches (at most kSmallBatchRows routed rows): both run here with 32-token
 // tiles, which stream weights without fetching 128- or 256-row token tiles.
+// CTA pairs (256-row tiles, 32 KB stages, six of them in flight) take
+//   - down when the experts average at least 512 rows, where 256-row tiles pad little
+//     (measured faster than 16-row padding here on Mixtral, Scout and the shared expert, equal
+//     at 256 rows per expert);
+//   - gate_up of a single dense group (the shared expert) of at least 512 rows. Routed gate_up
+//     measured slightly faster on the 128-row kernel.
+// Everything else (down of experts with fewer rows) runs here, padding each expert to 16 rows.
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
-    if (a.kind == kGateUp && a.R > kSmallBatchRows) return launch_grouped_gemm_bf16_rows(a, s);
+    const int groups = a.offsets ? a.E : 1;
+    if (a.kind == kGateUp && a.R > kSmallBatchRows) {
+        if (groups == 1) return launch_grouped_gemm_bf16_2sm(a, s);
+        return launch_grouped_gemm_bf16_rows(a, s);
+    }
+    if (a.kind == kDown && a.R > kSmallBatchRows && (long long)a.R >= 512ll * groups)
+        return launch_grouped_gemm_bf16_2sm(a, s);
     return launch_grouped_gemm_bf16_swap(a, s);
 }
 

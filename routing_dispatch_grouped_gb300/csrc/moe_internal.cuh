@@ -296,6 +296,8 @@ constexpr int kSmallBatchRows = 512;
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmArgs& a, cudaStream_t s);
 // tokens as the MMA M side (128-row tiles; gemm_tc.cu)
 cudaError_t launch_grouped_gemm_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
+// 256-row tiles on CTA pairs with tcgen05.mma.cta_group::2 (gemm_tc_2sm.cu)
+cudaError_t launch_grouped_gemm_bf16_2sm(const GroupedGemmArgs& a, cudaStream_t s);
 // weights as the MMA M side, tokens as N (tiles padded to 16 tokens; gemm_tc_swap.cu)
 cudaError_t launch_grouped_gemm_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s);
 // 2D/3D bf16 tensor map with 128-byte swizzle and zero fill outside the tensor.

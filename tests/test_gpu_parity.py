@@ -209,6 +209,7 @@ GEMM_SHAPES = [
     ([300], 200, 200),                  # K and N not multiples of 64 (TMA zero fill, masks)
     ([64] * 16 + [0] * 4, 512, 768),    # many groups
     ([1000, 24], 1024, 1024),           # several M tiles and N tiles per expert
+    ([700, 600], 384, 200),             # >= 512 rows per expert: down on CTA pairs, ragged K/N
 ]
 
 
@@ -246,8 +247,9 @@ def test_grouped_gemm_matches_oracle(dtype, shape):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_grouped_gemm_row_scale_and_weight(dtype):
-    counts, d, I = [100, 200, 1], 256, 256
+@pytest.mark.parametrize("counts", [[100, 200, 1], [900, 700], [1100]])
+def test_grouped_gemm_row_scale_and_weight(dtype, counts):
+    d, I = 256, 256
     offsets, xs, wgu, wd = _gemm_case(counts, d, I, dtype, seed=9)
     R = xs.shape[0]
     off_t = torch.from_numpy(offsets.astype(np.int32)).to(DEV)
@@ -265,9 +267,10 @@ def test_grouped_gemm_row_scale_and_weight(dtype):
     assert err_rms(f64(y2), y_ref2) <= TOL[dtype]
 
 
-def test_single_group_without_offsets():
-    """offsets NULL: one expert owning every row (the always-on shared expert's form)."""
-    R, d, I = 333, 384, 512
+@pytest.mark.parametrize("R,d,I", [(333, 384, 512), (1100, 384, 200), (2049, 512, 640)])
+def test_single_group_without_offsets(R, d, I):
+    """offsets NULL: one expert owning every row (the always-on shared expert's form). Above 512
+    rows both GEMMs run on CTA pairs; the 200-column case leaves a ragged h tile."""
     xs = synth.normal((R, d), torch.bfloat16, 4, "sx", 1.0, device=DEV)
     wgu = synth.normal((1, d, 2 * I), torch.bfloat16, 4, "swgu", 0.05, device=DEV)
     wd = synth.normal((1, I, d), torch.bfloat16, 4, "swd", 0.05, device=DEV)
@@ -275,6 +278,12 @@ def test_single_group_without_offsets():
     y = moe.moe_down(h, None, wd)
     ref = o.swiglu_ffn(f64(xs), f64(wgu[0]), f64(wd[0]), True)
     assert err_rms(f64(y), ref) <= TOL[torch.bfloat16]
+    # the same single group through explicit offsets and through packed weights
+    off_t = torch.tensor([0, R], dtype=torch.int32, device=DEV)
+    h2 = moe.moe_gate_up(xs, off_t, moe.pack_weights(wgu, moe.W_GATE_UP))
+    y2 = moe.moe_down(h2, off_t, moe.pack_weights(wd, moe.W_DOWN))
+    assert torch.equal(h2, h)
+    assert torch.equal(y2, y)
 
 
 # ------------------------------------------------------------------------------------------------
