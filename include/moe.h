@@ -257,6 +257,13 @@ moe_status moe_combine(const float* y_sorted, const int32_t* slot_to_sorted,
  *   each other) | MOE_WEIGHTS_PACKED (all expert weights, shared ones included, packed).
  *   workspace: at least moe_forward_workspace_size(...) bytes, 256-byte aligned. Holds counts,
  *   offsets, both permutations, x_sorted, h, y_sorted and the shared expert's h and y.
+ *   Decode batches (bf16, no shared expert, T <= 16, T*k <= 256) run the whole layer as one
+ *   cooperative kernel that routes in every block and streams the touched experts' weights
+ *   through every SM. It leaves topk_ids/topk_weights, counts, offsets, both permutations and
+ *   h as above but writes neither x_sorted nor y_sorted (the combine is folded into the down
+ *   step); its counters follow the status word and its partial sums take a region at the end
+ *   of the workspace (both included in moe_forward_workspace_size). MOE_FUSE_COMBINE_WEIGHT
+ *   changes nothing there.
  */
 moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, int d, int E,
                        int k, int I, moe_score_fn score_fn, unsigned flags, const void* w_gate_up,
@@ -268,9 +275,10 @@ size_t moe_forward_workspace_size(int T, int d, int E, int k, int I, int Is, moe
 /*
  * Number of kernels moe_forward enqueues for these sizes (dispatch, experts and combine
  * kernels included; the status-word clear is a memset, not counted). 0 for T == 0. Batches
- * with T*k <= 1024 route and build the dispatch indices in one fused launch.
+ * with T*k <= 1024 route and build the dispatch indices in one fused launch; decode batches
+ * (see moe_forward) run one kernel in all.
  */
-int moe_forward_kernel_count(int T, int k, int Is);
+int moe_forward_kernel_count(moe_dtype dt, int T, int k, int Is);
 
 /*
  * moe_read_device_status - synchronise `stream`, then return the status word the kernels of

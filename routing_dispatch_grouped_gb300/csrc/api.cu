@@ -56,7 +56,7 @@ moe_status launch_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 constexpr long long kMaxRowsF32 = 60000ll * 32;
 
 struct ForwardLayout {
-    size_t counts, offsets, chunk, s2p, p2s, x_sorted, h, y, h_sh, y_sh, total;
+    size_t fcnt, counts, offsets, chunk, s2p, p2s, x_sorted, h, y, h_sh, y_sh, fused, total;
 };
 
 ForwardLayout forward_layout(int T, int d, int E, int k, int I, int Is, moe_dtype dt) {
@@ -68,6 +68,11 @@ ForwardLayout forward_layout(int T, int d, int E, int k, int I, int Is, moe_dtyp
         o = round_up(o + bytes, 256);
         return at;
     };
+    // the fused decode kernel's counters follow the status word (one memset clears both);
+    // its partial sums go last
+    const bool fused = decode_fused_applies(dt, T, k, Is);
+    const DecodeFusedLayout F = decode_fused_layout(T, d, k, I);
+    L.fcnt = take(fused ? F.counter_bytes : 0);
     L.counts = take((size_t)E * 4);
     L.offsets = take((size_t)(E + 1) * 4);
     L.chunk = take(dispatch_scratch_bytes((int)R, E));
@@ -78,6 +83,7 @@ ForwardLayout forward_layout(int T, int d, int E, int k, int I, int Is, moe_dtyp
     L.y = take(R * (size_t)d * 4);
     L.h_sh = take(Is > 0 ? (size_t)T * Is * b : 0);
     L.y_sh = take(Is > 0 ? (size_t)T * d * 4 : 0);
+    L.fused = take(fused ? F.part_bytes : 0);
     L.total = o;
     return L;
 }
@@ -307,8 +313,9 @@ size_t moe_forward_workspace_size(int T, int d, int E, int k, int I, int Is, moe
     return forward_layout(T, d, E, k, I, Is, dt).total;
 }
 
-int moe_forward_kernel_count(int T, int k, int Is) {
+int moe_forward_kernel_count(moe_dtype dt, int T, int k, int Is) {
     if (T <= 0 || k <= 0) return 0;
+    if (decode_fused_applies(dt, T, k, Is)) return 1;
     const bool small = (long long)T * k <= kSmallDispatchMaxSlots;
     const int front = small ? 2 : 1 + dispatch_kernel_count(true);
     return front + 2 + (Is > 0 ? 2 : 0) + 1;
@@ -363,10 +370,40 @@ moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, 
     float* y_sh = reinterpret_cast<float*>(ws + L.y_sh);
     const int R = T * k;
 
-    if ((st = clear_status(workspace, s)) != MOE_OK) return st;
     const bool renorm = (flags & MOE_RENORMALIZE) != 0;
-    // The first kernel follows the caller's work in plain stream order; every later kernel of
-    // the chain may start early and waits for its predecessor itself (griddep_wait).
+    if (decode_fused_applies(dt, T, k, Is)) {
+        // decode: the whole layer in one cooperative kernel; its counters sit right after the
+        // status word and are cleared with it
+        if ((st = launch_status(cudaMemsetAsync(workspace, 0, L.counts, s))) != MOE_OK)
+            return st;
+        DecodeFusedArgs a;
+        a.x = x;
+        a.logits = logits;
+        a.w_gate_up = w_gate_up;
+        a.w_down = w_down;
+        a.packed = packed;
+        a.score_fn = (int)score_fn;
+        a.renorm = renorm;
+        a.scale_input = scale;
+        a.T = T;
+        a.d = d;
+        a.E = E;
+        a.k = k;
+        a.I = I;
+        a.topk_ids = topk_ids;
+        a.topk_weights = topk_weights;
+        a.counts = counts;
+        a.offsets = offsets;
+        a.sorted_to_slot = s2p;
+        a.slot_to_sorted = p2s;
+        a.h = h;
+        a.out = out;
+        a.counters = reinterpret_cast<int*>(ws + L.fcnt);
+        a.partials = ws + L.fused;
+        a.status = status;
+        return launch_status(launch_decode_fused(a, s));
+    }
+    if ((st = clear_status(workspace, s)) != MOE_OK) return st;
     if (R <= kSmallDispatchMaxSlots) {
         // few tokens: route and the dispatch indices in one launch, then the row copy
         if ((st = launch_status(launch_route_dispatch_small(logits, T, E, k, (int)score_fn,

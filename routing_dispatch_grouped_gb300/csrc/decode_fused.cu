@@ -1,0 +1,996 @@
+// Fused decode layer: router top-k, dispatch, gate_up + SwiGLU, down and the weighted combine
+// for a handful of tokens in one persistent kernel.
+//
+// Same definitions as the multi-kernel path (Expert parallelism page, "Adding an
+// implementation": the router returns top_k_index and top_k_weights, each expert runs on the
+// rows routed to it and the outputs are combined with the routing weights; "Token dispatch":
+// rows of an expert in ascending slot order; Tensor parallelism page, "Packed strategies":
+// gate_up [E, d, 2I] with the gate half first), organised for decode (Expert parallelism page,
+// "Choosing an implementation": a decode step must need no host synchronisation and be
+// graph-capturable). With at most 16 tokens every weight element meets at most 16 rows: the
+// layer is a stream of the touched experts' weights, and its cost is keeping every SM's memory
+// pipe full and the few dependent steps short.
+//
+// Every block first routes all tokens and builds the dispatch indices in shared memory (the
+// same warp router and counting sort as the stand-alone kernels, so the ids and the order
+// agree bit for bit); block 0 also writes them out. Then:
+// Work items are 32 KB weight chunks:
+//   gate_up item (q, jb, kc): K rows [128 kc, 128 kc + 128) of gate columns [64 jb, 64 jb + 64)
+//     of the q-th touched expert and the same rows of the matching up columns. Items are
+//     ordered (q, jb, kc); a group (q, jb) is one 64-column block of h.
+//   down item (c, q, kc): K rows [256 kc, 256 kc + 256) of output columns [64 c, 64 c + 64) of
+//     expert q. Items are ordered (c, q, kc); a group c is one 64-column block of the output.
+// Each list is split into G equal contiguous ranges (one per block, "stream-K"), so every SM
+// streams the same number of bytes. A producer warp streams a block's gate_up range and then
+// its down range through a 6-stage TMA ring; consumer warp w owns stage w and multiplies each
+// of its items alone with warp-level mma.sync (m16n8k16, bf16 in, fp32 accumulate: the weights
+// are the M side, read with ldmatrix.trans from the TMA tile, the at most 16 rows the N side),
+// so six items are in flight per SM and no barrier is taken per item. The layer is bound by
+// HBM, not by the tensor pipe: the MMAs only keep each warp's work per 32 KB item small. At
+// the end of a group the consumer warps hand their register sums to an epilogue warp through
+// a shared-memory buffer (an mbarrier pair) and go on streaming; the epilogue warp adds them
+// up and does everything that follows:
+//   - gate_up: a block that covers a whole group applies SwiGLU (and the router scale when it
+//     applies to the input) to its register sums, rounds h to bf16 and stores it. A group
+//     split between blocks leaves one fp32 partial per block; the last of them to arrive (a
+//     per-group counter) sums the partials in block order and stores h. Either way the writer
+//     then raises the group's h flag.
+//   - down: a consumer warp waits (bounded) until every h block of its expert is flagged and
+//     loads h; the epilogue warp adds weight * y of the expert's rows into a per-token
+//     accumulator in shared memory (the combine: an expert appears at most once per token).
+//     At the end of an output block it either writes bf16 out (sole contributor) or leaves
+//     the block's per-token partial; the last contributor sums them in block order, one
+//     rounding.
+// While a block waits, its producer keeps streaming down weights. The launch is cooperative,
+// so every block is resident and the waits end. Every sum runs in an order fixed by the sizes
+// alone: results do not depend on timing. The counters are zeroed by the caller's memset of
+// the workspace head that precedes the launch.
+#include <mutex>
+
+#include "route_warp.cuh"
+
+namespace rdg {
+namespace {
+
+constexpr int kStages = 6;
+constexpr int kConsumerWarps = kStages;         // warp w consumes the items of stage w
+constexpr int kProducerWarp = kConsumerWarps;  // streams the weights
+constexpr int kEpilogueWarp = kConsumerWarps + 1;  // reductions, h, combine
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kWarps = kThreads / 32;
+constexpr int kKcA = 128;                       // K rows of a gate_up item (two boxes)
+constexpr int kKcB = 256;                       // K rows of a down item (one box)
+constexpr int kBoxBytesA = 64 * kKcA * 2;       // 16 KB
+constexpr int kStageBytes = 64 * kKcB * 2;      // 32 KB
+constexpr int kPass = 8;                        // rows per MMA n-tile and reduction pass
+constexpr int kStrideA = 132;                   // reduction row strides (padded: no bank
+constexpr int kStrideB = 68;                    // conflicts on the fragment-layout stores)
+constexpr int kRedFloats = kConsumerWarps * kPass * kStrideA;  // [6][8][132] >= [6][8][68]
+constexpr int kOutFloats = kDecodeFusedMaxTokens * 64;         // per-token output accumulator
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr int kDecodeWaves = 1;                 // expert waves (gate_up of wave w + 1 hides the
+                                                // finishing of wave w's h)
+
+constexpr size_t kOffRed = (size_t)kStages * kStageBytes;
+constexpr size_t kOffOut = kOffRed + kRedFloats * 4;
+constexpr size_t kOffLists = kOffOut + kOutFloats * 4;
+constexpr size_t kListInts = 3 * kMaxE + 2 * kDecodeFusedMaxRows;
+constexpr size_t kOffBars = kOffLists + kListInts * 4;
+constexpr size_t kSmemBytes = kOffBars + (2 * kStages + 2) * 8 + 64 + 1024;  // + align slack
+static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a block may use");
+
+struct Params {
+    const __nv_bfloat16* x;  // [T, d]
+    const float* logits;     // [T, E]
+    int32_t* topk_ids;       // [T, k] out
+    float* topk_w;           // [T, k] out
+    int32_t* counts;         // [E] out
+    int32_t* offsets;        // [E + 1] out
+    int32_t* s2p;            // [R] out: sorted row -> slot t*k + j
+    int32_t* p2s;            // [R] out: slot -> sorted row
+    __nv_bfloat16* h;        // [R, I] out
+    __nv_bfloat16* out;      // [T, d] out
+    float* part_a;           // [G + groups_a][T][128] gate/up partials
+    float* part_b;           // [G + nbd][T][64] per-token partials of split output blocks
+    int* cnt_a;              // [R * nbh] contributors arrived, per h block
+    int* hflag;              // [R * nbh] h block stored
+    int* cnt_b;              // [nbd] per output block
+    int* status;
+    int T, d, E, k, I, R;
+    int score_fn, renorm;
+    int nbh, nka, nbd, nkb;
+    int scale_input, packed;
+    int gu_nb, dn_nb;        // packed blocks per expert (gate_up, down)
+};
+
+// What a block's consumers share.
+struct Ctx {
+    uint32_t stage0;         // shared address of stage 0
+    float* red;              // cross-warp reduction buffer
+    float* outacc;           // [T][64] per-token output accumulator
+    const int* s_off;        // touched expert q -> first sorted row
+    const int* s_tq;         // -> row count
+    const int* s_tok;        // sorted row -> token
+    const float* s_w;        // sorted row -> routing weight
+    uint64_t* full;
+    uint64_t* empty;
+    uint64_t* red_full;      // the consumer warps have written a dump
+    uint64_t* red_empty;     // the epilogue warp has read it
+    volatile int* flags;     // [0] something timed out
+    int warp, lane, G;
+    int nA;                  // gate_up items of the current wave
+    int slot_off;            // partial slot offset of the current wave (see the schedule)
+    int W, nq;               // waves, touched experts
+    int ready_q;             // touched expert whose h this warp has seen complete (-1: none)
+    int dumps;               // hand-overs so far
+};
+
+__device__ __forceinline__ int ld_acquire(const int* ptr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
+// First item of block b's range when n items are split into G ranges, and the block whose
+// range holds item u.
+__device__ __forceinline__ int range_lo(int n, int b, int G) {
+    return (int)((long long)n * b / G);
+}
+__device__ __forceinline__ int block_of(int n, int u, int G) {
+    return (int)(((long long)(u + 1) * G - 1) / n);
+}
+// With fewer items than blocks some ranges are empty; such blocks take part in no group.
+__device__ __forceinline__ bool range_empty(int n, int b, int G) {
+    return n < G && range_lo(n, b, G) == range_lo(n, b + 1, G);
+}
+__device__ __forceinline__ int contributors(int n, int G, int b_first, int b_last) {
+    if (n >= G) return b_last - b_first + 1;
+    int m = 0;
+    for (int b = b_first; b <= b_last; ++b) m += range_empty(n, b, G) ? 0 : 1;
+    return m;
+}
+
+// One m16n8k16 step: the A fragment of columns [m0, m0 + 16) x K rows [k0, k0 + 16) of a
+// 128-byte-swizzled [k][64 column] box, read with ldmatrix.trans (lanes 0-7 address rows
+// k0..k0+7 at columns m0.. -> a0, lanes 8-15 columns m0+8.. -> a1, lanes 16-23 rows k0+8.. ->
+// a2, lanes 24-31 both -> a3; PTX ISA, "Matrix fragments for mma.m16n8k16"), times NTILE B
+// fragments (8 rows each), accumulated into acc[n] (C: m = l/4 [+8], n = 2 (l%4) [+1]).
+template <int NTILE>
+__device__ __forceinline__ void mma_step(uint32_t box, int k0, int m0, int lane,
+                                         const uint32_t (&b)[NTILE][2], float (&acc)[NTILE][4]) {
+    const int k = k0 + (lane & 7) + ((lane >> 4) << 3);
+    const int chunk = (m0 >> 3) + ((lane >> 3) & 1);
+    const uint32_t addr = box + (uint32_t)k * 128 + (uint32_t)((chunk ^ (k & 7)) << 4);
+    uint32_t a0, a1, a2, a3;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                 : "r"(addr));
+#pragma unroll
+    for (int n = 0; n < NTILE; ++n) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(acc[n][0]), "+f"(acc[n][1]), "+f"(acc[n][2]), "+f"(acc[n][3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b[n][0]), "r"(b[n][1]));
+    }
+}
+
+// B fragments of the gate_up step for K rows [k0, k0 + 16): lane l holds row 8 n + l/4 of the
+// group (rows[n] points at that token's x row; null past the group's rows), K pairs
+// k0 + 2 (l%4) and k0 + 8 + 2 (l%4). K past d is zero.
+template <int NTILE>
+__device__ __forceinline__ void load_b_x(const unsigned int* const (&rows)[NTILE], int k0, int d,
+                                         int lane, uint32_t (&b)[NTILE][2]) {
+#pragma unroll
+    for (int n = 0; n < NTILE; ++n) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int kk = k0 + 8 * h + 2 * (lane & 3);
+            b[n][h] = (rows[n] != nullptr && kk < d) ? __ldg(rows[n] + kk / 2) : 0u;
+        }
+    }
+}
+
+// B fragments of the down step for K rows [k0, k0 + 16) (h columns): like load_b_x, from the
+// expert's h rows, which other blocks stored in this launch (read through L2).
+template <int NTILE>
+__device__ __forceinline__ void load_b_h(const unsigned int* const (&rows)[NTILE], int k0, int I,
+                                         int lane, uint32_t (&b)[NTILE][2]) {
+#pragma unroll
+    for (int n = 0; n < NTILE; ++n) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int kk = k0 + 8 * h + 2 * (lane & 3);
+            b[n][h] = (rows[n] != nullptr && kk < I) ? __ldcg(rows[n] + kk / 2) : 0u;
+        }
+    }
+}
+
+// Wait for the stage of block-local item i (warp i % kStages owns it).
+__device__ __forceinline__ bool take_stage(Ctx& c, const Params& p, int i) {
+    const bool ok = mbar_wait(&c.full[c.warp], (uint32_t)(i / kStages) & 1u, c.flags,
+                              kWaitLimitNs);
+    if (!ok) {
+        set_status(p.status, MOE_ERR_TIMEOUT);
+        c.flags[0] = 1;
+    }
+    return ok;
+}
+__device__ __forceinline__ void release_stage(Ctx& c) {
+    __syncwarp();
+    if (c.lane == 0) mbar_arrive(&c.empty[c.warp]);
+}
+
+// gate_up item in this warp's stage: 128 K rows x (64 gate + 64 up) columns; acc[mt], m-tiles
+// 0-3 gate, 4-7 up. The item's B fragments are all loaded before the first MMA.
+template <int NTILE>
+__device__ __forceinline__ void item_a(Ctx& c, const Params& p, int i, int kc,
+                                       const unsigned int* const (&rows)[NTILE],
+                                       float (&acc)[8][NTILE][4]) {
+    const uint32_t stage = c.stage0 + (uint32_t)c.warp * kStageBytes;
+    uint32_t b[kKcA / 16][NTILE][2];
+#pragma unroll
+    for (int ks = 0; ks < kKcA / 16; ++ks)
+        load_b_x<NTILE>(rows, kc * kKcA + 16 * ks, p.d, c.lane, b[ks]);
+    if (take_stage(c, p, i)) {
+#pragma unroll
+        for (int ks = 0; ks < kKcA / 16; ++ks)
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt)
+                mma_step<NTILE>(stage + (uint32_t)(mt >> 2) * kBoxBytesA, 16 * ks,
+                                16 * (mt & 3), c.lane, b[ks], acc[mt]);
+    }
+    release_stage(c);
+}
+
+// down item in this warp's stage: 256 K rows x 64 output columns; acc[mt], m-tiles of 16
+// columns. All B fragments are loaded before the first MMA.
+template <int NTILE>
+__device__ __forceinline__ void item_b(Ctx& c, const Params& p, int i, int kc,
+                                       const unsigned int* const (&rows)[NTILE],
+                                       float (&acc)[4][NTILE][4]) {
+    const uint32_t stage = c.stage0 + (uint32_t)c.warp * kStageBytes;
+    uint32_t b[kKcB / 16][NTILE][2];
+#pragma unroll
+    for (int ks = 0; ks < kKcB / 16; ++ks)
+        load_b_h<NTILE>(rows, kc * kKcB + 16 * ks, p.I, c.lane, b[ks]);
+    if (take_stage(c, p, i)) {
+#pragma unroll
+        for (int ks = 0; ks < kKcB / 16; ++ks)
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt)
+                mma_step<NTILE>(stage, 16 * ks, 16 * mt, c.lane, b[ks], acc[mt]);
+    }
+    release_stage(c);
+}
+
+__device__ __forceinline__ void store_h(const Params& p, const Ctx& c, int row, int hc, float g,
+                                        float u) {
+    const float s = p.scale_input ? c.s_w[row] : 1.0f;
+    p.h[(size_t)row * p.I + hc] = __float2bfloat16_rn(silu(g * s) * (u * s));
+}
+
+// First item of [i0, ...) that warp w owns (item i belongs to warp i % kStages).
+__device__ __forceinline__ int first_owned(int i0, int w) {
+    return i0 + ((w - i0 % kStages) + kStages) % kStages;
+}
+
+// ---- hand-over of register sums from the consumer warps to the epilogue warp: one
+// reduction buffer and an mbarrier pair (red_full: the six consumer warps have written dump d;
+// red_empty: the epilogue warp has read it)
+__device__ __forceinline__ void dump_begin(Ctx& c, const Params& p) {
+    if (!mbar_wait(c.red_empty, ((uint32_t)c.dumps & 1u) ^ 1u, c.flags, kWaitLimitNs)) {
+        set_status(p.status, MOE_ERR_TIMEOUT);
+        c.flags[0] = 1;
+    }
+}
+__device__ __forceinline__ void dump_end(Ctx& c) {
+    __syncwarp();
+    if (c.lane == 0) mbar_arrive(c.red_full);
+    ++c.dumps;
+}
+__device__ __forceinline__ void epi_take(Ctx& c, const Params& p) {
+    if (!mbar_wait(c.red_full, (uint32_t)c.dumps & 1u, c.flags, kWaitLimitNs)) {
+        set_status(p.status, MOE_ERR_TIMEOUT);
+        c.flags[0] = 1;
+    }
+}
+__device__ __forceinline__ void epi_give(Ctx& c) {
+    __syncwarp();
+    if (c.lane == 0) mbar_arrive(c.red_empty);
+    ++c.dumps;
+}
+
+// Bump a group counter after this warp's partial stores; true for the last contributor.
+__device__ __forceinline__ bool epi_arrive_last(const Ctx& c, int* counter, int contributors) {
+    __syncwarp();
+    int prev = 0;
+    if (c.lane == 0)  // releases this warp's partial stores, acquires the others'
+        asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;"
+                     : "=r"(prev)
+                     : "l"(counter)
+                     : "memory");
+    prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+    return prev == contributors - 1;
+}
+
+// ================= consumer side =================
+
+// gate_up group (q, jb) of this block: block-local items [i0, i0 + kc1 - kc0) = K chunks
+// [kc0, kc1); then its register sums go to the epilogue warp, 8 rows per dump, as
+// red[warp][row][column] (columns 0-63 gate, 64-127 up).
+template <int NTILE>
+__device__ void group_a(Ctx& c, const Params& p, int q, int i0, int kc0, int kc1) {
+    const int row0 = c.s_off[q], tq = c.s_tq[q];
+    const unsigned int* rows[NTILE];
+#pragma unroll
+    for (int n = 0; n < NTILE; ++n) {
+        const int r = 8 * n + (c.lane >> 2);
+        rows[n] = r < tq ? reinterpret_cast<const unsigned int*>(
+                               p.x + (size_t)c.s_tok[row0 + r] * p.d)
+                         : nullptr;
+    }
+    float acc[8][NTILE][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int n = 0; n < NTILE; ++n)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[mt][n][j] = 0.0f;
+    for (int i = first_owned(i0, c.warp); i < i0 + (kc1 - kc0); i += kStages)
+        item_a<NTILE>(c, p, i, kc0 + (i - i0), rows, acc);
+#pragma unroll
+    for (int pass = 0; pass < NTILE; ++pass) {
+        if (pass * kPass < tq) {
+            dump_begin(c, p);
+            float* rd = c.red + (c.warp * kPass + 2 * (c.lane & 3)) * kStrideA + (c.lane >> 2);
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                rd[16 * mt] = acc[mt][pass][0];
+                rd[kStrideA + 16 * mt] = acc[mt][pass][1];
+                rd[16 * mt + 8] = acc[mt][pass][2];
+                rd[kStrideA + 16 * mt + 8] = acc[mt][pass][3];
+            }
+            dump_end(c);
+        }
+    }
+}
+
+// Down items of expert q for one output block: block-local items [i0, i0 + kc1 - kc0) = K
+// chunks [kc0, kc1); then the register sums go to the epilogue warp as red[warp][row][column].
+template <int NTILE>
+__device__ void group_b(Ctx& c, const Params& p, int q, int i0, int kc0, int kc1) {
+    const int row0 = c.s_off[q], tq = c.s_tq[q];
+    const unsigned int* rows[NTILE];
+#pragma unroll
+    for (int n = 0; n < NTILE; ++n) {
+        const int r = 8 * n + (c.lane >> 2);
+        rows[n] = r < tq ? reinterpret_cast<const unsigned int*>(p.h + (size_t)(row0 + r) * p.I)
+                         : nullptr;
+    }
+    float acc[4][NTILE][4];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int n = 0; n < NTILE; ++n)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[mt][n][j] = 0.0f;
+    for (int i = first_owned(i0, c.warp); i < i0 + (kc1 - kc0); i += kStages) {
+        if (c.ready_q != q) {
+            // every h block of the expert must be stored (bounded wait; the launch is
+            // cooperative); lane j watches block j, j + 32, ...
+            for (int jb = c.lane; jb < p.nbh; jb += 32) {
+                const uint64_t t0 = globaltimer_ns();
+                while (ld_acquire(p.hflag + q * p.nbh + jb) == 0) {
+                    if (c.flags[0] || globaltimer_ns() - t0 > kWaitLimitNs) {
+                        set_status(p.status, MOE_ERR_TIMEOUT);
+                        c.flags[0] = 1;
+                        break;
+                    }
+                }
+            }
+            __syncwarp();
+            c.ready_q = q;
+        }
+        item_b<NTILE>(c, p, i, kc0 + (i - i0), rows, acc);
+    }
+#pragma unroll
+    for (int pass = 0; pass < NTILE; ++pass) {
+        if (pass * kPass < tq) {
+            dump_begin(c, p);
+            float* rd = c.red + (c.warp * kPass + 2 * (c.lane & 3)) * kStrideB + (c.lane >> 2);
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                rd[16 * mt] = acc[mt][pass][0];
+                rd[kStrideB + 16 * mt] = acc[mt][pass][1];
+                rd[16 * mt + 8] = acc[mt][pass][2];
+                rd[kStrideB + 16 * mt + 8] = acc[mt][pass][3];
+            }
+            dump_end(c);
+        }
+    }
+}
+
+// ================= epilogue side (one warp) =================
+
+// h of group g (rows of expert q at row0, h block jb) from the partials of its contributors,
+// summed in block order: per output of this lane, the loads of up to 8 contributors are issued
+// together before any of them is added.
+__device__ void epi_finish_h(const Ctx& c, const Params& p, int row0, int tq, int jb, int g,
+                             int b_first, int b_last) {
+    constexpr int kBatch = 8;
+    const int n = tq * 64;
+    for (int o = c.lane; o < n; o += 32) {
+        const int t = o >> 6, col = o & 63;
+        float gs = 0.0f, us = 0.0f;
+        for (int b0 = b_first; b0 <= b_last; b0 += kBatch) {
+            float gv[kBatch], uv[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                const int b = b0 + j;
+                gv[j] = uv[j] = 0.0f;
+                if (b <= b_last && !range_empty(c.nA, b, c.G)) {
+                    const float* src =
+                        p.part_a + ((size_t)(b + g + c.slot_off) * p.T + t) * 128 + col;
+                    gv[j] = __ldcg(src);
+                    uv[j] = __ldcg(src + 64);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                gs += gv[j];
+                us += uv[j];
+            }
+        }
+        if (jb * 64 + col < p.I) store_h(p, c, row0 + t, jb * 64 + col, gs, us);
+    }
+}
+
+// gate_up group (q, jb) = g: take the consumers' dumps, store h (whole group) or this block's
+// partial, and flag h once stored.
+template <int NTILE>
+__device__ void epi_a(Ctx& c, const Params& p, int q, int jb, int g, int b_first, int b_last) {
+    const int row0 = c.s_off[q], tq = c.s_tq[q];
+    const bool whole = b_first == b_last;
+    float* part = p.part_a + (size_t)(blockIdx.x + g + c.slot_off) * p.T * 128;
+#pragma unroll
+    for (int pass = 0; pass < NTILE; ++pass) {
+        if (pass * kPass < tq) {
+            epi_take(c, p);
+            const int nr = min(kPass, tq - pass * kPass);
+            for (int o = c.lane; o < nr * (whole ? 64 : 128); o += 32) {
+                const int t = whole ? (o >> 6) : (o >> 7), col = whole ? (o & 63) : (o & 127);
+                float v = 0.0f, uu = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float* rr = c.red + (w * kPass + t) * kStrideA + col;
+                    v += rr[0];
+                    if (whole) uu += rr[64];
+                }
+                if (whole) {
+                    if (jb * 64 + col < p.I)
+                        store_h(p, c, row0 + pass * kPass + t, jb * 64 + col, v, uu);
+                } else {
+                    __stcg(part + (size_t)(pass * kPass + t) * 128 + col, v);
+                }
+            }
+            epi_give(c);
+        }
+    }
+    bool stored = whole;
+    if (!whole && epi_arrive_last(c, p.cnt_a + g, contributors(c.nA, c.G, b_first, b_last))) {
+        epi_finish_h(c, p, row0, tq, jb, g, b_first, b_last);
+        stored = true;
+    }
+    if (stored) {
+        __syncwarp();  // every h store of this warp is issued
+        if (c.lane == 0)
+            asm volatile("st.release.gpu.global.s32 [%0], 1;" ::"l"(p.hflag + g) : "memory");
+    }
+}
+
+// Down sub-group of expert q: take the consumers' dumps and add weight * y of the expert's
+// rows into the per-token accumulator (the combine; an expert appears once per token).
+template <int NTILE>
+__device__ void epi_b(Ctx& c, const Params& p, int q) {
+    const int row0 = c.s_off[q], tq = c.s_tq[q];
+#pragma unroll
+    for (int pass = 0; pass < NTILE; ++pass) {
+        if (pass * kPass < tq) {
+            epi_take(c, p);
+            const int nr = min(kPass, tq - pass * kPass);
+            for (int o = c.lane; o < nr * 64; o += 32) {
+                const int t = o >> 6, col = o & 63;
+                float y = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) y += c.red[(w * kPass + t) * kStrideB + col];
+                const int row = row0 + pass * kPass + t;
+                const float wgt = p.scale_input ? 1.0f : c.s_w[row];
+                c.outacc[c.s_tok[row] * 64 + col] += wgt * y;
+            }
+            epi_give(c);
+        }
+    }
+}
+
+// Down items of wave w: experts [q_lo, q_hi), ordered (c, q, kc), perC per output block.
+struct WaveB {
+    int q_lo, perC, n;
+};
+__device__ __forceinline__ WaveB wave_b(const Ctx& c, const Params& p, int w) {
+    WaveB v;
+    v.q_lo = range_lo(c.nq, w, c.W);
+    v.perC = (range_lo(c.nq, w + 1, c.W) - v.q_lo) * p.nkb;
+    v.n = p.nbd * v.perC;
+    return v;
+}
+
+// End of output block cb in this block's range of the current wave: write out (when this is
+// the block's only contributor over all waves) or leave the per-token partial; the last
+// contributor sums them, waves in order and blocks in order within a wave. Clears the
+// accumulator.
+__device__ void epi_flush(Ctx& c, const Params& p, int cb) {
+    const int dc0 = cb * 64, n = p.T * 64;
+    int total = 0;
+    for (int w = 0; w < c.W; ++w) {
+        const WaveB v = wave_b(c, p, w);
+        total += contributors(v.n, c.G, block_of(v.n, cb * v.perC, c.G),
+                              block_of(v.n, (cb + 1) * v.perC - 1, c.G));
+    }
+    __syncwarp();
+    if (total == 1) {
+        for (int o = c.lane; o < n; o += 32) {
+            const int t = o >> 6, col = o & 63;
+            if (dc0 + col < p.d)
+                p.out[(size_t)t * p.d + dc0 + col] = __float2bfloat16_rn(c.outacc[o]);
+            c.outacc[o] = 0.0f;
+        }
+    } else {
+        float* part = p.part_b + (size_t)(blockIdx.x + cb + c.slot_off) * n;
+        for (int o = c.lane; o < n; o += 32) {
+            __stcg(part + o, c.outacc[o]);
+            c.outacc[o] = 0.0f;
+        }
+        if (epi_arrive_last(c, p.cnt_b + cb, total)) {
+            constexpr int kPer = kOutFloats / 32;
+            float acc[kPer];
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) acc[i] = 0.0f;
+            for (int w = 0; w < c.W; ++w) {
+                const WaveB v = wave_b(c, p, w);
+                const int bf = block_of(v.n, cb * v.perC, c.G);
+                const int bl = block_of(v.n, (cb + 1) * v.perC - 1, c.G);
+                for (int b = bf; b <= bl; ++b) {
+                    if (range_empty(v.n, b, c.G)) continue;
+                    const float* base = p.part_b + (size_t)(b + cb + w * (c.G + p.nbd)) * n;
+#pragma unroll
+                    for (int i = 0; i < kPer; ++i) {
+                        const int o = c.lane + 32 * i;
+                        if (o < n) acc[i] += __ldcg(base + o);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kPer; ++i) {
+                const int o = c.lane + 32 * i;
+                if (o < n && dc0 + (o & 63) < p.d)
+                    p.out[(size_t)(o >> 6) * p.d + dc0 + (o & 63)] = __float2bfloat16_rn(acc[i]);
+            }
+        }
+    }
+    __syncwarp();
+}
+
+template <int N>
+struct NtTag {
+    static constexpr int value = N;
+};
+
+// Run a group with one MMA n-tile per 8 of its rows.
+template <typename F>
+__device__ __forceinline__ void by_rows(int tq, F&& f) {
+    if (tq <= kPass)
+        f(NtTag<1>{});
+    else
+        f(NtTag<2>{});
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
+                    const __grid_constant__ CUtensorMap tmD, Params p, int vpl) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    int* s_eq = reinterpret_cast<int*>(smem + kOffLists);
+    int* s_off = s_eq + kMaxE;
+    int* s_tq = s_off + kMaxE;
+    int* s_tok = s_tq + kMaxE;
+    float* s_w = reinterpret_cast<float*>(s_tok + kDecodeFusedMaxRows);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
+    uint64_t* empty = full + kStages;
+    uint64_t* red_full = empty + kStages;
+    uint64_t* red_empty = red_full + 1;
+    volatile int* flags = reinterpret_cast<volatile int*>(red_empty + 1);
+    // flags: [0] a wait timed out (every bounded wait gives up at once after that; the status
+    // word says so and the results are void), [2] number of touched experts.
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(red_full, kConsumerWarps);
+        mbar_init(red_empty, 1);
+        fence_barrier_init();
+        for (int f = 0; f < 4; ++f) flags[f] = 0;
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        tma_prefetch_desc(&tmGU);
+        tma_prefetch_desc(&tmD);
+    }
+    float* outacc = reinterpret_cast<float*>(smem + kOffOut);
+    for (int i = threadIdx.x; i < kOutFloats; i += blockDim.x) outacc[i] = 0.0f;
+    griddep_wait();
+
+    // ---- router top-k and dispatch indices, in every block (scratch in the stage buffers,
+    // which no copy uses yet). Same warp router and counting sort as the stand-alone kernels.
+    const int R = p.R, E = p.E, nch = (R + 31) / 32;
+    int* ids_s = reinterpret_cast<int*>(smem);
+    float* w_s = reinterpret_cast<float*>(ids_s + kDecodeFusedMaxRows);
+    int* rank_s = reinterpret_cast<int*>(w_s + kDecodeFusedMaxRows);
+    int* cnt_s = rank_s + kDecodeFusedMaxRows;
+    int* off_s = cnt_s + kMaxE;
+    int* chunk_s = off_s + kMaxE + 32;  // [chunk of 32 slots][E]: counts, then bases
+    for (int i = threadIdx.x; i < nch * E; i += blockDim.x) chunk_s[i] = 0;
+    for (int t = warp; t < p.T; t += kWarps) {
+        const float* row = p.logits + (size_t)t * E;
+        int id;
+        float wt;
+        switch (vpl) {
+            case 1: route_token_warp<1>(row, E, p.k, p.score_fn, p.renorm, lane, &id, &wt); break;
+            case 2: route_token_warp<2>(row, E, p.k, p.score_fn, p.renorm, lane, &id, &wt); break;
+            case 4: route_token_warp<4>(row, E, p.k, p.score_fn, p.renorm, lane, &id, &wt); break;
+            default: route_token_warp<8>(row, E, p.k, p.score_fn, p.renorm, lane, &id, &wt); break;
+        }
+        if (lane < p.k) {
+            ids_s[t * p.k + lane] = id;
+            w_s[t * p.k + lane] = wt;
+        }
+    }
+    __syncthreads();
+    for (int ch = warp; ch < nch; ch += kWarps) {
+        const int s = ch * 32 + lane;
+        const int e = s < R ? ids_s[s] : -1;
+        const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+        if (e >= 0) {
+            rank_s[s] = __popc(peers & ((1u << lane) - 1u));
+            if (lane == __ffs(peers) - 1) chunk_s[ch * E + e] = __popc(peers);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int ch = 0; ch < nch; ++ch) {
+            const int v = chunk_s[ch * E + e];
+            chunk_s[ch * E + e] = run;
+            run += v;
+        }
+        cnt_s[e] = run;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive scan of the counts, and the touched experts in ascending id order
+        const int per = (E + 31) / 32;
+        const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
+        int run = 0;
+        for (int e = e0; e < e1; ++e) run += cnt_s[e];
+        int incl = run;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        int base = incl - run;
+        for (int e = e0; e < e1; ++e) {
+            off_s[e] = base;
+            base += cnt_s[e];
+        }
+        if (lane == 31) off_s[E] = incl;
+        int nq = 0;
+        for (int eb = 0; eb < E; eb += 32) {
+            const int e = eb + lane;
+            const int cnt = e < E ? cnt_s[e] : 0;
+            const unsigned m = __ballot_sync(0xFFFFFFFFu, cnt > 0);
+            if (cnt > 0) {
+                const int q = nq + __popc(m & ((1u << lane) - 1u));
+                s_eq[q] = e;
+                s_tq[q] = cnt;
+            }
+            nq += __popc(m);
+        }
+        if (lane == 0) flags[2] = nq;
+    }
+    __syncthreads();
+    const int nq = flags[2];
+    for (int q = threadIdx.x; q < nq; q += blockDim.x) s_off[q] = off_s[s_eq[q]];
+    const bool writer = blockIdx.x == 0;
+    for (int s = threadIdx.x; s < R; s += blockDim.x) {
+        const int e = ids_s[s];
+        const int pos = off_s[e] + chunk_s[(s >> 5) * E + e] + rank_s[s];
+        s_tok[pos] = s / p.k;
+        s_w[pos] = w_s[s];
+        if (writer) {
+            p.topk_ids[s] = e;
+            p.topk_w[s] = w_s[s];
+            p.s2p[pos] = s;
+            p.p2s[s] = pos;
+        }
+    }
+    if (writer) {
+        for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+            if (e < E) p.counts[e] = cnt_s[e];
+            p.offsets[e] = off_s[e];
+        }
+    }
+    __syncthreads();  // the stage buffers are free for the copies again
+
+    // Schedule. The touched experts form W waves; every block takes its stream-K share of the
+    // gate_up items of wave 0, then of wave 1, ..., then of the down items of wave 0, 1, ...
+    // The h of wave 0 is finished while the later waves' gate_up items stream, so the down
+    // items rarely wait for it.
+    const int G = gridDim.x, b = blockIdx.x;
+    const int W = nq < kDecodeWaves ? nq : kDecodeWaves;
+    auto wave_a = [&](int w, int& q_lo, int& n) {
+        q_lo = range_lo(nq, w, W);
+        n = (range_lo(nq, w + 1, W) - q_lo) * p.nbh * p.nka;
+    };
+
+    if (warp == kProducerWarp) {
+        // ============ producer: the block's items in schedule order ============
+        if (lane == 0) {
+            const uint32_t stage0 = smem_u32(smem);
+            int i = 0;
+            bool ok = true;
+            auto next_stage = [&](uint32_t& dst, uint64_t*& bar) {
+                const int st = i % kStages;
+                const uint32_t ph = (uint32_t)(i / kStages) & 1u;
+                if (!mbar_wait(&empty[st], ph ^ 1u, flags, kWaitLimitNs)) {
+                    set_status(p.status, MOE_ERR_TIMEOUT);
+                    flags[0] = 1;
+                    return false;
+                }
+                mbar_arrive_expect_tx(&full[st], kStageBytes);
+                dst = stage0 + (uint32_t)st * kStageBytes;
+                bar = &full[st];
+                ++i;
+                return true;
+            };
+            for (int w = 0; ok && w < W; ++w) {
+                int q_lo, n;
+                wave_a(w, q_lo, n);
+                for (int u = range_lo(n, b, G); ok && u < range_lo(n, b + 1, G); ++u) {
+                    uint32_t dst;
+                    uint64_t* bar;
+                    if (!(ok = next_stage(dst, bar))) break;
+                    const int g = q_lo * p.nbh + u / p.nka, kc = u % p.nka;
+                    const int q = g / p.nbh, jb = g % p.nbh, e = s_eq[q];
+                    if (p.packed) {
+                        tma_load_3d(dst, &tmGU, bar, 0, kc * kKcA, e * p.gu_nb + jb);
+                        tma_load_3d(dst + kBoxBytesA, &tmGU, bar, 0, kc * kKcA,
+                                    e * p.gu_nb + p.nbh + jb);
+                    } else {
+                        tma_load_3d(dst, &tmGU, bar, 64 * jb, kc * kKcA, e);
+                        tma_load_3d(dst + kBoxBytesA, &tmGU, bar, p.I + 64 * jb, kc * kKcA, e);
+                    }
+                }
+            }
+            for (int w = 0; ok && w < W; ++w) {
+                const int q_lo = range_lo(nq, w, W);
+                const int perC = (range_lo(nq, w + 1, W) - q_lo) * p.nkb, n = p.nbd * perC;
+                for (int u = range_lo(n, b, G); ok && u < range_lo(n, b + 1, G); ++u) {
+                    uint32_t dst;
+                    uint64_t* bar;
+                    if (!(ok = next_stage(dst, bar))) break;
+                    const int cb = u / perC, rem = u % perC;
+                    const int e = s_eq[q_lo + rem / p.nkb], kc = rem % p.nkb;
+                    if (p.packed)
+                        tma_load_3d(dst, &tmD, bar, 0, kc * kKcB, e * p.dn_nb + cb);
+                    else
+                        tma_load_3d(dst, &tmD, bar, 64 * cb, kc * kKcB, e);
+                }
+            }
+            // leave no copy in flight: the last (up to) kStages issued items must have landed
+            for (int j = i > kStages ? i - kStages : 0; j < i; ++j)
+                mbar_wait(&full[j % kStages], (uint32_t)(j / kStages) & 1u, nullptr,
+                          kWaitLimitNs);
+        }
+        return;
+    }
+
+    Ctx c;
+    c.stage0 = smem_u32(smem);
+    c.red = reinterpret_cast<float*>(smem + kOffRed);
+    c.outacc = outacc;
+    c.s_off = s_off;
+    c.s_tq = s_tq;
+    c.s_tok = s_tok;
+    c.s_w = s_w;
+    c.full = full;
+    c.empty = empty;
+    c.red_full = red_full;
+    c.red_empty = red_empty;
+    c.flags = flags;
+    c.warp = warp;
+    c.lane = lane;
+    c.G = G;
+    c.W = W;
+    c.nq = nq;
+    c.ready_q = -1;
+    c.dumps = 0;
+    const bool epilogue = warp == kEpilogueWarp;
+
+    // consumers (warp w: the items of stage w) and the epilogue warp walk the same groups
+    int i0 = 0;  // block-local index of the next item
+    for (int w = 0; w < W; ++w) {
+        int q_lo, n;
+        wave_a(w, q_lo, n);
+        c.nA = n;
+        c.slot_off = w * G;
+        const int hi = range_lo(n, b + 1, G);
+        for (int u = range_lo(n, b, G); u < hi;) {
+            const int gl = u / p.nka, kc0 = u % p.nka;  // group within the wave, K chunk
+            const int kc1 = min(p.nka, kc0 + (hi - u));
+            const int g = q_lo * p.nbh + gl, q = g / p.nbh, jb = g % p.nbh;
+            if (epilogue) {
+                const int bf = block_of(n, gl * p.nka, G), bl = block_of(n, (gl + 1) * p.nka - 1, G);
+                by_rows(s_tq[q],
+                        [&](auto tag) { epi_a<decltype(tag)::value>(c, p, q, jb, g, bf, bl); });
+            } else {
+                by_rows(s_tq[q], [&](auto tag) {
+                    group_a<decltype(tag)::value>(c, p, q, i0, kc0, kc1);
+                });
+            }
+            u += kc1 - kc0;
+            i0 += kc1 - kc0;
+        }
+    }
+    for (int w = 0; w < W; ++w) {
+        const WaveB v = wave_b(c, p, w);
+        c.slot_off = w * (G + p.nbd);
+        const int hi = range_lo(v.n, b + 1, G);
+        for (int u = range_lo(v.n, b, G); u < hi;) {
+            const int cb = u / v.perC;
+            const int c_end = min(hi, (cb + 1) * v.perC);
+            while (u < c_end) {
+                const int rem = u % v.perC, q = v.q_lo + rem / p.nkb, kc0 = rem % p.nkb;
+                const int kc1 = min(p.nkb, kc0 + (c_end - u));
+                if (epilogue)
+                    by_rows(s_tq[q], [&](auto tag) { epi_b<decltype(tag)::value>(c, p, q); });
+                else
+                    by_rows(s_tq[q], [&](auto tag) {
+                        group_b<decltype(tag)::value>(c, p, q, i0, kc0, kc1);
+                    });
+                u += kc1 - kc0;
+                i0 += kc1 - kc0;
+            }
+            if (epilogue) epi_flush(c, p, cb);
+        }
+    }
+}
+
+}  // namespace
+
+bool decode_fused_applies(moe_dtype dt, int T, int k, int Is) {
+    return dt == MOE_BF16 && Is == 0 && T >= 1 && T <= kDecodeFusedMaxTokens &&
+           T * k <= kDecodeFusedMaxRows;
+}
+
+DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I) {
+    DecodeFusedLayout L;
+    const size_t R = (size_t)T * k;
+    L.nbh = (I + 63) / 64;
+    L.nka = (d + kKcA - 1) / kKcA;
+    L.nbd = (d + 63) / 64;
+    L.nkb = (I + kKcB - 1) / kKcB;
+    auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+    L.counter_bytes = up((2 * R * L.nbh + L.nbd) * 4);
+    // partial slots: contributor block b of group g writes slot b + g (unique: a block's groups
+    // are consecutive and the next block starts at or after its last one)
+    // (gate_up slot b + g + w G and down slot b + c + w (G + nbd) for wave w: unique across
+    // waves too, as the gate_up groups of later waves have larger g)
+    L.part_a = 0;
+    L.part_b = up(((size_t)kDecodeWaves * kDecodeFusedMaxGrid + R * L.nbh) * T * 128 * 4);
+    L.part_bytes = L.part_b + up((size_t)kDecodeWaves * (kDecodeFusedMaxGrid + L.nbd) * T *
+                                 64 * 4);
+    return L;
+}
+
+cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(decode_fused_kernel,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    const DecodeFusedLayout L = decode_fused_layout(a.T, a.d, a.k, a.I);
+    const int R = a.T * a.k;
+    CUtensorMap tmGU, tmD;
+    const cuuint32_t box_a[3] = {64, kKcA, 1}, box_b[3] = {64, kKcB, 1};
+    bool ok;
+    if (a.packed) {
+        const PackedGeom gg = packed_geom(kGateUp, a.d, a.I);
+        const PackedGeom gd = packed_geom(kDown, a.I, a.d);
+        const cuuint64_t gu_dims[3] = {64, (cuuint64_t)gg.kpad, (cuuint64_t)a.E * gg.nb};
+        const cuuint64_t gu_str[2] = {128, (cuuint64_t)gg.kpad * 128};
+        const cuuint64_t dn_dims[3] = {64, (cuuint64_t)gd.kpad, (cuuint64_t)a.E * gd.nb};
+        const cuuint64_t dn_str[2] = {128, (cuuint64_t)gd.kpad * 128};
+        ok = encode_tensor_map_bf16(&tmGU, a.w_gate_up, 3, gu_dims, gu_str, box_a) &&
+             encode_tensor_map_bf16(&tmD, a.w_down, 3, dn_dims, dn_str, box_b);
+    } else {
+        const cuuint64_t gu_dims[3] = {2 * (cuuint64_t)a.I, (cuuint64_t)a.d, (cuuint64_t)a.E};
+        const cuuint64_t gu_str[2] = {4 * (cuuint64_t)a.I, 4 * (cuuint64_t)a.I * a.d};
+        const cuuint64_t dn_dims[3] = {(cuuint64_t)a.d, (cuuint64_t)a.I, (cuuint64_t)a.E};
+        const cuuint64_t dn_str[2] = {2 * (cuuint64_t)a.d, 2 * (cuuint64_t)a.d * a.I};
+        ok = encode_tensor_map_bf16(&tmGU, a.w_gate_up, 3, gu_dims, gu_str, box_a) &&
+             encode_tensor_map_bf16(&tmD, a.w_down, 3, dn_dims, dn_str, box_b);
+    }
+    if (!ok) return cudaErrorInvalidValue;
+
+    uint8_t* parts = static_cast<uint8_t*>(a.partials);
+    Params p;
+    p.x = static_cast<const __nv_bfloat16*>(a.x);
+    p.logits = a.logits;
+    p.topk_ids = a.topk_ids;
+    p.topk_w = a.topk_weights;
+    p.counts = a.counts;
+    p.offsets = a.offsets;
+    p.s2p = a.sorted_to_slot;
+    p.p2s = a.slot_to_sorted;
+    p.h = static_cast<__nv_bfloat16*>(a.h);
+    p.out = static_cast<__nv_bfloat16*>(a.out);
+    p.cnt_a = a.counters;
+    p.hflag = a.counters + (size_t)R * L.nbh;
+    p.cnt_b = a.counters + (size_t)2 * R * L.nbh;
+    p.part_a = reinterpret_cast<float*>(parts + L.part_a);
+    p.part_b = reinterpret_cast<float*>(parts + L.part_b);
+    p.status = a.status;
+    p.T = a.T;
+    p.d = a.d;
+    p.E = a.E;
+    p.k = a.k;
+    p.I = a.I;
+    p.R = R;
+    p.score_fn = a.score_fn;
+    p.renorm = a.renorm ? 1 : 0;
+    p.nbh = L.nbh;
+    p.nka = L.nka;
+    p.nbd = L.nbd;
+    p.nkb = L.nkb;
+    p.scale_input = a.scale_input ? 1 : 0;
+    p.packed = a.packed ? 1 : 0;
+    p.gu_nb = packed_geom(kGateUp, a.d, a.I).nb;
+    p.dn_nb = packed_geom(kDown, a.I, a.d).nb;
+    const int vpl = a.E <= 32 ? 1 : a.E <= 64 ? 2 : a.E <= 128 ? 4 : 8;
+
+    // one block per SM (its shared memory allows no more), all resident: cooperative launch.
+    // It is the first kernel of the layer, so it follows the caller's work in stream order.
+    int grid = device_sm_count();
+    if (grid > kDecodeFusedMaxGrid) grid = kDecodeFusedMaxGrid;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_fused_kernel, tmGU, tmD, p, vpl);
+}
+
+}  // namespace rdg

@@ -96,12 +96,7 @@ __device__ __forceinline__ TileInfo decode_tile(const SmemTail& st, int E, int n
     return ti;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
 
-__device__ __forceinline__ float silu(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
 
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)

@@ -128,7 +128,6 @@ __device__ __forceinline__ uint32_t idesc_swap(int n_tok) {
            ((uint32_t)(kWM >> 4) << 24);
 }
 
-__device__ __forceinline__ float silu(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
 
 // Barrier among the 128 epilogue threads only (id 1; id 0 is __syncthreads).
 __device__ __forceinline__ void epilogue_sync() {

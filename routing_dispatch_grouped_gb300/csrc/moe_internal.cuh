@@ -40,6 +40,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// SwiGLU's activation in fp32 (the GEMM epilogues and the fused decode kernel share it, so every
+// path rounds h from the same value)
+__device__ __forceinline__ float silu(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
 // ---- mbarrier ----
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
@@ -257,6 +266,44 @@ cudaError_t launch_route_dispatch_small(const float* logits, int T, int E, int k
                                         int32_t* counts, int32_t* offsets,
                                         int32_t* sorted_to_slot, int32_t* slot_to_sorted,
                                         cudaStream_t s);
+
+// Fused decode layer (decode_fused.cu): route, dispatch, gate_up + SwiGLU, down and combine in
+// one cooperative kernel, for bf16 layers without a shared expert and at most
+// kDecodeFusedMaxTokens tokens.
+constexpr int kDecodeFusedMaxTokens = 16;
+constexpr int kDecodeFusedMaxRows = 256;  // T * k
+constexpr int kDecodeFusedMaxGrid = 512;  // blocks (one per SM, at most this many)
+bool decode_fused_applies(moe_dtype dt, int T, int k, int Is);
+// Its scratch: counters (which must be zero at launch) and the partial sums.
+struct DecodeFusedLayout {
+    int nbh, nka, nbd, nkb;  // h blocks, gate_up K chunks, output blocks, down K chunks
+    size_t counter_bytes;    // int counters
+    size_t part_a, part_b, part_bytes;  // partial sums: offsets and total size
+};
+DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I);
+struct DecodeFusedArgs {
+    const void* x;                  // [T, d] bf16
+    const float* logits;            // [T, E]
+    const void* w_gate_up;          // [E, d, 2I] or packed
+    const void* w_down;             // [E, I, d] or packed
+    bool packed;
+    int score_fn;
+    bool renorm;
+    bool scale_input;               // router weight scales the expert input, combine weight 1
+    int T, d, E, k, I;
+    int32_t* topk_ids;              // outputs: router and dispatch results
+    float* topk_weights;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* sorted_to_slot;
+    int32_t* slot_to_sorted;
+    void* h;                        // [R, I] bf16
+    void* out;                      // [T, d] bf16
+    int* counters;                  // counter_bytes, zero at launch
+    void* partials;                 // part_bytes
+    int* status;
+};
+cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s);
 
 cudaError_t launch_combine(const float* y_sorted, const int32_t* slot_to_sorted,
                            const float* weights, const float* y_shared, int T, int d, int k,

@@ -41,7 +41,7 @@ SIGNATURES = {
     "moe_forward": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P, _P,
                          _P, _P, _S, _P]),
     "moe_forward_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
-    "moe_forward_kernel_count": (_I, [_I, _I, _I]),
+    "moe_forward_kernel_count": (_I, [_I, _I, _I, _I]),
     "moe_read_device_status": (_I, [_P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -254,8 +254,8 @@ def moe_forward_workspace_size(T, d, E, k, I, Is, dtype) -> int:
                                             else F32)
 
 
-def moe_forward_kernel_count(T, k, Is) -> int:
-    return lib().moe_forward_kernel_count(T, k, Is)
+def moe_forward_kernel_count(T, k, Is, dtype=torch.bfloat16) -> int:
+    return lib().moe_forward_kernel_count(BF16 if dtype == torch.bfloat16 else F32, T, k, Is)
 
 
 def moe_forward(x, logits, w_gate_up, w_down, k, score_fn=SOFTMAX, flags=RENORMALIZE,
@@ -291,13 +291,17 @@ def moe_read_device_status(workspace, stream=None) -> int:
 
 def forward_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is, dtype):
     """Views of the intermediates moe_forward leaves in its workspace (for tests and tools);
-    the offsets follow the library's layout rule: 256-byte status word, then counts, offsets,
+    the offsets follow the library's layout rule: 256-byte status word, then (decode batches
+    only) the one-kernel layer's counters, counts, offsets,
     dispatch scratch, sorted_to_slot, slot_to_sorted, x_sorted, h, y_sorted, shared h, shared y,
     each rounded up to 256 bytes."""
     R = T * k
     b = 2 if dtype == torch.bfloat16 else 4
     nchunks = (R + 255) // 256
-    sizes = [("counts", E * 4), ("offsets", (E + 1) * 4), ("chunk", nchunks * E * 4),
+    # decode batches run the one-kernel layer, whose counters follow the status word
+    fused = dtype == torch.bfloat16 and Is == 0 and 1 <= T <= 16 and R <= 256
+    fcnt = (2 * R * ((I + 63) // 64) + (d + 63) // 64) * 4 if fused else 0
+    sizes = [("fused_counters", fcnt), ("counts", E * 4), ("offsets", (E + 1) * 4), ("chunk", nchunks * E * 4),
              ("sorted_to_slot", R * 4), ("slot_to_sorted", R * 4), ("x_sorted", R * d * b),
              ("h", R * I * b), ("y_sorted", R * d * 4), ("h_shared", T * Is * b),
              ("y_shared", T * d * 4 if Is else 0)]

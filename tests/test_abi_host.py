@@ -156,10 +156,15 @@ def test_pack_validation_and_sizes(L):
 
 
 def test_kernel_count_and_strings(L):
-    assert L.moe_forward_kernel_count(0, 2, 0) == 0
-    assert L.moe_forward_kernel_count(10, 2, 0) == 5        # fused small-batch front end
-    assert L.moe_forward_kernel_count(10, 2, 128) == 7
-    assert L.moe_forward_kernel_count(4096, 2, 0) == 8
-    assert L.moe_forward_kernel_count(16384, 1, 8192) == 10
+    bf16, f32 = moe.BF16, moe.F32
+    assert L.moe_forward_kernel_count(bf16, 0, 2, 0) == 0
+    assert L.moe_forward_kernel_count(bf16, 10, 2, 0) == 1      # one-kernel decode layer
+    assert L.moe_forward_kernel_count(bf16, 16, 16, 0) == 1
+    assert L.moe_forward_kernel_count(bf16, 17, 2, 0) == 5      # fused small-batch front end
+    assert L.moe_forward_kernel_count(bf16, 16, 17, 0) == 5     # T*k above the decode limit
+    assert L.moe_forward_kernel_count(f32, 10, 2, 0) == 5       # fp32 layers: no decode kernel
+    assert L.moe_forward_kernel_count(bf16, 10, 2, 128) == 7    # shared expert: no decode kernel
+    assert L.moe_forward_kernel_count(bf16, 4096, 2, 0) == 8
+    assert L.moe_forward_kernel_count(bf16, 16384, 1, 8192) == 10
     for code in range(7):
         assert L.moe_status_string(code).decode().startswith(moe.STATUS[code])

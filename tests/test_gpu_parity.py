@@ -327,7 +327,9 @@ def test_forward_matches_oracle(name, T):
     assert np.array_equal(v["sorted_to_slot"].cpu().numpy(), ref["sorted_to_slot"])
     assert np.array_equal(v["slot_to_sorted"].cpu().numpy(), ref["slot_to_sorted"])
     tol = TOL[cfg.dtype]
-    assert err_rms(f64(v["y_sorted"]), ref["y_sorted"]) <= tol
+    if moe.moe_forward_kernel_count(cfg.T, cfg.k, cfg.I_shared, cfg.dtype) != 1:
+        # (the fused decode path folds the combine into the down step: no y_sorted)
+        assert err_rms(f64(v["y_sorted"]), ref["y_sorted"]) <= tol
     e = err_rms(f64(out), ref["out"])
     assert e <= tol, e
 
