@@ -213,9 +213,9 @@ def host_inputs(cfg, dev_inputs):
 
 
 # ------------------------------------------------------------------------------------------------
-def traffic_for(kernel_file: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
-    source of the kernel (matching sha256), else None."""
+def traffic_for(kernel_file: str, workload: str):
+    """DRAM bytes per launch of the kernel on this workload from the committed ncu summary, if it
+    was taken on the current source of the kernel (matching sha256), else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     src = os.path.join(ROOT, "routing_dispatch_grouped_gb300", "csrc", kernel_file)
     if not os.path.exists(p) or not os.path.exists(src):
@@ -227,7 +227,7 @@ def traffic_for(kernel_file: str):
     ent = d.get(kernel_file)
     if not ent or ent.get("sha256") != h:
         return None, None
-    return ent.get("bytes_per_launch"), ent
+    return ent.get("by_workload", {}).get(workload), ent
 
 
 def reduce_max(x: float, device) -> float:
@@ -450,7 +450,7 @@ def run_ours(args, rank, world):
         sh_ms = statistics.mean(per_stage["shared_gate_up"]) + statistics.mean(
             per_stage["shared_down"])
     ach = gu_flops / (gu_ms * 1e-3) / 1e12
-    traffic, _ = traffic_for("gemm_tc.cu")
+    traffic, _ = traffic_for("gemm_tc.cu", cfg.name)
     roof = {"bound": "tensor", "kernel": "tc_grouped_gemm<gate_up>", "achieved": round(ach, 1),
             "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
             "frac": round(ach / pk["bf16_tflops"], 4), "traffic": traffic,
@@ -466,7 +466,7 @@ def run_ours(args, rank, world):
         layer_bytes = (n_touched * 3.0 * d * I * 2 + T * d * 2 * 2 + T * E * 4 + T * k * 8)
         ach_gbs = layer_bytes / (graph_ms * 1e-3) / 1e9
         fused = moe.moe_forward_kernel_count(T, k, Is, dt) == 1
-        traffic, _ = traffic_for("decode_fused.cu") if fused else (None, None)
+        traffic, _ = traffic_for("decode_fused.cu", cfg.name) if fused else (None, None)
         roof = {"bound": "hbm",
                 "kernel": ("decode layer: decode_fused_kernel (route, dispatch, experts, combine)" if fused
                            else "decode layer: route/dispatch chain + grouped GEMMs + combine"),
