@@ -750,6 +750,8 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
         // ============ producer: the block's items in schedule order ============
         if (lane == 0) {
             const uint32_t stage0 = smem_u32(smem);
+            // the weights are read once: evict-first, so x, h and the partial sums stay in L2
+            const uint64_t pol = l2_evict_first();
             int i = 0;
             bool ok = true;
             auto next_stage = [&](uint32_t& dst, uint64_t*& bar) {
@@ -776,12 +778,12 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                     const int g = q_lo * p.nbh + u / p.nka, kc = u % p.nka;
                     const int q = g / p.nbh, jb = g % p.nbh, e = s_eq[q];
                     if (p.packed) {
-                        tma_load_3d(dst, &tmGU, bar, 0, kc * kKcA, e * p.gu_nb + jb);
-                        tma_load_3d(dst + kBoxBytesA, &tmGU, bar, 0, kc * kKcA,
-                                    e * p.gu_nb + p.nbh + jb);
+                        tma_load_3d_hint(dst, &tmGU, bar, 0, kc * kKcA, e * p.gu_nb + jb, pol);
+                        tma_load_3d_hint(dst + kBoxBytesA, &tmGU, bar, 0, kc * kKcA,
+                                    e * p.gu_nb + p.nbh + jb, pol);
                     } else {
-                        tma_load_3d(dst, &tmGU, bar, 64 * jb, kc * kKcA, e);
-                        tma_load_3d(dst + kBoxBytesA, &tmGU, bar, p.I + 64 * jb, kc * kKcA, e);
+                        tma_load_3d_hint(dst, &tmGU, bar, 64 * jb, kc * kKcA, e, pol);
+                        tma_load_3d_hint(dst + kBoxBytesA, &tmGU, bar, p.I + 64 * jb, kc * kKcA, e, pol);
                     }
                 }
             }
@@ -795,9 +797,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                     const int cb = u / perC, rem = u % perC;
                     const int e = s_eq[q_lo + rem / p.nkb], kc = rem % p.nkb;
                     if (p.packed)
-                        tma_load_3d(dst, &tmD, bar, 0, kc * kKcB, e * p.dn_nb + cb);
+                        tma_load_3d_hint(dst, &tmD, bar, 0, kc * kKcB, e * p.dn_nb + cb, pol);
                     else
-                        tma_load_3d(dst, &tmD, bar, 64 * cb, kc * kKcB, e);
+                        tma_load_3d_hint(dst, &tmD, bar, 64 * cb, kc * kKcB, e, pol);
                 }
             }
             // leave no copy in flight: the last (up to) kStages issued items must have landed
