@@ -118,6 +118,8 @@ struct Ctx {
     uint64_t* red_empty;     // the epilogue warp has read it
     volatile int* flags;     // [0] something timed out
     int warp, lane, G;
+    int GA;                  // blocks [0, GA) share the gate_up items
+    int B0, GB;              // blocks [B0, B0 + GB) share the down items
     int nA;                  // gate_up items of the current wave
     int slot_off;            // partial slot offset of the current wave (see the schedule)
     int W, nq;               // waves, touched experts
@@ -429,7 +431,7 @@ __device__ void epi_finish_h(const Ctx& c, const Params& p, int row0, int tq, in
             for (int j = 0; j < kBatch; ++j) {
                 const int b = b0 + j;
                 gv[j] = uv[j] = 0.0f;
-                if (b <= b_last && !range_empty(c.nA, b, c.G)) {
+                if (b <= b_last && !range_empty(c.nA, b, c.GA)) {
                     const float* src =
                         p.part_a + ((size_t)(b + g + c.slot_off) * p.T + t) * 128 + col;
                     gv[j] = __ldcg(src);
@@ -478,7 +480,7 @@ __device__ void epi_a(Ctx& c, const Params& p, int q, int jb, int g, int b_first
         }
     }
     bool stored = whole;
-    if (!whole && epi_arrive_last(c, p.cnt_a + g, contributors(c.nA, c.G, b_first, b_last))) {
+    if (!whole && epi_arrive_last(c, p.cnt_a + g, contributors(c.nA, c.GA, b_first, b_last))) {
         epi_finish_h(c, p, row0, tq, jb, g, b_first, b_last);
         stored = true;
     }
@@ -534,8 +536,8 @@ __device__ void epi_flush(Ctx& c, const Params& p, int cb) {
     int total = 0;
     for (int w = 0; w < c.W; ++w) {
         const WaveB v = wave_b(c, p, w);
-        total += contributors(v.n, c.G, block_of(v.n, cb * v.perC, c.G),
-                              block_of(v.n, (cb + 1) * v.perC - 1, c.G));
+        total += contributors(v.n, c.GB, block_of(v.n, cb * v.perC, c.GB),
+                              block_of(v.n, (cb + 1) * v.perC - 1, c.GB));
     }
     __syncwarp();
     if (total == 1) {
@@ -546,7 +548,7 @@ __device__ void epi_flush(Ctx& c, const Params& p, int cb) {
             c.outacc[o] = 0.0f;
         }
     } else {
-        float* part = p.part_b + (size_t)(blockIdx.x + cb + c.slot_off) * n;
+        float* part = p.part_b + (size_t)(blockIdx.x - c.B0 + cb + c.slot_off) * n;
         for (int o = c.lane; o < n; o += 32) {
             __stcg(part + o, c.outacc[o]);
             c.outacc[o] = 0.0f;
@@ -558,11 +560,11 @@ __device__ void epi_flush(Ctx& c, const Params& p, int cb) {
             for (int i = 0; i < kPer; ++i) acc[i] = 0.0f;
             for (int w = 0; w < c.W; ++w) {
                 const WaveB v = wave_b(c, p, w);
-                const int bf = block_of(v.n, cb * v.perC, c.G);
-                const int bl = block_of(v.n, (cb + 1) * v.perC - 1, c.G);
+                const int bf = block_of(v.n, cb * v.perC, c.GB);
+                const int bl = block_of(v.n, (cb + 1) * v.perC - 1, c.GB);
                 for (int b = bf; b <= bl; ++b) {
-                    if (range_empty(v.n, b, c.G)) continue;
-                    const float* base = p.part_b + (size_t)(b + cb + w * (c.G + p.nbd)) * n;
+                    if (range_empty(v.n, b, c.GB)) continue;
+                    const float* base = p.part_b + (size_t)(b + cb + w * (c.GB + p.nbd)) * n;
 #pragma unroll
                     for (int i = 0; i < kPer; ++i) {
                         const int o = c.lane + 32 * i;
@@ -741,6 +743,18 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     // items rarely wait for it.
     const int G = gridDim.x, b = blockIdx.x;
     const int W = nq < kDecodeWaves ? nq : kDecodeWaves;
+    // Partition. Stream-K: both lists over all G blocks. When there are fewer h blocks than
+    // SMs and the down items, spread over the remaining blocks, are not much more than one h
+    // block's worth of bytes each, blocks [0, ngA) each take one whole h block (no partial
+    // sums, h flagged as soon as it is stored) and blocks [ngA, G) take the down items,
+    // prefetching them while the gate_up items stream.
+    const int ngA = nq * p.nbh;
+    const bool whole_groups = W == 1 && ngA < G &&
+                              (long long)p.nbd * nq * p.nkb * 4 <= 5ll * p.nka * (G - ngA);
+    const int GA = whole_groups ? ngA : G;
+    const int B0 = whole_groups ? ngA : 0, GB = G - B0;
+    const int ba = b < GA ? b : GA;            // gate_up range index (GA: empty)
+    const int bb = b >= B0 ? b - B0 : GB;      // down range index (GB: empty)
     auto wave_a = [&](int w, int& q_lo, int& n) {
         q_lo = range_lo(nq, w, W);
         n = (range_lo(nq, w + 1, W) - q_lo) * p.nbh * p.nka;
@@ -771,7 +785,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
             for (int w = 0; ok && w < W; ++w) {
                 int q_lo, n;
                 wave_a(w, q_lo, n);
-                for (int u = range_lo(n, b, G); ok && u < range_lo(n, b + 1, G); ++u) {
+                const int lo = ba < GA ? range_lo(n, ba, GA) : 0;
+                const int hi = ba < GA ? range_lo(n, ba + 1, GA) : 0;
+                for (int u = lo; ok && u < hi; ++u) {
                     uint32_t dst;
                     uint64_t* bar;
                     if (!(ok = next_stage(dst, bar))) break;
@@ -790,7 +806,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
             for (int w = 0; ok && w < W; ++w) {
                 const int q_lo = range_lo(nq, w, W);
                 const int perC = (range_lo(nq, w + 1, W) - q_lo) * p.nkb, n = p.nbd * perC;
-                for (int u = range_lo(n, b, G); ok && u < range_lo(n, b + 1, G); ++u) {
+                const int lo = bb < GB ? range_lo(n, bb, GB) : 0;
+                const int hi = bb < GB ? range_lo(n, bb + 1, GB) : 0;
+                for (int u = lo; ok && u < hi; ++u) {
                     uint32_t dst;
                     uint64_t* bar;
                     if (!(ok = next_stage(dst, bar))) break;
@@ -826,6 +844,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     c.warp = warp;
     c.lane = lane;
     c.G = G;
+    c.GA = GA;
+    c.B0 = B0;
+    c.GB = GB;
     c.W = W;
     c.nq = nq;
     c.ready_q = -1;
@@ -839,13 +860,14 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
         wave_a(w, q_lo, n);
         c.nA = n;
         c.slot_off = w * G;
-        const int hi = range_lo(n, b + 1, G);
-        for (int u = range_lo(n, b, G); u < hi;) {
+        const int hi = ba < GA ? range_lo(n, ba + 1, GA) : 0;
+        for (int u = ba < GA ? range_lo(n, ba, GA) : 0; u < hi;) {
             const int gl = u / p.nka, kc0 = u % p.nka;  // group within the wave, K chunk
             const int kc1 = min(p.nka, kc0 + (hi - u));
             const int g = q_lo * p.nbh + gl, q = g / p.nbh, jb = g % p.nbh;
             if (epilogue) {
-                const int bf = block_of(n, gl * p.nka, G), bl = block_of(n, (gl + 1) * p.nka - 1, G);
+                const int bf = block_of(n, gl * p.nka, GA);
+                const int bl = block_of(n, (gl + 1) * p.nka - 1, GA);
                 by_rows(s_tq[q],
                         [&](auto tag) { epi_a<decltype(tag)::value>(c, p, q, jb, g, bf, bl); });
             } else {
@@ -859,9 +881,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     }
     for (int w = 0; w < W; ++w) {
         const WaveB v = wave_b(c, p, w);
-        c.slot_off = w * (G + p.nbd);
-        const int hi = range_lo(v.n, b + 1, G);
-        for (int u = range_lo(v.n, b, G); u < hi;) {
+        c.slot_off = w * (GB + p.nbd);
+        const int hi = bb < GB ? range_lo(v.n, bb + 1, GB) : 0;
+        for (int u = bb < GB ? range_lo(v.n, bb, GB) : 0; u < hi;) {
             const int cb = u / v.perC;
             const int c_end = min(hi, (cb + 1) * v.perC);
             while (u < c_end) {
