@@ -33,6 +33,7 @@ constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kPairRows = 2 * kTileM;            // 256 rows per pair tile
+constexpr int kBandTiles = 8;                    // row tiles per band of the tile order
 
 // ---- cta_group::2 forms and cluster helpers ----
 __device__ __forceinline__ uint32_t cta_rank() {
@@ -123,6 +124,7 @@ struct PairParams {
     int k_blocks;
     int row_scale;
     int packed, nb, nbh, kpad;
+    int band_m;    // groups of at least this many row tiles run in bands (see decode_pair)
 };
 
 struct __align__(8) SmemTail {
@@ -145,7 +147,8 @@ struct PairTile {
     int e, row0, row_end, n0;  // row0: this CTA's first row
 };
 
-__device__ __forceinline__ PairTile decode_pair(const SmemTail& st, int E, int n_tile, int tile,
+__device__ __forceinline__ PairTile decode_pair(const SmemTail& st, int E, int n_tile,
+                                                int n_tiles, int band_m, int tile,
                                                 uint32_t rank) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
@@ -155,9 +158,20 @@ __device__ __forceinline__ PairTile decode_pair(const SmemTail& st, int E, int n
         else
             hi = mid - 1;
     }
+    // A group's tiles run column block by column block, each over all the group's row tiles,
+    // so CTAs running together share each weight block through L2 and the weights stream once.
+    // A group whose rows outnumber its weight columns and whose row panel exceeds a share of L2
+    // (band_m row tiles or more: a dense shared expert) runs instead in bands of kBandTiles row
+    // tiles, every column block of a band before the next band: the band's rows stay in L2
+    // and the (smaller) weights stream once per band.
     const int local = tile - st.prefix[lo];
     const int m = st.mt[lo];
-    const int nb = local / m, mb = local - nb * m;
+    const int band_w = m >= band_m ? kBandTiles : m;
+    const int band = local / (band_w * n_tiles);
+    const int first_m = band * band_w;
+    const int bm = min(band_w, m - first_m);
+    const int r = local - band * kBandTiles * n_tiles;
+    const int nb = r / bm, mb = first_m + (r - (r / bm) * bm);
     PairTile t;
     t.e = lo;
     t.row0 = st.off[lo] + mb * kPairRows + (int)rank * kTileM;
@@ -232,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             for (int tile = pair0; tile < total && ok; tile += npairs) {
-                const PairTile t = decode_pair(st, E, p.n_tile, tile, rank);
+                const PairTile t = decode_pair(st, E, p.n_tile, p.n_tiles, p.band_m, tile, rank);
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(&st.empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
                         ok = false;
@@ -329,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tempty_leader0 = mapa(smem_u32(&st.tempty[0]), 0);
         const uint32_t tempty_leader1 = mapa(smem_u32(&st.tempty[1]), 0);
         for (int tile = pair0; tile < total; tile += npairs, ++it) {
-            const PairTile t = decode_pair(st, E, p.n_tile, tile, rank);
+            const PairTile t = decode_pair(st, E, p.n_tile, p.n_tiles, p.band_m, tile, rank);
             const uint32_t acc = it & 1u;
             if (!mbar_wait(&st.tfull[acc], (it >> 1) & 1u, abort_flag, kWaitLimitNs)) {
                 if (lane == 0) {
@@ -457,6 +471,14 @@ cudaError_t launch_pair_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     p.nb = g.nb;
     p.nbh = g.nbh;
     p.kpad = g.kpad;
+    {
+        // band a group when its rows outnumber its weight columns and its row panel exceeds
+        // 64 MB (half the L2)
+        const long long cols = (KIND == kGateUp) ? 2ll * a.N : (long long)a.N;
+        long long rows = (64ll << 20) / (2ll * a.K);
+        if (rows < cols) rows = cols;
+        p.band_m = (int)((rows + kPairRows - 1) / kPairRows);
+    }
 
     // clusters that can be resident at once (SMs pair up within a GPC)
     static int max_clusters[64] = {0};
