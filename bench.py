@@ -438,6 +438,26 @@ def run_ours(args, rank, world):
     if world > 1:
         e2e_ms = reduce_max(e2e_ms, dev)
 
+    # the router from hidden states (logits = x W_r + b and the top-k in one kernel): the step
+    # before the layer, timed on its own (not part of the layer's timed region above)
+    w_r = synth.make_router_weight(cfg, dev)
+    b_r = synth.router_bias(cfg, device=dev)
+    b_r = None if b_r is None else b_r.to(torch.float32).contiguous()
+    lg_r = torch.empty(T, E, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        moe.moe_route_hidden(inp["x"], w_r, k, cfg.score_fn, cfg.renormalize, bias=b_r,
+                             logits=lg_r, topk_ids=ids, topk_weights=w, stream=stream)
+    r_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in range(args.steps)]
+    for a_, b_ in r_ev:
+        flush_l2()
+        a_.record(stream)
+        moe.moe_route_hidden(inp["x"], w_r, k, cfg.score_fn, cfg.renormalize, bias=b_r,
+                             logits=lg_r, topk_ids=ids, topk_weights=w, stream=stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    router_hidden_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in r_ev)
+
     # roofline of the dominant kernel (the gate_up grouped GEMM: 2/3 of the expert FLOPs)
     pk, pk_src = peaks()
     gu_ms = statistics.mean(per_stage["gate_up"])
@@ -495,6 +515,7 @@ def run_ours(args, rank, world):
         "stages_ms": {n: round(statistics.mean(vv), 4) for n, vv in per_stage.items()},
         "staged_calls_ms_per_step": round(ms_per_step, 4),
         "forward_call_ms": round(forward_ms, 4),
+        "router_from_hidden_ms": round(router_hidden_ms, 4),
         "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": x_h.numel() * x_h.element_size()

@@ -129,6 +129,28 @@ moe_status moe_route(const float* logits, int T, int E, int k, moe_score_fn scor
                      unsigned flags, int32_t* topk_ids, float* topk_weights, moe_stream_t stream);
 
 /*
+ * moe_route_hidden - the router from hidden states: logits = x . w_router (+ bias) in fp32,
+ *   then the top-k and weights of moe_route, in one kernel ([EP-intro]: a router sends each
+ *   token to its experts; the workloads define the logits as x times a router weight [d, E]
+ *   plus an optional per-expert bias).
+ *   x             device [T, d] in dtype dt (MOE_BF16 or MOE_F32), read only.
+ *   w_router      device float [d, E], row-major, read only.
+ *   bias          device float [E] or NULL.
+ *   logits        device float [T, E] or NULL: when given, the logits the selection used.
+ *   topk_ids, topk_weights, score_fn, flags: as moe_route; for the same logits the results are
+ *                 bit-identical to moe_route's.
+ *   Each logit is the sequential fp32 sum over i = 0 .. d-1 of x[t][i] * w_router[i][e]
+ *   (fmaf, ascending i), then + bias[e]: it differs from an exact sum by at most about
+ *   d * 2^-24 * sum_i |x[t][i] * w_router[i][e]|, so logits closer than that may rank
+ *   differently than they would under exact arithmetic.
+ *   Constraints: 1 <= k <= E <= 256, d >= 1; pointers 16-byte aligned. T == 0 is a no-op.
+ */
+moe_status moe_route_hidden(const void* x, moe_dtype dt, const float* w_router,
+                            const float* bias, int T, int d, int E, int k,
+                            moe_score_fn score_fn, unsigned flags, float* logits,
+                            int32_t* topk_ids, float* topk_weights, moe_stream_t stream);
+
+/*
  * moe_dispatch - group the T*k routed slots by expert ([EP-dispatch]: every (token, expert)
  * pair goes to that expert; on one GPU this is a local permutation).
  *   topk_ids       device int32 [T, k], read. An id outside [0, E) sets MOE_ERR_DEVICE_BOUNDS in

@@ -55,6 +55,18 @@ def round_bf16(a) -> np.ndarray:
 # ----------------------------------------------------------------------------------------------
 # Step 1: router top-k gating
 # ----------------------------------------------------------------------------------------------
+def router_logits(x, w_router, bias=None):
+    """The router's logits from hidden states: x [T, d] @ w_router [d, E] (+ bias [E]), in
+    float64 ("Expert parallelism", intro: a router sends each token to its experts; the
+    workloads define the logits as the hidden states times a router weight, plus an optional
+    per-expert bias). No rounding: the GPU rounds once to fp32 at the end of a sequential fp32
+    sum, and the tests compare against this exact value within that sum's error bound."""
+    z = np.asarray(x, dtype=np.float64) @ np.asarray(w_router, dtype=np.float64)
+    if bias is not None:
+        z = z + np.asarray(bias, dtype=np.float64)[None, :]
+    return z
+
+
 def route(logits, k: int, score_fn: int = SOFTMAX, renormalize: bool = True):
     """Top-k experts per token and their weights ("top_k_index", "top_k_weights").
 

@@ -167,6 +167,26 @@ moe_status moe_route(const float* logits, int T, int E, int k, moe_score_fn scor
                                       (cudaStream_t)stream));
 }
 
+moe_status moe_route_hidden(const void* x, moe_dtype dt, const float* w_router,
+                            const float* bias, int T, int d, int E, int k,
+                            moe_score_fn score_fn, unsigned flags, float* logits,
+                            int32_t* topk_ids, float* topk_weights, moe_stream_t stream) {
+    moe_status st = check_tek(T, E, k);
+    if (st != MOE_OK) return st;
+    if (!dtype_ok(dt) || d < 1) return MOE_ERR_INVALID_ARG;
+    if (score_fn != MOE_SCORE_SOFTMAX && score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)MOE_RENORMALIZE) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !w_router || !topk_ids || !topk_weights) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, w_router, bias, logits, topk_ids, topk_weights};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    return launch_status(launch_route_hidden(x, dt == MOE_BF16, w_router, bias, T, d, E, k,
+                                             (int)score_fn, (flags & MOE_RENORMALIZE) != 0,
+                                             logits, topk_ids, topk_weights,
+                                             (cudaStream_t)stream));
+}
+
 size_t moe_dispatch_workspace_size(int T, int E, int k) {
     if (T < 0 || E < 1 || k < 1) return 0;
     return kStatusBytes + round_up(dispatch_scratch_bytes(T * k, E), 256);

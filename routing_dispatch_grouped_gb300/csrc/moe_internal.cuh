@@ -275,6 +275,12 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 cudaError_t launch_route(const float* logits, int T, int E, int k, int score_fn, bool renorm,
                          int32_t* ids, float* weights, cudaStream_t s);
 
+// Router logits from hidden states (fp32, sequential in K) and the top-k in one kernel.
+cudaError_t launch_route_hidden(const void* x, bool bf16, const float* w_router,
+                                const float* bias, int T, int d, int E, int k, int score_fn,
+                                bool renorm, float* logits, int32_t* ids, float* weights,
+                                cudaStream_t s);
+
 // Dispatch scratch (in a workspace after the status word): per-chunk counts/bases int32
 // [nchunks * E].
 size_t dispatch_scratch_bytes(int R, int E);

@@ -1,0 +1,211 @@
+// Router from hidden states: logits = x . W_r (+ b) in fp32, then the router top-k, in one
+// kernel.
+//
+// Expert parallelism page, introduction: a router sends each token to its experts; the
+// workloads define the router's logits as the hidden states times a router weight [d, E]
+// (plus a per-expert bias on two of them). This is the step right before the routing kernel;
+// fusing it saves writing the [T, E] logits and reading them back, and gives decode one launch
+// less. The top-k and weights are the warp router of route.cu (route_select_warp), fed from
+// registers, so for the same logits the ids and weights are bit-identical to moe_route.
+//
+// Layout: a block has 8 warps; lane l accumulates experts l, l+32, ... of 8 tokens (the
+// register layout the warp router reads). K is walked in chunks of 64 rows staged in shared
+// memory (x as fp32, W_r); the loads of chunk c + 1 are issued into registers before chunk c
+// is multiplied, so their latency hides behind the FMAs.
+//   - large batches (KS = 1): warp w owns tokens 8w .. 8w+7 of the block's 64 and sums each
+//     logit over K in ascending order;
+//   - small batches (KS = 8): the 8 warps share the block's 8 tokens and split each chunk's
+//     rows (warp w takes rows w, w+8, ...); the 8 partial sums are then added in warp order.
+// Either way every logit's summation order is fixed by the sizes, so results do not depend on
+// timing.
+#include <mutex>
+
+#include "route_warp.cuh"
+
+namespace rdg {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kTokPerWarp = 8;
+constexpr int kChunk = 64;  // K rows per shared-memory step
+
+template <int VPL, int KS>
+struct RhShape {
+    static constexpr int kTok = kWarps / KS * kTokPerWarp;               // tokens per block
+    static constexpr int kXPer = kTok * kChunk / (kWarps * 32);           // x values per thread
+    static constexpr int kWPer = kChunk * VPL * 32 / (kWarps * 32);       // W values per thread
+    static constexpr size_t kSmem = (size_t)(kTok * (kChunk + 1) + kChunk * VPL * 32) * 4 +
+                                    (KS > 1 ? (size_t)kWarps * kTokPerWarp * VPL * 32 * 4 : 0);
+};
+
+template <int VPL, bool kBf16, int KS>
+__global__ void __launch_bounds__(kWarps * 32)
+route_hidden_kernel(const void* __restrict__ x_raw, const float* __restrict__ w_router,
+                    const float* __restrict__ bias, int T, int d, int E, int k, int score_fn,
+                    int renorm, float* __restrict__ logits, int32_t* __restrict__ ids,
+                    float* __restrict__ weights) {
+    using S = RhShape<VPL, KS>;
+    extern __shared__ float rh_smem[];
+    float* xs = rh_smem;                          // [kTok][kChunk + 1]
+    float* ws = xs + S::kTok * (kChunk + 1);      // [kChunk][VPL * 32]
+    float* red = ws + kChunk * VPL * 32;          // [kWarps][8][VPL * 32] (KS > 1)
+    griddep_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t0 = blockIdx.x * S::kTok;
+    const int tg = (KS == 1) ? warp : 0;          // this warp's 8 tokens within the block
+    const int ks = (KS == 1) ? 0 : warp;          // this warp's rows: ks, ks + KS, ...
+
+    float acc[kTokPerWarp][VPL];
+#pragma unroll
+    for (int t = 0; t < kTokPerWarp; ++t)
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) acc[t][j] = 0.0f;
+
+    // thread i of the block loads x element (i + 256 m) and W element (i + 256 m) of a chunk
+    float xr[S::kXPer], wr[S::kWPer];
+    auto load_chunk = [&](int k0) {
+#pragma unroll
+        for (int m = 0; m < S::kXPer; ++m) {
+            const int i = threadIdx.x + m * kWarps * 32;
+            const int t = i / kChunk, kk = i % kChunk;
+            const int tok = t0 + t, col = k0 + kk;
+            float v = 0.0f;
+            if (tok < T && col < d) {
+                if (kBf16)
+                    v = __bfloat162float(
+                        static_cast<const __nv_bfloat16*>(x_raw)[(size_t)tok * d + col]);
+                else
+                    v = static_cast<const float*>(x_raw)[(size_t)tok * d + col];
+            }
+            xr[m] = v;
+        }
+#pragma unroll
+        for (int m = 0; m < S::kWPer; ++m) {
+            const int i = threadIdx.x + m * kWarps * 32;
+            const int kk = i / (VPL * 32), e = i % (VPL * 32);
+            const int row = k0 + kk;
+            wr[m] = (row < d && e < E) ? __ldg(w_router + (size_t)row * E + e) : 0.0f;
+        }
+    };
+    auto store_chunk = [&]() {
+#pragma unroll
+        for (int m = 0; m < S::kXPer; ++m) {
+            const int i = threadIdx.x + m * kWarps * 32;
+            xs[(i / kChunk) * (kChunk + 1) + i % kChunk] = xr[m];
+        }
+#pragma unroll
+        for (int m = 0; m < S::kWPer; ++m) ws[threadIdx.x + m * kWarps * 32] = wr[m];
+    };
+
+    load_chunk(0);
+    for (int k0 = 0; k0 < d; k0 += kChunk) {
+        store_chunk();
+        __syncthreads();
+        if (k0 + kChunk < d) load_chunk(k0 + kChunk);  // in flight during the FMAs below
+#pragma unroll 4
+        for (int kk = ks; kk < kChunk; kk += KS) {
+            float w[VPL];
+#pragma unroll
+            for (int j = 0; j < VPL; ++j) w[j] = ws[kk * VPL * 32 + lane + 32 * j];
+#pragma unroll
+            for (int t = 0; t < kTokPerWarp; ++t) {
+                const float xv = xs[(tg * kTokPerWarp + t) * (kChunk + 1) + kk];
+#pragma unroll
+                for (int j = 0; j < VPL; ++j) acc[t][j] = fmaf(xv, w[j], acc[t][j]);
+            }
+        }
+        __syncthreads();
+    }
+
+    if (KS > 1) {
+        // add the warps' partial sums in warp order; warp 0 keeps the result
+#pragma unroll
+        for (int t = 0; t < kTokPerWarp; ++t)
+#pragma unroll
+            for (int j = 0; j < VPL; ++j)
+                red[((warp * kTokPerWarp) + t) * VPL * 32 + lane + 32 * j] = acc[t][j];
+        __syncthreads();
+        if (warp != 0) return;
+#pragma unroll
+        for (int t = 0; t < kTokPerWarp; ++t)
+#pragma unroll
+            for (int j = 0; j < VPL; ++j) {
+                float s = 0.0f;
+                for (int w = 0; w < kWarps; ++w)
+                    s += red[((w * kTokPerWarp) + t) * VPL * 32 + lane + 32 * j];
+                acc[t][j] = s;
+            }
+    }
+
+#pragma unroll
+    for (int t = 0; t < kTokPerWarp; ++t) {
+        const int tok = t0 + tg * kTokPerWarp + t;
+        if (tok >= T) break;  // uniform across the warp
+        float v[VPL];
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+            const int e = lane + 32 * j;
+            v[j] = -INFINITY;
+            if (e < E) {
+                v[j] = bias ? acc[t][j] + __ldg(bias + e) : acc[t][j];
+                if (logits) logits[(size_t)tok * E + e] = v[j];
+            }
+        }
+        int id;
+        float wt;
+        route_select_warp<VPL>(v, E, k, score_fn, renorm, lane, &id, &wt);
+        if (lane < k) {
+            ids[(size_t)tok * k + lane] = id;
+            weights[(size_t)tok * k + lane] = wt;
+        }
+    }
+}
+
+template <int VPL, int KS>
+cudaError_t launch_shape(const void* x, bool bf16, const float* w_router, const float* bias,
+                         int T, int d, int E, int k, int score_fn, int renorm, float* logits,
+                         int32_t* ids, float* weights, cudaStream_t s) {
+    using S = RhShape<VPL, KS>;
+    auto kern = bf16 ? route_hidden_kernel<VPL, true, KS> : route_hidden_kernel<VPL, false, KS>;
+    if (S::kSmem > 48 * 1024) {
+        static std::once_flag once[2];
+        static cudaError_t attr_err[2] = {cudaSuccess, cudaSuccess};
+        const int which = bf16 ? 1 : 0;
+        std::call_once(once[which], [&] {
+            attr_err[which] = cudaFuncSetAttribute(
+                kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kSmem);
+        });
+        if (attr_err[which] != cudaSuccess) return attr_err[which];
+    }
+    const dim3 grid((T + S::kTok - 1) / S::kTok), block(kWarps * 32);
+    return launch_kernel(kern, grid, block, S::kSmem, s, x, w_router, bias, T, d, E, k,
+                         score_fn, renorm, logits, ids, weights);
+}
+
+template <int VPL>
+cudaError_t launch_vpl(const void* x, bool bf16, const float* w_router, const float* bias, int T,
+                       int d, int E, int k, int score_fn, int renorm, float* logits,
+                       int32_t* ids, float* weights, cudaStream_t s) {
+    // up to 1024 tokens: 8 tokens per block, K split over the warps (more blocks, shorter
+    // dependent chains); beyond: 64 tokens per block
+    if (T <= 1024)
+        return launch_shape<VPL, 8>(x, bf16, w_router, bias, T, d, E, k, score_fn, renorm,
+                                    logits, ids, weights, s);
+    return launch_shape<VPL, 1>(x, bf16, w_router, bias, T, d, E, k, score_fn, renorm, logits,
+                                ids, weights, s);
+}
+
+}  // namespace
+
+cudaError_t launch_route_hidden(const void* x, bool bf16, const float* w_router,
+                                const float* bias, int T, int d, int E, int k, int score_fn,
+                                bool renorm, float* logits, int32_t* ids, float* weights,
+                                cudaStream_t s) {
+    const int rn = renorm ? 1 : 0;
+    if (E <= 32) return launch_vpl<1>(x, bf16, w_router, bias, T, d, E, k, score_fn, rn, logits, ids, weights, s);
+    if (E <= 64) return launch_vpl<2>(x, bf16, w_router, bias, T, d, E, k, score_fn, rn, logits, ids, weights, s);
+    if (E <= 128) return launch_vpl<4>(x, bf16, w_router, bias, T, d, E, k, score_fn, rn, logits, ids, weights, s);
+    return launch_vpl<8>(x, bf16, w_router, bias, T, d, E, k, score_fn, rn, logits, ids, weights, s);
+}
+
+}  // namespace rdg

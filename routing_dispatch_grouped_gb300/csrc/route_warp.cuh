@@ -19,20 +19,16 @@ __device__ __forceinline__ uint32_t route_order_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Lane l holds experts l, l+32, ... (VPL = ceil(E/32) values). After the call lane j < k holds
-// slot j: *id = the expert, *w = its weight. All 32 lanes must call it together.
+// Lane l holds experts l, l+32, ... (VPL = ceil(E/32) values; entries at or past E are
+// ignored). After the call lane j < k holds slot j: *id = the expert, *w = its weight. All 32
+// lanes must call it together.
 template <int VPL>
-__device__ __forceinline__ void route_token_warp(const float* __restrict__ row, int E, int k,
-                                                 int score_fn, int renorm, int lane, int* id,
-                                                 float* wt) {
-    float v[VPL];
+__device__ __forceinline__ void route_select_warp(const float (&v)[VPL], int E, int k,
+                                                  int score_fn, int renorm, int lane, int* id,
+                                                  float* wt) {
     uint32_t key[VPL];
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-        const int e = lane + 32 * i;
-        v[i] = (e < E) ? __ldg(row + e) : -INFINITY;
-        key[i] = (e < E) ? route_order_key(v[i]) : 0u;
-    }
+    for (int i = 0; i < VPL; ++i) key[i] = (lane + 32 * i < E) ? route_order_key(v[i]) : 0u;
     int my_id = 0;
     float my_val = 0.0f;
     for (int r = 0; r < k; ++r) {
@@ -93,6 +89,20 @@ __device__ __forceinline__ void route_token_warp(const float* __restrict__ row, 
     }
     *id = my_id;
     *wt = w;
+}
+
+// Router top-k of one token from its logits row in global memory.
+template <int VPL>
+__device__ __forceinline__ void route_token_warp(const float* __restrict__ row, int E, int k,
+                                                 int score_fn, int renorm, int lane, int* id,
+                                                 float* wt) {
+    float v[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = (e < E) ? __ldg(row + e) : -INFINITY;
+    }
+    route_select_warp<VPL>(v, E, k, score_fn, renorm, lane, id, wt);
 }
 
 }  // namespace rdg

@@ -28,6 +28,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 _P, _I, _U, _S = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_size_t
 SIGNATURES = {
     "moe_route": (_I, [_P, _I, _I, _I, _I, _U, _P, _P, _P]),
+    "moe_route_hidden": (_I, [_P, _I, _P, _P, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P]),
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_dispatch_workspace_size": (_S, [_I, _I, _I]),
     "moe_dispatch_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
@@ -153,6 +154,27 @@ def moe_route(logits, k, score_fn=SOFTMAX, renormalize=True, topk_ids=None, topk
                                         RENORMALIZE if renormalize else 0, _p(ids), _p(w),
                                         _stream(stream)))
     return ids, w
+
+
+def moe_route_hidden(x, w_router, k, score_fn=SOFTMAX, renormalize=True, bias=None,
+                     logits=None, topk_ids=None, topk_weights=None, want_logits=True,
+                     stream=None):
+    """Router logits x @ w_router (+ bias) and the top-k in one kernel. Returns
+    (topk_ids, topk_weights, logits or None)."""
+    _need(x, "x")
+    _need(w_router, "w_router")
+    T, d = x.shape
+    E = w_router.shape[1]
+    dev = x.device
+    ids = topk_ids if topk_ids is not None else torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = topk_weights if topk_weights is not None else torch.empty(T, k, dtype=torch.float32,
+                                                                  device=dev)
+    if logits is None and want_logits:
+        logits = torch.empty(T, E, dtype=torch.float32, device=dev)
+    _check("moe_route_hidden", lib().moe_route_hidden(
+        _p(x), _dt(x), _p(w_router), _p(bias), T, d, E, k, score_fn,
+        RENORMALIZE if renormalize else 0, _p(logits), _p(ids), _p(w), _stream(stream)))
+    return ids, w, logits
 
 
 def moe_dispatch_workspace_size(T, E, k) -> int:

@@ -59,6 +59,20 @@ def test_route_validation(L):
     assert r(FAKE, 1 << 28, 8, 8, 0, 1, FAKE, FAKE, NULL) == 2    # T*k >= 2^31
 
 
+def test_route_hidden_validation(L):
+    r = L.moe_route_hidden
+    # (x, dt, w_router, bias, T, d, E, k, fn, flags, logits, ids, weights, stream)
+    assert r(FAKE, 1, FAKE, NULL, 4, 64, 8, 9, 0, 1, NULL, FAKE, FAKE, NULL) == 1   # k > E
+    assert r(FAKE, 1, FAKE, NULL, 4, 64, 300, 2, 0, 1, NULL, FAKE, FAKE, NULL) == 2  # E > 256
+    assert r(FAKE, 1, FAKE, NULL, 4, 0, 8, 2, 0, 1, NULL, FAKE, FAKE, NULL) == 1    # d = 0
+    assert r(FAKE, 5, FAKE, NULL, 4, 64, 8, 2, 0, 1, NULL, FAKE, FAKE, NULL) == 1   # bad dtype
+    assert r(FAKE, 1, FAKE, NULL, 4, 64, 8, 2, 7, 1, NULL, FAKE, FAKE, NULL) == 1   # bad fn
+    assert r(FAKE, 1, FAKE, NULL, 4, 64, 8, 2, 0, 2, NULL, FAKE, FAKE, NULL) == 1   # bad flag
+    assert r(FAKE, 1, NULL, NULL, 4, 64, 8, 2, 0, 1, NULL, FAKE, FAKE, NULL) == 1   # no weight
+    assert r(FAKE, 1, FAKE, MIS, 4, 64, 8, 2, 0, 1, NULL, FAKE, FAKE, NULL) == 1    # misaligned
+    assert r(NULL, 1, NULL, NULL, 0, 64, 8, 2, 0, 1, NULL, NULL, NULL, NULL) == 0   # T = 0
+
+
 def test_dispatch_validation(L):
     d = L.moe_dispatch
     ws_need = L.moe_dispatch_workspace_size(100, 8, 2)

@@ -404,3 +404,35 @@ def test_planted_mistakes_are_caught():
 
     for bad in (swapped, no_gate, wrong_sign):
         assert np.max(np.abs(bad(x)[0] - np.array(c["y"]))) > 1.0
+
+
+# ----------------------------------------------------------------------------------------------
+# router logits from hidden states
+# ----------------------------------------------------------------------------------------------
+def test_router_logits_one_hot_rows_pick_weight_rows():
+    """x = one-hot rows: each logit row is a row of the router weight (+ bias), exactly."""
+    rng = np.random.default_rng(3)
+    d, E = 7, 5
+    w = rng.standard_normal((d, E)).astype(np.float32)
+    b = rng.standard_normal(E).astype(np.float32)
+    x = np.eye(d)[[3, 0, 6, 3]]
+    z = o.router_logits(x, w, b)
+    assert np.array_equal(z, w[[3, 0, 6, 3]].astype(np.float64) + b.astype(np.float64))
+    assert np.array_equal(o.router_logits(x, w), w[[3, 0, 6, 3]].astype(np.float64))
+
+
+def test_router_logits_match_plain_loops():
+    """Brute force in plain Python with exact rational arithmetic on small shapes."""
+    rng = np.random.default_rng(4)
+    T, d, E = 3, 6, 4
+    x = rng.standard_normal((T, d)).astype(np.float32)
+    w = rng.standard_normal((d, E)).astype(np.float32)
+    b = rng.standard_normal(E).astype(np.float32)
+    z = o.router_logits(x, w, b)
+    for t in range(T):
+        for e in range(E):
+            exact = sum(Fraction(float(x[t, i])) * Fraction(float(w[i, e])) for i in range(d))
+            exact += Fraction(float(b[e]))
+            assert abs(z[t, e] - float(exact)) <= 1e-15 * (1 + abs(float(exact)))
+    # a transposed weight (a plausible mistake) gives different logits
+    assert not np.allclose(o.router_logits(x[:, :4], w[:4, :].T), z[:, :4])
