@@ -14,8 +14,11 @@
 // is multiplied, so their latency hides behind the FMAs.
 //   - large batches (KS = 1): warp w owns tokens 8w .. 8w+7 of the block's 64 and sums each
 //     logit over K in ascending order;
-//   - small batches (KS = 8): the 8 warps share the block's 8 tokens and split each chunk's
-//     rows (warp w takes rows w, w+8, ...); the 8 partial sums are then added in warp order.
+//   - small batches (KS = 8): a cluster of 8 blocks shares 8 tokens; block r of the cluster
+//     takes K rows [r D, r D + D) (D = d/8 rounded up to the chunk), its 8 warps split each
+//     chunk's rows (warp w takes rows w, w+8, ...) and add their sums in warp order; block 0
+//     then adds the 8 blocks' sums in rank order from their shared memory (distributed shared
+//     memory within the cluster) and selects.
 // Either way every logit's summation order is fixed by the sizes, so results do not depend on
 // timing.
 #include <mutex>
@@ -28,6 +31,26 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kTokPerWarp = 8;
 constexpr int kChunk = 64;  // K rows per shared-memory step
+constexpr int kCluster = 8; // blocks per cluster on the small-batch path
+
+__device__ __forceinline__ uint32_t cta_rank_in_cluster() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+__device__ __forceinline__ float ld_cluster_f32(const float* local, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(remote)
+                 : "r"(smem_u32(local)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
 
 template <int VPL, int KS>
 struct RhShape {
@@ -51,7 +74,12 @@ route_hidden_kernel(const void* __restrict__ x_raw, const float* __restrict__ w_
     float* red = ws + kChunk * VPL * 32;          // [kWarps][8][VPL * 32] (KS > 1)
     griddep_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int t0 = blockIdx.x * S::kTok;
+    // KS = 1: one block per 64 tokens, all of K. KS > 1: a cluster per 8 tokens, block r of
+    // it taking K rows [k_lo, k_hi)
+    const int crank = (KS == 1) ? 0 : (int)cta_rank_in_cluster();
+    const int t0 = (KS == 1 ? blockIdx.x : blockIdx.x / kCluster) * S::kTok;
+    const int k_span = (KS == 1) ? d : ((d + kCluster * kChunk - 1) / (kCluster * kChunk)) * kChunk;
+    const int k_lo = crank * k_span, k_hi = min(d, k_lo + k_span);
     const int tg = (KS == 1) ? warp : 0;          // this warp's 8 tokens within the block
     const int ks = (KS == 1) ? 0 : warp;          // this warp's rows: ks, ks + KS, ...
 
@@ -70,7 +98,7 @@ route_hidden_kernel(const void* __restrict__ x_raw, const float* __restrict__ w_
             const int t = i / kChunk, kk = i % kChunk;
             const int tok = t0 + t, col = k0 + kk;
             float v = 0.0f;
-            if (tok < T && col < d) {
+            if (tok < T && col < k_hi) {
                 if (kBf16)
                     v = __bfloat162float(
                         static_cast<const __nv_bfloat16*>(x_raw)[(size_t)tok * d + col]);
@@ -84,7 +112,7 @@ route_hidden_kernel(const void* __restrict__ x_raw, const float* __restrict__ w_
             const int i = threadIdx.x + m * kWarps * 32;
             const int kk = i / (VPL * 32), e = i % (VPL * 32);
             const int row = k0 + kk;
-            wr[m] = (row < d && e < E) ? __ldg(w_router + (size_t)row * E + e) : 0.0f;
+            wr[m] = (row < k_hi && e < E) ? __ldg(w_router + (size_t)row * E + e) : 0.0f;
         }
     };
     auto store_chunk = [&]() {
@@ -97,11 +125,11 @@ route_hidden_kernel(const void* __restrict__ x_raw, const float* __restrict__ w_
         for (int m = 0; m < S::kWPer; ++m) ws[threadIdx.x + m * kWarps * 32] = wr[m];
     };
 
-    load_chunk(0);
-    for (int k0 = 0; k0 < d; k0 += kChunk) {
+    if (k_lo < k_hi) load_chunk(k_lo);
+    for (int k0 = k_lo; k0 < k_hi; k0 += kChunk) {
         store_chunk();
         __syncthreads();
-        if (k0 + kChunk < d) load_chunk(k0 + kChunk);  // in flight during the FMAs below
+        if (k0 + kChunk < k_hi) load_chunk(k0 + kChunk);  // in flight during the FMAs below
 #pragma unroll 4
         for (int kk = ks; kk < kChunk; kk += KS) {
             float w[VPL];
@@ -118,23 +146,47 @@ route_hidden_kernel(const void* __restrict__ x_raw, const float* __restrict__ w_
     }
 
     if (KS > 1) {
-        // add the warps' partial sums in warp order; warp 0 keeps the result
+        // add the warps' partial sums in warp order (warp 0 keeps the block's sum in red
+        // slot 0), then the blocks' sums in rank order (block 0, through distributed shared
+        // memory); every block stays until block 0 has read its sum
 #pragma unroll
         for (int t = 0; t < kTokPerWarp; ++t)
 #pragma unroll
             for (int j = 0; j < VPL; ++j)
                 red[((warp * kTokPerWarp) + t) * VPL * 32 + lane + 32 * j] = acc[t][j];
         __syncthreads();
-        if (warp != 0) return;
+        if (warp == 0) {
 #pragma unroll
-        for (int t = 0; t < kTokPerWarp; ++t)
+            for (int t = 0; t < kTokPerWarp; ++t)
 #pragma unroll
-            for (int j = 0; j < VPL; ++j) {
-                float s = 0.0f;
-                for (int w = 0; w < kWarps; ++w)
-                    s += red[((w * kTokPerWarp) + t) * VPL * 32 + lane + 32 * j];
-                acc[t][j] = s;
-            }
+                for (int j = 0; j < VPL; ++j) {
+                    float s = 0.0f;
+                    for (int w = 0; w < kWarps; ++w)
+                        s += red[((w * kTokPerWarp) + t) * VPL * 32 + lane + 32 * j];
+                    acc[t][j] = s;
+                }
+        }
+        __syncthreads();  // every warp has read red before warp 0 overwrites slot 0
+        if (warp == 0) {
+#pragma unroll
+            for (int t = 0; t < kTokPerWarp; ++t)
+#pragma unroll
+                for (int j = 0; j < VPL; ++j) red[t * VPL * 32 + lane + 32 * j] = acc[t][j];
+        }
+        cluster_sync_all();
+        if (crank == 0 && warp == 0) {
+#pragma unroll
+            for (int t = 0; t < kTokPerWarp; ++t)
+#pragma unroll
+                for (int j = 0; j < VPL; ++j) {
+                    float s = 0.0f;
+                    for (int r = 0; r < kCluster; ++r)
+                        s += ld_cluster_f32(red + t * VPL * 32 + lane + 32 * j, (uint32_t)r);
+                    acc[t][j] = s;
+                }
+        }
+        cluster_sync_all();
+        if (crank != 0 || warp != 0) return;
     }
 
 #pragma unroll
@@ -177,17 +229,19 @@ cudaError_t launch_shape(const void* x, bool bf16, const float* w_router, const 
         });
         if (attr_err[which] != cudaSuccess) return attr_err[which];
     }
-    const dim3 grid((T + S::kTok - 1) / S::kTok), block(kWarps * 32);
-    return launch_kernel(kern, grid, block, S::kSmem, s, x, w_router, bias, T, d, E, k,
-                         score_fn, renorm, logits, ids, weights);
+    const int groups = (T + S::kTok - 1) / S::kTok;
+    const int cl = KS > 1 ? kCluster : 1;
+    return launch_kernel_ex(kern, dim3((unsigned)(groups * cl)), dim3(kWarps * 32), S::kSmem, s,
+                            cl, x, w_router, bias, T, d, E, k, score_fn, renorm, logits, ids,
+                            weights);
 }
 
 template <int VPL>
 cudaError_t launch_vpl(const void* x, bool bf16, const float* w_router, const float* bias, int T,
                        int d, int E, int k, int score_fn, int renorm, float* logits,
                        int32_t* ids, float* weights, cudaStream_t s) {
-    // up to 1024 tokens: 8 tokens per block, K split over the warps (more blocks, shorter
-    // dependent chains); beyond: 64 tokens per block
+    // up to 1024 tokens: a cluster of 8 blocks per 8 tokens, K split over blocks and warps
+    // (many blocks, short dependent chains); beyond: 64 tokens per block
     if (T <= 1024)
         return launch_shape<VPL, 8>(x, bf16, w_router, bias, T, d, E, k, score_fn, renorm,
                                     logits, ids, weights, s);

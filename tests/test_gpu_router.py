@@ -5,6 +5,8 @@ top-k in one kernel) with the CPU oracle.
   the fp32 roundings of the bias add and of the result), against the exact value;
 - ids and weights: bit-identical to moe_route run on the kernel's own logits (same warp
   router), and ids bit-exact against the oracle's route on those fp32 logits;
+- both launch shapes: clusters of 8 blocks splitting K (up to 1024 tokens) and 64 tokens per
+  block (above);
 - against the oracle's exact logits the ids may differ only where two experts' exact logits
   are closer than twice that bound (a near tie the fp32 sum cannot order); every such case is
   checked to be one.
@@ -30,6 +32,9 @@ CASES = [
     ("tiny_fp32", 256, 128, 8, 2, torch.float32, o.SOFTMAX, True, None),
     ("ragged", 67, 100, 37, 5, torch.bfloat16, o.SOFTMAX, False, "normal0.5"),
     ("e256", 70, 64, 256, 8, torch.float32, o.SIGMOID, True, None),
+    # above 1024 tokens: 64 tokens per block, all of K in one block (a ragged last block)
+    ("large_T", 1100, 2880, 128, 4, torch.bfloat16, o.SOFTMAX, True, "normal0.5"),
+    ("large_T_e256", 1090, 96, 256, 8, torch.bfloat16, o.SOFTMAX, True, None),
 ]
 
 
