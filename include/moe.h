@@ -139,10 +139,11 @@ moe_status moe_route(const float* logits, int T, int E, int k, moe_score_fn scor
  *   logits        device float [T, E] or NULL: when given, the logits the selection used.
  *   topk_ids, topk_weights, score_fn, flags: as moe_route; for the same logits the results are
  *                 bit-identical to moe_route's.
- *   Each logit is the sequential fp32 sum over i = 0 .. d-1 of x[t][i] * w_router[i][e]
- *   (fmaf, ascending i), then + bias[e]: it differs from an exact sum by at most about
- *   d * 2^-24 * sum_i |x[t][i] * w_router[i][e]|, so logits closer than that may rank
- *   differently than they would under exact arithmetic.
+ *   Each logit is an fp32 sum of the d products in an order fixed by the sizes (on the FP32
+ *   pipes; for more than 1024 bf16 tokens on the tensor pipe with w_router split into three
+ *   bf16 terms), then + bias[e]: it differs from the exact value by at most about
+ *   d * 2^-22 * sum_i |x[t][i] * w_router[i][e]|, so logits closer than that may rank
+ *   differently than they would under exact arithmetic. The results do not depend on timing.
  *   Constraints: 1 <= k <= E <= 256, d >= 1; pointers 16-byte aligned. T == 0 is a no-op.
  */
 moe_status moe_route_hidden(const void* x, moe_dtype dt, const float* w_router,

@@ -8,10 +8,11 @@
 // less. The top-k and weights are the warp router of route.cu (route_select_warp), fed from
 // registers, so for the same logits the ids and weights are bit-identical to moe_route.
 //
-// Layout: a block has 8 warps; lane l accumulates experts l, l+32, ... of 8 tokens (the
-// register layout the warp router reads). K is walked in chunks of 64 rows staged in shared
-// memory (x as fp32, W_r); the loads of chunk c + 1 are issued into registers before chunk c
-// is multiplied, so their latency hides behind the FMAs.
+// More than 1024 tokens of bf16 x run on the tensor pipe (route_hidden_mma_kernel below);
+// otherwise on the FP32 pipes. FP32-pipe layout: a block has 8 warps; lane l accumulates
+// experts l, l+32, ... of 8 tokens (the register layout the warp router reads). K is walked
+// in chunks of 64 rows staged in shared memory (x as fp32, W_r); the loads of chunk c + 1 are
+// issued into registers before chunk c is multiplied, so their latency hides behind the FMAs.
 //   - large batches (KS = 1): warp w owns tokens 8w .. 8w+7 of the block's 64 and sums each
 //     logit over K in ascending order;
 //   - small batches (KS = 8): a cluster of 8 blocks shares 8 tokens; block r of the cluster
@@ -213,6 +214,182 @@ route_hidden_kernel(const void* __restrict__ x_raw, const float* __restrict__ w_
     }
 }
 
+// ---- large batches of bf16 x on the tensor pipe ----
+// logits[64 tokens][EPAD experts] of a block = x (bf16, exact) times W_r split into three bf16
+// terms hi + mid + lo (together about 24 significant bits), each product on mma.sync
+// m16n8k16 with fp32 accumulation; K in chunks of 64 (the next chunk's loads in flight during
+// the MMAs). Warp w: tokens 16 (w % 4) .. +15, experts EPAD/2 * (w / 4) .. +EPAD/2. Then the
+// logits go through shared memory to the warp router's register layout (8 tokens per warp).
+template <int EPAD>
+struct MmaShape {
+    static constexpr int kNT = EPAD / 16;                 // n-tiles of 8 experts per warp
+    static constexpr int kXStride = kChunk * 2 + 16;      // bytes per x row (padded)
+    static constexpr int kWStride = EPAD * 2 + 16;        // bytes per W row of one plane
+    static constexpr int kXBytes = 64 * kXStride;
+    static constexpr int kPlaneBytes = kChunk * kWStride;
+    static constexpr int kWPer = kChunk * EPAD / 256;     // W values per thread per chunk
+    static constexpr size_t kSmem = (size_t)kXBytes + 3 * kPlaneBytes;
+    static_assert(3 * kPlaneBytes >= 64 * EPAD * 4, "logits must fit in the W planes");
+};
+
+template <int EPAD>
+__global__ void __launch_bounds__(256)
+route_hidden_mma_kernel(const __nv_bfloat16* __restrict__ x, const float* __restrict__ w_router,
+                        const float* __restrict__ bias, int T, int d, int E, int k,
+                        int score_fn, int renorm, float* __restrict__ logits,
+                        int32_t* __restrict__ ids, float* __restrict__ weights) {
+    using S = MmaShape<EPAD>;
+    extern __shared__ __align__(16) uint8_t rm_smem[];
+    uint8_t* xs = rm_smem;
+    uint8_t* wp = rm_smem + S::kXBytes;  // planes hi, mid, lo
+    griddep_wait();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t0 = blockIdx.x * 64;
+    const int m0 = 16 * (warp & 3), n_base = (EPAD / 2) * (warp >> 2);
+
+    float acc[S::kNT][4];
+#pragma unroll
+    for (int n = 0; n < S::kNT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.0f;
+
+    uint4 xr[2];
+    float wr[S::kWPer];
+    auto load_chunk = [&](int k0) {
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {  // 64 rows x 8 vectors of 8 bf16
+            const int i = threadIdx.x + 256 * m, r = i >> 3, c = (i & 7) * 8;
+            const int tok = t0 + r, col = k0 + c;
+            xr[m] = (tok < T && col < d)
+                        ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)tok * d + col))
+                        : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int m = 0; m < S::kWPer; ++m) {
+            const int i = threadIdx.x + 256 * m, r = i / EPAD, e = i % EPAD;
+            const int row = k0 + r;
+            wr[m] = (row < d && e < E) ? __ldg(w_router + (size_t)row * E + e) : 0.0f;
+        }
+    };
+    auto store_chunk = [&]() {
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int i = threadIdx.x + 256 * m, r = i >> 3, c = (i & 7) * 8;
+            *reinterpret_cast<uint4*>(xs + r * S::kXStride + c * 2) = xr[m];
+        }
+#pragma unroll
+        for (int m = 0; m < S::kWPer; ++m) {
+            const int i = threadIdx.x + 256 * m, r = i / EPAD, e = i % EPAD;
+            const float w = wr[m];
+            const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+            const float r1 = w - __bfloat162float(hi);
+            const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+            const int off = r * S::kWStride + e * 2;
+            *reinterpret_cast<__nv_bfloat16*>(wp + off) = hi;
+            *reinterpret_cast<__nv_bfloat16*>(wp + S::kPlaneBytes + off) = mid;
+            *reinterpret_cast<__nv_bfloat16*>(wp + 2 * S::kPlaneBytes + off) = lo;
+        }
+    };
+
+    load_chunk(0);
+    for (int k0 = 0; k0 < d; k0 += kChunk) {
+        store_chunk();
+        __syncthreads();
+        if (k0 + kChunk < d) load_chunk(k0 + kChunk);
+#pragma unroll
+        for (int ks = 0; ks < kChunk / 16; ++ks) {
+            // A: rows m0 + (l & 15), columns 16 ks + 8 (l >> 4) (ldmatrix.x4)
+            uint32_t a0, a1, a2, a3;
+            const uint32_t a_addr = smem_u32(xs + (m0 + (lane & 15)) * S::kXStride +
+                                             (16 * ks + 8 * (lane >> 4)) * 2);
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(a0), "=r"(a1), "=r"(a2), "=r"(a3)
+                         : "r"(a_addr));
+#pragma unroll
+            for (int np = 0; np < S::kNT / 2; ++np) {
+                // B of two n-tiles: rows 16 ks + (l & 7) + 8 ((l >> 3) & 1), columns
+                // n_base + 16 np + 8 (l >> 4) (ldmatrix.x4.trans from the [k][e] plane)
+                const int brow = 16 * ks + (lane & 7) + 8 * ((lane >> 3) & 1);
+                const int bcol = n_base + 16 * np + 8 * (lane >> 4);
+#pragma unroll
+                for (int pl = 0; pl < 3; ++pl) {
+                    uint32_t b0, b1, b2, b3;
+                    const uint32_t b_addr =
+                        smem_u32(wp + pl * S::kPlaneBytes + brow * S::kWStride + bcol * 2);
+                    asm volatile(
+                        "ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                        : "=r"(b0), "=r"(b1), "=r"(b2), "=r"(b3)
+                        : "r"(b_addr));
+                    asm volatile(
+                        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                        : "+f"(acc[2 * np][0]), "+f"(acc[2 * np][1]), "+f"(acc[2 * np][2]),
+                          "+f"(acc[2 * np][3])
+                        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+                    asm volatile(
+                        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+                        : "+f"(acc[2 * np + 1][0]), "+f"(acc[2 * np + 1][1]),
+                          "+f"(acc[2 * np + 1][2]), "+f"(acc[2 * np + 1][3])
+                        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b2), "r"(b3));
+                }
+            }
+        }
+        __syncthreads();
+    }
+
+    // C fragments (token m0 + l/4 [+8], expert 2 (l%4) [+1]) -> logits in shared memory
+    float* ls = reinterpret_cast<float*>(wp);  // [64][EPAD]
+#pragma unroll
+    for (int n = 0; n < S::kNT; ++n) {
+        const int e = n_base + 8 * n + 2 * (lane & 3), r = m0 + (lane >> 2);
+        ls[r * EPAD + e] = acc[n][0];
+        ls[r * EPAD + e + 1] = acc[n][1];
+        ls[(r + 8) * EPAD + e] = acc[n][2];
+        ls[(r + 8) * EPAD + e + 1] = acc[n][3];
+    }
+    __syncthreads();
+    constexpr int VPL = EPAD / 32;
+#pragma unroll 1
+    for (int t = 0; t < 8; ++t) {
+        const int r = 8 * warp + t, tok = t0 + r;
+        if (tok >= T) break;  // uniform across the warp
+        float v[VPL];
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) {
+            const int e = lane + 32 * j;
+            v[j] = -INFINITY;
+            if (e < E) {
+                v[j] = bias ? ls[r * EPAD + e] + __ldg(bias + e) : ls[r * EPAD + e];
+                if (logits) logits[(size_t)tok * E + e] = v[j];
+            }
+        }
+        int id;
+        float wt;
+        route_select_warp<VPL>(v, E, k, score_fn, renorm, lane, &id, &wt);
+        if (lane < k) {
+            ids[(size_t)tok * k + lane] = id;
+            weights[(size_t)tok * k + lane] = wt;
+        }
+    }
+}
+
+template <int EPAD>
+cudaError_t launch_mma(const void* x, const float* w_router, const float* bias, int T, int d,
+                       int E, int k, int score_fn, int renorm, float* logits, int32_t* ids,
+                       float* weights, cudaStream_t s) {
+    using S = MmaShape<EPAD>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(route_hidden_mma_kernel<EPAD>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kSmem);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    return launch_kernel(route_hidden_mma_kernel<EPAD>, dim3((T + 63) / 64), dim3(256), S::kSmem,
+                         s, static_cast<const __nv_bfloat16*>(x), w_router, bias, T, d, E, k,
+                         score_fn, renorm, logits, ids, weights);
+}
+
 template <int VPL, int KS>
 cudaError_t launch_shape(const void* x, bool bf16, const float* w_router, const float* bias,
                          int T, int d, int E, int k, int score_fn, int renorm, float* logits,
@@ -256,6 +433,12 @@ cudaError_t launch_route_hidden(const void* x, bool bf16, const float* w_router,
                                 bool renorm, float* logits, int32_t* ids, float* weights,
                                 cudaStream_t s) {
     const int rn = renorm ? 1 : 0;
+    // more than 1024 tokens of bf16 x (and d a multiple of 8): the tensor-pipe kernel
+    if (bf16 && T > 1024 && d % 8 == 0) {
+        if (E <= 64) return launch_mma<64>(x, w_router, bias, T, d, E, k, score_fn, rn, logits, ids, weights, s);
+        if (E <= 128) return launch_mma<128>(x, w_router, bias, T, d, E, k, score_fn, rn, logits, ids, weights, s);
+        return launch_mma<256>(x, w_router, bias, T, d, E, k, score_fn, rn, logits, ids, weights, s);
+    }
     if (E <= 32) return launch_vpl<1>(x, bf16, w_router, bias, T, d, E, k, score_fn, rn, logits, ids, weights, s);
     if (E <= 64) return launch_vpl<2>(x, bf16, w_router, bias, T, d, E, k, score_fn, rn, logits, ids, weights, s);
     if (E <= 128) return launch_vpl<4>(x, bf16, w_router, bias, T, d, E, k, score_fn, rn, logits, ids, weights, s);

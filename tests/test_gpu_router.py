@@ -1,8 +1,10 @@
 """Parity of the router from hidden states (moe_route_hidden: fp32 logits x @ W_r + b and the
 top-k in one kernel) with the CPU oracle.
 
-- logits: within the error bound of a sequential fp32 sum, d * 2^-24 * sum_i |x_i w_ie| (plus
-  the fp32 roundings of the bias add and of the result), against the exact value;
+- logits: within d * 2^-22 * sum_i |x_i w_ie| (plus the fp32 roundings of the bias add and of
+  the result) of the exact value: the error bound of an fp32 sum of d products, with room for
+  the tensor pipe's fp32 accumulation and the three-term bf16 split of W_r on the large-batch
+  bf16 path;
 - ids and weights: bit-identical to moe_route run on the kernel's own logits (same warp
   router), and ids bit-exact against the oracle's route on those fp32 logits;
 - both launch shapes: clusters of 8 blocks splitting K (up to 1024 tokens) and 64 tokens per
@@ -32,7 +34,8 @@ CASES = [
     ("tiny_fp32", 256, 128, 8, 2, torch.float32, o.SOFTMAX, True, None),
     ("ragged", 67, 100, 37, 5, torch.bfloat16, o.SOFTMAX, False, "normal0.5"),
     ("e256", 70, 64, 256, 8, torch.float32, o.SIGMOID, True, None),
-    # above 1024 tokens: 64 tokens per block, all of K in one block (a ragged last block)
+    # above 1024 tokens: 64 tokens per block, all of K in one block (a ragged last block); bf16
+    # x takes the tensor-pipe kernel
     ("large_T", 1100, 2880, 128, 4, torch.bfloat16, o.SOFTMAX, True, "normal0.5"),
     ("large_T_e256", 1090, 96, 256, 8, torch.bfloat16, o.SOFTMAX, True, None),
 ]
@@ -59,7 +62,7 @@ def test_route_hidden_matches_oracle(case):
     w64 = w.double().cpu().numpy()
     b64 = None if b is None else b.double().cpu().numpy()
     exact = o.router_logits(x64, w64, b64)
-    bound = (d * 2.0 ** -24 * (np.abs(x64) @ np.abs(w64))
+    bound = (d * 2.0 ** -22 * (np.abs(x64) @ np.abs(w64))
              + 2.0 ** -23 * np.abs(exact) + (0 if b64 is None else 2.0 ** -24 * np.abs(b64)))
     got = logits.double().cpu().numpy()
     assert np.all(np.abs(got - exact) <= bound), np.max(np.abs(got - exact) / bound)
