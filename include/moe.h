@@ -303,6 +303,144 @@ size_t moe_forward_workspace_size(int T, int d, int E, int k, int I, int Is, moe
  */
 int moe_forward_kernel_count(moe_dtype dt, int T, int k, int Is);
 
+/* ============================== training: backward pass ==============================
+ * [EP-intro] / [EP-dispatch]: the routing weights multiply the expert outputs, so a training
+ * step differentiates the layer with respect to x, the expert weights, the routing weights and,
+ * through the router's score function, the logits. Same conventions as above (caller-owned
+ * memory, checks before any launch, no host sync, graph-capturable). Readings (the pages give
+ * no backward formulas; each is the chain rule through the forward's steps in reverse):
+ *   - a bf16 layer keeps a = x W_gate, b = x W_up (before any router scale) as bf16 for the
+ *     backward pass ("ab" [R, 2I]); dy = w dout and d_ab are rounded to bf16 between kernels;
+ *     weight gradients, dx_sorted and the routing gradients are fp32; dx is rounded once.
+ *   - the top-k choice is piecewise constant: the logits' gradient flows only through the
+ *     weights of the selected experts.
+ * Layouts (row-major): dout dtype [T, d]; dy_sorted dtype [R, d]; ab, d_ab dtype [R, 2I]
+ * (gate half first); dx_sorted float [R, d]; d_w_gate_up float [E, d, 2I]; d_w_down float
+ * [E, I, d]; d_topk_weights float [T, k]; d_logits float [T, E]; dx dtype [T, d].
+ */
+
+/*
+ * moe_gate_up_train - moe_gate_up that also stores ab[p] = [x_rows[p] . W_gate | x_rows[p] .
+ *   W_up] (the fp32 accumulators before the MOE_SCALE_INPUT scale, rounded to dt) for
+ *   moe_down_backward. ab device dtype [R, 2I]; other arguments as moe_gate_up.
+ */
+moe_status moe_gate_up_train(const void* x_rows, const int32_t* offsets,
+                             const int32_t* sorted_to_slot, const float* topk_weights,
+                             moe_dtype dt, int R, int d, int E, int I, const void* w_gate_up,
+                             unsigned flags, void* h, void* ab, void* workspace,
+                             size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_combine_backward - gradient of moe_combine:
+ *   dy_sorted[p] = w[t, j] * dout[t] for p = slot_to_sorted[t*k + j] (w = 1 when topk_weights
+ *   is NULL), computed in fp32 and stored in dt; rows of negative slot_to_sorted entries are
+ *   not written.
+ *   d_topk_weights[t, j] = sum_c dout[t, c] * y_sorted[p, c] (fp32, one fixed-order sum per
+ *   slot; 0 for a negative entry). y_sorted is the forward's fp32 [R, d]; pass both y_sorted
+ *   and d_topk_weights, or neither.
+ */
+moe_status moe_combine_backward(const void* dout, const float* y_sorted,
+                                const int32_t* slot_to_sorted, const float* topk_weights,
+                                moe_dtype dt, int T, int d, int k, void* dy_sorted,
+                                float* d_topk_weights, moe_stream_t stream);
+
+/*
+ * moe_down_backward - gradient through the down projection and SwiGLU, for rows p of expert e:
+ *   dh = dy_sorted[p] . w_down[e]^T (fp32); s = topk_weights[sorted_to_slot[p]] with
+ *   MOE_SCALE_INPUT, else 1; a, b = ab[p] halves; g = s a, u = s b; sig = 1 / (1 + exp(-g));
+ *   dg = dh u sig (1 + g (1 - sig)), du = dh g sig;
+ *   d_ab[p] = [s dg | s du] stored in dt;
+ *   with MOE_SCALE_INPUT also d_topk_weights[sorted_to_slot[p]] = sum_c (dg_c a_c + du_c b_c)
+ *   (fp32; indexed by slot, R entries), the gradient of the score that scaled the input.
+ *   flags: MOE_SCALE_INPUT, MOE_WEIGHTS_PACKED (w_down packed by moe_pack_weights).
+ *   workspace: at least moe_down_backward_workspace_size(R, I, dt) bytes, 256-byte aligned.
+ */
+size_t moe_down_backward_workspace_size(int R, int I, moe_dtype dt);
+moe_status moe_down_backward(const void* dy_sorted, const void* ab, const int32_t* offsets,
+                             const int32_t* sorted_to_slot, const float* topk_weights,
+                             moe_dtype dt, int R, int d, int E, int I, const void* w_down,
+                             unsigned flags, void* d_ab, float* d_topk_weights, void* workspace,
+                             size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_gate_up_backward - dx_sorted[p] = d_ab[p] . w_gate_up[e]^T (fp32 [R, d]) for rows p of
+ *   expert e. flags: MOE_WEIGHTS_PACKED or 0. workspace: moe_experts_workspace_size() bytes.
+ */
+moe_status moe_gate_up_backward(const void* d_ab, const int32_t* offsets, moe_dtype dt, int R,
+                                int d, int E, int I, const void* w_gate_up, unsigned flags,
+                                float* dx_sorted, void* workspace, size_t ws_bytes,
+                                moe_stream_t stream);
+
+/*
+ * moe_weight_grad - per-expert weight gradient: dw[e] = a[rows of e]^T . b[rows of e]
+ *   (fp32 accumulate, fp32 out). a device dt [R, M], b device dt [R, N], dw device float
+ *   [E, M, N], every expert's block written (zero for an expert with no rows). offsets as for
+ *   moe_gate_up (NULL: one expert owning all R rows). M and N multiples of 8 (bf16) / 4 (fp32).
+ *   (x_sorted, d_ab) gives d_w_gate_up [E, d, 2I]; (h, dy_sorted) gives d_w_down [E, I, d].
+ *   workspace: moe_experts_workspace_size() bytes.
+ */
+moe_status moe_weight_grad(const void* a, const void* b, const int32_t* offsets, moe_dtype dt,
+                           int R, int M, int N, int E, float* dw, void* workspace,
+                           size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_route_backward - gradient of moe_route's weights with respect to the logits, the
+ *   selected ids held fixed (g = d_topk_weights[t], w = topk_weights[t], inner = sum_j w_j g_j):
+ *   softmax, renormalised:   d_logits[t, ids_j] = w_j (g_j - inner), 0 for other experts;
+ *   softmax over all E:      d_logits[t, m] = p_m (G_m - inner), p = softmax of the row,
+ *                            G_m = g_j if m = ids_j else 0;
+ *   sigmoid:                 d_logits[t, ids_j] = g_j w_j (1 - w_j);
+ *   sigmoid, renormalised:   d_logits[t, ids_j] = (g_j - inner) / S * sig_j (1 - sig_j),
+ *                            sig_j = 1 / (1 + exp(-l_j)), S = sum_j sig_j.
+ *   flags: MOE_RENORMALIZE or 0 (as given to moe_route). d_logits device float [T, E], all of
+ *   it written.
+ */
+moe_status moe_route_backward(const float* logits, const int32_t* topk_ids,
+                              const float* topk_weights, const float* d_topk_weights, int T,
+                              int E, int k, moe_score_fn score_fn, unsigned flags,
+                              float* d_logits, moe_stream_t stream);
+
+/*
+ * moe_forward_train - moe_forward for a training step: the same outputs, plus what
+ *   moe_backward reads, kept in its workspace (counts, offsets, both permutations, x_sorted,
+ *   h, y_sorted and ab; for a shared expert its h and ab). Never takes the one-kernel decode
+ *   path; MOE_FUSE_COMBINE_WEIGHT returns MOE_ERR_UNSUPPORTED (the routing weights' gradient
+ *   needs the unweighted y_sorted). workspace: moe_forward_train_workspace_size(...) bytes.
+ */
+size_t moe_forward_train_workspace_size(int T, int d, int E, int k, int I, int Is,
+                                        moe_dtype dt);
+moe_status moe_forward_train(const void* x, const float* logits, moe_dtype dt, int T, int d,
+                             int E, int k, int I, moe_score_fn score_fn, unsigned flags,
+                             const void* w_gate_up, const void* w_down,
+                             const void* w_shared_gate_up, const void* w_shared_down, int Is,
+                             int32_t* topk_ids, float* topk_weights, void* out, void* workspace,
+                             size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_backward - the whole backward pass of the layer moe_forward_train ran (same x, logits,
+ *   weights, flags, topk_ids/topk_weights and its workspace `fwd_workspace`, unchanged):
+ *   combine backward, the down and gate/up projections' weight and input gradients (the
+ *   SwiGLU backward in between), the shared expert's (dy = dout), the transpose of the
+ *   dispatch (dx[t] = sum_j dx_sorted[slot_to_sorted[t*k + j]] + the shared expert's, fp32
+ *   sum, rounded once to dt), then the router backward.
+ *   Outputs: dx dtype [T, d]; d_w_gate_up, d_w_down (and the shared d_w_shared_gate_up [d, 2Is],
+ *   d_w_shared_down [Is, d]) fp32; d_topk_weights fp32 [T, k] (may be NULL); d_logits fp32
+ *   [T, E] (may be NULL; needs logits). flags: MOE_RENORMALIZE | MOE_SCALE_INPUT |
+ *   MOE_WEIGHTS_PACKED. workspace: moe_backward_workspace_size(...) bytes, 256-byte aligned.
+ */
+size_t moe_backward_workspace_size(int T, int d, int E, int k, int I, int Is, moe_dtype dt);
+moe_status moe_backward(const void* dout, const void* x, const float* logits, moe_dtype dt, int T,
+                        int d, int E, int k, int I, moe_score_fn score_fn, unsigned flags,
+                        const void* w_gate_up, const void* w_down, const void* w_shared_gate_up,
+                        const void* w_shared_down, int Is, const int32_t* topk_ids,
+                        const float* topk_weights, const void* fwd_workspace,
+                        size_t fwd_ws_bytes, void* dx, float* d_w_gate_up, float* d_w_down,
+                        float* d_w_shared_gate_up, float* d_w_shared_down,
+                        float* d_topk_weights, float* d_logits, void* workspace,
+                        size_t ws_bytes, moe_stream_t stream);
+/* Number of kernels moe_backward enqueues (memsets not counted). */
+int moe_backward_kernel_count(int T, int k, int Is, unsigned flags, int want_logits);
+
 /*
  * moe_read_device_status - synchronise `stream`, then return the status word the kernels of
  * the last call that used `workspace` left there (MOE_OK if none). Diagnostics only.

@@ -56,10 +56,14 @@ moe_status launch_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE
 constexpr long long kMaxRowsF32 = 60000ll * 32;
 
 struct ForwardLayout {
-    size_t fcnt, counts, offsets, chunk, s2p, p2s, x_sorted, h, y, h_sh, y_sh, fused, total;
+    size_t fcnt, counts, offsets, chunk, s2p, p2s, x_sorted, h, y, h_sh, y_sh, fused, ab, ab_sh,
+        total;
 };
 
-ForwardLayout forward_layout(int T, int d, int E, int k, int I, int Is, moe_dtype dt) {
+// train: the layout of moe_forward_train (no one-kernel decode path; the gate/up accumulators
+// of the routed rows and of the shared expert are kept for the backward pass, after the rest)
+ForwardLayout forward_layout(int T, int d, int E, int k, int I, int Is, moe_dtype dt,
+                             bool train = false) {
     const size_t R = (size_t)T * k, b = dtype_bytes(dt);
     ForwardLayout L;
     size_t o = kStatusBytes;
@@ -70,7 +74,7 @@ ForwardLayout forward_layout(int T, int d, int E, int k, int I, int Is, moe_dtyp
     };
     // the fused decode kernel's counters follow the status word (one memset clears both);
     // its partial sums go last
-    const bool fused = decode_fused_applies(dt, T, k, Is);
+    const bool fused = !train && decode_fused_applies(dt, T, k, Is);
     const DecodeFusedLayout F = decode_fused_layout(T, d, k, I);
     L.fcnt = take(fused ? F.counter_bytes : 0);
     L.counts = take((size_t)E * 4);
@@ -84,6 +88,35 @@ ForwardLayout forward_layout(int T, int d, int E, int k, int I, int Is, moe_dtyp
     L.h_sh = take(Is > 0 ? (size_t)T * Is * b : 0);
     L.y_sh = take(Is > 0 ? (size_t)T * d * 4 : 0);
     L.fused = take(fused ? F.part_bytes : 0);
+    L.ab = take(train ? R * 2 * (size_t)I * b : 0);
+    L.ab_sh = take(train && Is > 0 ? (size_t)T * 2 * Is * b : 0);
+    L.total = o;
+    return L;
+}
+
+struct BackwardLayout {
+    size_t dy, d_ab, dx_sorted, part, dw_tmp, d_ab_sh, dx_sh, total;
+};
+
+// moe_backward's workspace: status word, dy_sorted, d_ab, dx_sorted, the router-score partial
+// sums, a [T, k] buffer for the routing weights' gradient (when the caller wants only the
+// logits'), and the shared expert's d_ab and dx, each rounded up to 256 bytes
+BackwardLayout backward_layout(int T, int d, int k, int I, int Is, moe_dtype dt) {
+    const size_t R = (size_t)T * k, b = dtype_bytes(dt);
+    BackwardLayout L;
+    size_t o = kStatusBytes;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = round_up(o + bytes, 256);
+        return at;
+    };
+    L.dy = take(R * d * b);
+    L.d_ab = take(R * 2 * (size_t)I * b);
+    L.dx_sorted = take(R * d * 4);
+    L.part = take(R * (size_t)((I + 31) / 32) * 4);
+    L.dw_tmp = take(R * 4);
+    L.d_ab_sh = take(Is > 0 ? (size_t)T * 2 * Is * b : 0);
+    L.dx_sh = take(Is > 0 ? (size_t)T * d * 4 : 0);
     L.total = o;
     return L;
 }
@@ -95,7 +128,7 @@ moe_status clear_status(void* workspace, cudaStream_t s) {
 moe_status run_gemm(GemmKind kind, const void* a, const void* b, bool packed,
                     const int32_t* offsets, const int32_t* s2p, const float* w, bool scale,
                     moe_dtype dt, int R, int K, int N, int E, void* out, int* status,
-                    cudaStream_t s) {
+                    cudaStream_t s, void* ab = nullptr) {
     GroupedGemmArgs g;
     g.kind = kind;
     g.a = a;
@@ -112,6 +145,7 @@ moe_status run_gemm(GemmKind kind, const void* a, const void* b, bool packed,
     g.E = E;
     g.out = out;
     g.status = status;
+    g.ab = ab;
     const cudaError_t e =
         dt == MOE_BF16 ? launch_grouped_gemm_bf16(g, s) : launch_grouped_gemm_f32(g, s);
     return launch_status(e);
@@ -341,11 +375,14 @@ int moe_forward_kernel_count(moe_dtype dt, int T, int k, int Is) {
     return front + 2 + (Is > 0 ? 2 : 0) + 1;
 }
 
-moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, int d, int E,
-                       int k, int I, moe_score_fn score_fn, unsigned flags, const void* w_gate_up,
-                       const void* w_down, const void* w_shared_gate_up,
-                       const void* w_shared_down, int Is, int32_t* topk_ids, float* topk_weights,
-                       void* out, void* workspace, size_t ws_bytes, moe_stream_t stream) {
+// moe_forward, and with train = true moe_forward_train
+static moe_status forward_impl(const void* x, const float* logits, moe_dtype dt, int T, int d,
+                               int E, int k, int I, moe_score_fn score_fn, unsigned flags,
+                               const void* w_gate_up, const void* w_down,
+                               const void* w_shared_gate_up, const void* w_shared_down, int Is,
+                               int32_t* topk_ids, float* topk_weights, void* out,
+                               void* workspace, size_t ws_bytes, moe_stream_t stream,
+                               bool train) {
     moe_status st = check_tek(T, E, k);
     if (st != MOE_OK) return st;
     if (!dtype_ok(dt)) return MOE_ERR_INVALID_ARG;
@@ -358,6 +395,8 @@ moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, 
     const bool packed = (flags & MOE_WEIGHTS_PACKED) != 0;
     if (packed && dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     if (scale && fuse_w) return MOE_ERR_INVALID_ARG;
+    // training keeps y_sorted unweighted: the routing weights' gradient reads it
+    if (train && fuse_w) return MOE_ERR_UNSUPPORTED;
     if (d < 1 || I < 1 || Is < 0) return MOE_ERR_INVALID_ARG;
     if (d % row_multiple(dt) != 0 || I % row_multiple(dt) != 0 || Is % row_multiple(dt) != 0)
         return MOE_ERR_INVALID_ARG;
@@ -372,7 +411,7 @@ moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, 
                           topk_ids, topk_weights, out};
     for (const void* q : ptrs)
         if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
-    const ForwardLayout L = forward_layout(T, d, E, k, I, Is, dt);
+    const ForwardLayout L = forward_layout(T, d, E, k, I, Is, dt, train);
     if (!workspace || !aligned256(workspace) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
 
     cudaStream_t s = (cudaStream_t)stream;
@@ -391,7 +430,7 @@ moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, 
     const int R = T * k;
 
     const bool renorm = (flags & MOE_RENORMALIZE) != 0;
-    if (decode_fused_applies(dt, T, k, Is)) {
+    if (!train && decode_fused_applies(dt, T, k, Is)) {
         // decode: the whole layer in one cooperative kernel; its counters sit right after the
         // status word and are cleared with it
         if ((st = launch_status(cudaMemsetAsync(workspace, 0, L.counts, s))) != MOE_OK)
@@ -448,14 +487,15 @@ moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, 
             return st;
     }
     if ((st = run_gemm(kGateUp, xs, w_gate_up, packed, offsets, s2p, topk_weights, scale, dt, R,
-                       d, I, E, h, status, s)) != MOE_OK)
+                       d, I, E, h, status, s, train ? ws + L.ab : nullptr)) != MOE_OK)
         return st;
     if ((st = run_gemm(kDown, h, w_down, packed, offsets, s2p, topk_weights, fuse_w, dt, R, I, d,
                        E, y, status, s)) != MOE_OK)
         return st;
     if (shared) {
         if ((st = run_gemm(kGateUp, x, w_shared_gate_up, packed, nullptr, nullptr, nullptr, false,
-                           dt, T, d, Is, 1, h_sh, status, s)) != MOE_OK)
+                           dt, T, d, Is, 1, h_sh, status, s,
+                           train ? ws + L.ab_sh : nullptr)) != MOE_OK)
             return st;
         if ((st = run_gemm(kDown, h_sh, w_shared_down, packed, nullptr, nullptr, nullptr, false,
                            dt, T, Is, d, 1, y_sh, status, s)) != MOE_OK)
@@ -464,6 +504,347 @@ moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, 
     const float* comb_w = (scale || fuse_w) ? nullptr : topk_weights;
     return launch_status(launch_combine(y, p2s, comb_w, shared ? y_sh : nullptr, T, d, k,
                                         dt == MOE_BF16, out, s));
+}
+
+moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, int d, int E,
+                       int k, int I, moe_score_fn score_fn, unsigned flags, const void* w_gate_up,
+                       const void* w_down, const void* w_shared_gate_up,
+                       const void* w_shared_down, int Is, int32_t* topk_ids, float* topk_weights,
+                       void* out, void* workspace, size_t ws_bytes, moe_stream_t stream) {
+    return forward_impl(x, logits, dt, T, d, E, k, I, score_fn, flags, w_gate_up, w_down,
+                        w_shared_gate_up, w_shared_down, Is, topk_ids, topk_weights, out,
+                        workspace, ws_bytes, stream, false);
+}
+
+moe_status moe_forward_train(const void* x, const float* logits, moe_dtype dt, int T, int d,
+                             int E, int k, int I, moe_score_fn score_fn, unsigned flags,
+                             const void* w_gate_up, const void* w_down,
+                             const void* w_shared_gate_up, const void* w_shared_down, int Is,
+                             int32_t* topk_ids, float* topk_weights, void* out, void* workspace,
+                             size_t ws_bytes, moe_stream_t stream) {
+    return forward_impl(x, logits, dt, T, d, E, k, I, score_fn, flags, w_gate_up, w_down,
+                        w_shared_gate_up, w_shared_down, Is, topk_ids, topk_weights, out,
+                        workspace, ws_bytes, stream, true);
+}
+
+size_t moe_forward_train_workspace_size(int T, int d, int E, int k, int I, int Is,
+                                        moe_dtype dt) {
+    if (T < 0 || d < 1 || E < 1 || k < 1 || I < 1 || Is < 0 || !dtype_ok(dt)) return 0;
+    return forward_layout(T, d, E, k, I, Is, dt, true).total;
+}
+
+moe_status moe_gate_up_train(const void* x_rows, const int32_t* offsets,
+                             const int32_t* sorted_to_slot, const float* topk_weights,
+                             moe_dtype dt, int R, int d, int E, int I, const void* w_gate_up,
+                             unsigned flags, void* h, void* ab, void* workspace,
+                             size_t ws_bytes, moe_stream_t stream) {
+    if (flags & ~(unsigned)(MOE_SCALE_INPUT | MOE_WEIGHTS_PACKED)) return MOE_ERR_INVALID_ARG;
+    const bool scale = (flags & MOE_SCALE_INPUT) != 0;
+    const bool packed = (flags & MOE_WEIGHTS_PACKED) != 0;
+    if (packed && dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    moe_status st = check_experts_args(offsets, sorted_to_slot, topk_weights, scale, dt, R, d, E,
+                                       I, workspace, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (R == 0) return MOE_OK;
+    if (!x_rows || !w_gate_up || !h || !ab) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_rows) || !aligned16(w_gate_up) || !aligned16(h) || !aligned16(ab))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((st = clear_status(workspace, s)) != MOE_OK) return st;
+    return run_gemm(kGateUp, x_rows, w_gate_up, packed, offsets, sorted_to_slot, topk_weights,
+                    scale, dt, R, d, I, E, h, static_cast<int*>(workspace), s, ab);
+}
+
+moe_status moe_combine_backward(const void* dout, const float* y_sorted,
+                                const int32_t* slot_to_sorted, const float* topk_weights,
+                                moe_dtype dt, int T, int d, int k, void* dy_sorted,
+                                float* d_topk_weights, moe_stream_t stream) {
+    if (!dtype_ok(dt) || T < 0 || d < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+    if (k > kMaxK || (long long)T * k >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+    if (d % row_multiple(dt) != 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!dout || !slot_to_sorted || !dy_sorted) return MOE_ERR_INVALID_ARG;
+    if ((d_topk_weights != nullptr) != (y_sorted != nullptr)) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {dout, y_sorted, slot_to_sorted, topk_weights, dy_sorted,
+                          d_topk_weights};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    return launch_status(launch_combine_backward(dout, dt == MOE_BF16, y_sorted, slot_to_sorted,
+                                                 topk_weights, T, d, k, dy_sorted,
+                                                 d_topk_weights, (cudaStream_t)stream));
+}
+
+size_t moe_down_backward_workspace_size(int R, int I, moe_dtype dt) {
+    if (R < 0 || I < 1 || !dtype_ok(dt)) return 0;
+    // per-(row, column tile) partial sums of the router-score gradient: 256-column tiles on the
+    // tensor cores, 32-column tiles on the fp32 path
+    const int tiles = (I + 31) / 32;
+    return kStatusBytes + round_up((size_t)R * tiles * 4, 256);
+}
+
+static int scale_tiles(moe_dtype dt, int I) {
+    return dt == MOE_BF16 ? (I + kBwdTileN - 1) / kBwdTileN : (I + 31) / 32;
+}
+
+static moe_status run_dgrad(BwdKind kind, const void* a, const void* w, bool packed,
+                            const int32_t* offsets, const int32_t* s2p, const float* tw,
+                            bool scale, const void* ab, void* out, float* part, moe_dtype dt,
+                            int R, int d, int I, int E, int* status, cudaStream_t s) {
+    DgradArgs g;
+    g.kind = kind;
+    g.a = a;
+    g.w = w;
+    g.packed = packed;
+    g.offsets = offsets;
+    g.sorted_to_slot = s2p;
+    g.topk_weights = tw;
+    g.scale_rows = scale;
+    g.ab = ab;
+    g.out = out;
+    g.scale_part = part;
+    g.R = R;
+    g.d = d;
+    g.I = I;
+    g.E = E;
+    g.status = status;
+    return launch_status(dt == MOE_BF16 ? launch_dgrad_bf16(g, s) : launch_dgrad_f32(g, s));
+}
+
+static moe_status run_wgrad(const void* a, const void* b, const int32_t* offsets, moe_dtype dt,
+                            int R, int M, int N, int E, float* dw, int* status, cudaStream_t s) {
+    const int groups = offsets ? E : 1;
+    if (R == 0)  // no rows at all: every expert's gradient is zero
+        return launch_status(cudaMemsetAsync(dw, 0, (size_t)groups * M * N * 4, s));
+    WgradArgs g;
+    g.a = a;
+    g.b = b;
+    g.offsets = offsets;
+    g.R = R;
+    g.M = M;
+    g.N = N;
+    g.E = E;
+    g.dw = dw;
+    g.status = status;
+    return launch_status(dt == MOE_BF16 ? launch_wgrad_bf16(g, s) : launch_wgrad_f32(g, s));
+}
+
+moe_status moe_down_backward(const void* dy_sorted, const void* ab, const int32_t* offsets,
+                             const int32_t* sorted_to_slot, const float* topk_weights,
+                             moe_dtype dt, int R, int d, int E, int I, const void* w_down,
+                             unsigned flags, void* d_ab, float* d_topk_weights, void* workspace,
+                             size_t ws_bytes, moe_stream_t stream) {
+    if (flags & ~(unsigned)(MOE_SCALE_INPUT | MOE_WEIGHTS_PACKED)) return MOE_ERR_INVALID_ARG;
+    const bool scale = (flags & MOE_SCALE_INPUT) != 0;
+    const bool packed = (flags & MOE_WEIGHTS_PACKED) != 0;
+    if (packed && dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    moe_status st = check_experts_args(offsets, sorted_to_slot, topk_weights, scale, dt, R, d, E,
+                                       I, workspace, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (ws_bytes < moe_down_backward_workspace_size(R, I, dt)) return MOE_ERR_WORKSPACE;
+    if (scale && !d_topk_weights) return MOE_ERR_INVALID_ARG;
+    if (R == 0) return MOE_OK;
+    if (!dy_sorted || !ab || !w_down || !d_ab) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {dy_sorted, ab, sorted_to_slot, topk_weights, w_down, d_ab,
+                          d_topk_weights};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((st = clear_status(workspace, s)) != MOE_OK) return st;
+    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
+    if ((st = run_dgrad(kDgradDown, dy_sorted, w_down, packed, offsets, sorted_to_slot,
+                        topk_weights, scale, ab, d_ab, part, dt, R, d, I, E,
+                        static_cast<int*>(workspace), s)) != MOE_OK)
+        return st;
+    if (!scale) return MOE_OK;
+    PdlScope pdl(true);
+    return launch_status(
+        launch_scale_grad(part, R, scale_tiles(dt, I), sorted_to_slot, d_topk_weights, s));
+}
+
+moe_status moe_gate_up_backward(const void* d_ab, const int32_t* offsets, moe_dtype dt, int R,
+                                int d, int E, int I, const void* w_gate_up, unsigned flags,
+                                float* dx_sorted, void* workspace, size_t ws_bytes,
+                                moe_stream_t stream) {
+    if (flags & ~(unsigned)MOE_WEIGHTS_PACKED) return MOE_ERR_INVALID_ARG;
+    const bool packed = (flags & MOE_WEIGHTS_PACKED) != 0;
+    if (packed && dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    moe_status st = check_experts_args(offsets, nullptr, nullptr, false, dt, R, d, E, I,
+                                       workspace, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (R == 0) return MOE_OK;
+    if (!d_ab || !w_gate_up || !dx_sorted) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(d_ab) || !aligned16(w_gate_up) || !aligned16(dx_sorted))
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if ((st = clear_status(workspace, s)) != MOE_OK) return st;
+    return run_dgrad(kDgradGateUp, d_ab, w_gate_up, packed, offsets, nullptr, nullptr, false,
+                     nullptr, dx_sorted, nullptr, dt, R, d, I, E, static_cast<int*>(workspace),
+                     s);
+}
+
+moe_status moe_weight_grad(const void* a, const void* b, const int32_t* offsets, moe_dtype dt,
+                           int R, int M, int N, int E, float* dw, void* workspace,
+                           size_t ws_bytes, moe_stream_t stream) {
+    if (!dtype_ok(dt) || R < 0 || M < 1 || N < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+    if (E > kMaxE) return MOE_ERR_UNSUPPORTED;
+    if (offsets == nullptr && E != 1) return MOE_ERR_INVALID_ARG;
+    if (M % row_multiple(dt) != 0 || N % row_multiple(dt) != 0) return MOE_ERR_INVALID_ARG;
+    if (!dw || (R > 0 && (!a || !b))) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {a, b, offsets, dw};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    if (workspace == nullptr || !aligned256(workspace) || ws_bytes < kStatusBytes)
+        return MOE_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    moe_status st = clear_status(workspace, s);
+    if (st != MOE_OK) return st;
+    return run_wgrad(a, b, offsets, dt, R, M, N, E, dw, static_cast<int*>(workspace), s);
+}
+
+moe_status moe_route_backward(const float* logits, const int32_t* topk_ids,
+                              const float* topk_weights, const float* d_topk_weights, int T,
+                              int E, int k, moe_score_fn score_fn, unsigned flags,
+                              float* d_logits, moe_stream_t stream) {
+    moe_status st = check_tek(T, E, k);
+    if (st != MOE_OK) return st;
+    if (score_fn != MOE_SCORE_SOFTMAX && score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)MOE_RENORMALIZE) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!logits || !topk_ids || !topk_weights || !d_topk_weights || !d_logits)
+        return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {logits, topk_ids, topk_weights, d_topk_weights, d_logits};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
+    return launch_status(launch_route_backward(logits, topk_ids, topk_weights, d_topk_weights, T,
+                                               E, k, (int)score_fn,
+                                               (flags & MOE_RENORMALIZE) != 0, d_logits,
+                                               (cudaStream_t)stream));
+}
+
+size_t moe_backward_workspace_size(int T, int d, int E, int k, int I, int Is, moe_dtype dt) {
+    if (T < 0 || d < 1 || E < 1 || k < 1 || I < 1 || Is < 0 || !dtype_ok(dt)) return 0;
+    return backward_layout(T, d, k, I, Is, dt).total;
+}
+
+int moe_backward_kernel_count(int T, int k, int Is, unsigned flags, int want_logits) {
+    if (T <= 0 || k <= 0) return 0;
+    const bool scale = (flags & MOE_SCALE_INPUT) != 0;
+    // combine backward, down wgrad, down dgrad (+ score gradient), gate_up wgrad and dgrad,
+    // the shared expert's four, the transpose of the dispatch, the router backward
+    return 1 + 2 + (scale ? 1 : 0) + 2 + (Is > 0 ? 4 : 0) + 1 + (want_logits ? 1 : 0);
+}
+
+moe_status moe_backward(const void* dout, const void* x, const float* logits, moe_dtype dt, int T,
+                        int d, int E, int k, int I, moe_score_fn score_fn, unsigned flags,
+                        const void* w_gate_up, const void* w_down, const void* w_shared_gate_up,
+                        const void* w_shared_down, int Is, const int32_t* topk_ids,
+                        const float* topk_weights, const void* fwd_workspace,
+                        size_t fwd_ws_bytes, void* dx, float* d_w_gate_up, float* d_w_down,
+                        float* d_w_shared_gate_up, float* d_w_shared_down,
+                        float* d_topk_weights, float* d_logits, void* workspace,
+                        size_t ws_bytes, moe_stream_t stream) {
+    moe_status st = check_tek(T, E, k);
+    if (st != MOE_OK) return st;
+    if (!dtype_ok(dt)) return MOE_ERR_INVALID_ARG;
+    if (score_fn != MOE_SCORE_SOFTMAX && score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)(MOE_RENORMALIZE | MOE_SCALE_INPUT | MOE_WEIGHTS_PACKED))
+        return MOE_ERR_INVALID_ARG;
+    const bool scale = (flags & MOE_SCALE_INPUT) != 0;
+    const bool packed = (flags & MOE_WEIGHTS_PACKED) != 0;
+    if (packed && dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (d < 1 || I < 1 || Is < 0) return MOE_ERR_INVALID_ARG;
+    if (d % row_multiple(dt) != 0 || I % row_multiple(dt) != 0 || Is % row_multiple(dt) != 0)
+        return MOE_ERR_INVALID_ARG;
+    const bool shared = Is > 0;
+    if (shared != (w_shared_gate_up != nullptr) || shared != (w_shared_down != nullptr) ||
+        shared != (d_w_shared_gate_up != nullptr) || shared != (d_w_shared_down != nullptr))
+        return MOE_ERR_INVALID_ARG;
+    if (dt == MOE_F32 && ((long long)T * k > kMaxRowsF32)) return MOE_ERR_UNSUPPORTED;
+    if (d_logits && !logits) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!dout || !x || !w_gate_up || !w_down || !topk_ids || !topk_weights || !dx ||
+        !d_w_gate_up || !d_w_down || !fwd_workspace)
+        return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {dout, x, logits, w_gate_up, w_down, w_shared_gate_up, w_shared_down,
+                          topk_ids, topk_weights, dx, d_w_gate_up, d_w_down, d_w_shared_gate_up,
+                          d_w_shared_down, d_topk_weights, d_logits};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    const ForwardLayout F = forward_layout(T, d, E, k, I, Is, dt, true);
+    if (!aligned256(fwd_workspace) || fwd_ws_bytes < F.total) return MOE_ERR_WORKSPACE;
+    const BackwardLayout L = backward_layout(T, d, k, I, Is, dt);
+    if (!workspace || !aligned256(workspace) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    const uint8_t* fw = static_cast<const uint8_t*>(fwd_workspace);
+    const int32_t* offsets = reinterpret_cast<const int32_t*>(fw + F.offsets);
+    const int32_t* s2p = reinterpret_cast<const int32_t*>(fw + F.s2p);
+    const int32_t* p2s = reinterpret_cast<const int32_t*>(fw + F.p2s);
+    const void* xs = fw + F.x_sorted;
+    const void* h = fw + F.h;
+    const float* y = reinterpret_cast<const float*>(fw + F.y);
+    const void* ab = fw + F.ab;
+    const void* h_sh = fw + F.h_sh;
+    const void* ab_sh = fw + F.ab_sh;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* status = reinterpret_cast<int*>(ws);
+    void* dy = ws + L.dy;
+    void* d_ab = ws + L.d_ab;
+    float* dxs = reinterpret_cast<float*>(ws + L.dx_sorted);
+    float* part = reinterpret_cast<float*>(ws + L.part);
+    float* dw = d_topk_weights ? d_topk_weights : reinterpret_cast<float*>(ws + L.dw_tmp);
+    void* d_ab_sh = ws + L.d_ab_sh;
+    float* dx_sh = reinterpret_cast<float*>(ws + L.dx_sh);
+    const int R = T * k;
+
+    if ((st = clear_status(workspace, s)) != MOE_OK) return st;
+    // combine: dy = w dout (dout itself when the score scaled the input), d w = dout . y
+    if ((st = launch_status(launch_combine_backward(dout, dt == MOE_BF16, scale ? nullptr : y,
+                                                    p2s, scale ? nullptr : topk_weights, T, d,
+                                                    k, dy, scale ? nullptr : dw, s))) != MOE_OK)
+        return st;
+    PdlScope pdl(true);
+    // down projection: d W_down = h^T dy; dh = dy W_down^T through the SwiGLU backward
+    if ((st = run_wgrad(h, dy, offsets, dt, R, I, d, E, d_w_down, status, s)) != MOE_OK)
+        return st;
+    if ((st = run_dgrad(kDgradDown, dy, w_down, packed, offsets, s2p, topk_weights, scale, ab,
+                        d_ab, part, dt, R, d, I, E, status, s)) != MOE_OK)
+        return st;
+    if (scale && (st = launch_status(launch_scale_grad(part, R, scale_tiles(dt, I), s2p, dw,
+                                                       s))) != MOE_OK)
+        return st;
+    // gate/up projection: d W_gate_up = x_sorted^T d_ab; dx_sorted = d_ab W_gate_up^T
+    if ((st = run_wgrad(xs, d_ab, offsets, dt, R, d, 2 * I, E, d_w_gate_up, status, s)) !=
+        MOE_OK)
+        return st;
+    if ((st = run_dgrad(kDgradGateUp, d_ab, w_gate_up, packed, offsets, nullptr, nullptr, false,
+                        nullptr, dxs, nullptr, dt, R, d, I, E, status, s)) != MOE_OK)
+        return st;
+    if (shared) {
+        // the shared expert sees the unscaled x with weight 1: its dy is dout
+        if ((st = run_wgrad(h_sh, dout, nullptr, dt, T, Is, d, 1, d_w_shared_down, status, s)) !=
+            MOE_OK)
+            return st;
+        if ((st = run_dgrad(kDgradDown, dout, w_shared_down, packed, nullptr, nullptr, nullptr,
+                            false, ab_sh, d_ab_sh, nullptr, dt, T, d, Is, 1, status, s)) !=
+            MOE_OK)
+            return st;
+        if ((st = run_wgrad(x, d_ab_sh, nullptr, dt, T, d, 2 * Is, 1, d_w_shared_gate_up, status,
+                            s)) != MOE_OK)
+            return st;
+        if ((st = run_dgrad(kDgradGateUp, d_ab_sh, w_shared_gate_up, packed, nullptr, nullptr,
+                            nullptr, false, nullptr, dx_sh, nullptr, dt, T, d, Is, 1, status,
+                            s)) != MOE_OK)
+            return st;
+    }
+    // the dispatch's transpose: dx[t] = sum_j dx_sorted[slot_to_sorted[t k + j]] (+ shared)
+    if ((st = launch_status(launch_combine(dxs, p2s, nullptr, shared ? dx_sh : nullptr, T, d, k,
+                                           dt == MOE_BF16, dx, s))) != MOE_OK)
+        return st;
+    if (!d_logits) return MOE_OK;
+    return launch_status(launch_route_backward(logits, topk_ids, topk_weights, dw, T, E, k,
+                                               (int)score_fn, (flags & MOE_RENORMALIZE) != 0,
+                                               d_logits, s));
 }
 
 moe_status moe_read_device_status(const void* workspace, moe_stream_t stream) {

@@ -91,6 +91,11 @@ __global__ void __launch_bounds__(256) simt_grouped_gemm(GroupedGemmArgs p) {
             const int col = n0 + tx * 2 + j;
             if (col >= N) continue;
             if (kGU) {
+                if (p.ab) {  // the unscaled accumulators, kept for the backward pass
+                    float* ab = static_cast<float*>(p.ab) + (size_t)row * 2 * N;
+                    ab[col] = acc[0][i][j];
+                    ab[N + col] = acc[1][i][j];
+                }
                 const float g = acc[0][i][j] * s, u = acc[1][i][j] * s;
                 out[(size_t)row * N + col] = g / (1.0f + expf(-g)) * u;
             } else {

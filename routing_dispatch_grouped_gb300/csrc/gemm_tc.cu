@@ -52,6 +52,7 @@ struct TcParams {
     int row_scale;   // gate_up: scale accumulators; down: weight rows
     int packed;      // weights in the packed layout (PackedGeom below)
     int nb, nbh, kpad;
+    __nv_bfloat16* ab;  // gate_up for training: [g | u] before the row scale, [R, 2N]
 };
 
 struct __align__(8) SmemTail {
@@ -343,6 +344,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld_32x32b_x32(tbase + 128 + c * 32, u);
                     tmem_ld_wait();
                     const int col0 = ti.n0 + c * 32;
+                    if (row_ok && p.ab) {
+                        // the unscaled accumulators, kept for the backward pass
+                        __nv_bfloat16* ab = p.ab + (size_t)row * 2 * p.N + col0;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            if (col0 + v * 8 < p.N) {
+                                uint32_t wg[4], wu[4];
+#pragma unroll
+                                for (int h2 = 0; h2 < 4; ++h2) {
+                                    const int i = v * 8 + h2 * 2;
+                                    wg[h2] = pack_bf16x2(__uint_as_float(g[i]),
+                                                         __uint_as_float(g[i + 1]));
+                                    wu[h2] = pack_bf16x2(__uint_as_float(u[i]),
+                                                         __uint_as_float(u[i + 1]));
+                                }
+                                reinterpret_cast<uint4*>(ab)[v] = make_uint4(wg[0], wg[1], wg[2], wg[3]);
+                                reinterpret_cast<uint4*>(ab + p.N)[v] =
+                                    make_uint4(wu[0], wu[1], wu[2], wu[3]);
+                            }
+                        }
+                    }
                     if (row_ok) {
                         uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * p.N + col0);
 #pragma unroll
@@ -485,6 +507,7 @@ cudaError_t launch_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     p.nb = g.nb;
     p.nbh = g.nbh;
     p.kpad = g.kpad;
+    p.ab = static_cast<__nv_bfloat16*>(a.ab);
 
     // upper bound on tiles: sum_e ceil(n_e / 128) <= R / 128 + groups
     const long long m_ub = (long long)(a.R + kTileM - 1) / kTileM + groups;

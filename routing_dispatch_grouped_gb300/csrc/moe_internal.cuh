@@ -215,6 +215,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
     return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// The same with A's major-ness chosen too (bit 15 = 1: A MN-major).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_ab(int M, int N, bool a_mn_major,
+                                                         bool b_mn_major) {
+    return idesc_bf16_f32(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
+}
 
 // ---------------------------------------------------------------------------------------------
 // programmatic dependent launch
@@ -372,6 +377,9 @@ struct GroupedGemmArgs {
     int R, K, N, E;           // N = I for gate_up (h columns), d for down
     void* out;                // h [R, I] (layer dtype) or y_sorted [R, d] fp32
     int* status;
+    void* ab = nullptr;       // gate_up for training: also store [g | u] before the row scale
+                              // ([R, 2I], layer dtype); only the 128-row-tile kernel and the
+                              // fp32 kernel write it
 };
 // Batches with at most this many routed rows use the small-batch (decode) GEMM configuration.
 constexpr int kSmallBatchRows = 512;
@@ -389,5 +397,55 @@ bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const cu
 cudaError_t launch_grouped_gemm_f32(const GroupedGemmArgs& a, cudaStream_t s);
 
 int device_sm_count();
+
+// ---------------------------------------------------------------------------------------------
+// backward pass (gemm_bwd.cu: tensor cores; backward.cu: fp32 layers and the small kernels)
+// ---------------------------------------------------------------------------------------------
+// dgrad: out[p] = a[p] . W[e]^T for the rows p of expert e (a [R, K] in the layer dtype).
+//   kDgradDown: a = dy_sorted [R, d], W = w_down [E, I, d] (K = d, N = I); the epilogue is the
+//     SwiGLU backward: reads ab [R, 2I], writes d_ab [R, 2I] (layer dtype) and, with a row
+//     scale, per-(row, 256-column tile) partial sums of d_scale into scale_part [R, n_tiles].
+//   kDgradGateUp: a = d_ab [R, 2I], W = w_gate_up [E, d, 2I] (K = 2I, N = d); fp32 output
+//     dx_sorted [R, d].
+enum BwdKind { kDgradDown = 0, kDgradGateUp = 1 };
+constexpr int kBwdTileN = 256;  // output columns per dgrad tile (scale_part has one per tile)
+struct DgradArgs {
+    BwdKind kind;
+    const void* a;            // dy_sorted or d_ab
+    const void* w;            // w_down or w_gate_up ([TP-packed] layout or packed)
+    bool packed;
+    const int32_t* offsets;   // [E + 1] or nullptr (one group of R rows)
+    const int32_t* sorted_to_slot;
+    const float* topk_weights;
+    bool scale_rows;          // kDgradDown: router score scales the expert input
+    const void* ab;           // kDgradDown: saved accumulators [R, 2I]
+    void* out;                // d_ab (layer dtype) or dx_sorted (fp32)
+    float* scale_part;        // kDgradDown with scale_rows: [R, ceil(I / 256)]
+    int R, d, I, E;
+    int* status;
+};
+cudaError_t launch_dgrad_bf16(const DgradArgs& a, cudaStream_t s);
+cudaError_t launch_dgrad_f32(const DgradArgs& a, cudaStream_t s);
+// wgrad: dw[e] = a[rows of e]^T . b[rows of e], a [R, M], b [R, N] (layer dtype), dw fp32
+// [E, M, N]; every expert's block is written (zero for an expert without rows).
+struct WgradArgs {
+    const void* a;
+    const void* b;
+    const int32_t* offsets;   // [E + 1] or nullptr
+    int R, M, N, E;
+    float* dw;
+    int* status;
+};
+cudaError_t launch_wgrad_bf16(const WgradArgs& a, cudaStream_t s);
+cudaError_t launch_wgrad_f32(const WgradArgs& a, cudaStream_t s);
+cudaError_t launch_combine_backward(const void* dout, bool bf16, const float* y_sorted,
+                                    const int32_t* slot_to_sorted, const float* weights, int T,
+                                    int d, int k, void* dy_sorted, float* d_weights,
+                                    cudaStream_t s);
+cudaError_t launch_scale_grad(const float* scale_part, int R, int n_tiles,
+                              const int32_t* sorted_to_slot, float* d_weights, cudaStream_t s);
+cudaError_t launch_route_backward(const float* logits, const int32_t* ids, const float* weights,
+                                  const float* d_weights, int T, int E, int k, int score_fn,
+                                  bool renorm, float* d_logits, cudaStream_t s);
 
 }  // namespace rdg

@@ -43,6 +43,22 @@ SIGNATURES = {
                          _P, _P, _S, _P]),
     "moe_forward_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_forward_kernel_count": (_I, [_I, _I, _I, _I]),
+    "moe_gate_up_train": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _U, _P, _P, _P, _S,
+                               _P]),
+    "moe_combine_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
+    "moe_down_backward_workspace_size": (_S, [_I, _I, _I]),
+    "moe_down_backward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _U, _P, _P, _P, _S,
+                               _P]),
+    "moe_gate_up_backward": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _U, _P, _P, _S, _P]),
+    "moe_weight_grad": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _S, _P]),
+    "moe_route_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _U, _P, _P]),
+    "moe_forward_train_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
+    "moe_forward_train": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P,
+                               _P, _P, _P, _S, _P]),
+    "moe_backward_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
+    "moe_backward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P,
+                          _P, _P, _S, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
+    "moe_backward_kernel_count": (_I, [_I, _I, _I, _U, _I]),
     "moe_read_device_status": (_I, [_P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -344,4 +360,244 @@ def forward_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is, dtype):
     if Is:
         out["h_shared"] = v["h_shared"].view(dtype).view(T, Is)
         out["y_shared"] = v["y_shared"].view(torch.float32).view(T, d)
+    return out
+
+
+# ------------------------------------------------------------------------------------------------
+# training: the forward that keeps what the backward reads, and the backward pass
+# ------------------------------------------------------------------------------------------------
+def _code(dtype):
+    return BF16 if dtype == torch.bfloat16 else F32
+
+
+def moe_gate_up_train(x_rows, offsets, w_gate_up, sorted_to_slot=None, topk_weights=None,
+                      scale_input=False, h=None, ab=None, workspace=None, stream=None):
+    """moe_gate_up that also returns ab = [x W_gate | x W_up] (unscaled, layer dtype)."""
+    _need(x_rows, "x_rows")
+    R, d = x_rows.shape
+    E, _, I, pk = _w_dims(w_gate_up, W_GATE_UP)
+    dev = x_rows.device
+    h = h if h is not None else torch.empty(R, I, dtype=x_rows.dtype, device=dev)
+    ab = ab if ab is not None else torch.empty(R, 2 * I, dtype=x_rows.dtype, device=dev)
+    ws = workspace if workspace is not None else _workspace(moe_experts_workspace_size(), dev)
+    _check("moe_gate_up_train", lib().moe_gate_up_train(
+        _p(x_rows), _p(offsets), _p(sorted_to_slot), _p(topk_weights), _dt(x_rows), R, d, E, I,
+        _p(w_gate_up), (SCALE_INPUT if scale_input else 0) | pk, _p(h), _p(ab), _p(ws),
+        ws.numel(), _stream(stream)))
+    return h, ab
+
+
+def moe_combine_backward(dout, slot_to_sorted, k, topk_weights=None, y_sorted=None,
+                         want_weight_grad=True, dy_sorted=None, d_topk_weights=None,
+                         stream=None):
+    """Returns (dy_sorted [R, d] in dout's dtype, d_topk_weights [T, k] fp32 or None)."""
+    _need(dout, "dout")
+    T, d = dout.shape
+    R = slot_to_sorted.numel()
+    dev = dout.device
+    dy = dy_sorted if dy_sorted is not None else torch.empty(R, d, dtype=dout.dtype, device=dev)
+    dw = None
+    if want_weight_grad:
+        dw = d_topk_weights if d_topk_weights is not None else torch.empty(
+            T, k, dtype=torch.float32, device=dev)
+    _check("moe_combine_backward", lib().moe_combine_backward(
+        _p(dout), _p(y_sorted if want_weight_grad else None), _p(slot_to_sorted),
+        _p(topk_weights), _dt(dout), T, d, k, _p(dy), _p(dw), _stream(stream)))
+    return dy, dw
+
+
+def moe_down_backward(dy_sorted, ab, offsets, w_down, sorted_to_slot=None, topk_weights=None,
+                      scale_input=False, d_ab=None, d_topk_weights=None, workspace=None,
+                      stream=None):
+    """Returns (d_ab [R, 2I], d_topk_weights by slot [R] fp32 or None)."""
+    _need(dy_sorted, "dy_sorted")
+    R, d = dy_sorted.shape
+    E, I, _, pk = _w_dims(w_down, W_DOWN)
+    dev = dy_sorted.device
+    d_ab = d_ab if d_ab is not None else torch.empty(R, 2 * I, dtype=dy_sorted.dtype, device=dev)
+    dw = None
+    if scale_input:
+        dw = d_topk_weights if d_topk_weights is not None else torch.empty(
+            R, dtype=torch.float32, device=dev)
+    ws = workspace if workspace is not None else _workspace(
+        lib().moe_down_backward_workspace_size(R, I, _dt(dy_sorted)), dev)
+    _check("moe_down_backward", lib().moe_down_backward(
+        _p(dy_sorted), _p(ab), _p(offsets), _p(sorted_to_slot), _p(topk_weights), _dt(dy_sorted),
+        R, d, E, I, _p(w_down), (SCALE_INPUT if scale_input else 0) | pk, _p(d_ab), _p(dw),
+        _p(ws), ws.numel(), _stream(stream)))
+    return d_ab, dw
+
+
+def moe_gate_up_backward(d_ab, offsets, w_gate_up, dx_sorted=None, workspace=None, stream=None):
+    """Returns dx_sorted [R, d] fp32."""
+    _need(d_ab, "d_ab")
+    R = d_ab.shape[0]
+    E, d, I, pk = _w_dims(w_gate_up, W_GATE_UP)
+    dev = d_ab.device
+    dx = dx_sorted if dx_sorted is not None else torch.empty(R, d, dtype=torch.float32, device=dev)
+    ws = workspace if workspace is not None else _workspace(moe_experts_workspace_size(), dev)
+    _check("moe_gate_up_backward", lib().moe_gate_up_backward(
+        _p(d_ab), _p(offsets), _dt(d_ab), R, d, E, I, _p(w_gate_up), pk, _p(dx), _p(ws),
+        ws.numel(), _stream(stream)))
+    return dx
+
+
+def moe_weight_grad(a, b, offsets, E, dw=None, workspace=None, stream=None):
+    """dw[e] = a[rows of e]^T b[rows of e]: [E, M, N] fp32."""
+    _need(a, "a")
+    _need(b, "b")
+    R, M = a.shape
+    N = b.shape[1]
+    dev = a.device
+    dw = dw if dw is not None else torch.empty(E, M, N, dtype=torch.float32, device=dev)
+    ws = workspace if workspace is not None else _workspace(moe_experts_workspace_size(), dev)
+    _check("moe_weight_grad", lib().moe_weight_grad(
+        _p(a), _p(b), _p(offsets), _dt(a), R, M, N, E, _p(dw), _p(ws), ws.numel(),
+        _stream(stream)))
+    return dw
+
+
+def moe_route_backward(logits, topk_ids, topk_weights, d_topk_weights, score_fn=SOFTMAX,
+                       renormalize=True, d_logits=None, stream=None):
+    _need(logits, "logits")
+    T, E = logits.shape
+    k = topk_ids.shape[1]
+    dl = d_logits if d_logits is not None else torch.empty(T, E, dtype=torch.float32,
+                                                           device=logits.device)
+    _check("moe_route_backward", lib().moe_route_backward(
+        _p(logits), _p(topk_ids), _p(topk_weights), _p(d_topk_weights), T, E, k, score_fn,
+        RENORMALIZE if renormalize else 0, _p(dl), _stream(stream)))
+    return dl
+
+
+def moe_forward_train_workspace_size(T, d, E, k, I, Is, dtype) -> int:
+    return lib().moe_forward_train_workspace_size(T, d, E, k, I, Is, _code(dtype))
+
+
+def moe_forward_train(x, logits, w_gate_up, w_down, k, score_fn=SOFTMAX, flags=RENORMALIZE,
+                      w_shared_gate_up=None, w_shared_down=None, out=None, topk_ids=None,
+                      topk_weights=None, workspace=None, stream=None):
+    """moe_forward for training. Returns (out, topk_ids, topk_weights, workspace); the
+    workspace holds what moe_backward reads."""
+    _need(x, "x")
+    _need(logits, "logits")
+    T, d = x.shape
+    E, _, I, pk = _w_dims(w_gate_up, W_GATE_UP)
+    flags |= pk
+    Is = _shared_width(w_shared_gate_up)
+    dev = x.device
+    out = out if out is not None else torch.empty(T, d, dtype=x.dtype, device=dev)
+    ids = topk_ids if topk_ids is not None else torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = topk_weights if topk_weights is not None else torch.empty(T, k, dtype=torch.float32,
+                                                                  device=dev)
+    ws = workspace if workspace is not None else _workspace(
+        moe_forward_train_workspace_size(T, d, E, k, I, Is, x.dtype), dev)
+    _check("moe_forward_train", lib().moe_forward_train(
+        _p(x), _p(logits), _dt(x), T, d, E, k, I, score_fn, flags, _p(w_gate_up), _p(w_down),
+        _p(w_shared_gate_up), _p(w_shared_down), Is, _p(ids), _p(w), _p(out), _p(ws), ws.numel(),
+        _stream(stream)))
+    return out, ids, w, ws
+
+
+def _shared_width(w_shared_gate_up):
+    if w_shared_gate_up is None:
+        return 0
+    return (w_shared_gate_up.N if isinstance(w_shared_gate_up, PackedWeights)
+            else w_shared_gate_up.shape[-1] // 2)
+
+
+def moe_backward_workspace_size(T, d, E, k, I, Is, dtype) -> int:
+    return lib().moe_backward_workspace_size(T, d, E, k, I, Is, _code(dtype))
+
+
+def moe_backward_kernel_count(T, k, Is, flags, want_logits=True) -> int:
+    return lib().moe_backward_kernel_count(T, k, Is, flags, 1 if want_logits else 0)
+
+
+def moe_backward(dout, x, logits, w_gate_up, w_down, k, topk_ids, topk_weights, fwd_workspace,
+                 score_fn=SOFTMAX, flags=RENORMALIZE, w_shared_gate_up=None, w_shared_down=None,
+                 want_logits=True, out=None, workspace=None, stream=None):
+    """The whole backward pass for a moe_forward_train call with the same arguments.
+    Returns a dict: dx, d_w_gate_up, d_w_down, d_topk_weights, d_logits (None unless
+    want_logits) and, with a shared expert, d_w_shared_gate_up, d_w_shared_down. `out` may
+    pass preallocated tensors under those names."""
+    _need(dout, "dout")
+    T, d = dout.shape
+    E, _, I, pk = _w_dims(w_gate_up, W_GATE_UP)
+    flags |= pk
+    Is = _shared_width(w_shared_gate_up)
+    dev = dout.device
+    o = dict(out or {})
+    f32 = torch.float32
+
+    def get(name, shape, dtype):
+        if o.get(name) is None:
+            o[name] = torch.empty(*shape, dtype=dtype, device=dev)
+        return o[name]
+
+    dx = get("dx", (T, d), dout.dtype)
+    dwgu = get("d_w_gate_up", (E, d, 2 * I), f32)
+    dwd = get("d_w_down", (E, I, d), f32)
+    dtw = get("d_topk_weights", (T, k), f32)
+    dl = get("d_logits", (T, E), f32) if want_logits else None
+    o.setdefault("d_logits", dl)
+    dsgu = get("d_w_shared_gate_up", (d, 2 * Is), f32) if Is else None
+    dsd = get("d_w_shared_down", (Is, d), f32) if Is else None
+    ws = workspace if workspace is not None else _workspace(
+        moe_backward_workspace_size(T, d, E, k, I, Is, dout.dtype), dev)
+    _check("moe_backward", lib().moe_backward(
+        _p(dout), _p(x), _p(logits), _dt(dout), T, d, E, k, I, score_fn, flags, _p(w_gate_up),
+        _p(w_down), _p(w_shared_gate_up), _p(w_shared_down), Is, _p(topk_ids), _p(topk_weights),
+        _p(fwd_workspace), fwd_workspace.numel(), _p(dx), _p(dwgu), _p(dwd), _p(dsgu), _p(dsd),
+        _p(dtw), _p(dl), _p(ws), ws.numel(), _stream(stream)))
+    o["workspace"] = ws
+    return o
+
+
+def backward_workspace_views(ws: torch.Tensor, T, d, k, I, dtype):
+    """Views of the intermediates moe_backward leaves in its workspace (for tests): dy_sorted
+    [R, d], d_ab [R, 2I] (layer dtype) and dx_sorted [R, d] fp32, after the 256-byte status word,
+    each rounded up to 256 bytes."""
+    R = T * k
+    b = 2 if dtype == torch.bfloat16 else 4
+    views, o = {}, 256
+    for name, nbytes in [("dy_sorted", R * d * b), ("d_ab", R * 2 * I * b),
+                         ("dx_sorted", R * d * 4)]:
+        views[name] = ws[o:o + nbytes]
+        o = (o + nbytes + 255) // 256 * 256
+    return {"dy_sorted": views["dy_sorted"].view(dtype).view(R, d),
+            "d_ab": views["d_ab"].view(dtype).view(R, 2 * I),
+            "dx_sorted": views["dx_sorted"].view(torch.float32).view(R, d)}
+
+
+def forward_train_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is, dtype):
+    """forward_workspace_views for moe_forward_train's workspace, plus "ab" [R, 2I] and (shared
+    expert) "ab_shared" [T, 2Is]."""
+    R = T * k
+    b = 2 if dtype == torch.bfloat16 else 4
+    nchunks = (R + 255) // 256
+    sizes = [("counts", E * 4), ("offsets", (E + 1) * 4), ("chunk", nchunks * E * 4),
+             ("sorted_to_slot", R * 4), ("slot_to_sorted", R * 4), ("x_sorted", R * d * b),
+             ("h", R * I * b), ("y_sorted", R * d * 4), ("h_shared", T * Is * b),
+             ("y_shared", T * d * 4 if Is else 0), ("fused", 0), ("ab", R * 2 * I * b),
+             ("ab_shared", T * 2 * Is * b)]
+    views, o = {}, 256
+    for name, nbytes in sizes:
+        views[name] = ws[o:o + nbytes]
+        o = (o + nbytes + 255) // 256 * 256
+    v = views
+    out = {
+        "counts": v["counts"].view(torch.int32),
+        "offsets": v["offsets"].view(torch.int32),
+        "sorted_to_slot": v["sorted_to_slot"].view(torch.int32),
+        "slot_to_sorted": v["slot_to_sorted"].view(torch.int32),
+        "x_sorted": v["x_sorted"].view(dtype).view(R, d),
+        "h": v["h"].view(dtype).view(R, I),
+        "y_sorted": v["y_sorted"].view(torch.float32).view(R, d),
+        "ab": v["ab"].view(dtype).view(R, 2 * I),
+    }
+    if Is:
+        out["h_shared"] = v["h_shared"].view(dtype).view(T, Is)
+        out["y_shared"] = v["y_shared"].view(torch.float32).view(T, d)
+        out["ab_shared"] = v["ab_shared"].view(dtype).view(T, 2 * Is)
     return out
