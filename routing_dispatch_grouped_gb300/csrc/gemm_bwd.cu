@@ -31,7 +31,7 @@
 namespace rdg {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kMaxStages = 4;
 constexpr int kABytes = 128 * 64 * 2;              // 16 KB: 128 rows x 64 K (dgrad) or 2 x 8 KB
 constexpr int kBBytes = 256 * 64 * 2;              // 32 KB: 256 rows x 64 K or 4 x 8 KB
 constexpr int kStageBytes = kABytes + kBBytes;     // 48 KB
@@ -62,8 +62,8 @@ struct BwdParams {
 };
 
 struct __align__(8) SmemTail {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
@@ -76,7 +76,26 @@ struct __align__(8) SmemTail {
     int order[kMaxE];       // wgrad: experts by descending row count
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(SmemTail);
+// Shared memory of each mode (after 1024-byte alignment):
+//   dgrad: 4 stages | tail | (gate_up) a per-warp 32 x 32 fp32 transpose buffer, rows padded to
+//          33 floats (no bank conflicts either way), so each store instruction writes 128
+//          contiguous bytes of one row of dx_sorted;
+//   wgrad: 3 stages | per-warp double-buffered 32 x 32 fp32 staging tiles in the 128-byte
+//          swizzled layout of a TMA store (the tensor map clips the dW block's edges) | tail.
+// The wgrad epilogue moves 128 KB per tile against a K loop of a few blocks: full-line TMA
+// stores keep it off the shared-memory and L2 request paths that per-row stores saturate.
+constexpr int kXposeFloats = 4 * 32 * 33;
+constexpr int kStagingBytes = 4 * 2 * 32 * 32 * 4;  // 32 KB
+template <int MODE>
+struct Layout {
+    static constexpr int stages = MODE == kModeWgrad ? 3 : 4;
+    static constexpr size_t staging = (size_t)stages * kStageBytes;  // 1024-byte aligned
+    static constexpr size_t tail = staging + (MODE == kModeWgrad ? kStagingBytes : 0);
+    static constexpr size_t xpose = tail + sizeof(SmemTail);
+    static constexpr size_t bytes =
+        1024 + xpose + (MODE == kModeDgradGateUp ? (size_t)kXposeFloats * 4 : 0);
+    static_assert(bytes <= 232448, "exceeds the 227 KB of shared memory a block may use");
+};
 
 struct Tile {
     int e;        // expert
@@ -135,11 +154,13 @@ __device__ __forceinline__ Tile decode_tile(const SmemTail& st, const BwdParams&
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const BwdParams p) {
+                const __grid_constant__ CUtensorMap tmO, const BwdParams p) {
+    constexpr int kStages = Layout<MODE>::stages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + (size_t)kStages * kStageBytes);
+    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + Layout<MODE>::tail);
+    float* xpose = reinterpret_cast<float*>(smem + Layout<MODE>::xpose);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
 
@@ -296,12 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (valid < 64) {
                         // rows [valid, 64) belong to the next expert (or lie past R): zero them
                         // in the six 8 KB blocks (2 of a, 4 of b); a block row is 128 bytes
-                        const int nrow = 64 - valid;
-                        for (int i = lane; i < 6 * nrow * 8; i += 32) {
-                            const int blk = i / (nrow * 8), rem = i - blk * (nrow * 8);
-                            const int r = valid + rem / 8, c16 = rem & 7;
-                            *reinterpret_cast<uint4*>(sa + blk * kBlk + r * 128 + c16 * 16) =
-                                make_uint4(0u, 0u, 0u, 0u);
+                        for (int i = valid * 8 + lane; i < 64 * 8; i += 32) {
+                            // 16-byte chunk i & 7 of block row i >> 3, in all six blocks
+                            uint8_t* row = sa + (i >> 3) * 128 + (i & 7) * 16;
+#pragma unroll
+                            for (int blk = 0; blk < 6; ++blk)
+                                *reinterpret_cast<uint4*>(row + blk * kBlk) =
+                                    make_uint4(0u, 0u, 0u, 0u);
                         }
                         fence_proxy_async_smem();  // generic stores -> tensor-core reads
                         __syncwarp();
@@ -354,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ================= epilogue (warps 2..5) =================
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         uint32_t it = 0;
+        uint32_t n_store = 0;    // wgrad: TMA stores this warp issued
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
             const Tile t = decode_tile<MODE>(st, p, tile);
             const uint32_t acc = it & 1u;
@@ -367,53 +390,67 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t tbase = tmem_base + acc * 256 + ((uint32_t)(q * 32) << 16);
             if (MODE == kModeWgrad) {
-                const int m = t.m0 + q * 32 + lane;  // dW row of this thread
-                float* dst_row = static_cast<float*>(p.out) +
-                                 ((size_t)t.e * p.M + (m < p.M ? m : 0)) * p.N;
+                // dW rows [m0 + 32 q, +32) of this warp, 32 columns at a time: lane = row writes
+                // its 32 values into a swizzled staging tile (16-byte chunk c of row r at chunk
+                // c ^ (r & 7)), then lane 0 stores the tile with TMA. Two tiles per warp: a tile
+                // is rewritten only after the store issued two chunks earlier has read it.
+                const uint32_t stg = smem_u32(smem + Layout<MODE>::staging) + q * 8192;
+                const bool zero = t.kbs == 0;  // an expert without rows: zero gradient
 #pragma unroll 1
                 for (int c = 0; c < 8; ++c) {
+                    if (t.n0 + c * 32 >= p.N) break;
                     uint32_t v[32];
-                    if (t.kbs > 0) {
+                    if (!zero) {
                         tmem_ld_32x32b_x32(tbase + c * 32, v);
                         tmem_ld_wait();
                     } else {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = 0u;
                     }
-                    const int col0 = t.n0 + c * 32;
-                    if (m < p.M) {
+                    const uint32_t buf = stg + (uint32_t)(n_store & 1) * 4096;
+                    if (lane == 0) bulk_wait_read<1>();
+                    __syncwarp();
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            if (col0 + 4 * j < p.N)
-                                *reinterpret_cast<float4*>(dst_row + col0 + 4 * j) =
-                                    make_float4(__uint_as_float(v[4 * j]),
-                                                __uint_as_float(v[4 * j + 1]),
-                                                __uint_as_float(v[4 * j + 2]),
-                                                __uint_as_float(v[4 * j + 3]));
-                        }
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t a = buf + lane * 128 + ((j ^ (lane & 7)) << 4);
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                     "r"(v[4 * j]), "r"(v[4 * j + 1]), "r"(v[4 * j + 2]),
+                                     "r"(v[4 * j + 3])
+                                     : "memory");
                     }
+                    fence_proxy_async_smem();  // generic stores -> the TMA engine's reads
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_3d(&tmO, buf, t.n0 + c * 32, t.m0 + q * 32, t.e);
+                        bulk_commit();
+                    }
+                    ++n_store;
                 }
             } else if (MODE == kModeDgradGateUp) {
-                const int row = t.row0 + q * 32 + lane;
-                const bool row_ok = row < t.row_end;
-                float* dst_row = static_cast<float*>(p.out) + (size_t)(row_ok ? row : 0) * p.N;
+                // fp32 rows [row0 + 32 q, +32) of dx_sorted, written row by row after a transpose
+                // through shared memory (lane = column inside a 32-column chunk); rows past the
+                // expert's end belong to another tile and are not written
+                float* xp = xpose + q * 32 * 33;
+                const int r0 = t.row0 + q * 32;
+                float* base = static_cast<float*>(p.out);
 #pragma unroll 1
                 for (int c = 0; c < 8; ++c) {
+                    const int col = t.n0 + c * 32 + lane;
+                    if (t.n0 + c * 32 >= p.N) break;
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tbase + c * 32, v);
                     tmem_ld_wait();
-                    const int col0 = t.n0 + c * 32;
-                    if (row_ok) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            if (col0 + 4 * j < p.N)
-                                *reinterpret_cast<float4*>(dst_row + col0 + 4 * j) =
-                                    make_float4(__uint_as_float(v[4 * j]),
-                                                __uint_as_float(v[4 * j + 1]),
-                                                __uint_as_float(v[4 * j + 2]),
-                                                __uint_as_float(v[4 * j + 3]));
+                    for (int j = 0; j < 32; ++j) xp[lane * 33 + j] = __uint_as_float(v[j]);
+                    __syncwarp();
+                    if (col < p.N) {
+#pragma unroll 4
+                        for (int r = 0; r < 32; ++r) {
+                            if (r0 + r < t.row_end)
+                                base[(size_t)(r0 + r) * p.N + col] = xp[r * 33 + lane];
                         }
                     }
+                    __syncwarp();
                 }
             } else {
                 // SwiGLU backward on dh (the accumulator) with the saved a, b of this row
@@ -478,6 +515,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&st.tempty[acc]);
         }
+        // the staging tiles must stay valid until the stores have read them, and the stores
+        // must be done before the kernel ends
+        if (MODE == kModeWgrad && lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     // ---- teardown ----
@@ -497,21 +538,21 @@ cudaError_t set_smem_attr() {
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
         err = cudaFuncSetAttribute(tc_bwd_gemm<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)kSmemBytes);
+                                   (int)Layout<MODE>::bytes);
     });
     return err;
 }
 
 template <int MODE>
-cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const BwdParams& p,
-                        long long tiles_ub, cudaStream_t s) {
+cudaError_t launch_mode(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO,
+                        const BwdParams& p, long long tiles_ub, cudaStream_t s) {
     const cudaError_t e = set_smem_attr<MODE>();
     if (e != cudaSuccess) return e;
     int grid = device_sm_count();
     if (tiles_ub < grid) grid = (int)tiles_ub;
     if (grid < 1) grid = 1;
-    return launch_kernel(tc_bwd_gemm<MODE>, dim3(grid), dim3(kThreads), kSmemBytes, s, tmA, tmB,
-                         p);
+    return launch_kernel(tc_bwd_gemm<MODE>, dim3(grid), dim3(kThreads), Layout<MODE>::bytes, s,
+                         tmA, tmB, tmO, p);
 }
 
 }  // namespace
@@ -561,8 +602,9 @@ cudaError_t launch_dgrad_bf16(const DgradArgs& a, cudaStream_t s) {
     p.nbh = g.nbh;
     p.ldab = 2 * a.I;
     const long long tiles_ub = ((long long)(a.R + 127) / 128 + groups) * p.n_tiles;
-    return down ? launch_mode<kModeDgradDown>(tmA, tmB, p, tiles_ub, s)
-                : launch_mode<kModeDgradGateUp>(tmA, tmB, p, tiles_ub, s);
+    // no tensor-map store in dgrad: tmA stands in for the unused output map
+    return down ? launch_mode<kModeDgradDown>(tmA, tmB, tmA, p, tiles_ub, s)
+                : launch_mode<kModeDgradGateUp>(tmA, tmB, tmA, p, tiles_ub, s);
 }
 
 cudaError_t launch_wgrad_bf16(const WgradArgs& a, cudaStream_t s) {
@@ -574,8 +616,14 @@ cudaError_t launch_wgrad_bf16(const WgradArgs& a, cudaStream_t s) {
     const cuuint64_t b_dims[2] = {(cuuint64_t)a.N, rows};
     const cuuint64_t b_str[1] = {(cuuint64_t)a.N * 2};
     const cuuint32_t box[2] = {64, 64};
+    // dW [E, M, N] fp32, stored 32 x 32 at a time
+    CUtensorMap tmO;
+    const cuuint64_t o_dims[3] = {(cuuint64_t)a.N, (cuuint64_t)a.M, (cuuint64_t)groups};
+    const cuuint64_t o_str[2] = {(cuuint64_t)a.N * 4, (cuuint64_t)a.N * 4 * a.M};
+    const cuuint32_t o_box[3] = {32, 32, 1};
     if (!encode_tensor_map_bf16(&tmA, a.a, 2, a_dims, a_str, box) ||
-        !encode_tensor_map_bf16(&tmB, a.b, 2, b_dims, b_str, box))
+        !encode_tensor_map_bf16(&tmB, a.b, 2, b_dims, b_str, box) ||
+        !encode_tensor_map_f32(&tmO, a.dw, 3, o_dims, o_str, o_box))
         return cudaErrorInvalidValue;
     BwdParams p = {};
     p.offsets = a.offsets;
@@ -588,7 +636,7 @@ cudaError_t launch_wgrad_bf16(const WgradArgs& a, cudaStream_t s) {
     p.m_tiles = (a.M + 127) / 128;
     p.n_tiles = (a.N + 255) / 256;
     const long long tiles = (long long)groups * p.m_tiles * p.n_tiles;
-    return launch_mode<kModeWgrad>(tmA, tmB, p, tiles, s);
+    return launch_mode<kModeWgrad>(tmA, tmB, tmO, p, tiles, s);
 }
 
 }  // namespace rdg
