@@ -380,6 +380,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
             const Tile t = decode_tile<MODE>(st, p, tile);
             const uint32_t acc = it & 1u;
+            if (MODE == kModeDgradDown) {
+                // the saved a, b of this thread's row do not depend on the accumulator: ask L2
+                // for them while the tile's MMAs run (five 64-column steps cover the 256
+                // columns' lines of each half)
+                const int row = t.row0 + q * 32 + lane;
+                if (row < t.row_end) {
+                    const __nv_bfloat16* ra = p.ab + (size_t)row * p.ldab;
+#pragma unroll
+                    for (int k = 0; k < 5; ++k) {
+                        const int col = min(t.n0 + 64 * k, t.n0 + 255);
+                        if (col < p.I) {
+                            asm volatile("prefetch.global.L2 [%0];" ::"l"(ra + col));
+                            asm volatile("prefetch.global.L2 [%0];" ::"l"(ra + p.I + col));
+                        }
+                    }
+                }
+            }
             if (!mbar_wait(&st.tfull[acc], (it >> 1) & 1u, abort_flag, kWaitLimitNs)) {
                 if (lane == 0) {
                     st.abort = 1;
@@ -461,8 +478,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const size_t rbase = (size_t)(row_ok ? row : 0) * p.ldab;
                 __nv_bfloat16* dab = static_cast<__nv_bfloat16*>(p.out);
                 float ds = 0.0f;
+                // a, b of 32 columns, loaded one chunk ahead of the math
+                uint4 ca[4], cb[4], na[4], nb[4];
+                auto load_chunk = [&](int c, uint4(&a_)[4], uint4(&b_)[4]) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int col = t.n0 + c * 32 + 8 * j;
+                        if (row_ok && col < p.I) {
+                            a_[j] = __ldg(reinterpret_cast<const uint4*>(p.ab + rbase + col));
+                            b_[j] = __ldg(reinterpret_cast<const uint4*>(p.ab + rbase + p.I + col));
+                        } else {
+                            a_[j] = b_[j] = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                };
+                load_chunk(0, ca, cb);
 #pragma unroll 1
                 for (int c = 0; c < 8; ++c) {
+                    if (c + 1 < 8) load_chunk(c + 1, na, nb);
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(tbase + c * 32, v);
                     tmem_ld_wait();
@@ -472,10 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < 4; ++j) {
                             const int col = col0 + 8 * j;
                             if (col < p.I) {
-                                const uint4 av = __ldg(reinterpret_cast<const uint4*>(
-                                    p.ab + rbase + col));
-                                const uint4 bv = __ldg(reinterpret_cast<const uint4*>(
-                                    p.ab + rbase + p.I + col));
+                                const uint4 av = ca[j];
+                                const uint4 bv = cb[j];
                                 const uint32_t aw[4] = {av.x, av.y, av.z, av.w};
                                 const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
                                 uint32_t oa[4], ob[4];
@@ -506,6 +537,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     make_uint4(ob[0], ob[1], ob[2], ob[3]);
                             }
                         }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        ca[j] = na[j];
+                        cb[j] = nb[j];
                     }
                 }
                 if (p.row_scale && row_ok)
