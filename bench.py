@@ -458,6 +458,67 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     router_hidden_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in r_ev)
 
+    # training step of the same layer (not part of the headline value): moe_forward_train, which
+    # keeps what the backward reads, then moe_backward (dx, both weight gradients in fp32, the
+    # routing-weight and logit gradients), each step with its own events, L2 flushed before it
+    bwd = None
+    if not cfg.name.startswith("decode"):
+        tflags = flags & ~moe.FUSE_COMBINE_WEIGHT
+        dout = synth.normal((T, d), dt, 0, "dout", 1.0, device=dev)
+        fws = torch.empty(moe.moe_forward_train_workspace_size(T, d, E, k, I, Is, dt),
+                          dtype=torch.uint8, device=dev)
+
+        def train_fwd():
+            moe.moe_forward_train(inp["x"], inp["logits"], wts["w_gate_up"], wts["w_down"], k,
+                                  cfg.score_fn, tflags, wts["w_shared_gate_up"],
+                                  wts["w_shared_down"], out=out, topk_ids=ids, topk_weights=w,
+                                  workspace=fws, stream=stream)
+
+        train_fwd()
+        grads = moe.moe_backward(dout, inp["x"], inp["logits"], wts["w_gate_up"], wts["w_down"],
+                                 k, ids, w, fws, cfg.score_fn, tflags, wts["w_shared_gate_up"],
+                                 wts["w_shared_down"], stream=stream)
+        bws = grads["workspace"]
+
+        def train_bwd():
+            moe.moe_backward(dout, inp["x"], inp["logits"], wts["w_gate_up"], wts["w_down"], k,
+                             ids, w, fws, cfg.score_fn, tflags, wts["w_shared_gate_up"],
+                             wts["w_shared_down"], out=grads, workspace=bws, stream=stream)
+
+        for _ in range(3):
+            train_fwd()
+            train_bwd()
+        torch.cuda.synchronize()
+        t_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                for _ in range(args.steps)]
+        for ev in t_ev:
+            flush_l2()
+            ev[0].record(stream)
+            train_fwd()
+            ev[1].record(stream)
+            train_bwd()
+            ev[2].record(stream)
+        torch.cuda.synchronize()
+        assert moe.moe_read_device_status(bws) == 0
+        tf_ms = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in t_ev)
+        tb_ms = statistics.mean(ev[1].elapsed_time(ev[2]) for ev in t_ev)
+        if world > 1:
+            tf_ms, tb_ms = reduce_max(tf_ms, dev), reduce_max(tb_ms, dev)
+        bwd_flops = 2.0 * (6.0 * d * I * R + 6.0 * d * Is * T)  # dgrad + wgrad of each GEMM
+        pk_b, pk_b_src = peaks()
+        b_tf = bwd_flops / (tb_ms * 1e-3) / 1e12
+        bwd = {"backward_ms": round(tb_ms, 4), "backward_tflops": round(b_tf, 1),
+               "backward_frac_of_peak": round(b_tf / pk_b["bf16_tflops"], 4)
+               if dt == torch.bfloat16 else None,
+               "peak_source": f"{pk_b_src} bf16_tflops (burst)",
+               "forward_train_ms": round(tf_ms, 4),
+               "train_step_ms": round(tf_ms + tb_ms, 4),
+               "train_tokens_per_s": round(T * world / ((tf_ms + tb_ms) * 1e-3), 1),
+               "backward_kernels": moe.moe_backward_kernel_count(T, k, Is, tflags, True),
+               "outputs": "dx, fp32 dW_gate_up/dW_down (and shared), d topk_weights, d logits",
+               "time": "per-step events around each call, L2 flushed before each step"}
+        del grads, bws, fws
+
     # roofline of the dominant kernel (the gate_up grouped GEMM: 2/3 of the expert FLOPs)
     pk, pk_src = peaks()
     gu_ms = statistics.mean(per_stage["gate_up"])
@@ -516,6 +577,7 @@ def run_ours(args, rank, world):
         "staged_calls_ms_per_step": round(ms_per_step, 4),
         "forward_call_ms": round(forward_ms, 4),
         "router_from_hidden_ms": round(router_hidden_ms, 4),
+        "training": bwd,
         "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": x_h.numel() * x_h.element_size()
