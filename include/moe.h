@@ -441,6 +441,56 @@ moe_status moe_backward(const void* dout, const void* x, const float* logits, mo
 /* Number of kernels moe_backward enqueues (memsets not counted). */
 int moe_backward_kernel_count(int T, int k, int Is, unsigned flags, int want_logits);
 
+/* ===================== block-scaled low precision (MX formats) =====================
+ * The pages name FP8 activations times FP4 weights with block scales as the low-precision
+ * expert variant of the newest GPUs ("Expert parallelism", the Mega MoE paragraph) without a
+ * format; these calls follow the OCP Microscaling (MX) specification v1.0:
+ *   - blocks of 32 consecutive elements along the reduction axis K share one E8M0 scale 2^s,
+ *     s = floor(log2(max |v|)) - emax (emax 2 for FP4 E2M1, 8 for FP8 E4M3), clamped to
+ *     [-127, 127] (-127 for an all-zero block), stored as s + 127;
+ *   - elements are v / 2^s rounded to nearest even and saturated at the largest finite value
+ *     (6 for E2M1, 448 for E4M3).
+ * The MX layer (moe_forward_mx): expert weights MXFP4 (blocks along d for gate_up, along I for
+ * down); x rounded to MXFP8 (blocks along d) once per token; the SwiGLU activation h rounded
+ * to MXFP8 (blocks along I) from its fp32 value, in place of the bf16 layer's bf16 rounding;
+ * accumulation in fp32; y_sorted, the combine and the output as in the bf16 layer. bf16
+ * layers only.
+ *
+ * MX weight buffer of one kind (gate_up: K = d, columns 2I; down: K = I, columns d; N as for
+ * moe_pack_weights): codes [E][K][columns / 2] bytes (byte j of row k: column 2j in the low
+ * nibble, 2j + 1 in the high nibble), then at the next 256-byte boundary the scales
+ * [E][ceil(K / 32)][columns] (E8M0). 16-byte aligned; moe_mx_weights_size(...) bytes.
+ */
+size_t moe_mx_weights_size(moe_weight_kind kind, int E, int K, int N);
+/* bf16 weights in the pages' layout ([E, d, 2I] or [E, I, d]) -> MX buffer. */
+moe_status moe_quantize_weights_mx(moe_weight_kind kind, const void* w, void* mx, int E, int K,
+                                   int N, moe_stream_t stream);
+/* MX buffer -> bf16 weights (exact: every MXFP4 value is a bf16 value). */
+moe_status moe_dequantize_weights_mx(moe_weight_kind kind, const void* mx, void* w, int E, int K,
+                                     int N, moe_stream_t stream);
+/*
+ * moe_quantize_rows_mx - bf16 rows [R, K] (K a multiple of 8) to MXFP8 along K: x_out (bf16
+ *   [R, K], the rounded values, may equal x, may be NULL), codes (uint8 E4M3 [R, K]) and
+ *   scales (uint8 E8M0 [R, ceil(K / 32)]) (both or neither).
+ */
+moe_status moe_quantize_rows_mx(const void* x, int R, int K, void* x_out, void* codes,
+                                void* scales, moe_stream_t stream);
+/*
+ * moe_forward_mx - the whole layer with MX weights (moe_forward's arguments; w_gate_up_mx /
+ *   w_down_mx and the shared expert's (E = 1) are MX buffers). flags: MOE_RENORMALIZE |
+ *   MOE_SCALE_INPUT | MOE_FUSE_COMBINE_WEIGHT. The experts that received rows get their weights
+ *   dequantized into the workspace and run on the bf16 tensor-core GEMMs (the MX values are
+ *   exact in bf16). workspace: moe_forward_mx_workspace_size(...) bytes, 256-byte aligned; its
+ *   head has moe_forward's layout without the decode regions.
+ */
+size_t moe_forward_mx_workspace_size(int T, int d, int E, int k, int I, int Is);
+moe_status moe_forward_mx(const void* x, const float* logits, int T, int d, int E, int k, int I,
+                          moe_score_fn score_fn, unsigned flags, const void* w_gate_up_mx,
+                          const void* w_down_mx, const void* w_shared_gate_up_mx,
+                          const void* w_shared_down_mx, int Is, int32_t* topk_ids,
+                          float* topk_weights, void* out, void* workspace, size_t ws_bytes,
+                          moe_stream_t stream);
+
 /*
  * moe_read_device_status - synchronise `stream`, then return the status word the kernels of
  * the last call that used `workspace` left there (MOE_OK if none). Diagnostics only.

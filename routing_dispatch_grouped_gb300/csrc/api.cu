@@ -57,13 +57,15 @@ constexpr long long kMaxRowsF32 = 60000ll * 32;
 
 struct ForwardLayout {
     size_t fcnt, counts, offsets, chunk, s2p, p2s, x_sorted, h, y, h_sh, y_sh, fused, ab, ab_sh,
-        total;
+        x_q, w_gu, w_dn, w_sgu, w_sdn, total;
 };
 
 // train: the layout of moe_forward_train (no one-kernel decode path; the gate/up accumulators
 // of the routed rows and of the shared expert are kept for the backward pass, after the rest)
+// mx: the layout of moe_forward_mx (no one-kernel decode path; after the rest: x rounded to
+// MXFP8 [T, d] and the dequantized bf16 weights of the routed and the shared experts)
 ForwardLayout forward_layout(int T, int d, int E, int k, int I, int Is, moe_dtype dt,
-                             bool train = false) {
+                             bool train = false, bool mx = false) {
     const size_t R = (size_t)T * k, b = dtype_bytes(dt);
     ForwardLayout L;
     size_t o = kStatusBytes;
@@ -74,7 +76,7 @@ ForwardLayout forward_layout(int T, int d, int E, int k, int I, int Is, moe_dtyp
     };
     // the fused decode kernel's counters follow the status word (one memset clears both);
     // its partial sums go last
-    const bool fused = !train && decode_fused_applies(dt, T, k, Is);
+    const bool fused = !train && !mx && decode_fused_applies(dt, T, k, Is);
     const DecodeFusedLayout F = decode_fused_layout(T, d, k, I);
     L.fcnt = take(fused ? F.counter_bytes : 0);
     L.counts = take((size_t)E * 4);
@@ -90,6 +92,11 @@ ForwardLayout forward_layout(int T, int d, int E, int k, int I, int Is, moe_dtyp
     L.fused = take(fused ? F.part_bytes : 0);
     L.ab = take(train ? R * 2 * (size_t)I * b : 0);
     L.ab_sh = take(train && Is > 0 ? (size_t)T * 2 * Is * b : 0);
+    L.x_q = take(mx ? (size_t)T * d * 2 : 0);
+    L.w_gu = take(mx ? (size_t)E * d * 2 * I * 2 : 0);
+    L.w_dn = take(mx ? (size_t)E * I * d * 2 : 0);
+    L.w_sgu = take(mx ? (size_t)d * 2 * Is * 2 : 0);
+    L.w_sdn = take(mx ? (size_t)Is * d * 2 : 0);
     L.total = o;
     return L;
 }
@@ -128,7 +135,7 @@ moe_status clear_status(void* workspace, cudaStream_t s) {
 moe_status run_gemm(GemmKind kind, const void* a, const void* b, bool packed,
                     const int32_t* offsets, const int32_t* s2p, const float* w, bool scale,
                     moe_dtype dt, int R, int K, int N, int E, void* out, int* status,
-                    cudaStream_t s, void* ab = nullptr) {
+                    cudaStream_t s, void* ab = nullptr, bool mx_h = false) {
     GroupedGemmArgs g;
     g.kind = kind;
     g.a = a;
@@ -146,6 +153,7 @@ moe_status run_gemm(GemmKind kind, const void* a, const void* b, bool packed,
     g.out = out;
     g.status = status;
     g.ab = ab;
+    g.mx_h = mx_h;
     const cudaError_t e =
         dt == MOE_BF16 ? launch_grouped_gemm_bf16(g, s) : launch_grouped_gemm_f32(g, s);
     return launch_status(e);
@@ -382,7 +390,7 @@ static moe_status forward_impl(const void* x, const float* logits, moe_dtype dt,
                                const void* w_shared_gate_up, const void* w_shared_down, int Is,
                                int32_t* topk_ids, float* topk_weights, void* out,
                                void* workspace, size_t ws_bytes, moe_stream_t stream,
-                               bool train) {
+                               bool train, bool mx = false) {
     moe_status st = check_tek(T, E, k);
     if (st != MOE_OK) return st;
     if (!dtype_ok(dt)) return MOE_ERR_INVALID_ARG;
@@ -394,6 +402,7 @@ static moe_status forward_impl(const void* x, const float* logits, moe_dtype dt,
     const bool fuse_w = (flags & MOE_FUSE_COMBINE_WEIGHT) != 0;
     const bool packed = (flags & MOE_WEIGHTS_PACKED) != 0;
     if (packed && dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    if (mx && (dt != MOE_BF16 || packed || train)) return MOE_ERR_UNSUPPORTED;
     if (scale && fuse_w) return MOE_ERR_INVALID_ARG;
     // training keeps y_sorted unweighted: the routing weights' gradient reads it
     if (train && fuse_w) return MOE_ERR_UNSUPPORTED;
@@ -411,7 +420,7 @@ static moe_status forward_impl(const void* x, const float* logits, moe_dtype dt,
                           topk_ids, topk_weights, out};
     for (const void* q : ptrs)
         if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
-    const ForwardLayout L = forward_layout(T, d, E, k, I, Is, dt, train);
+    const ForwardLayout L = forward_layout(T, d, E, k, I, Is, dt, train, mx);
     if (!workspace || !aligned256(workspace) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
 
     cudaStream_t s = (cudaStream_t)stream;
@@ -430,7 +439,16 @@ static moe_status forward_impl(const void* x, const float* logits, moe_dtype dt,
     const int R = T * k;
 
     const bool renorm = (flags & MOE_RENORMALIZE) != 0;
-    if (!train && decode_fused_applies(dt, T, k, Is)) {
+    // MX layers: x rounded to MXFP8 once per token (the routed rows are copies of it)
+    const void* x_in = x;
+    if (mx) {
+        if ((st = clear_status(workspace, s)) != MOE_OK) return st;
+        if ((st = launch_status(launch_mx_rows(x, T, d, ws + L.x_q, nullptr, nullptr, s))) !=
+            MOE_OK)
+            return st;
+        x_in = ws + L.x_q;
+    }
+    if (!train && !mx && decode_fused_applies(dt, T, k, Is)) {
         // decode: the whole layer in one cooperative kernel; its counters sit right after the
         // status word and are cleared with it
         if ((st = launch_status(cudaMemsetAsync(workspace, 0, L.counts, s))) != MOE_OK)
@@ -462,7 +480,7 @@ static moe_status forward_impl(const void* x, const float* logits, moe_dtype dt,
         a.status = status;
         return launch_status(launch_decode_fused(a, s));
     }
-    if ((st = clear_status(workspace, s)) != MOE_OK) return st;
+    if (!mx && (st = clear_status(workspace, s)) != MOE_OK) return st;
     if (R <= kSmallDispatchMaxSlots) {
         // few tokens: route and the dispatch indices in one launch, then the row copy
         if ((st = launch_status(launch_route_dispatch_small(logits, T, E, k, (int)score_fn,
@@ -477,28 +495,51 @@ static moe_status forward_impl(const void* x, const float* logits, moe_dtype dt,
     }
     PdlScope pdl(true);
     if (R <= kSmallDispatchMaxSlots) {
-        if ((st = launch_status(launch_dispatch_copy(x, (size_t)d * dtype_bytes(dt), T, k, p2s,
-                                                     xs, s))) != MOE_OK)
+        if ((st = launch_status(launch_dispatch_copy(x_in, (size_t)d * dtype_bytes(dt), T, k,
+                                                     p2s, xs, s))) != MOE_OK)
             return st;
     } else {
-        if ((st = launch_status(launch_dispatch(topk_ids, x, (size_t)d * dtype_bytes(dt), T, E,
-                                                k, counts, offsets, s2p, p2s, xs, chunk, status,
-                                                s))) != MOE_OK)
+        if ((st = launch_status(launch_dispatch(topk_ids, x_in, (size_t)d * dtype_bytes(dt), T,
+                                                E, k, counts, offsets, s2p, p2s, xs, chunk,
+                                                status, s))) != MOE_OK)
             return st;
     }
-    if ((st = run_gemm(kGateUp, xs, w_gate_up, packed, offsets, s2p, topk_weights, scale, dt, R,
-                       d, I, E, h, status, s, train ? ws + L.ab : nullptr)) != MOE_OK)
+    // MX layers: the experts that received rows get their weights dequantized to bf16 (exact)
+    const void* wgu = w_gate_up;
+    const void* wdn = w_down;
+    const void* wsgu = w_shared_gate_up;
+    const void* wsdn = w_shared_down;
+    if (mx) {
+        if ((st = launch_status(launch_mx_dequant_weights(w_gate_up, E, d, 2 * I, offsets,
+                                                          ws + L.w_gu, s))) != MOE_OK ||
+            (st = launch_status(launch_mx_dequant_weights(w_down, E, I, d, offsets,
+                                                          ws + L.w_dn, s))) != MOE_OK)
+            return st;
+        wgu = ws + L.w_gu;
+        wdn = ws + L.w_dn;
+        if (shared) {
+            if ((st = launch_status(launch_mx_dequant_weights(
+                     w_shared_gate_up, 1, d, 2 * Is, nullptr, ws + L.w_sgu, s))) != MOE_OK ||
+                (st = launch_status(launch_mx_dequant_weights(w_shared_down, 1, Is, d, nullptr,
+                                                              ws + L.w_sdn, s))) != MOE_OK)
+                return st;
+            wsgu = ws + L.w_sgu;
+            wsdn = ws + L.w_sdn;
+        }
+    }
+    if ((st = run_gemm(kGateUp, xs, wgu, packed, offsets, s2p, topk_weights, scale, dt, R, d, I,
+                       E, h, status, s, train ? ws + L.ab : nullptr, mx)) != MOE_OK)
         return st;
-    if ((st = run_gemm(kDown, h, w_down, packed, offsets, s2p, topk_weights, fuse_w, dt, R, I, d,
-                       E, y, status, s)) != MOE_OK)
+    if ((st = run_gemm(kDown, h, wdn, packed, offsets, s2p, topk_weights, fuse_w, dt, R, I, d, E,
+                       y, status, s)) != MOE_OK)
         return st;
     if (shared) {
-        if ((st = run_gemm(kGateUp, x, w_shared_gate_up, packed, nullptr, nullptr, nullptr, false,
-                           dt, T, d, Is, 1, h_sh, status, s,
-                           train ? ws + L.ab_sh : nullptr)) != MOE_OK)
+        if ((st = run_gemm(kGateUp, x_in, wsgu, packed, nullptr, nullptr, nullptr, false, dt, T,
+                           d, Is, 1, h_sh, status, s, train ? ws + L.ab_sh : nullptr, mx)) !=
+            MOE_OK)
             return st;
-        if ((st = run_gemm(kDown, h_sh, w_shared_down, packed, nullptr, nullptr, nullptr, false,
-                           dt, T, Is, d, 1, y_sh, status, s)) != MOE_OK)
+        if ((st = run_gemm(kDown, h_sh, wsdn, packed, nullptr, nullptr, nullptr, false, dt, T,
+                           Is, d, 1, y_sh, status, s)) != MOE_OK)
             return st;
     }
     const float* comb_w = (scale || fuse_w) ? nullptr : topk_weights;
@@ -845,6 +886,68 @@ moe_status moe_backward(const void* dout, const void* x, const float* logits, mo
     return launch_status(launch_route_backward(logits, topk_ids, topk_weights, dw, T, E, k,
                                                (int)score_fn, (flags & MOE_RENORMALIZE) != 0,
                                                d_logits, s));
+}
+
+// ---- MX (block-scaled FP8 activations, FP4 weights) ----
+static int mx_cols(moe_weight_kind kind, int N) { return kind == MOE_W_GATE_UP ? 2 * N : N; }
+
+size_t moe_mx_weights_size(moe_weight_kind kind, int E, int K, int N) {
+    if ((kind != MOE_W_GATE_UP && kind != MOE_W_DOWN) || E < 1 || K < 1 || N < 1 || N % 8)
+        return 0;
+    return mx_geom(K, mx_cols(kind, N), E).total;
+}
+
+static moe_status check_mx_weights(moe_weight_kind kind, const void* a, const void* b, int E,
+                                   int K, int N) {
+    if (kind != MOE_W_GATE_UP && kind != MOE_W_DOWN) return MOE_ERR_INVALID_ARG;
+    if (E < 1 || K < 1 || N < 1 || N % 8 != 0 || K % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (!a || !b || !aligned16(a) || !aligned16(b)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status moe_quantize_weights_mx(moe_weight_kind kind, const void* w, void* mx, int E, int K,
+                                   int N, moe_stream_t stream) {
+    const moe_status st = check_mx_weights(kind, w, mx, E, K, N);
+    if (st != MOE_OK) return st;
+    return launch_status(launch_mx_quant_weights(w, E, K, mx_cols(kind, N), mx,
+                                                 (cudaStream_t)stream));
+}
+
+moe_status moe_dequantize_weights_mx(moe_weight_kind kind, const void* mx, void* w, int E, int K,
+                                     int N, moe_stream_t stream) {
+    const moe_status st = check_mx_weights(kind, mx, w, E, K, N);
+    if (st != MOE_OK) return st;
+    return launch_status(launch_mx_dequant_weights(mx, E, K, mx_cols(kind, N), nullptr, w,
+                                                   (cudaStream_t)stream));
+}
+
+moe_status moe_quantize_rows_mx(const void* x, int R, int K, void* x_out, void* codes,
+                                void* scales, moe_stream_t stream) {
+    if (R < 0 || K < 1 || K % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if ((codes == nullptr) != (scales == nullptr)) return MOE_ERR_INVALID_ARG;
+    if (R == 0) return MOE_OK;
+    if (!x || (!x_out && !codes)) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, x_out, codes};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    return launch_status(launch_mx_rows(x, R, K, x_out, codes, scales, (cudaStream_t)stream));
+}
+
+size_t moe_forward_mx_workspace_size(int T, int d, int E, int k, int I, int Is) {
+    if (T < 0 || d < 1 || E < 1 || k < 1 || I < 1 || Is < 0) return 0;
+    return forward_layout(T, d, E, k, I, Is, MOE_BF16, false, true).total;
+}
+
+moe_status moe_forward_mx(const void* x, const float* logits, int T, int d, int E, int k, int I,
+                          moe_score_fn score_fn, unsigned flags, const void* w_gate_up_mx,
+                          const void* w_down_mx, const void* w_shared_gate_up_mx,
+                          const void* w_shared_down_mx, int Is, int32_t* topk_ids,
+                          float* topk_weights, void* out, void* workspace, size_t ws_bytes,
+                          moe_stream_t stream) {
+    if (flags & MOE_WEIGHTS_PACKED) return MOE_ERR_INVALID_ARG;
+    return forward_impl(x, logits, MOE_BF16, T, d, E, k, I, score_fn, flags, w_gate_up_mx,
+                        w_down_mx, w_shared_gate_up_mx, w_shared_down_mx, Is, topk_ids,
+                        topk_weights, out, workspace, ws_bytes, stream, false, true);
 }
 
 moe_status moe_read_device_status(const void* workspace, moe_stream_t stream) {

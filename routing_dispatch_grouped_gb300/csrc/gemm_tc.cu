@@ -25,7 +25,7 @@
 // returns.
 #include <mutex>
 
-#include "moe_internal.cuh"
+#include "mx.cuh"
 
 namespace rdg {
 namespace {
@@ -53,6 +53,7 @@ struct TcParams {
     int packed;      // weights in the packed layout (PackedGeom below)
     int nb, nbh, kpad;
     __nv_bfloat16* ab;  // gate_up for training: [g | u] before the row scale, [R, 2N]
+    int mx_h;           // gate_up: round h to MXFP8 (32-column blocks) before storing it
 };
 
 struct __align__(8) SmemTail {
@@ -365,7 +366,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                     }
-                    if (row_ok) {
+                    if (row_ok && p.mx_h) {
+                        // the chunk's 32 columns are one MX block of h (col0 is a multiple of
+                        // 32): SwiGLU in fp32, rounded to MXFP8 (exact in bf16)
+                        float hv[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float gi = __uint_as_float(g[i]) * s;
+                            hv[i] = silu(gi) * (__uint_as_float(u[i]) * s);
+                        }
+                        mx_fakequant_e4m3_block(hv, min(32, p.N - col0));
+                        uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * p.N + col0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            if (col0 + v * 8 < p.N)
+                                dst[v] = make_uint4(pack_bf16x2(hv[8 * v], hv[8 * v + 1]),
+                                                    pack_bf16x2(hv[8 * v + 2], hv[8 * v + 3]),
+                                                    pack_bf16x2(hv[8 * v + 4], hv[8 * v + 5]),
+                                                    pack_bf16x2(hv[8 * v + 6], hv[8 * v + 7]));
+                        }
+                    } else if (row_ok) {
                         uint4* dst = reinterpret_cast<uint4*>(out + (size_t)row * p.N + col0);
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
@@ -519,6 +539,7 @@ cudaError_t launch_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     p.nbh = g.nbh;
     p.kpad = g.kpad;
     p.ab = static_cast<__nv_bfloat16*>(a.ab);
+    p.mx_h = a.mx_h ? 1 : 0;
 
     // upper bound on tiles: sum_e ceil(n_e / 128) <= R / 128 + groups
     const long long m_ub = (long long)(a.R + kTileM - 1) / kTileM + groups;

@@ -532,7 +532,8 @@ cudaError_t launch_grouped_gemm_bf16_swap(const GroupedGemmArgs& a, cudaStream_t
 // Everything else (down of experts with fewer rows) runs here, padding each expert to 16 rows.
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
     const int groups = a.offsets ? a.E : 1;
-    if (a.kind == kGateUp && a.ab) return launch_grouped_gemm_bf16_rows(a, s);  // training
+    // training (saved accumulators) and MX layers (h rounded to MXFP8) use the 128-row kernel
+    if (a.kind == kGateUp && (a.ab || a.mx_h)) return launch_grouped_gemm_bf16_rows(a, s);
     if (a.kind == kGateUp && a.R > kSmallBatchRows) {
         if (groups == 1) return launch_grouped_gemm_bf16_2sm(a, s);
         return launch_grouped_gemm_bf16_rows(a, s);

@@ -402,6 +402,8 @@ struct GroupedGemmArgs {
     void* ab = nullptr;       // gate_up for training: also store [g | u] before the row scale
                               // ([R, 2I], layer dtype); only the 128-row-tile kernel and the
                               // fp32 kernel write it
+    bool mx_h = false;        // gate_up: round h to MXFP8 (blocks of 32 along I) before storing
+                              // it (bf16 holds the value exactly); 128-row-tile kernel only
 };
 // Batches with at most this many routed rows use the small-batch (decode) GEMM configuration.
 constexpr int kSmallBatchRows = 512;
@@ -422,6 +424,27 @@ bool encode_tensor_map_f32(CUtensorMap* m, const void* base, int rank, const cuu
 cudaError_t launch_grouped_gemm_f32(const GroupedGemmArgs& a, cudaStream_t s);
 
 int device_sm_count();
+
+// ---------------------------------------------------------------------------------------------
+// MX formats (mx.cu): MXFP4 expert weights, MXFP8 activations
+// ---------------------------------------------------------------------------------------------
+struct MxGeom {
+    size_t codes;       // bytes of E2M1 codes: G * K * N / 2
+    size_t scales_off;  // offset of the E8M0 scales (256-byte aligned)
+    size_t total;       // buffer size
+};
+MxGeom mx_geom(int K, int N, int G);
+// bf16 weights [G, K, N] -> MX buffer (codes, then scales)
+cudaError_t launch_mx_quant_weights(const void* w, int G, int K, int N, void* mx,
+                                    cudaStream_t s);
+// MX buffer -> bf16 [G, K, N]; groups g with offsets[g + 1] == offsets[g] are skipped (offsets
+// may be null)
+cudaError_t launch_mx_dequant_weights(const void* mx, int G, int K, int N,
+                                      const int32_t* offsets, void* w, cudaStream_t s);
+// bf16 rows [R, K] rounded to MXFP8 and back into out (may be in; null: not written); codes
+// [R, K] and scales [R, ceil(K / 32)] written when not null
+cudaError_t launch_mx_rows(const void* in, int R, int K, void* out, void* codes, void* scales,
+                           cudaStream_t s);
 
 // ---------------------------------------------------------------------------------------------
 // backward pass (gemm_bwd.cu: tensor cores; backward.cu: fp32 layers and the small kernels)

@@ -59,6 +59,13 @@ SIGNATURES = {
     "moe_backward": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P,
                           _P, _P, _S, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P]),
     "moe_backward_kernel_count": (_I, [_I, _I, _I, _U, _I]),
+    "moe_mx_weights_size": (_S, [_I, _I, _I, _I]),
+    "moe_quantize_weights_mx": (_I, [_I, _P, _P, _I, _I, _I, _P]),
+    "moe_dequantize_weights_mx": (_I, [_I, _P, _P, _I, _I, _I, _P]),
+    "moe_quantize_rows_mx": (_I, [_P, _I, _I, _P, _P, _P, _P]),
+    "moe_forward_mx_workspace_size": (_S, [_I, _I, _I, _I, _I, _I]),
+    "moe_forward_mx": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P, _P, _P,
+                            _P, _S, _P]),
     "moe_read_device_status": (_I, [_P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
 }
@@ -327,8 +334,9 @@ def moe_read_device_status(workspace, stream=None) -> int:
     return lib().moe_read_device_status(_p(workspace), _stream(stream))
 
 
-def forward_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is, dtype):
-    """Views of the intermediates moe_forward leaves in its workspace (for tests and tools);
+def forward_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is, dtype, mx=False):
+    """Views of the intermediates moe_forward (moe_forward_mx with mx=True) leaves in its
+    workspace (for tests and tools);
     the offsets follow the library's layout rule: 256-byte status word, then (decode batches
     only) the one-kernel layer's counters, counts, offsets,
     dispatch scratch, sorted_to_slot, slot_to_sorted, x_sorted, h, y_sorted, shared h, shared y,
@@ -337,7 +345,7 @@ def forward_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is, dtype):
     b = 2 if dtype == torch.bfloat16 else 4
     nchunks = (R + 255) // 256
     # decode batches run the one-kernel layer, whose counters follow the status word
-    fused = dtype == torch.bfloat16 and Is == 0 and 1 <= T <= 16 and R <= 256
+    fused = dtype == torch.bfloat16 and Is == 0 and 1 <= T <= 16 and R <= 256 and not mx
     fcnt = (2 * R * ((I + 63) // 64) + (d + 63) // 64) * 4 if fused else 0
     sizes = [("fused_counters", fcnt), ("counts", E * 4), ("offsets", (E + 1) * 4), ("chunk", nchunks * E * 4),
              ("sorted_to_slot", R * 4), ("slot_to_sorted", R * 4), ("x_sorted", R * d * b),
@@ -601,3 +609,89 @@ def forward_train_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is, dtype):
         out["y_shared"] = v["y_shared"].view(torch.float32).view(T, d)
         out["ab_shared"] = v["ab_shared"].view(dtype).view(T, 2 * Is)
     return out
+
+
+# ------------------------------------------------------------------------------------------------
+# MX formats: MXFP4 expert weights, MXFP8 activations
+# ------------------------------------------------------------------------------------------------
+class MxWeights:
+    """Expert weights in the MX buffer layout (moe_quantize_weights_mx): `data` holds the E2M1
+    codes then the E8M0 scales; kind W_GATE_UP (logical [E, K=d, 2I], N = I) or W_DOWN
+    ([E, K=I, N=d])."""
+
+    def __init__(self, data: torch.Tensor, kind: int, E: int, K: int, N: int):
+        self.data, self.kind, self.E, self.K, self.N = data, kind, E, K, N
+
+    def data_ptr(self):
+        return self.data.data_ptr()
+
+    def views(self):
+        """(codes uint8 [E, K, cols / 2], scales uint8 [E, ceil(K / 32), cols])."""
+        cols = 2 * self.N if self.kind == W_GATE_UP else self.N
+        n = self.E * self.K * cols // 2
+        off = (n + 255) // 256 * 256
+        kb = (self.K + 31) // 32
+        return (self.data[:n].view(self.E, self.K, cols // 2),
+                self.data[off:off + self.E * kb * cols].view(self.E, kb, cols))
+
+
+def quantize_weights_mx(w: torch.Tensor, kind: int, stream=None) -> MxWeights:
+    """bf16 gate_up ([E, d, 2I] or [d, 2I]) or down ([E, I, d] or [I, d]) weights to MXFP4."""
+    _need(w, "w")
+    w3 = w.unsqueeze(0) if w.dim() == 2 else w
+    E, K, C = w3.shape
+    N = C // 2 if kind == W_GATE_UP else C
+    out = torch.empty(lib().moe_mx_weights_size(kind, E, K, N), dtype=torch.uint8,
+                      device=w.device)
+    _check("moe_quantize_weights_mx", lib().moe_quantize_weights_mx(
+        kind, _p(w3), _p(out), E, K, N, _stream(stream)))
+    return MxWeights(out, kind, E, K, N)
+
+
+def dequantize_weights_mx(mx: MxWeights, stream=None) -> torch.Tensor:
+    cols = 2 * mx.N if mx.kind == W_GATE_UP else mx.N
+    w = torch.empty(mx.E, mx.K, cols, dtype=torch.bfloat16, device=mx.data.device)
+    _check("moe_dequantize_weights_mx", lib().moe_dequantize_weights_mx(
+        mx.kind, _p(mx.data), _p(w), mx.E, mx.K, mx.N, _stream(stream)))
+    return w
+
+
+def quantize_rows_mx(x: torch.Tensor, want_codes=True, stream=None):
+    """bf16 rows [R, K] to MXFP8 along K: (rounded bf16 rows, codes uint8 [R, K] or None,
+    scales uint8 [R, ceil(K/32)] or None)."""
+    _need(x, "x")
+    R, K = x.shape
+    xo = torch.empty_like(x)
+    codes = torch.empty(R, K, dtype=torch.uint8, device=x.device) if want_codes else None
+    scales = (torch.empty(R, (K + 31) // 32, dtype=torch.uint8, device=x.device)
+              if want_codes else None)
+    _check("moe_quantize_rows_mx", lib().moe_quantize_rows_mx(
+        _p(x), R, K, _p(xo), _p(codes), _p(scales), _stream(stream)))
+    return xo, codes, scales
+
+
+def moe_forward_mx_workspace_size(T, d, E, k, I, Is) -> int:
+    return lib().moe_forward_mx_workspace_size(T, d, E, k, I, Is)
+
+
+def moe_forward_mx(x, logits, w_gate_up: MxWeights, w_down: MxWeights, k, score_fn=SOFTMAX,
+                   flags=RENORMALIZE, w_shared_gate_up=None, w_shared_down=None, out=None,
+                   topk_ids=None, topk_weights=None, workspace=None, stream=None):
+    """The MX layer. Returns (out, topk_ids, topk_weights, workspace)."""
+    _need(x, "x")
+    _need(logits, "logits")
+    T, d = x.shape
+    E, I = w_gate_up.E, w_gate_up.N
+    Is = w_shared_gate_up.N if w_shared_gate_up is not None else 0
+    dev = x.device
+    out = out if out is not None else torch.empty(T, d, dtype=x.dtype, device=dev)
+    ids = topk_ids if topk_ids is not None else torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = topk_weights if topk_weights is not None else torch.empty(T, k, dtype=torch.float32,
+                                                                  device=dev)
+    ws = workspace if workspace is not None else _workspace(
+        moe_forward_mx_workspace_size(T, d, E, k, I, Is), dev)
+    _check("moe_forward_mx", lib().moe_forward_mx(
+        _p(x), _p(logits), T, d, E, k, I, score_fn, flags, _p(w_gate_up), _p(w_down),
+        _p(w_shared_gate_up), _p(w_shared_down), Is, _p(ids), _p(w), _p(out), _p(ws), ws.numel(),
+        _stream(stream)))
+    return out, ids, w, ws
