@@ -519,6 +519,48 @@ def run_ours(args, rank, world):
                "time": "per-step events around each call, L2 flushed before each step"}
         del grads, bws, fws
 
+    # the MX form of the same layer (MXFP4 expert weights quantised once at load, MXFP8 x and
+    # h): moe_forward_mx with per-step events, L2 flushed before each step (not part of the
+    # headline value)
+    mxr = None
+    if dt == torch.bfloat16:
+        mxw = {n_: (moe.quantize_weights_mx(inp[n_], moe.W_GATE_UP if "gate_up" in n_
+                                            else moe.W_DOWN) if inp[n_] is not None else None)
+               for n_ in ("w_gate_up", "w_down", "w_shared_gate_up", "w_shared_down")}
+        mws = torch.empty(moe.moe_forward_mx_workspace_size(T, d, E, k, I, Is),
+                          dtype=torch.uint8, device=dev)
+
+        def mx_fwd():
+            moe.moe_forward_mx(inp["x"], inp["logits"], mxw["w_gate_up"], mxw["w_down"], k,
+                               cfg.score_fn, flags, mxw["w_shared_gate_up"],
+                               mxw["w_shared_down"], out=out, topk_ids=ids, topk_weights=w,
+                               workspace=mws, stream=stream)
+
+        for _ in range(3):
+            mx_fwd()
+        torch.cuda.synchronize()
+        m_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+        for a_, b_ in m_ev:
+            flush_l2()
+            a_.record(stream)
+            mx_fwd()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        assert moe.moe_read_device_status(mws) == 0
+        mx_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in m_ev)
+        if world > 1:
+            mx_ms = reduce_max(mx_ms, dev)
+        mx_bytes = sum(v_.data.numel() for v_ in mxw.values() if v_ is not None)
+        bf_bytes = sum(inp[n_].numel() * 2 for n_ in mxw if inp[n_] is not None)
+        mxr = {"ms_per_step": round(mx_ms, 4),
+               "tokens_per_s": round(T * world / (mx_ms * 1e-3), 1),
+               "weight_bytes": mx_bytes, "weight_bytes_bf16": bf_bytes,
+               "path": "x and h rounded to MXFP8; the touched experts' MXFP4 weights "
+                       "dequantized to bf16 (exact) for the bf16 tensor-core GEMMs",
+               "time": "per-step events around moe_forward_mx, L2 flushed before each step"}
+        del mxw, mws
+
     # roofline of the dominant kernel (the gate_up grouped GEMM: 2/3 of the expert FLOPs)
     pk, pk_src = peaks()
     gu_ms = statistics.mean(per_stage["gate_up"])
@@ -578,6 +620,7 @@ def run_ours(args, rank, world):
         "forward_call_ms": round(forward_ms, 4),
         "router_from_hidden_ms": round(router_hidden_ms, 4),
         "training": bwd,
+        "mx": mxr,
         "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
                 "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": x_h.numel() * x_h.element_size()

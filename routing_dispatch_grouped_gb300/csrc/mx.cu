@@ -62,24 +62,39 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// One thread per (group, row k, column pair); groups without rows (offsets) are skipped.
+// One block per (group, 32-row K block); a group without rows (offsets) leaves at once. Thread
+// t takes 8-column chunks t, t + blockDim, ...: its 8 scales once, then 4 code bytes and 16
+// bytes of bf16 per row (aligned for any N that is a multiple of 8).
 __global__ void __launch_bounds__(256)
     mx_dequant_weights_kernel(const uint8_t* __restrict__ codes,
                               const uint8_t* __restrict__ scales, int G, int K, int N,
-                              const int32_t* __restrict__ offsets, uint32_t* __restrict__ w) {
+                              const int32_t* __restrict__ offsets, __nv_bfloat16* __restrict__ w) {
     griddep_wait();
-    const int NP = N / 2, KB = (K + 31) / 32;
-    const long long per = (long long)K * NP;
-    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < (long long)G * per;
-         i += (long long)gridDim.x * blockDim.x) {
-        const int g = (int)(i / per);
+    const int NP = N / 2, KB = (K + 31) / 32, chunks = N / 8;
+    for (int bid = blockIdx.x; bid < G * KB; bid += gridDim.x) {
+        const int g = bid / KB, kb = bid - g * KB;
         if (offsets && __ldg(offsets + g + 1) == __ldg(offsets + g)) continue;
-        const long long r = i - (long long)g * per;
-        const int k = (int)(r / NP), j = (int)(r % NP);
-        const uint8_t* sc = scales + ((size_t)g * KB + k / 32) * N + 2 * j;
-        const float2 q = e2m1x2_to_f32(__ldg(codes + i));
-        w[i] = pack_bf16x2(q.x * pow2_f32((int)__ldg(sc) - 127),
-                           q.y * pow2_f32((int)__ldg(sc + 1) - 127));
+        const int k0 = kb * 32, nr = min(32, K - k0);
+        for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+            const uint2 sv = __ldg(reinterpret_cast<const uint2*>(
+                scales + ((size_t)g * KB + kb) * N + 8 * c));
+            float sc[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                sc[i] = pow2_f32((int)(((i < 4 ? sv.x : sv.y) >> (8 * (i % 4))) & 0xFF) - 127);
+            const uint8_t* src = codes + ((size_t)g * K + k0) * NP + 4 * c;
+            __nv_bfloat16* dst = w + ((size_t)g * K + k0) * N + 8 * c;
+            for (int r = 0; r < nr; ++r) {
+                const uint32_t cw = __ldg(reinterpret_cast<const uint32_t*>(src + (size_t)r * NP));
+                uint32_t o[4];
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const float2 q = e2m1x2_to_f32((cw >> (8 * b)) & 0xFF);
+                    o[b] = pack_bf16x2(q.x * sc[2 * b], q.y * sc[2 * b + 1]);
+                }
+                *reinterpret_cast<uint4*>(dst + (size_t)r * N) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
     }
 }
 
@@ -170,9 +185,11 @@ cudaError_t launch_mx_dequant_weights(const void* mx, int G, int K, int N,
                                       const int32_t* offsets, void* w, cudaStream_t s) {
     const MxGeom m = mx_geom(K, N, G);
     const uint8_t* base = static_cast<const uint8_t*>(mx);
-    const long long work = (long long)G * K * (N / 2);
-    return launch_kernel(mx_dequant_weights_kernel, dim3(grid_for(work)), dim3(256), 0, s, base,
-                         base + m.scales_off, G, K, N, offsets, static_cast<uint32_t*>(w));
+    const long long blocks = (long long)G * ((K + 31) / 32);
+    const long long cap = (long long)device_sm_count() * 16;
+    return launch_kernel(mx_dequant_weights_kernel, dim3((unsigned)(blocks < cap ? blocks : cap)),
+                         dim3(256), 0, s, base, base + m.scales_off, G, K, N, offsets,
+                         static_cast<__nv_bfloat16*>(w));
 }
 
 cudaError_t launch_mx_rows(const void* in, int R, int K, void* out, void* codes, void* scales,

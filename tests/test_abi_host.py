@@ -182,3 +182,29 @@ def test_kernel_count_and_strings(L):
     assert L.moe_forward_kernel_count(bf16, 16384, 1, 8192) == 10
     for code in range(7):
         assert L.moe_status_string(code).decode().startswith(moe.STATUS[code])
+
+
+def test_mx_validation_and_sizes(L):
+    # gate_up [E=2, K=64, 2I=2*64]: codes 2*64*64 bytes, scales 2*2*128 after 256-byte rounding
+    assert L.moe_mx_weights_size(0, 2, 64, 64) == 2 * 64 * 64 + 2 * 2 * 128
+    assert L.moe_mx_weights_size(1, 1, 200, 96) == (200 * 48 + 255) // 256 * 256 + 7 * 96
+    assert L.moe_mx_weights_size(0, 1, 64, 60) == 0                     # N % 8
+    q = L.moe_quantize_weights_mx
+    assert q(7, FAKE, FAKE, 1, 64, 64, NULL) == 1                          # unknown kind
+    assert q(0, FAKE, FAKE, 1, 60, 64, NULL) == 1                          # K % 8
+    assert q(0, MIS, FAKE, 1, 64, 64, NULL) == 1                           # misaligned
+    r = L.moe_quantize_rows_mx
+    assert r(FAKE, 4, 60, FAKE, None, None, NULL) == 1                     # K % 8
+    assert r(FAKE, 4, 64, FAKE, FAKE, None, NULL) == 1                     # codes without scales
+    assert r(None, 0, 64, None, None, None, NULL) == 0                     # R = 0
+    f = L.moe_forward_mx
+    sz = L.moe_forward_mx_workspace_size(64, 128, 8, 2, 256, 0)
+    assert sz > L.moe_forward_workspace_size(64, 128, 8, 2, 256, 0, 1)
+    args = [FAKE, FAKE, 64, 128, 8, 2, 256, 0, 1, FAKE, FAKE, None, None, 0, FAKE, FAKE, FAKE,
+            0x100000, sz, NULL]
+    bad = list(args); bad[8] = 1 | 8
+    assert f(*bad) == 1                                                    # packed: not MX
+    bad = list(args); bad[18] = sz - 256
+    assert f(*bad) == 3                                                    # short workspace
+    bad = list(args); bad[2] = 0
+    assert f(*bad) == 0                                                    # T = 0
