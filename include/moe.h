@@ -456,10 +456,15 @@ int moe_backward_kernel_count(int T, int k, int Is, unsigned flags, int want_log
  * accumulation in fp32; y_sorted, the combine and the output as in the bf16 layer. bf16
  * layers only.
  *
- * MX weight buffer of one kind (gate_up: K = d, columns 2I; down: K = I, columns d; N as for
- * moe_pack_weights): codes [E][K][columns / 2] bytes (byte j of row k: column 2j in the low
- * nibble, 2j + 1 in the high nibble), then at the next 256-byte boundary the scales
- * [E][ceil(K / 32)][columns] (E8M0). 16-byte aligned; moe_mx_weights_size(...) bytes.
+ * MX weight buffer of one kind (gate_up: K = d, columns 2I, its gate and up halves blocked
+ * separately; down: K = I, columns d; N as for moe_pack_weights), in blocks of 64 columns x 32
+ * K rows: block (e, nb, kb) holds 1 KB of E2M1 codes at ((e * NB + nb) * KB + kb) * 1024, laid
+ * out as the A fragments of mma.m16n8k16 (256 words [k-step (2)][16-column m-tile (4)][lane
+ * (32)]; word byte hi + 2 kh, nibble bit holds column 16 mt + (lane >> 2) + 8 hi and row
+ * 16 ks + 2 (lane & 3) + bit + 8 kh of the block), and its 64 E8M0 scales (per column) at
+ * E * NB * KB * 1024 + ((e * NB + nb) * KB + kb) * 64. NB = ceil(N / 64) for down,
+ * 2 ceil(I / 64) for gate_up (gate blocks first), KB = ceil(K / 32); padding holds code 0.
+ * 16-byte aligned; moe_mx_weights_size(...) bytes.
  */
 size_t moe_mx_weights_size(moe_weight_kind kind, int E, int K, int N);
 /* bf16 weights in the pages' layout ([E, d, 2I] or [E, I, d]) -> MX buffer. */

@@ -510,18 +510,19 @@ static moe_status forward_impl(const void* x, const float* logits, moe_dtype dt,
     const void* wsgu = w_shared_gate_up;
     const void* wsdn = w_shared_down;
     if (mx) {
-        if ((st = launch_status(launch_mx_dequant_weights(w_gate_up, E, d, 2 * I, offsets,
+        if ((st = launch_status(launch_mx_dequant_weights(true, w_gate_up, E, d, I, offsets,
                                                           ws + L.w_gu, s))) != MOE_OK ||
-            (st = launch_status(launch_mx_dequant_weights(w_down, E, I, d, offsets,
+            (st = launch_status(launch_mx_dequant_weights(false, w_down, E, I, d, offsets,
                                                           ws + L.w_dn, s))) != MOE_OK)
             return st;
         wgu = ws + L.w_gu;
         wdn = ws + L.w_dn;
         if (shared) {
             if ((st = launch_status(launch_mx_dequant_weights(
-                     w_shared_gate_up, 1, d, 2 * Is, nullptr, ws + L.w_sgu, s))) != MOE_OK ||
-                (st = launch_status(launch_mx_dequant_weights(w_shared_down, 1, Is, d, nullptr,
-                                                              ws + L.w_sdn, s))) != MOE_OK)
+                     true, w_shared_gate_up, 1, d, Is, nullptr, ws + L.w_sgu, s))) != MOE_OK ||
+                (st = launch_status(launch_mx_dequant_weights(false, w_shared_down, 1, Is, d,
+                                                              nullptr, ws + L.w_sdn, s))) !=
+                    MOE_OK)
                 return st;
             wsgu = ws + L.w_sgu;
             wsdn = ws + L.w_sdn;
@@ -889,12 +890,10 @@ moe_status moe_backward(const void* dout, const void* x, const float* logits, mo
 }
 
 // ---- MX (block-scaled FP8 activations, FP4 weights) ----
-static int mx_cols(moe_weight_kind kind, int N) { return kind == MOE_W_GATE_UP ? 2 * N : N; }
-
 size_t moe_mx_weights_size(moe_weight_kind kind, int E, int K, int N) {
     if ((kind != MOE_W_GATE_UP && kind != MOE_W_DOWN) || E < 1 || K < 1 || N < 1 || N % 8)
         return 0;
-    return mx_geom(K, mx_cols(kind, N), E).total;
+    return mx_geom(kind == MOE_W_GATE_UP, K, N, E).total;
 }
 
 static moe_status check_mx_weights(moe_weight_kind kind, const void* a, const void* b, int E,
@@ -909,7 +908,7 @@ moe_status moe_quantize_weights_mx(moe_weight_kind kind, const void* w, void* mx
                                    int N, moe_stream_t stream) {
     const moe_status st = check_mx_weights(kind, w, mx, E, K, N);
     if (st != MOE_OK) return st;
-    return launch_status(launch_mx_quant_weights(w, E, K, mx_cols(kind, N), mx,
+    return launch_status(launch_mx_quant_weights(kind == MOE_W_GATE_UP, w, E, K, N, mx,
                                                  (cudaStream_t)stream));
 }
 
@@ -917,8 +916,8 @@ moe_status moe_dequantize_weights_mx(moe_weight_kind kind, const void* mx, void*
                                      int N, moe_stream_t stream) {
     const moe_status st = check_mx_weights(kind, mx, w, E, K, N);
     if (st != MOE_OK) return st;
-    return launch_status(launch_mx_dequant_weights(mx, E, K, mx_cols(kind, N), nullptr, w,
-                                                   (cudaStream_t)stream));
+    return launch_status(launch_mx_dequant_weights(kind == MOE_W_GATE_UP, mx, E, K, N, nullptr,
+                                                   w, (cudaStream_t)stream));
 }
 
 moe_status moe_quantize_rows_mx(const void* x, int R, int K, void* x_out, void* codes,

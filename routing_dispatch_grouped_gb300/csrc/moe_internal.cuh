@@ -428,18 +428,29 @@ int device_sm_count();
 // ---------------------------------------------------------------------------------------------
 // MX formats (mx.cu): MXFP4 expert weights, MXFP8 activations
 // ---------------------------------------------------------------------------------------------
+// MX weights are stored in blocks of 64 columns x 32 K rows (mx.cu); gate_up blocks its gate
+// and up halves separately (gate blocks first), like the packed bf16 layout.
+struct MxBlocks {
+    int half;  // gate_up: I (columns of a half); down: 0
+    int nbh;   // 64-column blocks per half (gate_up) or in all (down)
+    int nb;    // column blocks per expert
+    int kb;    // 32-row K blocks
+    int cols;  // columns of the logical weight (2I or d)
+};
 struct MxGeom {
-    size_t codes;       // bytes of E2M1 codes: G * K * N / 2
-    size_t scales_off;  // offset of the E8M0 scales (256-byte aligned)
+    MxBlocks blocks;
+    size_t codes;       // bytes of codes: G * NB * KB * 1024
+    size_t scales_off;  // offset of the scales (G * NB * KB * 64 bytes)
     size_t total;       // buffer size
 };
-MxGeom mx_geom(int K, int N, int G);
-// bf16 weights [G, K, N] -> MX buffer (codes, then scales)
-cudaError_t launch_mx_quant_weights(const void* w, int G, int K, int N, void* mx,
+MxBlocks mx_blocks(bool gate_up, int K, int N);  // N = I (gate_up) or d (down)
+MxGeom mx_geom(bool gate_up, int K, int N, int G);
+// bf16 weights [G, K, cols] -> MX buffer
+cudaError_t launch_mx_quant_weights(bool gate_up, const void* w, int G, int K, int N, void* mx,
                                     cudaStream_t s);
-// MX buffer -> bf16 [G, K, N]; groups g with offsets[g + 1] == offsets[g] are skipped (offsets
-// may be null)
-cudaError_t launch_mx_dequant_weights(const void* mx, int G, int K, int N,
+// MX buffer -> bf16 [G, K, cols]; groups g with offsets[g + 1] == offsets[g] are skipped
+// (offsets may be null)
+cudaError_t launch_mx_dequant_weights(bool gate_up, const void* mx, int G, int K, int N,
                                       const int32_t* offsets, void* w, cudaStream_t s);
 // bf16 rows [R, K] rounded to MXFP8 and back into out (may be in; null: not written); codes
 // [R, K] and scales [R, ceil(K / 32)] written when not null

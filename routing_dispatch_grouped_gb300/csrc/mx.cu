@@ -7,10 +7,17 @@
 // [-127, 127] (-127 for an all-zero block); each element is v / 2^s rounded to nearest even and
 // saturated at the format's largest finite value (cvt.rn.satfinite does exactly that).
 //
-// Storage:
-//   MX weights of one kind (gate_up: K = d, N = 2I; down: K = I, N = d), [E, K, N] logically:
-//     codes  [E][K][N / 2] bytes, byte j of row k holding column 2j (low nibble) and 2j + 1
-//     scales [E][ceil(K / 32)][N] bytes (E8M0: s + 127), after the codes at a 256-byte boundary.
+// Storage of MX weights (one kind; gate_up: K = d, columns 2I with the gate and up halves
+// blocked separately; down: K = I, columns d), in blocks of 64 columns x 32 K rows:
+//   block (e, nb, kb): 1 KB of E2M1 codes at ((e * NB + nb) * KB + kb) * 1024, as 256 words
+//     [k-step ks (2)][16-column m-tile mt (4)][lane l (32)]; word byte b = hi + 2 kh, nibble
+//     bit, holds column 16 mt + (l >> 2) + 8 hi and K row 32 kb + 16 ks + 2 (l & 3) + bit + 8 kh
+//     of the block: lane l's A fragment of mma.m16n8k16 (weights as the M side, K along the
+//     MMA's K) for that m-tile and k-step, one byte per A register;
+//   its 64 E8M0 scales (one per column, s + 127) at scales_off + ((e * NB + nb) * KB + kb) * 64.
+// NB = ceil(cols / 64) (gate_up: 2 ceil(I / 64), gate blocks first), KB = ceil(K / 32); padding
+// columns and rows hold code 0. A decode consumer reads its whole A fragment with one 4-byte
+// load; a run of K blocks of one column block is contiguous.
 //   MXFP8 rows [R, K]: codes [R][K] (E4M3) and scales [R][ceil(K / 32)].
 // Every MX value is exact in bf16 (E2M1 times 2^s for s in [-127, 125], and E4M3 times 2^s
 // down to bf16's smallest subnormal), so the layer runs the bf16 tensor-core GEMMs on the
@@ -26,74 +33,75 @@ namespace {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// One thread per (group, K block, column pair): 32 rows of columns 2j, 2j + 1.
+// One thread per (group, column block, K block, column m of the block): 32 rows of one column.
 __global__ void __launch_bounds__(256)
-    mx_quant_weights_kernel(const uint32_t* __restrict__ w, int G, int K, int N,
-                            uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+    mx_quant_weights_kernel(const __nv_bfloat16* __restrict__ w, int G, int K, int cols,
+                            MxBlocks bl, uint8_t* __restrict__ codes,
+                            uint8_t* __restrict__ scales) {
     griddep_wait();
-    const int NP = N / 2, KB = (K + 31) / 32;
-    const long long total = (long long)G * KB * NP;
+    const long long total = (long long)G * bl.nb * bl.kb * 64;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
          i += (long long)gridDim.x * blockDim.x) {
-        const int j = (int)(i % NP);
-        const long long gk = i / NP;
-        const int kb = (int)(gk % KB), g = (int)(gk / KB);
-        const int k0 = kb * 32, n = min(32, K - k0);
-        const uint32_t* src = w + ((size_t)g * K + k0) * NP + j;
-        float a[32], b[32];
-        float ma = 0.0f, mb = 0.0f;
+        const int m = (int)(i & 63);
+        const long long blk = i >> 6;  // (g * NB + nb) * KB + kb
+        const int kb = (int)(blk % bl.kb);
+        const long long gn = blk / bl.kb;
+        const int nb = (int)(gn % bl.nb), g = (int)(gn / bl.nb);
+        const int col = mx_block_col(bl, nb, m);  // -1: padding
+        const int k0 = kb * 32, nr = min(32, K - k0);
+        float v[32];
+        float amax = 0.0f;
 #pragma unroll
         for (int r = 0; r < 32; ++r) {
-            const uint32_t v = r < n ? __ldg(src + (size_t)r * NP) : 0u;
-            a[r] = bf_lo(v);
-            b[r] = bf_hi(v);
-            ma = fmaxf(ma, fabsf(a[r]));
-            mb = fmaxf(mb, fabsf(b[r]));
+            v[r] = (col >= 0 && r < nr)
+                       ? __bfloat162float(w[((size_t)g * K + k0 + r) * cols + col])
+                       : 0.0f;
+            amax = fmaxf(amax, fabsf(v[r]));
         }
-        const int sa = mx_scale_exp(ma, 2), sb = mx_scale_exp(mb, 2);
-        const float ia = pow2_f32(-sa), ib = pow2_f32(-sb);
-        uint8_t* dst = codes + ((size_t)g * K + k0) * NP + j;
+        const int s = mx_scale_exp(amax, 2);
+        const float inv = pow2_f32(-s);
+        uint8_t* cb = codes + blk * 1024;
+        const int mt = m >> 4, r16 = m & 15, hi = r16 >> 3, lq = r16 & 7;
 #pragma unroll
-        for (int r = 0; r < 32; ++r)
-            if (r < n) dst[(size_t)r * NP] = (uint8_t)e2m1x2(a[r] * ia, b[r] * ib);
-        uint8_t* sc = scales + ((size_t)g * KB + kb) * N + 2 * j;
-        sc[0] = (uint8_t)(sa + 127);
-        sc[1] = (uint8_t)(sb + 127);
+        for (int kk = 0; kk < 32; kk += 2) {
+            // rows kk, kk + 1 of column m share a byte (even row in the low nibble)
+            const int ks = kk >> 4, kx = kk & 15, kh = kx >> 3, l = lq * 4 + ((kx & 7) >> 1);
+            cb[(((ks * 4 + mt) * 32 + l) << 2) + hi + 2 * kh] =
+                (uint8_t)e2m1x2(v[kk] * inv, v[kk + 1] * inv);
+        }
+        scales[blk * 64 + m] = (uint8_t)(s + 127);
     }
 }
 
-// One block per (group, 32-row K block); a group without rows (offsets) leaves at once. Thread
-// t takes 8-column chunks t, t + blockDim, ...: its 8 scales once, then 4 code bytes and 16
-// bytes of bf16 per row (aligned for any N that is a multiple of 8).
-__global__ void __launch_bounds__(256)
+// One block of 64 threads per (group, column block, K block); thread m dequantizes column m
+// (16 code bytes, one scale) into 32 rows of bf16 [G, K, cols]. A group without rows (offsets)
+// is skipped.
+__global__ void __launch_bounds__(64)
     mx_dequant_weights_kernel(const uint8_t* __restrict__ codes,
-                              const uint8_t* __restrict__ scales, int G, int K, int N,
-                              const int32_t* __restrict__ offsets, __nv_bfloat16* __restrict__ w) {
+                              const uint8_t* __restrict__ scales, int G, int K, int cols,
+                              MxBlocks bl, const int32_t* __restrict__ offsets,
+                              __nv_bfloat16* __restrict__ w) {
     griddep_wait();
-    const int NP = N / 2, KB = (K + 31) / 32, chunks = N / 8;
-    for (int bid = blockIdx.x; bid < G * KB; bid += gridDim.x) {
-        const int g = bid / KB, kb = bid - g * KB;
+    const long long nblk = (long long)G * bl.nb * bl.kb;
+    const int m = threadIdx.x;
+    for (long long blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+        const int kb = (int)(blk % bl.kb);
+        const long long gn = blk / bl.kb;
+        const int nb = (int)(gn % bl.nb), g = (int)(gn / bl.nb);
         if (offsets && __ldg(offsets + g + 1) == __ldg(offsets + g)) continue;
+        const int col = mx_block_col(bl, nb, m);
+        if (col < 0) continue;
+        const float sc = pow2_f32((int)__ldg(scales + blk * 64 + m) - 127);
+        const uint8_t* cb = codes + blk * 1024;
+        const int mt = m >> 4, r16 = m & 15, hi = r16 >> 3, lq = r16 & 7;
         const int k0 = kb * 32, nr = min(32, K - k0);
-        for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
-            const uint2 sv = __ldg(reinterpret_cast<const uint2*>(
-                scales + ((size_t)g * KB + kb) * N + 8 * c));
-            float sc[8];
+        __nv_bfloat16* dst = w + ((size_t)g * K + k0) * cols + col;
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                sc[i] = pow2_f32((int)(((i < 4 ? sv.x : sv.y) >> (8 * (i % 4))) & 0xFF) - 127);
-            const uint8_t* src = codes + ((size_t)g * K + k0) * NP + 4 * c;
-            __nv_bfloat16* dst = w + ((size_t)g * K + k0) * N + 8 * c;
-            for (int r = 0; r < nr; ++r) {
-                const uint32_t cw = __ldg(reinterpret_cast<const uint32_t*>(src + (size_t)r * NP));
-                uint32_t o[4];
-#pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    const float2 q = e2m1x2_to_f32((cw >> (8 * b)) & 0xFF);
-                    o[b] = pack_bf16x2(q.x * sc[2 * b], q.y * sc[2 * b + 1]);
-                }
-                *reinterpret_cast<uint4*>(dst + (size_t)r * N) = make_uint4(o[0], o[1], o[2], o[3]);
-            }
+        for (int kk = 0; kk < 32; kk += 2) {
+            const int ks = kk >> 4, kx = kk & 15, kh = kx >> 3, l = lq * 4 + ((kx & 7) >> 1);
+            const float2 q = e2m1x2_to_f32(__ldg(cb + (((ks * 4 + mt) * 32 + l) << 2) + hi + 2 * kh));
+            if (kk < nr) dst[(size_t)kk * cols] = __float2bfloat16_rn(q.x * sc);
+            if (kk + 1 < nr) dst[(size_t)(kk + 1) * cols] = __float2bfloat16_rn(q.y * sc);
         }
     }
 }
@@ -164,32 +172,45 @@ int grid_for(long long work) {
 
 }  // namespace
 
-MxGeom mx_geom(int K, int N, int G) {
+MxBlocks mx_blocks(bool gate_up, int K, int N) {
+    MxBlocks b;
+    b.half = gate_up ? N : 0;
+    b.nbh = gate_up ? (N + 63) / 64 : (N + 63) / 64;
+    b.nb = gate_up ? 2 * b.nbh : b.nbh;
+    b.kb = (K + 31) / 32;
+    b.cols = gate_up ? 2 * N : N;
+    return b;
+}
+
+MxGeom mx_geom(bool gate_up, int K, int N, int G) {
+    const MxBlocks b = mx_blocks(gate_up, K, N);
     MxGeom m;
-    m.codes = (size_t)G * K * (N / 2);
-    m.scales_off = (m.codes + 255) / 256 * 256;
-    m.total = m.scales_off + (size_t)G * ((K + 31) / 32) * N;
+    m.blocks = b;
+    m.codes = (size_t)G * b.nb * b.kb * 1024;
+    m.scales_off = m.codes;  // a multiple of 1024
+    m.total = m.codes + (size_t)G * b.nb * b.kb * 64;
     return m;
 }
 
-cudaError_t launch_mx_quant_weights(const void* w, int G, int K, int N, void* mx,
+cudaError_t launch_mx_quant_weights(bool gate_up, const void* w, int G, int K, int N, void* mx,
                                     cudaStream_t s) {
-    const MxGeom m = mx_geom(K, N, G);
+    const MxGeom m = mx_geom(gate_up, K, N, G);
     uint8_t* base = static_cast<uint8_t*>(mx);
-    const long long work = (long long)G * ((K + 31) / 32) * (N / 2);
+    const long long work = (long long)G * m.blocks.nb * m.blocks.kb * 64;
     return launch_kernel(mx_quant_weights_kernel, dim3(grid_for(work)), dim3(256), 0, s,
-                         static_cast<const uint32_t*>(w), G, K, N, base, base + m.scales_off);
+                         static_cast<const __nv_bfloat16*>(w), G, K, m.blocks.cols, m.blocks,
+                         base, base + m.scales_off);
 }
 
-cudaError_t launch_mx_dequant_weights(const void* mx, int G, int K, int N,
+cudaError_t launch_mx_dequant_weights(bool gate_up, const void* mx, int G, int K, int N,
                                       const int32_t* offsets, void* w, cudaStream_t s) {
-    const MxGeom m = mx_geom(K, N, G);
+    const MxGeom m = mx_geom(gate_up, K, N, G);
     const uint8_t* base = static_cast<const uint8_t*>(mx);
-    const long long blocks = (long long)G * ((K + 31) / 32);
-    const long long cap = (long long)device_sm_count() * 16;
+    const long long blocks = (long long)G * m.blocks.nb * m.blocks.kb;
+    const long long cap = (long long)device_sm_count() * 32;
     return launch_kernel(mx_dequant_weights_kernel, dim3((unsigned)(blocks < cap ? blocks : cap)),
-                         dim3(256), 0, s, base, base + m.scales_off, G, K, N, offsets,
-                         static_cast<__nv_bfloat16*>(w));
+                         dim3(64), 0, s, base, base + m.scales_off, G, K, m.blocks.cols,
+                         m.blocks, offsets, static_cast<__nv_bfloat16*>(w));
 }
 
 cudaError_t launch_mx_rows(const void* in, int R, int K, void* out, void* codes, void* scales,

@@ -77,4 +77,15 @@ __device__ __forceinline__ void mx_fakequant_e4m3_block(float (&v)[32], int n) {
     }
 }
 
+// Column of the logical weight that column m of column block nb holds (-1: padding).
+__device__ __forceinline__ int mx_block_col(const MxBlocks& b, int nb, int m) {
+    if (b.half) {
+        const int up = nb >= b.nbh;
+        const int c = (nb - (up ? b.nbh : 0)) * 64 + m;
+        return c < b.half ? c + (up ? b.half : 0) : -1;
+    }
+    const int c = nb * 64 + m;
+    return c < b.cols ? c : -1;
+}
+
 }  // namespace rdg

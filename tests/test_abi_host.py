@@ -185,9 +185,10 @@ def test_kernel_count_and_strings(L):
 
 
 def test_mx_validation_and_sizes(L):
-    # gate_up [E=2, K=64, 2I=2*64]: codes 2*64*64 bytes, scales 2*2*128 after 256-byte rounding
-    assert L.moe_mx_weights_size(0, 2, 64, 64) == 2 * 64 * 64 + 2 * 2 * 128
-    assert L.moe_mx_weights_size(1, 1, 200, 96) == (200 * 48 + 255) // 256 * 256 + 7 * 96
+    # blocks of 64 columns x 32 rows: 1 KB of codes + 64 B of scales each. gate_up [E=2, K=64,
+    # I=64]: 2 column blocks (gate, up) x 2 K blocks per expert; down [E=1, K=200, d=96]: 2 x 7
+    assert L.moe_mx_weights_size(0, 2, 64, 64) == 2 * 2 * 2 * (1024 + 64)
+    assert L.moe_mx_weights_size(1, 1, 200, 96) == 2 * 7 * (1024 + 64)
     assert L.moe_mx_weights_size(0, 1, 64, 60) == 0                     # N % 8
     q = L.moe_quantize_weights_mx
     assert q(7, FAKE, FAKE, 1, 64, 64, NULL) == 1                          # unknown kind
