@@ -57,13 +57,15 @@ constexpr long long kMaxRowsF32 = 60000ll * 32;
 
 struct ForwardLayout {
     size_t fcnt, counts, offsets, chunk, s2p, p2s, x_sorted, h, y, h_sh, y_sh, fused, ab, ab_sh,
-        x_q, w_gu, w_dn, w_sgu, w_sdn, total;
+        x_q, w_gu, w_dn, w_sgu, w_sdn, h_codes, h_scales, total;
 };
 
 // train: the layout of moe_forward_train (no one-kernel decode path; the gate/up accumulators
 // of the routed rows and of the shared expert are kept for the backward pass, after the rest)
-// mx: the layout of moe_forward_mx (no one-kernel decode path; after the rest: x rounded to
-// MXFP8 [T, d] and the dequantized bf16 weights of the routed and the shared experts)
+// mx: the layout of moe_forward_mx. Decode batches run the one-kernel layer on the MX weights:
+// after its partial sums, h's MXFP8 codes [R, I] and scales [R, ceil(I / 32)]. Other batches:
+// after the rest, x rounded to MXFP8 [T, d] and the dequantized bf16 weights of the routed and
+// the shared experts.
 ForwardLayout forward_layout(int T, int d, int E, int k, int I, int Is, moe_dtype dt,
                              bool train = false, bool mx = false) {
     const size_t R = (size_t)T * k, b = dtype_bytes(dt);
@@ -76,8 +78,8 @@ ForwardLayout forward_layout(int T, int d, int E, int k, int I, int Is, moe_dtyp
     };
     // the fused decode kernel's counters follow the status word (one memset clears both);
     // its partial sums go last
-    const bool fused = !train && !mx && decode_fused_applies(dt, T, k, Is);
-    const DecodeFusedLayout F = decode_fused_layout(T, d, k, I);
+    const bool fused = !train && decode_fused_applies(dt, T, k, Is);
+    const DecodeFusedLayout F = decode_fused_layout(T, d, k, I, mx);
     L.fcnt = take(fused ? F.counter_bytes : 0);
     L.counts = take((size_t)E * 4);
     L.offsets = take((size_t)(E + 1) * 4);
@@ -92,11 +94,14 @@ ForwardLayout forward_layout(int T, int d, int E, int k, int I, int Is, moe_dtyp
     L.fused = take(fused ? F.part_bytes : 0);
     L.ab = take(train ? R * 2 * (size_t)I * b : 0);
     L.ab_sh = take(train && Is > 0 ? (size_t)T * 2 * Is * b : 0);
-    L.x_q = take(mx ? (size_t)T * d * 2 : 0);
-    L.w_gu = take(mx ? (size_t)E * d * 2 * I * 2 : 0);
-    L.w_dn = take(mx ? (size_t)E * I * d * 2 : 0);
-    L.w_sgu = take(mx ? (size_t)d * 2 * Is * 2 : 0);
-    L.w_sdn = take(mx ? (size_t)Is * d * 2 : 0);
+    const bool mx_chain = mx && !fused;
+    L.x_q = take(mx_chain ? (size_t)T * d * 2 : 0);
+    L.w_gu = take(mx_chain ? (size_t)E * d * 2 * I * 2 : 0);
+    L.w_dn = take(mx_chain ? (size_t)E * I * d * 2 : 0);
+    L.w_sgu = take(mx_chain ? (size_t)d * 2 * Is * 2 : 0);
+    L.w_sdn = take(mx_chain ? (size_t)Is * d * 2 : 0);
+    L.h_codes = take(mx && fused ? R * (size_t)I : 0);
+    L.h_scales = take(mx && fused ? R * (size_t)((I + 31) / 32) : 0);
     L.total = o;
     return L;
 }
@@ -439,16 +444,18 @@ static moe_status forward_impl(const void* x, const float* logits, moe_dtype dt,
     const int R = T * k;
 
     const bool renorm = (flags & MOE_RENORMALIZE) != 0;
-    // MX layers: x rounded to MXFP8 once per token (the routed rows are copies of it)
+    // MX layers: x rounded to MXFP8 once per token (the routed rows are copies of it); the
+    // one-kernel decode layer rounds its own
+    const bool fused = !train && decode_fused_applies(dt, T, k, Is);
     const void* x_in = x;
-    if (mx) {
+    if (mx && !fused) {
         if ((st = clear_status(workspace, s)) != MOE_OK) return st;
         if ((st = launch_status(launch_mx_rows(x, T, d, ws + L.x_q, nullptr, nullptr, s))) !=
             MOE_OK)
             return st;
         x_in = ws + L.x_q;
     }
-    if (!train && !mx && decode_fused_applies(dt, T, k, Is)) {
+    if (fused) {
         // decode: the whole layer in one cooperative kernel; its counters sit right after the
         // status word and are cleared with it
         if ((st = launch_status(cudaMemsetAsync(workspace, 0, L.counts, s))) != MOE_OK)
@@ -478,9 +485,14 @@ static moe_status forward_impl(const void* x, const float* logits, moe_dtype dt,
         a.counters = reinterpret_cast<int*>(ws + L.fcnt);
         a.partials = ws + L.fused;
         a.status = status;
+        a.mx = mx;
+        if (mx) {
+            a.h_codes = ws + L.h_codes;
+            a.h_scales = ws + L.h_scales;
+        }
         return launch_status(launch_decode_fused(a, s));
     }
-    if (!mx && (st = clear_status(workspace, s)) != MOE_OK) return st;
+    if (!(mx && !fused) && (st = clear_status(workspace, s)) != MOE_OK) return st;
     if (R <= kSmallDispatchMaxSlots) {
         // few tokens: route and the dispatch indices in one launch, then the row copy
         if ((st = launch_status(launch_route_dispatch_small(logits, T, E, k, (int)score_fn,

@@ -47,6 +47,7 @@
 // the workspace head that precedes the launch.
 #include <mutex>
 
+#include "mx.cuh"
 #include "route_warp.cuh"
 
 namespace rdg {
@@ -68,6 +69,16 @@ constexpr int kStrideB = 68;                    // conflicts on the fragment-lay
 constexpr int kRedFloats = kConsumerWarps * kPass * kStrideA;  // [6][8][132] >= [6][8][68]
 constexpr int kOutFloats = kDecodeFusedMaxTokens * 64;         // per-token output accumulator
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// MX weights (MXFP4 codes in 1 KB blocks of 64 columns x 32 K rows, 64 scale bytes each): a
+// gate_up item is up to 15 K blocks of its gate and up column blocks, a down item up to 30 K
+// blocks of one output column block; codes, then scales, within the 32 KB stage.
+constexpr int kMxKbA = 15;
+constexpr int kMxKbB = 30;
+constexpr uint32_t kMxUpCodes = 15 * 1024;     // up codes after the gate codes (gate_up item)
+constexpr uint32_t kMxScales = 30 * 1024;      // scales after the codes
+constexpr uint32_t kMxUpScales = kMxScales + 15 * 64;
+static_assert(kMxUpScales + 15 * 64 <= kStageBytes && kMxScales + 30 * 64 <= kStageBytes,
+              "MX items exceed a stage");
 constexpr int kDecodeWaves = 1;                 // expert waves (gate_up of wave w + 1 hides the
                                                 // finishing of wave w's h)
 
@@ -100,7 +111,16 @@ struct Params {
     int score_fn, renorm;
     int nbh, nka, nbd, nkb;
     int scale_input, packed;
-    int gu_nb, dn_nb;        // packed blocks per expert (gate_up, down)
+    int gu_nb, dn_nb;        // packed blocks per expert (gate_up, down); MX: column blocks
+    // MX layers: weights as MX buffers (codes then scales), h rounded to MXFP8 into h_codes
+    // [R, I] / h_scales [R, kbi] for the down items (and its values into h, bf16)
+    const uint8_t* mx_gu;
+    const uint8_t* mx_dn;
+    size_t mx_gu_scales, mx_dn_scales;  // scale offsets in the buffers
+    uint8_t* h_codes;
+    uint8_t* h_scales;
+    int kbd, kbi;            // 32-row K blocks of d and I
+    int mx;
 };
 
 // What a block's consumers share.
@@ -175,6 +195,56 @@ __device__ __forceinline__ void mma_step(uint32_t box, int k0, int m0, int lane,
             : "+f"(acc[n][0]), "+f"(acc[n][1]), "+f"(acc[n][2]), "+f"(acc[n][3])
             : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b[n][0]), "r"(b[n][1]));
     }
+}
+
+// ---- MX helpers ----
+// f16x2 from one byte of two E2M1 codes (low nibble in the low half) / two E4M3 codes.
+__device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t byte) {
+    uint32_t h2;
+    asm("{\n\t.reg .b8 t;\n\tcvt.u8.u32 t, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(h2)
+        : "r"(byte));
+    return h2;
+}
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)two));
+    return h2;
+}
+// acc[n] += A (16 x 16, f16) . B[n] (16 x 8, f16), fp32 accumulate
+template <int NTILE>
+__device__ __forceinline__ void mma_f16(const uint32_t (&a)[4], const uint32_t (&b)[NTILE][2],
+                                        float (&acc)[NTILE][4]) {
+#pragma unroll
+    for (int n = 0; n < NTILE; ++n)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(acc[n][0]), "+f"(acc[n][1]), "+f"(acc[n][2]), "+f"(acc[n][3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[n][0]), "r"(b[n][1]));
+}
+// 1D bulk copy global -> shared completing on an mbarrier, with an L2 policy.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+// An E8M0 scale code c as fp32: 2^(c - 127) (c = 0: 2^-127, a subnormal; 255 is not produced).
+__device__ __forceinline__ float e8m0_f32(uint32_t c) {
+    return __uint_as_float(c ? c << 23 : 0x400000u);
+}
+__device__ __forceinline__ uint32_t lds8(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
 }
 
 // B fragments of the gate_up step for K rows [k0, k0 + 16): lane l holds row 8 n + l/4 of the
@@ -272,6 +342,26 @@ __device__ __forceinline__ void store_h(const Params& p, const Ctx& c, int row, 
     p.h[(size_t)row * p.I + hc] = __float2bfloat16_rn(silu(g * s) * (u * s));
 }
 
+// MX layers: h rounded to MXFP8 (blocks of 32 along I). Called by all 32 lanes of the epilogue
+// warp together, lane l holding column hc of the same 32-column block of one row (valid: hc < I):
+// the block's largest magnitude is a warp maximum. Stores the E4M3 code and scale the down items
+// read, and the rounded value into h.
+__device__ __forceinline__ void store_h_mx(const Params& p, const Ctx& c, int row, int hc,
+                                           float g, float u, bool valid) {
+    const float s = p.scale_input ? c.s_w[row] : 1.0f;
+    const float hv = valid ? silu(g * s) * (u * s) : 0.0f;
+    float amax = fabsf(hv);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const int se = mx_scale_exp(amax, 8);
+    const uint32_t code = e4m3x2(hv * pow2_f32(-se), 0.0f) & 0xFFu;
+    if (valid) {
+        p.h_codes[(size_t)row * p.I + hc] = (uint8_t)code;
+        p.h[(size_t)row * p.I + hc] = __float2bfloat16_rn(e4m3x2_to_f32(code).x * pow2_f32(se));
+        if (c.lane == 0) p.h_scales[(size_t)row * p.kbi + hc / 32] = (uint8_t)(se + 127);
+    }
+}
+
 // First item of [i0, ...) that warp w owns (item i belongs to warp i % kStages).
 __device__ __forceinline__ int first_owned(int i0, int w) {
     return i0 + ((w - i0 % kStages) + kStages) % kStages;
@@ -316,12 +406,209 @@ __device__ __forceinline__ bool epi_arrive_last(const Ctx& c, int* counter, int 
     return prev == contributors - 1;
 }
 
+// ---- MX items (MXFP4 weights, MXFP8 activations) ----
+// Per 32-row K block: the lanes' A fragments are one word each (two k-steps per block), the
+// MMA runs on the element values in f16 (exact), and the block's partial sums are added to the
+// fp32 accumulators times the weight column's and the token's block scales.
+
+// This lane's x words of K block kbg (bf16 pairs): for token row 8 n + l/4, K values
+// kbg 32 + 16 ks + 8 h + 2 (l & 3) + {0, 1} in w[n][2 ks + h]. Loaded ahead of their use.
+template <int NTILE>
+__device__ __forceinline__ void mx_x_load(const unsigned int* const (&rows)[NTILE], int kbg,
+                                          int d, int lane, uint32_t (&w)[NTILE][4]) {
+#pragma unroll
+    for (int n = 0; n < NTILE; ++n)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int kk = kbg * 32 + 16 * (j >> 1) + 8 * (j & 1) + 2 * (lane & 3);
+            w[n][j] = (rows[n] != nullptr && kk < d) ? __ldg(rows[n] + kk / 2) : 0u;
+        }
+}
+
+// B fragments of one K block from its x words, rounded to MXFP8 as the row quantiser rounds x:
+// the four lanes of a token hold its 32 values, so two shuffles give the block's largest
+// magnitude. sxc[n][j]: the block scale of token 8 n + 2 (l & 3) + j (the C fragment's columns).
+template <int NTILE>
+__device__ __forceinline__ void mx_x_quant(const uint32_t (&w)[NTILE][4], int lane,
+                                           uint32_t (&b)[2][NTILE][2], float (&sxc)[NTILE][2]) {
+#pragma unroll
+    for (int n = 0; n < NTILE; ++n) {
+        float v[4][2];
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[j][0] = __uint_as_float(w[n][j] << 16);
+            v[j][1] = __uint_as_float(w[n][j] & 0xFFFF0000u);
+            amax = fmaxf(amax, fmaxf(fabsf(v[j][0]), fabsf(v[j][1])));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        const int se = mx_scale_exp(amax, 8);
+        const float inv = pow2_f32(-se), sc = pow2_f32(se);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            b[j >> 1][n][j & 1] = e4m3x2_f16x2(e4m3x2(v[j][0] * inv, v[j][1] * inv));
+        sxc[n][0] = __shfl_sync(0xFFFFFFFFu, sc, 8 * (lane & 3));
+        sxc[n][1] = __shfl_sync(0xFFFFFFFFu, sc, 8 * (lane & 3) + 4);
+    }
+}
+
+// A fragment registers of m-tile mt, k-step ks of K block kbl from a stage's code words.
+__device__ __forceinline__ void mx_a(uint32_t codes, int kbl, int ks, int mt, int lane,
+                                     uint32_t (&a)[4]) {
+    const uint32_t w = lds32(codes + ((((kbl * 2 + ks) * 4 + mt) * 32 + lane) << 2));
+    a[0] = e2m1x2_f16x2(w & 0xFF);
+    a[1] = e2m1x2_f16x2((w >> 8) & 0xFF);
+    a[2] = e2m1x2_f16x2((w >> 16) & 0xFF);
+    a[3] = e2m1x2_f16x2(w >> 24);
+}
+
+// acc[n] += part[n] times the scales of its rows (weight columns: sw0 for l/4, sw1 for l/4 + 8)
+// and columns (tokens: sxc[n][0], sxc[n][1])
+template <int NTILE>
+__device__ __forceinline__ void mx_rescale(const float (&part)[NTILE][4], float sw0, float sw1,
+                                           const float (&sxc)[NTILE][2], float (&acc)[NTILE][4]) {
+#pragma unroll
+    for (int n = 0; n < NTILE; ++n) {
+        acc[n][0] = fmaf(part[n][0], sw0 * sxc[n][0], acc[n][0]);
+        acc[n][1] = fmaf(part[n][1], sw0 * sxc[n][1], acc[n][1]);
+        acc[n][2] = fmaf(part[n][2], sw1 * sxc[n][0], acc[n][2]);
+        acc[n][3] = fmaf(part[n][3], sw1 * sxc[n][1], acc[n][3]);
+    }
+}
+
+// gate_up item: K blocks [15 kc, ...) of the gate and up column blocks; acc[mt], m-tiles 0-3
+// gate, 4-7 up.
+template <int NTILE>
+__device__ __forceinline__ void item_a_mx(Ctx& c, const Params& p, int i, int kc,
+                                          const unsigned int* const (&rows)[NTILE],
+                                          float (&acc)[8][NTILE][4]) {
+    const uint32_t stage = c.stage0 + (uint32_t)c.warp * kStageBytes;
+    const int kb0 = kc * kMxKbA, nk = min(kMxKbA, p.kbd - kb0);
+    // x words two K blocks ahead of the math (the first two before the stage wait)
+    uint32_t w0[NTILE][4], w1[NTILE][4], w2[NTILE][4];
+    mx_x_load<NTILE>(rows, kb0, p.d, c.lane, w0);
+    mx_x_load<NTILE>(rows, kb0 + 1, p.d, c.lane, w1);
+    if (take_stage(c, p, i)) {
+        for (int kbl = 0; kbl < nk; ++kbl) {
+            mx_x_load<NTILE>(rows, kb0 + kbl + 2, p.d, c.lane, w2);  // past d: zeros, no load
+            uint32_t b[2][NTILE][2];
+            float sxc[NTILE][2];
+            mx_x_quant<NTILE>(w0, c.lane, b, sxc);
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const uint32_t half = (uint32_t)(mt >> 2);
+                const uint32_t codes = stage + half * kMxUpCodes;
+                const uint32_t scl = stage + kMxScales + half * (kMxUpScales - kMxScales) +
+                                     kbl * 64 + (mt & 3) * 16 + (c.lane >> 2);
+                float part[NTILE][4];
+#pragma unroll
+                for (int n = 0; n < NTILE; ++n)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) part[n][j] = 0.0f;
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    uint32_t a[4];
+                    mx_a(codes, kbl, ks, mt & 3, c.lane, a);
+                    mma_f16<NTILE>(a, b[ks], part);
+                }
+                mx_rescale<NTILE>(part, e8m0_f32(lds8(scl)), e8m0_f32(lds8(scl + 8)), sxc,
+                                  acc[mt]);
+            }
+#pragma unroll
+            for (int n = 0; n < NTILE; ++n)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    w0[n][j] = w1[n][j];
+                    w1[n][j] = w2[n][j];
+                }
+        }
+    }
+    release_stage(c);
+}
+
+// down item: K blocks [30 kc, ...) of one output column block. hrow[n]: the expert's h code row
+// of this lane's B token (8 n + l/4); hsc[n][j]: the h scale row of token 8 n + 2 (l & 3) + j.
+// This lane's h words of K block kbg: codes (two per 16 bits) of its B token row for
+// k-steps and halves, and the block scales of its C fragment's token rows.
+template <int NTILE>
+__device__ __forceinline__ void mx_h_load(const Params& p, const uint8_t* const (&hrow)[NTILE],
+                                          const uint8_t* const (&hsc)[NTILE][2], int kbg,
+                                          int lane, uint32_t (&w)[NTILE][6]) {
+#pragma unroll
+    for (int n = 0; n < NTILE; ++n) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int kk = kbg * 32 + 16 * (j >> 1) + 8 * (j & 1) + 2 * (lane & 3);
+            w[n][j] = (hrow[n] != nullptr && kk < p.I)
+                          ? (uint32_t)__ldcg(reinterpret_cast<const unsigned short*>(hrow[n] + kk))
+                          : 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            w[n][4 + j] = (hsc[n][j] != nullptr && kbg < p.kbi) ? (uint32_t)__ldcg(hsc[n][j] + kbg)
+                                                                 : 0u;
+    }
+}
+
+template <int NTILE>
+__device__ __forceinline__ void item_b_mx(Ctx& c, const Params& p, int i, int kc,
+                                          const uint8_t* const (&hrow)[NTILE],
+                                          const uint8_t* const (&hsc)[NTILE][2],
+                                          float (&acc)[4][NTILE][4]) {
+    const uint32_t stage = c.stage0 + (uint32_t)c.warp * kStageBytes;
+    const int kb0 = kc * kMxKbB, nk = min(kMxKbB, p.kbi - kb0);
+    uint32_t w0[NTILE][6], w1[NTILE][6], w2[NTILE][6];
+    mx_h_load<NTILE>(p, hrow, hsc, kb0, c.lane, w0);
+    mx_h_load<NTILE>(p, hrow, hsc, kb0 + 1, c.lane, w1);
+    if (take_stage(c, p, i)) {
+        for (int kbl = 0; kbl < nk; ++kbl) {
+            mx_h_load<NTILE>(p, hrow, hsc, kb0 + kbl + 2, c.lane, w2);
+            uint32_t b[2][NTILE][2];
+            float sxc[NTILE][2];
+#pragma unroll
+            for (int n = 0; n < NTILE; ++n) {
+#pragma unroll
+                for (int j = 0; j < 4; ++j) b[j >> 1][n][j & 1] = e4m3x2_f16x2(w0[n][j]);
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    sxc[n][j] = hsc[n][j] != nullptr ? e8m0_f32(w0[n][4 + j]) : 0.0f;
+            }
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                const uint32_t scl = stage + kMxScales + kbl * 64 + mt * 16 + (c.lane >> 2);
+                float part[NTILE][4];
+#pragma unroll
+                for (int n = 0; n < NTILE; ++n)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) part[n][j] = 0.0f;
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    uint32_t a[4];
+                    mx_a(stage, kbl, ks, mt, c.lane, a);
+                    mma_f16<NTILE>(a, b[ks], part);
+                }
+                mx_rescale<NTILE>(part, e8m0_f32(lds8(scl)), e8m0_f32(lds8(scl + 8)), sxc,
+                                  acc[mt]);
+            }
+#pragma unroll
+            for (int n = 0; n < NTILE; ++n)
+#pragma unroll
+                for (int j = 0; j < 6; ++j) {
+                    w0[n][j] = w1[n][j];
+                    w1[n][j] = w2[n][j];
+                }
+        }
+    }
+    release_stage(c);
+}
+
 // ================= consumer side =================
 
 // gate_up group (q, jb) of this block: block-local items [i0, i0 + kc1 - kc0) = K chunks
 // [kc0, kc1); then its register sums go to the epilogue warp, 8 rows per dump, as
 // red[warp][row][column] (columns 0-63 gate, 64-127 up).
-template <int NTILE>
+template <int NTILE, bool MX>
 __device__ void group_a(Ctx& c, const Params& p, int q, int i0, int kc0, int kc1) {
     const int row0 = c.s_off[q], tq = c.s_tq[q];
     const unsigned int* rows[NTILE];
@@ -339,8 +626,12 @@ __device__ void group_a(Ctx& c, const Params& p, int q, int i0, int kc0, int kc1
         for (int n = 0; n < NTILE; ++n)
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[mt][n][j] = 0.0f;
-    for (int i = first_owned(i0, c.warp); i < i0 + (kc1 - kc0); i += kStages)
-        item_a<NTILE>(c, p, i, kc0 + (i - i0), rows, acc);
+    for (int i = first_owned(i0, c.warp); i < i0 + (kc1 - kc0); i += kStages) {
+        if (MX)
+            item_a_mx<NTILE>(c, p, i, kc0 + (i - i0), rows, acc);
+        else
+            item_a<NTILE>(c, p, i, kc0 + (i - i0), rows, acc);
+    }
 #pragma unroll
     for (int pass = 0; pass < NTILE; ++pass) {
         if (pass * kPass < tq) {
@@ -360,15 +651,25 @@ __device__ void group_a(Ctx& c, const Params& p, int q, int i0, int kc0, int kc1
 
 // Down items of expert q for one output block: block-local items [i0, i0 + kc1 - kc0) = K
 // chunks [kc0, kc1); then the register sums go to the epilogue warp as red[warp][row][column].
-template <int NTILE>
+template <int NTILE, bool MX>
 __device__ void group_b(Ctx& c, const Params& p, int q, int i0, int kc0, int kc1) {
     const int row0 = c.s_off[q], tq = c.s_tq[q];
     const unsigned int* rows[NTILE];
+    const uint8_t* hrow[NTILE];
+    const uint8_t* hsc[NTILE][2];
 #pragma unroll
     for (int n = 0; n < NTILE; ++n) {
         const int r = 8 * n + (c.lane >> 2);
         rows[n] = r < tq ? reinterpret_cast<const unsigned int*>(p.h + (size_t)(row0 + r) * p.I)
                          : nullptr;
+        if (MX) {
+            hrow[n] = r < tq ? p.h_codes + (size_t)(row0 + r) * p.I : nullptr;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int t = 8 * n + 2 * (c.lane & 3) + j;
+                hsc[n][j] = t < tq ? p.h_scales + (size_t)(row0 + t) * p.kbi : nullptr;
+            }
+        }
     }
     float acc[4][NTILE][4];
 #pragma unroll
@@ -394,7 +695,10 @@ __device__ void group_b(Ctx& c, const Params& p, int q, int i0, int kc0, int kc1
             __syncwarp();
             c.ready_q = q;
         }
-        item_b<NTILE>(c, p, i, kc0 + (i - i0), rows, acc);
+        if (MX)
+            item_b_mx<NTILE>(c, p, i, kc0 + (i - i0), hrow, hsc, acc);
+        else
+            item_b<NTILE>(c, p, i, kc0 + (i - i0), rows, acc);
     }
 #pragma unroll
     for (int pass = 0; pass < NTILE; ++pass) {
@@ -444,7 +748,10 @@ __device__ void epi_finish_h(const Ctx& c, const Params& p, int row0, int tq, in
                 us += uv[j];
             }
         }
-        if (jb * 64 + col < p.I) store_h(p, c, row0 + t, jb * 64 + col, gs, us);
+        if (p.mx)
+            store_h_mx(p, c, row0 + t, jb * 64 + col, gs, us, jb * 64 + col < p.I);
+        else if (jb * 64 + col < p.I)
+            store_h(p, c, row0 + t, jb * 64 + col, gs, us);
     }
 }
 
@@ -470,7 +777,10 @@ __device__ void epi_a(Ctx& c, const Params& p, int q, int jb, int g, int b_first
                     if (whole) uu += rr[64];
                 }
                 if (whole) {
-                    if (jb * 64 + col < p.I)
+                    if (p.mx)
+                        store_h_mx(p, c, row0 + pass * kPass + t, jb * 64 + col, v, uu,
+                                   jb * 64 + col < p.I);
+                    else if (jb * 64 + col < p.I)
                         store_h(p, c, row0 + pass * kPass + t, jb * 64 + col, v, uu);
                 } else {
                     __stcg(part + (size_t)(pass * kPass + t) * 128 + col, v);
@@ -597,6 +907,7 @@ __device__ __forceinline__ void by_rows(int tq, F&& f) {
         f(NtTag<2>{});
 }
 
+template <bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                     const __grid_constant__ CUtensorMap tmD, Params p, int vpl) {
@@ -627,7 +938,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
         fence_barrier_init();
         for (int f = 0; f < 4; ++f) flags[f] = 0;
     }
-    if (warp == kProducerWarp && lane == 0) {
+    if (!MX && warp == kProducerWarp && lane == 0) {  // MX items are plain bulk copies
         tma_prefetch_desc(&tmGU);
         tma_prefetch_desc(&tmD);
     }
@@ -768,7 +1079,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
             const uint64_t pol = l2_evict_first();
             int i = 0;
             bool ok = true;
-            auto next_stage = [&](uint32_t& dst, uint64_t*& bar) {
+            auto next_stage = [&](uint32_t& dst, uint64_t*& bar, uint32_t bytes) {
                 const int st = i % kStages;
                 const uint32_t ph = (uint32_t)(i / kStages) & 1u;
                 if (!mbar_wait(&empty[st], ph ^ 1u, flags, kWaitLimitNs)) {
@@ -776,7 +1087,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                     flags[0] = 1;
                     return false;
                 }
-                mbar_arrive_expect_tx(&full[st], kStageBytes);
+                mbar_arrive_expect_tx(&full[st], bytes);
                 dst = stage0 + (uint32_t)st * kStageBytes;
                 bar = &full[st];
                 ++i;
@@ -790,9 +1101,24 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                 for (int u = lo; ok && u < hi; ++u) {
                     uint32_t dst;
                     uint64_t* bar;
-                    if (!(ok = next_stage(dst, bar))) break;
                     const int g = q_lo * p.nbh + u / p.nka, kc = u % p.nka;
                     const int q = g / p.nbh, jb = g % p.nbh, e = s_eq[q];
+                    if (MX) {
+                        // K blocks [15 kc, ...) of the gate and up column blocks: runs of 1 KB
+                        // code blocks and 64 B scale blocks
+                        const int kb0 = kc * kMxKbA, nk = min(kMxKbA, p.kbd - kb0);
+                        const size_t bg = ((size_t)e * p.gu_nb + jb) * p.kbd + kb0;
+                        const size_t bu = ((size_t)e * p.gu_nb + p.nbh + jb) * p.kbd + kb0;
+                        if (!(ok = next_stage(dst, bar, (uint32_t)nk * 2 * (1024 + 64)))) break;
+                        bulk_load(dst, p.mx_gu + bg * 1024, nk * 1024, bar, pol);
+                        bulk_load(dst + kMxUpCodes, p.mx_gu + bu * 1024, nk * 1024, bar, pol);
+                        bulk_load(dst + kMxScales, p.mx_gu + p.mx_gu_scales + bg * 64, nk * 64,
+                                  bar, pol);
+                        bulk_load(dst + kMxUpScales, p.mx_gu + p.mx_gu_scales + bu * 64, nk * 64,
+                                  bar, pol);
+                        continue;
+                    }
+                    if (!(ok = next_stage(dst, bar, kStageBytes))) break;
                     if (p.packed) {
                         tma_load_3d_hint(dst, &tmGU, bar, 0, kc * kKcA, e * p.gu_nb + jb, pol);
                         tma_load_3d_hint(dst + kBoxBytesA, &tmGU, bar, 0, kc * kKcA,
@@ -811,9 +1137,18 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                 for (int u = lo; ok && u < hi; ++u) {
                     uint32_t dst;
                     uint64_t* bar;
-                    if (!(ok = next_stage(dst, bar))) break;
                     const int cb = u / perC, rem = u % perC;
                     const int e = s_eq[q_lo + rem / p.nkb], kc = rem % p.nkb;
+                    if (MX) {
+                        const int kb0 = kc * kMxKbB, nk = min(kMxKbB, p.kbi - kb0);
+                        const size_t bd = ((size_t)e * p.dn_nb + cb) * p.kbi + kb0;
+                        if (!(ok = next_stage(dst, bar, (uint32_t)nk * (1024 + 64)))) break;
+                        bulk_load(dst, p.mx_dn + bd * 1024, nk * 1024, bar, pol);
+                        bulk_load(dst + kMxScales, p.mx_dn + p.mx_dn_scales + bd * 64, nk * 64,
+                                  bar, pol);
+                        continue;
+                    }
+                    if (!(ok = next_stage(dst, bar, kStageBytes))) break;
                     if (p.packed)
                         tma_load_3d_hint(dst, &tmD, bar, 0, kc * kKcB, e * p.dn_nb + cb, pol);
                     else
@@ -872,7 +1207,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                         [&](auto tag) { epi_a<decltype(tag)::value>(c, p, q, jb, g, bf, bl); });
             } else {
                 by_rows(s_tq[q], [&](auto tag) {
-                    group_a<decltype(tag)::value>(c, p, q, i0, kc0, kc1);
+                    group_a<decltype(tag)::value, MX>(c, p, q, i0, kc0, kc1);
                 });
             }
             u += kc1 - kc0;
@@ -893,7 +1228,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                     by_rows(s_tq[q], [&](auto tag) { epi_b<decltype(tag)::value>(c, p, q); });
                 else
                     by_rows(s_tq[q], [&](auto tag) {
-                        group_b<decltype(tag)::value>(c, p, q, i0, kc0, kc1);
+                        group_b<decltype(tag)::value, MX>(c, p, q, i0, kc0, kc1);
                     });
                 u += kc1 - kc0;
                 i0 += kc1 - kc0;
@@ -910,13 +1245,18 @@ bool decode_fused_applies(moe_dtype dt, int T, int k, int Is) {
            T * k <= kDecodeFusedMaxRows;
 }
 
-DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I) {
+DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I, bool mx) {
     DecodeFusedLayout L;
     const size_t R = (size_t)T * k;
     L.nbh = (I + 63) / 64;
-    L.nka = (d + kKcA - 1) / kKcA;
     L.nbd = (d + 63) / 64;
-    L.nkb = (I + kKcB - 1) / kKcB;
+    if (mx) {  // items of up to 15 (gate_up) / 30 (down) 32-row K blocks
+        L.nka = ((d + 31) / 32 + kMxKbA - 1) / kMxKbA;
+        L.nkb = ((I + 31) / 32 + kMxKbB - 1) / kMxKbB;
+    } else {
+        L.nka = (d + kKcA - 1) / kKcA;
+        L.nkb = (I + kKcB - 1) / kKcB;
+    }
     auto up = [](size_t v) { return (v + 255) / 256 * 256; };
     L.counter_bytes = up((2 * R * L.nbh + L.nbd) * 4);
     // partial slots: contributor block b of group g writes slot b + g (unique: a block's groups
@@ -934,18 +1274,23 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(decode_fused_kernel,
+        attr_err = cudaFuncSetAttribute(decode_fused_kernel<false>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kSmemBytes);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(decode_fused_kernel<true>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            (int)kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
 
-    const DecodeFusedLayout L = decode_fused_layout(a.T, a.d, a.k, a.I);
+    const DecodeFusedLayout L = decode_fused_layout(a.T, a.d, a.k, a.I, a.mx);
     const int R = a.T * a.k;
-    CUtensorMap tmGU, tmD;
+    CUtensorMap tmGU = {}, tmD = {};  // MX: unused (items are plain bulk copies)
     const cuuint32_t box_a[3] = {64, kKcA, 1}, box_b[3] = {64, kKcB, 1};
-    bool ok;
-    if (a.packed) {
+    bool ok = true;
+    if (a.mx) {
+    } else if (a.packed) {
         const PackedGeom gg = packed_geom(kGateUp, a.d, a.I);
         const PackedGeom gd = packed_geom(kDown, a.I, a.d);
         const cuuint64_t gu_dims[3] = {64, (cuuint64_t)gg.kpad, (cuuint64_t)a.E * gg.nb};
@@ -998,6 +1343,23 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
     p.packed = a.packed ? 1 : 0;
     p.gu_nb = packed_geom(kGateUp, a.d, a.I).nb;
     p.dn_nb = packed_geom(kDown, a.I, a.d).nb;
+    p.mx = a.mx ? 1 : 0;
+    p.mx_gu = p.mx_dn = nullptr;
+    p.mx_gu_scales = p.mx_dn_scales = 0;
+    p.h_codes = p.h_scales = nullptr;
+    p.kbd = (a.d + 31) / 32;
+    p.kbi = (a.I + 31) / 32;
+    if (a.mx) {
+        const MxGeom gg = mx_geom(true, a.d, a.I, a.E), gd = mx_geom(false, a.I, a.d, a.E);
+        p.mx_gu = static_cast<const uint8_t*>(a.w_gate_up);
+        p.mx_dn = static_cast<const uint8_t*>(a.w_down);
+        p.mx_gu_scales = gg.scales_off;
+        p.mx_dn_scales = gd.scales_off;
+        p.gu_nb = gg.blocks.nb;
+        p.dn_nb = gd.blocks.nb;
+        p.h_codes = static_cast<uint8_t*>(a.h_codes);
+        p.h_scales = static_cast<uint8_t*>(a.h_scales);
+    }
     const int vpl = a.E <= 32 ? 1 : a.E <= 64 ? 2 : a.E <= 128 ? 4 : 8;
 
     // one block per SM (its shared memory allows no more), all resident: cooperative launch.
@@ -1014,7 +1376,8 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_fused_kernel, tmGU, tmD, p, vpl);
+    return a.mx ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<true>, tmGU, tmD, p, vpl)
+                : cudaLaunchKernelEx(&cfg, decode_fused_kernel<false>, tmGU, tmD, p, vpl);
 }
 
 }  // namespace rdg

@@ -343,7 +343,7 @@ struct DecodeFusedLayout {
     size_t counter_bytes;    // int counters
     size_t part_a, part_b, part_bytes;  // partial sums: offsets and total size
 };
-DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I);
+DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I, bool mx = false);
 struct DecodeFusedArgs {
     const void* x;                  // [T, d] bf16
     const float* logits;            // [T, E]
@@ -365,6 +365,12 @@ struct DecodeFusedArgs {
     int* counters;                  // counter_bytes, zero at launch
     void* partials;                 // part_bytes
     int* status;
+    // MX layers: w_gate_up / w_down are MX buffers (packed is false); x and h are rounded to
+    // MXFP8 in the kernel, h's codes [R, I] and scales [R, ceil(I / 32)] going here (and its
+    // values into h)
+    bool mx = false;
+    void* h_codes = nullptr;
+    void* h_scales = nullptr;
 };
 cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s);
 

@@ -345,7 +345,7 @@ def forward_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is, dtype, mx=False
     b = 2 if dtype == torch.bfloat16 else 4
     nchunks = (R + 255) // 256
     # decode batches run the one-kernel layer, whose counters follow the status word
-    fused = dtype == torch.bfloat16 and Is == 0 and 1 <= T <= 16 and R <= 256 and not mx
+    fused = dtype == torch.bfloat16 and Is == 0 and 1 <= T <= 16 and R <= 256
     fcnt = (2 * R * ((I + 63) // 64) + (d + 63) // 64) * 4 if fused else 0
     sizes = [("fused_counters", fcnt), ("counts", E * 4), ("offsets", (E + 1) * 4), ("chunk", nchunks * E * 4),
              ("sorted_to_slot", R * 4), ("slot_to_sorted", R * 4), ("x_sorted", R * d * b),
@@ -356,6 +356,14 @@ def forward_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is, dtype, mx=False
         views[name] = ws[o:o + nbytes]
         o = (o + nbytes + 255) // 256 * 256
     v = views
+    if mx and fused:
+        # the one-kernel layer on MX weights: its partial sums, then h's MXFP8 codes and scales
+        part_b = ((512 + R * ((I + 63) // 64)) * T * 128 * 4 + 255) // 256 * 256
+        part = part_b + ((512 + (d + 63) // 64) * T * 64 * 4 + 255) // 256 * 256
+        o = (o + part + 255) // 256 * 256
+        views["h_codes"] = ws[o:o + R * I]
+        o = (o + R * I + 255) // 256 * 256
+        views["h_scales"] = ws[o:o + R * ((I + 31) // 32)]
     out = {
         "counts": v["counts"].view(torch.int32),
         "offsets": v["offsets"].view(torch.int32),
@@ -368,6 +376,9 @@ def forward_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is, dtype, mx=False
     if Is:
         out["h_shared"] = v["h_shared"].view(dtype).view(T, Is)
         out["y_shared"] = v["y_shared"].view(torch.float32).view(T, d)
+    if "h_codes" in v:
+        out["h_codes"] = v["h_codes"].view(R, I)
+        out["h_scales"] = v["h_scales"].view(R, (I + 31) // 32)
     return out
 
 

@@ -73,8 +73,13 @@ CASES = [  # (name, T, d, E, k, I, score fn, renorm, scaled input, shared I, bia
     ("mixtral_like", 200, 512, 8, 2, 640, M.fwd.SOFTMAX, True, False, 0, "none"),
     ("gptoss_like", 150, 264, 16, 4, 200, M.fwd.SOFTMAX, True, False, 0, "normal0.5"),
     ("scout_like", 96, 256, 4, 1, 384, M.fwd.SIGMOID, False, True, 192, "zipf1.2"),
+    # decode batches: the one-kernel layer on the MX weights (x and h rounded in the kernel)
     ("decode_T1", 1, 1024, 32, 8, 384, M.fwd.SOFTMAX, True, False, 0, "none"),
     ("decode_T8", 8, 1024, 32, 8, 384, M.fwd.SOFTMAX, True, False, 0, "none"),
+    ("decode_T16", 16, 2048, 128, 8, 768, M.fwd.SOFTMAX, True, False, 0, "none"),
+    ("decode_ragged", 5, 264, 16, 4, 200, M.fwd.SOFTMAX, False, False, 0, "normal0.5"),
+    ("decode_sigmoid_scaled", 6, 512, 8, 1, 136, M.fwd.SIGMOID, False, True, 0, "none"),
+    ("decode_one_expert", 3, 256, 4, 4, 64, M.fwd.SOFTMAX, True, False, 0, "none"),
 ]
 
 
@@ -102,8 +107,13 @@ def test_mx_layer_matches_oracle(case):
                        Expertwise(deq_dn), k, fn, renorm, scale, **sh)
     assert np.array_equal(ids.cpu().numpy(), ref["topk_ids"])
     v = moe.forward_workspace_views(ws, T, d, E, k, I, Is, bf16, mx=True)
-    # x_sorted: the MXFP8 rounding of x, permuted (bit-exact)
-    assert np.array_equal(f64(v["x_sorted"]), ref["x_sorted"])
+    fused = moe.moe_forward_kernel_count(T, k, Is) == 1
+    if not fused:  # x_sorted: the MXFP8 rounding of x, permuted (bit-exact)
+        assert np.array_equal(f64(v["x_sorted"]), ref["x_sorted"])
+    else:  # the kernel keeps h's codes for its down items: they encode the h it wrote
+        hc = v["h_codes"].cpu().numpy()
+        hs = v["h_scales"].cpu().numpy()
+        assert np.array_equal(M.dequantize_mx(hc, hs, M.E4M3, axis=1), f64(v["h"]))
     # h: MXFP8 values; where the GPU's fp32 h and the oracle's float64 h round apart it is by
     # one E4M3 step (2^-3 of the value) or, when the block's largest value crosses a power of
     # two, by the scale step; such places are rare
