@@ -556,8 +556,11 @@ def run_ours(args, rank, world):
         mxr = {"ms_per_step": round(mx_ms, 4),
                "tokens_per_s": round(T * world / (mx_ms * 1e-3), 1),
                "weight_bytes": mx_bytes, "weight_bytes_bf16": bf_bytes,
-               "path": "x and h rounded to MXFP8; the touched experts' MXFP4 weights "
-                       "dequantized to bf16 (exact) for the bf16 tensor-core GEMMs",
+               "path": ("one-kernel decode layer streaming the MXFP4 codes (x and h rounded "
+                        "to MXFP8 in the kernel, f16 MMAs on the element values rescaled per "
+                        "32-row K block)" if moe.moe_forward_kernel_count(T, k, Is, dt) == 1
+                        else "x and h rounded to MXFP8; the touched experts' MXFP4 weights "
+                        "dequantized to bf16 (exact) for the bf16 tensor-core GEMMs"),
                "time": "per-step events around moe_forward_mx, L2 flushed before each step"}
         del mxw, mws
 
