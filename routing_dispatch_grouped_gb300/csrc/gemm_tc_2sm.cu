@@ -19,7 +19,7 @@
 // Every mbarrier wait is bounded in time as in the 1-SM kernels.
 #include <mutex>
 
-#include "moe_internal.cuh"
+#include "pair.cuh"
 
 namespace rdg {
 namespace {
@@ -34,83 +34,6 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kPairRows = 2 * kTileM;            // 256 rows per pair tile
 constexpr int kBandTiles = 8;                    // row tiles per band of the tile order
-
-// ---- cta_group::2 forms and cluster helpers ----
-__device__ __forceinline__ uint32_t cta_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_idx() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_cnt() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-                 ::: "memory");
-}
-// shared::cluster address of `local` (a shared::cta address) in CTA `rank` of this cluster
-__device__ __forceinline__ uint32_t mapa(uint32_t local, uint32_t rank) {
-    uint32_t r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
-    return r;
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-__device__ __forceinline__ void tmem_alloc_2sm(uint32_t* dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc_2sm(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-__device__ __forceinline__ void umma_bf16_2sm(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                              uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Arrive on the mbarrier at this shared-memory offset in both CTAs of the pair once every MMA
-// this thread issued has completed.
-__device__ __forceinline__ void umma_commit_2sm(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_u32(bar)),
-        "h"((uint16_t)0x3)
-        : "memory");
-}
-// Tile loads into this CTA's shared memory that complete on the mbarrier at `bar_cluster` (a
-// shared::cluster address, here the leader's stage barrier).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map,
-                                                 uint32_t bar_cluster, int c0, int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
-        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-        "l"(map), "r"(bar_cluster), "r"(c0), "r"(c1)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
-                                                 uint32_t bar_cluster, int c0, int c1, int c2) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
-        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-        "l"(map), "r"(bar_cluster), "r"(c0), "r"(c1), "r"(c2)
-        : "memory");
-}
 
 struct PairParams {
     const int32_t* offsets;
@@ -485,24 +408,8 @@ cudaError_t launch_pair_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
-    if (max_clusters[dev] == 0) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(device_sm_count() & ~1);
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = kSmemBytes;
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = 2;
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, tc_grouped_gemm_2sm<KIND>, &cfg) != cudaSuccess ||
-            n < 1)
-            n = device_sm_count() / 2;
-        max_clusters[dev] = n;
-    }
+    if (max_clusters[dev] == 0)
+        max_clusters[dev] = max_pair_clusters(tc_grouped_gemm_2sm<KIND>, kThreads, kSmemBytes);
     const long long pair_ub = ((long long)(a.R + kPairRows - 1) / kPairRows + groups) * p.n_tiles;
     long long clusters = max_clusters[dev];
     if (pair_ub < clusters) clusters = pair_ub;

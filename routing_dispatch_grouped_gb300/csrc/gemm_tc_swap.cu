@@ -523,23 +523,25 @@ cudaError_t launch_grouped_gemm_bf16_swap(const GroupedGemmArgs& a, cudaStream_t
 // SiLU work to two of the four epilogue warps, which measured slower on every prefill
 // workload). Small batches (at most kSmallBatchRows routed rows): both run here with 32-token
 // tiles, which stream weights without fetching 128- or 256-row token tiles.
-// CTA pairs (256-row tiles, 32 KB stages, six of them in flight) take
-//   - down when the experts average at least 512 rows, where 256-row tiles pad little
-//     (measured faster than 16-row padding here on Mixtral, Scout and the shared expert, equal
-//     at 256 rows per expert);
-//   - gate_up of a single dense group (the shared expert) of at least 512 rows. Routed gate_up
-//     measured slightly faster on the 128-row kernel.
-// Everything else (down of experts with fewer rows) runs here, padding each expert to 16 rows.
+// CTA pairs take the rest of the large batches:
+//   - gate_up of a single dense group (the shared expert): 256-row tiles (gemm_tc_2sm.cu);
+//     routed gate_up measured faster on the 128-row kernel (Mixtral, gpt-oss, Scout);
+//   - down of a single dense group: 256-row tiles (gemm_tc_2sm.cu), faster than the weights-
+//     as-M pair on Scout's shared expert (0.76-0.81 ms against 0.93);
+//   - routed down: weights as the M = 256 side, tokens as N padded to 16 (gemm_tc_swap_pair.cu),
+//     measured faster than both 256-row tiles and this kernel on gpt-oss (0.52-0.53 ms against
+//     0.58 and 0.56), Mixtral (0.59-0.60 against 0.61-0.62 and 0.65) and Scout's routed
+//     experts (0.82-0.84 against 0.85-0.87 and 1.01).
+// Small batches (at most kSmallBatchRows routed rows) run here.
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
     const int groups = a.offsets ? a.E : 1;
     // training (saved accumulators) and MX layers (h rounded to MXFP8) use the 128-row kernel
     if (a.kind == kGateUp && (a.ab || a.mx_h)) return launch_grouped_gemm_bf16_rows(a, s);
-    if (a.kind == kGateUp && a.R > kSmallBatchRows) {
+    if (a.R > kSmallBatchRows) {
         if (groups == 1) return launch_grouped_gemm_bf16_2sm(a, s);
-        return launch_grouped_gemm_bf16_rows(a, s);
+        return a.kind == kGateUp ? launch_grouped_gemm_bf16_rows(a, s)
+                                 : launch_grouped_gemm_bf16_swap_pair(a, s);
     }
-    if (a.kind == kDown && a.R > kSmallBatchRows && (long long)a.R >= 512ll * groups)
-        return launch_grouped_gemm_bf16_2sm(a, s);
     return launch_grouped_gemm_bf16_swap(a, s);
 }
 

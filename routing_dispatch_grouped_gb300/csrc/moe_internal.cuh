@@ -413,7 +413,7 @@ struct GroupedGemmArgs {
 };
 // Batches with at most this many routed rows use the small-batch (decode) GEMM configuration.
 constexpr int kSmallBatchRows = 512;
-// bf16 tensor-core path; picks one of the two kernels below.
+// bf16 tensor-core path; picks one of the kernels below.
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmArgs& a, cudaStream_t s);
 // tokens as the MMA M side (128-row tiles; gemm_tc.cu)
 cudaError_t launch_grouped_gemm_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
@@ -421,6 +421,8 @@ cudaError_t launch_grouped_gemm_bf16_rows(const GroupedGemmArgs& a, cudaStream_t
 cudaError_t launch_grouped_gemm_bf16_2sm(const GroupedGemmArgs& a, cudaStream_t s);
 // weights as the MMA M side, tokens as N (tiles padded to 16 tokens; gemm_tc_swap.cu)
 cudaError_t launch_grouped_gemm_bf16_swap(const GroupedGemmArgs& a, cudaStream_t s);
+// weights as the M = 256 side on CTA pairs, up to 256 tokens as N (gemm_tc_swap_pair.cu)
+cudaError_t launch_grouped_gemm_bf16_swap_pair(const GroupedGemmArgs& a, cudaStream_t s);
 // 2D/3D bf16 tensor map with 128-byte swizzle and zero fill outside the tensor.
 bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
                             const cuuint64_t* strides, const cuuint32_t* box);

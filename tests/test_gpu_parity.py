@@ -210,6 +210,9 @@ GEMM_SHAPES = [
     ([64] * 16 + [0] * 4, 512, 768),    # many groups
     ([1000, 24], 1024, 1024),           # several M tiles and N tiles per expert
     ([700, 600], 384, 200),             # >= 512 rows per expert: down on CTA pairs, ragged K/N
+    # more than 512 rows: routed down with the weights as the M side of CTA pairs; the experts'
+    # last token tiles (5, 44, 17, 100, 250 rows) take the 8-, 32-, 16-, 64- and 128-row boxes
+    ([5, 300, 0, 17, 100, 250], 320, 256),
 ]
 
 
