@@ -507,6 +507,35 @@ def run_ours(args, rank, world):
         bwd_flops = 2.0 * (6.0 * d * I * R + 6.0 * d * Is * T)  # dgrad + wgrad of each GEMM
         pk_b, pk_b_src = peaks()
         b_tf = bwd_flops / (tb_ms * 1e-3) / 1e12
+        # the same backward with the weight gradients rounded once to bf16 (MOE_WGRAD_BF16)
+        tb16_ms = None
+        if dt == torch.bfloat16:
+            g16 = moe.moe_backward(dout, inp["x"], inp["logits"], wts["w_gate_up"],
+                                   wts["w_down"], k, ids, w, fws, cfg.score_fn,
+                                   tflags | moe.WGRAD_BF16, wts["w_shared_gate_up"],
+                                   wts["w_shared_down"], workspace=bws, stream=stream)
+
+            def train_bwd16():
+                moe.moe_backward(dout, inp["x"], inp["logits"], wts["w_gate_up"], wts["w_down"],
+                                 k, ids, w, fws, cfg.score_fn, tflags | moe.WGRAD_BF16,
+                                 wts["w_shared_gate_up"], wts["w_shared_down"], out=g16,
+                                 workspace=bws, stream=stream)
+
+            for _ in range(3):
+                train_bwd16()
+            b_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                    for _ in range(args.steps)]
+            for ev in b_ev:
+                flush_l2()
+                ev[0].record(stream)
+                train_bwd16()
+                ev[1].record(stream)
+            torch.cuda.synchronize()
+            assert moe.moe_read_device_status(bws) == 0
+            tb16_ms = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in b_ev)
+            if world > 1:
+                tb16_ms = reduce_max(tb16_ms, dev)
+            del g16
         bwd = {"backward_ms": round(tb_ms, 4), "backward_tflops": round(b_tf, 1),
                "backward_frac_of_peak": round(b_tf / pk_b["bf16_tflops"], 4)
                if dt == torch.bfloat16 else None,
@@ -516,6 +545,9 @@ def run_ours(args, rank, world):
                "train_tokens_per_s": round(T * world / ((tf_ms + tb_ms) * 1e-3), 1),
                "backward_kernels": moe.moe_backward_kernel_count(T, k, Is, tflags, True),
                "outputs": "dx, fp32 dW_gate_up/dW_down (and shared), d topk_weights, d logits",
+               "backward_bf16_wgrad_ms": None if tb16_ms is None else round(tb16_ms, 4),
+               "backward_bf16_wgrad_tflops": None if tb16_ms is None else
+               round(bwd_flops / (tb16_ms * 1e-3) / 1e12, 1),
                "time": "per-step events around each call, L2 flushed before each step"}
         del grads, bws, fws
 

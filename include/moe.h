@@ -104,7 +104,8 @@ enum {
     MOE_RENORMALIZE = 1u,          /* divide the k selected weights by their sum */
     MOE_SCALE_INPUT = 2u,          /* router weight multiplies the expert input; combine weight 1 */
     MOE_FUSE_COMBINE_WEIGHT = 4u,  /* down-projection epilogue multiplies rows by their weight */
-    MOE_WEIGHTS_PACKED = 8u        /* expert weights were repacked by moe_pack_weights */
+    MOE_WEIGHTS_PACKED = 8u,       /* expert weights were repacked by moe_pack_weights */
+    MOE_WGRAD_BF16 = 16u           /* moe_backward: weight gradients rounded once to bf16 */
 };
 
 /* Which expert weight a packed buffer holds. */
@@ -382,6 +383,15 @@ moe_status moe_gate_up_backward(const void* d_ab, const int32_t* offsets, moe_dt
 moe_status moe_weight_grad(const void* a, const void* b, const int32_t* offsets, moe_dtype dt,
                            int R, int M, int N, int E, float* dw, void* workspace,
                            size_t ws_bytes, moe_stream_t stream);
+/*
+ * moe_weight_grad_bf16 - moe_weight_grad for bf16 a and b with dw bf16 [E, M, N]: the fp32 sum
+ *   of each element rounded once to nearest even. Halves the gradient bytes written, which
+ *   bind the weight gradient when experts have few rows (each dW element is M x N output for
+ *   only R_e multiply-adds). Same arguments, alignment and errors as moe_weight_grad.
+ */
+moe_status moe_weight_grad_bf16(const void* a, const void* b, const int32_t* offsets, int R,
+                                int M, int N, int E, void* dw, void* workspace, size_t ws_bytes,
+                                moe_stream_t stream);
 
 /*
  * moe_route_backward - gradient of moe_route's weights with respect to the logits, the
@@ -426,7 +436,10 @@ moe_status moe_forward_train(const void* x, const float* logits, moe_dtype dt, i
  *   Outputs: dx dtype [T, d]; d_w_gate_up, d_w_down (and the shared d_w_shared_gate_up [d, 2Is],
  *   d_w_shared_down [Is, d]) fp32; d_topk_weights fp32 [T, k] (may be NULL); d_logits fp32
  *   [T, E] (may be NULL; needs logits). flags: MOE_RENORMALIZE | MOE_SCALE_INPUT |
- *   MOE_WEIGHTS_PACKED. workspace: moe_backward_workspace_size(...) bytes, 256-byte aligned.
+ *   MOE_WEIGHTS_PACKED | MOE_WGRAD_BF16. With MOE_WGRAD_BF16 (bf16 layers) the four weight
+ *   gradient pointers hold bf16 [same shapes] instead of fp32: each element's fp32 sum rounded
+ *   once (as for bf16 parameters whose gradients keep their dtype). workspace:
+ *   moe_backward_workspace_size(...) bytes, 256-byte aligned.
  */
 size_t moe_backward_workspace_size(int T, int d, int E, int k, int I, int Is, moe_dtype dt);
 moe_status moe_backward(const void* dout, const void* x, const float* logits, moe_dtype dt, int T,

@@ -665,10 +665,12 @@ static moe_status run_dgrad(BwdKind kind, const void* a, const void* w, bool pac
 }
 
 static moe_status run_wgrad(const void* a, const void* b, const int32_t* offsets, moe_dtype dt,
-                            int R, int M, int N, int E, float* dw, int* status, cudaStream_t s) {
+                            int R, int M, int N, int E, void* dw, bool dw_bf16, int* status,
+                            cudaStream_t s) {
     const int groups = offsets ? E : 1;
     if (R == 0)  // no rows at all: every expert's gradient is zero
-        return launch_status(cudaMemsetAsync(dw, 0, (size_t)groups * M * N * 4, s));
+        return launch_status(
+            cudaMemsetAsync(dw, 0, (size_t)groups * M * N * (dw_bf16 ? 2 : 4), s));
     WgradArgs g;
     g.a = a;
     g.b = b;
@@ -678,6 +680,7 @@ static moe_status run_wgrad(const void* a, const void* b, const int32_t* offsets
     g.N = N;
     g.E = E;
     g.dw = dw;
+    g.dw_bf16 = dw_bf16;
     g.status = status;
     return launch_status(dt == MOE_BF16 ? launch_wgrad_bf16(g, s) : launch_wgrad_f32(g, s));
 }
@@ -736,9 +739,9 @@ moe_status moe_gate_up_backward(const void* d_ab, const int32_t* offsets, moe_dt
                      s);
 }
 
-moe_status moe_weight_grad(const void* a, const void* b, const int32_t* offsets, moe_dtype dt,
-                           int R, int M, int N, int E, float* dw, void* workspace,
-                           size_t ws_bytes, moe_stream_t stream) {
+static moe_status weight_grad(const void* a, const void* b, const int32_t* offsets,
+                              moe_dtype dt, int R, int M, int N, int E, void* dw, bool dw_bf16,
+                              void* workspace, size_t ws_bytes, cudaStream_t s) {
     if (!dtype_ok(dt) || R < 0 || M < 1 || N < 1 || E < 1) return MOE_ERR_INVALID_ARG;
     if (E > kMaxE) return MOE_ERR_UNSUPPORTED;
     if (offsets == nullptr && E != 1) return MOE_ERR_INVALID_ARG;
@@ -749,10 +752,24 @@ moe_status moe_weight_grad(const void* a, const void* b, const int32_t* offsets,
         if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
     if (workspace == nullptr || !aligned256(workspace) || ws_bytes < kStatusBytes)
         return MOE_ERR_WORKSPACE;
-    cudaStream_t s = (cudaStream_t)stream;
     moe_status st = clear_status(workspace, s);
     if (st != MOE_OK) return st;
-    return run_wgrad(a, b, offsets, dt, R, M, N, E, dw, static_cast<int*>(workspace), s);
+    return run_wgrad(a, b, offsets, dt, R, M, N, E, dw, dw_bf16, static_cast<int*>(workspace),
+                     s);
+}
+
+moe_status moe_weight_grad(const void* a, const void* b, const int32_t* offsets, moe_dtype dt,
+                           int R, int M, int N, int E, float* dw, void* workspace,
+                           size_t ws_bytes, moe_stream_t stream) {
+    return weight_grad(a, b, offsets, dt, R, M, N, E, dw, false, workspace, ws_bytes,
+                       (cudaStream_t)stream);
+}
+
+moe_status moe_weight_grad_bf16(const void* a, const void* b, const int32_t* offsets, int R,
+                                int M, int N, int E, void* dw, void* workspace, size_t ws_bytes,
+                                moe_stream_t stream) {
+    return weight_grad(a, b, offsets, MOE_BF16, R, M, N, E, dw, true, workspace, ws_bytes,
+                       (cudaStream_t)stream);
 }
 
 moe_status moe_route_backward(const float* logits, const int32_t* topk_ids,
@@ -801,11 +818,13 @@ moe_status moe_backward(const void* dout, const void* x, const float* logits, mo
     if (st != MOE_OK) return st;
     if (!dtype_ok(dt)) return MOE_ERR_INVALID_ARG;
     if (score_fn != MOE_SCORE_SOFTMAX && score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
-    if (flags & ~(unsigned)(MOE_RENORMALIZE | MOE_SCALE_INPUT | MOE_WEIGHTS_PACKED))
+    if (flags & ~(unsigned)(MOE_RENORMALIZE | MOE_SCALE_INPUT | MOE_WEIGHTS_PACKED |
+                            MOE_WGRAD_BF16))
         return MOE_ERR_INVALID_ARG;
     const bool scale = (flags & MOE_SCALE_INPUT) != 0;
     const bool packed = (flags & MOE_WEIGHTS_PACKED) != 0;
-    if (packed && dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+    const bool wbf16 = (flags & MOE_WGRAD_BF16) != 0;
+    if ((packed || wbf16) && dt != MOE_BF16) return MOE_ERR_UNSUPPORTED;
     if (d < 1 || I < 1 || Is < 0) return MOE_ERR_INVALID_ARG;
     if (d % row_multiple(dt) != 0 || I % row_multiple(dt) != 0 || Is % row_multiple(dt) != 0)
         return MOE_ERR_INVALID_ARG;
@@ -859,7 +878,7 @@ moe_status moe_backward(const void* dout, const void* x, const float* logits, mo
         return st;
     PdlScope pdl(true);
     // down projection: d W_down = h^T dy; dh = dy W_down^T through the SwiGLU backward
-    if ((st = run_wgrad(h, dy, offsets, dt, R, I, d, E, d_w_down, status, s)) != MOE_OK)
+    if ((st = run_wgrad(h, dy, offsets, dt, R, I, d, E, d_w_down, wbf16, status, s)) != MOE_OK)
         return st;
     if ((st = run_dgrad(kDgradDown, dy, w_down, packed, offsets, s2p, topk_weights, scale, ab,
                         d_ab, part, dt, R, d, I, E, status, s)) != MOE_OK)
@@ -868,23 +887,23 @@ moe_status moe_backward(const void* dout, const void* x, const float* logits, mo
                                                        s))) != MOE_OK)
         return st;
     // gate/up projection: d W_gate_up = x_sorted^T d_ab; dx_sorted = d_ab W_gate_up^T
-    if ((st = run_wgrad(xs, d_ab, offsets, dt, R, d, 2 * I, E, d_w_gate_up, status, s)) !=
-        MOE_OK)
+    if ((st = run_wgrad(xs, d_ab, offsets, dt, R, d, 2 * I, E, d_w_gate_up, wbf16, status,
+                        s)) != MOE_OK)
         return st;
     if ((st = run_dgrad(kDgradGateUp, d_ab, w_gate_up, packed, offsets, nullptr, nullptr, false,
                         nullptr, dxs, nullptr, dt, R, d, I, E, status, s)) != MOE_OK)
         return st;
     if (shared) {
         // the shared expert sees the unscaled x with weight 1: its dy is dout
-        if ((st = run_wgrad(h_sh, dout, nullptr, dt, T, Is, d, 1, d_w_shared_down, status, s)) !=
-            MOE_OK)
+        if ((st = run_wgrad(h_sh, dout, nullptr, dt, T, Is, d, 1, d_w_shared_down, wbf16, status,
+                            s)) != MOE_OK)
             return st;
         if ((st = run_dgrad(kDgradDown, dout, w_shared_down, packed, nullptr, nullptr, nullptr,
                             false, ab_sh, d_ab_sh, nullptr, dt, T, d, Is, 1, status, s)) !=
             MOE_OK)
             return st;
-        if ((st = run_wgrad(x, d_ab_sh, nullptr, dt, T, d, 2 * Is, 1, d_w_shared_gate_up, status,
-                            s)) != MOE_OK)
+        if ((st = run_wgrad(x, d_ab_sh, nullptr, dt, T, d, 2 * Is, 1, d_w_shared_gate_up, wbf16,
+                            status, s)) != MOE_OK)
             return st;
         if ((st = run_dgrad(kDgradGateUp, d_ab_sh, w_shared_gate_up, packed, nullptr, nullptr,
                             nullptr, false, nullptr, dx_sh, nullptr, dt, T, d, Is, 1, status,

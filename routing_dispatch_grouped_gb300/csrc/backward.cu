@@ -306,7 +306,8 @@ __global__ void __launch_bounds__(256) simt_wgrad(WgradArgs p) {
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             const int m = m0 + ty * 2 + i, n = n0 + tx * 2 + j;
-            if (m < p.M && n < p.N) p.dw[((size_t)e * p.M + m) * p.N + n] = acc[i][j];
+            if (m < p.M && n < p.N)
+                static_cast<float*>(p.dw)[((size_t)e * p.M + m) * p.N + n] = acc[i][j];
         }
 }
 

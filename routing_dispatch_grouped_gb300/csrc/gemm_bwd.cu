@@ -47,7 +47,7 @@ struct BwdParams {
     const int32_t* sorted_to_slot;
     const float* topk_weights;
     const __nv_bfloat16* ab;   // dgrad down: saved accumulators [R, 2I]
-    void* out;                 // d_ab (bf16) / dx_sorted (fp32) / dW (fp32)
+    void* out;                 // d_ab (bf16) / dx_sorted (fp32) / dW (fp32 or bf16)
     float* scale_part;         // dgrad down with row scale: [R, n_tiles]
     int* status;
     int R, E;
@@ -59,6 +59,7 @@ struct BwdParams {
     int packed;
     int nb_w, nbh;             // packed geometry of the weight
     int ldab;                  // 2I
+    int dw_bf16;               // wgrad: dW rounded to bf16 (else fp32)
 };
 
 struct __align__(8) SmemTail {
@@ -413,8 +414,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // is rewritten only after the store issued two chunks earlier has read it.
                 const uint32_t stg = smem_u32(smem + Layout<MODE>::staging) + q * 8192;
                 const bool zero = t.kbs == 0;  // an expert without rows: zero gradient
+                if (p.dw_bf16) {
+                    // bf16 dW: 64 columns per staging tile (two TMEM loads), the same 32 rows x
+                    // 128 bytes and swizzle as the fp32 tiles
 #pragma unroll 1
-                for (int c = 0; c < 8; ++c) {
+                    for (int c = 0; c < 4; ++c) {
+                        if (t.n0 + c * 64 >= p.N) break;
+                        uint32_t v0[32], v1[32];
+                        if (!zero) {
+                            tmem_ld_32x32b_x32(tbase + c * 64, v0);
+                            tmem_ld_32x32b_x32(tbase + c * 64 + 32, v1);
+                            tmem_ld_wait();
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v0[i] = v1[i] = 0u;
+                        }
+                        const uint32_t buf = stg + (uint32_t)(n_store & 1) * 4096;
+                        if (lane == 0) bulk_wait_read<1>();
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            // chunk j: columns 8j .. 8j+7 of the 64
+                            const uint32_t* src = j < 4 ? v0 + 8 * j : v1 + 8 * (j - 4);
+                            uint32_t w[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h)
+                                w[h] = pack_bf16x2(__uint_as_float(src[2 * h]),
+                                                   __uint_as_float(src[2 * h + 1]));
+                            const uint32_t a = buf + lane * 128 + ((j ^ (lane & 7)) << 4);
+                            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a),
+                                         "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                                         : "memory");
+                        }
+                        fence_proxy_async_smem();  // generic stores -> the TMA engine's reads
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_3d(&tmO, buf, t.n0 + c * 64, t.m0 + q * 32, t.e);
+                            bulk_commit();
+                        }
+                        ++n_store;
+                    }
+                }
+#pragma unroll 1
+                for (int c = 0; c < 8 && !p.dw_bf16; ++c) {
                     if (t.n0 + c * 32 >= p.N) break;
                     uint32_t v[32];
                     if (!zero) {
@@ -652,18 +694,21 @@ cudaError_t launch_wgrad_bf16(const WgradArgs& a, cudaStream_t s) {
     const cuuint64_t b_dims[2] = {(cuuint64_t)a.N, rows};
     const cuuint64_t b_str[1] = {(cuuint64_t)a.N * 2};
     const cuuint32_t box[2] = {64, 64};
-    // dW [E, M, N] fp32, stored 32 x 32 at a time
+    // dW [E, M, N], stored 32 rows x 128 bytes at a time: 32 fp32 or 64 bf16 columns
     CUtensorMap tmO;
+    const cuuint64_t esz = a.dw_bf16 ? 2 : 4;
     const cuuint64_t o_dims[3] = {(cuuint64_t)a.N, (cuuint64_t)a.M, (cuuint64_t)groups};
-    const cuuint64_t o_str[2] = {(cuuint64_t)a.N * 4, (cuuint64_t)a.N * 4 * a.M};
-    const cuuint32_t o_box[3] = {32, 32, 1};
+    const cuuint64_t o_str[2] = {(cuuint64_t)a.N * esz, (cuuint64_t)a.N * esz * a.M};
+    const cuuint32_t o_box[3] = {a.dw_bf16 ? 64u : 32u, 32, 1};
     if (!encode_tensor_map_bf16(&tmA, a.a, 2, a_dims, a_str, box) ||
         !encode_tensor_map_bf16(&tmB, a.b, 2, b_dims, b_str, box) ||
-        !encode_tensor_map_f32(&tmO, a.dw, 3, o_dims, o_str, o_box))
+        !(a.dw_bf16 ? encode_tensor_map_bf16(&tmO, a.dw, 3, o_dims, o_str, o_box)
+                    : encode_tensor_map_f32(&tmO, a.dw, 3, o_dims, o_str, o_box)))
         return cudaErrorInvalidValue;
     BwdParams p = {};
     p.offsets = a.offsets;
     p.out = a.dw;
+    p.dw_bf16 = a.dw_bf16 ? 1 : 0;
     p.status = a.status;
     p.R = a.R;
     p.E = groups;

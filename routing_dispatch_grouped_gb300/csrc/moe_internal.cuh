@@ -500,8 +500,9 @@ struct WgradArgs {
     const void* b;
     const int32_t* offsets;   // [E + 1] or nullptr
     int R, M, N, E;
-    float* dw;
+    void* dw;                 // [E, M, N]: fp32, or bf16 when dw_bf16 (bf16 layers only)
     int* status;
+    bool dw_bf16 = false;
 };
 cudaError_t launch_wgrad_bf16(const WgradArgs& a, cudaStream_t s);
 cudaError_t launch_wgrad_f32(const WgradArgs& a, cudaStream_t s);

@@ -17,7 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmoe.so")
 
 SOFTMAX, SIGMOID = 0, 1
-RENORMALIZE, SCALE_INPUT, FUSE_COMBINE_WEIGHT, WEIGHTS_PACKED = 1, 2, 4, 8
+RENORMALIZE, SCALE_INPUT, FUSE_COMBINE_WEIGHT, WEIGHTS_PACKED, WGRAD_BF16 = 1, 2, 4, 8, 16
 W_GATE_UP, W_DOWN = 0, 1
 F32, BF16 = 0, 1
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
@@ -51,6 +51,7 @@ SIGNATURES = {
                                _P]),
     "moe_gate_up_backward": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _U, _P, _P, _S, _P]),
     "moe_weight_grad": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _S, _P]),
+    "moe_weight_grad_bf16": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _S, _P]),
     "moe_route_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _U, _P, _P]),
     "moe_forward_train_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_forward_train": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P,
@@ -461,18 +462,24 @@ def moe_gate_up_backward(d_ab, offsets, w_gate_up, dx_sorted=None, workspace=Non
     return dx
 
 
-def moe_weight_grad(a, b, offsets, E, dw=None, workspace=None, stream=None):
-    """dw[e] = a[rows of e]^T b[rows of e]: [E, M, N] fp32."""
+def moe_weight_grad(a, b, offsets, E, dw=None, workspace=None, stream=None,
+                    out_dtype=torch.float32):
+    """dw[e] = a[rows of e]^T b[rows of e]: [E, M, N] fp32, or bf16 (bf16 a, b) with
+    out_dtype=torch.bfloat16 (moe_weight_grad_bf16)."""
     _need(a, "a")
     _need(b, "b")
     R, M = a.shape
     N = b.shape[1]
     dev = a.device
-    dw = dw if dw is not None else torch.empty(E, M, N, dtype=torch.float32, device=dev)
+    dw = dw if dw is not None else torch.empty(E, M, N, dtype=out_dtype, device=dev)
     ws = workspace if workspace is not None else _workspace(moe_experts_workspace_size(), dev)
-    _check("moe_weight_grad", lib().moe_weight_grad(
-        _p(a), _p(b), _p(offsets), _dt(a), R, M, N, E, _p(dw), _p(ws), ws.numel(),
-        _stream(stream)))
+    if dw.dtype == torch.bfloat16:
+        _check("moe_weight_grad_bf16", lib().moe_weight_grad_bf16(
+            _p(a), _p(b), _p(offsets), R, M, N, E, _p(dw), _p(ws), ws.numel(), _stream(stream)))
+    else:
+        _check("moe_weight_grad", lib().moe_weight_grad(
+            _p(a), _p(b), _p(offsets), _dt(a), R, M, N, E, _p(dw), _p(ws), ws.numel(),
+            _stream(stream)))
     return dw
 
 
@@ -539,7 +546,8 @@ def moe_backward(dout, x, logits, w_gate_up, w_down, k, topk_ids, topk_weights, 
     """The whole backward pass for a moe_forward_train call with the same arguments.
     Returns a dict: dx, d_w_gate_up, d_w_down, d_topk_weights, d_logits (None unless
     want_logits) and, with a shared expert, d_w_shared_gate_up, d_w_shared_down. `out` may
-    pass preallocated tensors under those names."""
+    pass preallocated tensors under those names. flags may include WGRAD_BF16: the weight
+    gradients are then bf16."""
     _need(dout, "dout")
     T, d = dout.shape
     E, _, I, pk = _w_dims(w_gate_up, W_GATE_UP)
@@ -554,14 +562,15 @@ def moe_backward(dout, x, logits, w_gate_up, w_down, k, topk_ids, topk_weights, 
             o[name] = torch.empty(*shape, dtype=dtype, device=dev)
         return o[name]
 
+    wdt = torch.bfloat16 if flags & WGRAD_BF16 else f32
     dx = get("dx", (T, d), dout.dtype)
-    dwgu = get("d_w_gate_up", (E, d, 2 * I), f32)
-    dwd = get("d_w_down", (E, I, d), f32)
+    dwgu = get("d_w_gate_up", (E, d, 2 * I), wdt)
+    dwd = get("d_w_down", (E, I, d), wdt)
     dtw = get("d_topk_weights", (T, k), f32)
     dl = get("d_logits", (T, E), f32) if want_logits else None
     o.setdefault("d_logits", dl)
-    dsgu = get("d_w_shared_gate_up", (d, 2 * Is), f32) if Is else None
-    dsd = get("d_w_shared_down", (Is, d), f32) if Is else None
+    dsgu = get("d_w_shared_gate_up", (d, 2 * Is), wdt) if Is else None
+    dsd = get("d_w_shared_down", (Is, d), wdt) if Is else None
     ws = workspace if workspace is not None else _workspace(
         moe_backward_workspace_size(T, d, E, k, I, Is, dout.dtype), dev)
     _check("moe_backward", lib().moe_backward(

@@ -23,7 +23,7 @@ def L():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_five_steps():
@@ -209,3 +209,20 @@ def test_mx_validation_and_sizes(L):
     assert f(*bad) == 3                                                    # short workspace
     bad = list(args); bad[2] = 0
     assert f(*bad) == 0                                                    # T = 0
+
+
+def test_weight_grad_validation(L):
+    w = L.moe_weight_grad_bf16
+    ws = 0x100000
+    assert w(FAKE, FAKE, FAKE, 10, 64, 60, 4, FAKE, ws, 256, NULL) == 1     # N % 8
+    assert w(FAKE, FAKE, None, 10, 64, 64, 4, FAKE, ws, 256, NULL) == 1     # NULL offsets, E > 1
+    assert w(FAKE, FAKE, FAKE, 10, 64, 64, 4, MIS, ws, 256, NULL) == 1      # misaligned dw
+    assert w(FAKE, FAKE, FAKE, 10, 64, 64, 4, FAKE, ws, 16, NULL) == 3      # workspace
+    assert w(FAKE, FAKE, FAKE, 10, 64, 64, 300, FAKE, ws, 256, NULL) == 2   # E > 256
+    b = L.moe_backward
+    args = [FAKE, FAKE, FAKE, 1, 64, 128, 8, 2, 256, 0, 1, FAKE, FAKE, None, None, 0, FAKE, FAKE,
+            FAKE, 1 << 30, FAKE, FAKE, FAKE, None, None, FAKE, FAKE, 0x100000, 1 << 30, NULL]
+    bad = list(args); bad[3] = 0; bad[10] = 1 | 16
+    assert b(*bad) == 2                                      # bf16 weight gradients of fp32 layers
+    bad = list(args); bad[10] = 1 | 32
+    assert b(*bad) == 1                                      # unknown flag

@@ -192,6 +192,45 @@ def test_weight_grad_ragged_and_empty_experts(dtype):
         assert np.all(np.abs(got[e] - ref) <= bound + 1e-30), e
 
 
+@pytest.mark.parametrize("M,N", [(136, 264), (64, 200), (256, 512)])
+def test_weight_grad_bf16_is_the_fp32_gradient_rounded_once(M, N):
+    """moe_weight_grad_bf16 rounds the same fp32 accumulators moe_weight_grad stores: bit for bit
+    the fp32 result rounded to nearest even, with ragged and empty experts and column tails that
+    end inside a 64-column store tile (N = 200, 264)."""
+    counts = [0, 1, 63, 64, 65, 130, 0, 200]
+    off = torch.from_numpy(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)).to(DEV)
+    R = int(off[-1])
+    a = synth.normal((R, M), bf16, 0, "wgb_a", 1.0, device=DEV)
+    b = synth.normal((R, N), bf16, 0, "wgb_b", 1.0, device=DEV)
+    dw32 = moe.moe_weight_grad(a, b, off, len(counts))
+    dw16 = torch.full((len(counts), M, N), 3.0, dtype=bf16, device=DEV)  # every element written
+    moe.moe_weight_grad(a, b, off, len(counts), dw=dw16)
+    torch.cuda.synchronize()
+    assert torch.equal(dw16, dw32.to(bf16))
+    assert torch.count_nonzero(dw16[0]).item() == 0 and torch.count_nonzero(dw16[6]).item() == 0
+
+
+@pytest.mark.parametrize("idx", [0, 2, 4])
+def test_backward_bf16_weight_gradients(idx):
+    """moe_backward with WGRAD_BF16: the weight gradients are the fp32 run's rounded once, and
+    every other output is unchanged."""
+    cfg, _ = CASES[idx]
+    if cfg.dtype != bf16:
+        pytest.skip("bf16 layers only")
+    inp, dout, out, ids, w, ws, g = _run(cfg, False)
+    sgu, sdn = inp["w_shared_gate_up"], inp["w_shared_down"]
+    g16 = moe.moe_backward(dout, inp["x"], inp["logits"], inp["w_gate_up"], inp["w_down"], cfg.k,
+                           ids, w, ws, cfg.score_fn, _flags(cfg) | moe.WGRAD_BF16, sgu, sdn,
+                           want_logits=True)
+    torch.cuda.synchronize()
+    names = ["d_w_gate_up", "d_w_down"] + (["d_w_shared_gate_up", "d_w_shared_down"]
+                                           if cfg.I_shared else [])
+    for n in names:
+        assert g16[n].dtype == bf16 and torch.equal(g16[n], g[n].to(bf16)), n
+    for n in ("dx", "d_topk_weights", "d_logits"):
+        assert torch.equal(g16[n], g[n]), n
+
+
 def test_weight_grad_without_rows_writes_zeros():
     off = torch.zeros(5, dtype=torch.int32, device=DEV)
     a = torch.empty(0, 64, dtype=bf16, device=DEV)

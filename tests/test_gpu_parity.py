@@ -5,6 +5,8 @@ router weights, h, y_sorted and the layer output. Sizes span several tiles with 
 the workloads' own shapes run at reduced token counts here (the whole oracle finishes in
 seconds) and at full size in test_gpu_fullsize.py.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -335,6 +337,23 @@ def test_forward_matches_oracle(name, T):
         assert err_rms(f64(v["y_sorted"]), ref["y_sorted"]) <= tol
     e = err_rms(f64(out), ref["out"])
     assert e <= tol, e
+
+
+def test_forward_256_experts_matches_oracle():
+    """The largest expert count the ABI takes (256), top-8 over 96 tokens: 768 routed rows, so
+    the chain (not the one-kernel decode layer) runs, most experts get 1-6 rows and the down
+    projection runs on CTA pairs with one 16-token tile per expert."""
+    cfg = dataclasses.replace(synth.CONFIGS["decode"], name="e256", T=96, d=256, E=256, k=8,
+                              I=192)
+    inp = synth.make_inputs(cfg, DEV)
+    out, ids, w, ws = _run_forward(cfg, inp)
+    ref = _oracle_forward(cfg, inp)
+    assert moe.moe_read_device_status(ws) == 0
+    assert np.array_equal(ids.cpu().numpy(), ref["topk_ids"])
+    v = moe.forward_workspace_views(ws, cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.I_shared, cfg.dtype)
+    assert np.array_equal(v["offsets"].cpu().numpy(), ref["offsets"])
+    assert err_rms(f64(v["y_sorted"]), ref["y_sorted"]) <= TOL[cfg.dtype]
+    assert err_rms(f64(out), ref["out"]) <= TOL[cfg.dtype]
 
 
 def test_forward_fused_combine_weight_matches():
