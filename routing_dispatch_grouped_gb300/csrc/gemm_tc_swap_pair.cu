@@ -31,18 +31,30 @@ namespace rdg {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kStages = 6;
 constexpr int kWBlock = 64 * kTileK * 2;          // one 64-column x 64-k MN-major block: 8 KB
 constexpr int kABytes = 2 * kWBlock;              // 16 KB of weights per CTA and stage
-constexpr int kHalfTok = 128;                     // tokens per CTA at most
-constexpr int kPairTok = 2 * kHalfTok;            // tokens per pair tile at most
-constexpr int kBBytes = kHalfTok * kTileK * 2;    // 16 KB
-constexpr int kStageBytes = kABytes + kBBytes;    // 32 KB
-constexpr int kBoxes = 5;                         // token boxes of 128 >> i rows
 constexpr int kXchFloats = 32 * 64;               // one exchange buffer: 32 tokens x 64 columns
-constexpr uint32_t kAccCols = kPairTok;           // one accumulator: 256 fp32 columns
-constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// Token tile and ring depth: HALF tokens per CTA at most (a pair tile of 2 HALF), STAGES stages
+// of 16 KB of weights + HALF token rows.
+template <int HALF, int STAGES>
+struct PairCfg {
+    static constexpr int kHalfTok = HALF;
+    static constexpr int kPairTok = 2 * HALF;
+    static constexpr int kStages = STAGES;
+    static constexpr int kBBytes = HALF * kTileK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kBoxes = HALF == 128 ? 5 : 4;   // token boxes of HALF >> i rows, >= 8
+    static constexpr uint32_t kAccCols = 2 * HALF;        // one accumulator: the tile's tokens
+    static constexpr uint32_t kTmemCols = 4 * HALF;       // two accumulators (a power of 2)
+    static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte alignment");
+    static_assert((HALF >> (kBoxes - 1)) == 8, "smallest token box: one 8-row swizzle atom");
+};
+// 256-token tiles, six stages. 128-token tiles with eight 24 KB stages (more weight bytes in
+// flight, but the weights staged twice as often) measured slower: gpt-oss down 0.74 ms against
+// 0.53, Mixtral 1.01 against 0.59.
+using PairWide = PairCfg<128, 6>;
 
 // Output columns of one pair tile: 128 h columns (gate_up) or 256 y columns (down).
 template <int KIND>
@@ -64,9 +76,10 @@ struct Params {
     int nb, nbh, kpad;
 };
 
+template <int STAGES>
 struct __align__(8) SmemTail {
-    uint64_t full[kStages];   // used in the leader: both CTAs' copies complete here
-    uint64_t empty[kStages];  // in both CTAs: released by the leader's commits
+    uint64_t full[STAGES];    // used in the leader: both CTAs' copies complete here
+    uint64_t empty[STAGES];   // in both CTAs: released by the leader's commits
     uint64_t tfull[2];        // in both CTAs
     uint64_t tempty[2];       // used in the leader: 4 epilogue warps of each CTA
     uint64_t drain;
@@ -78,8 +91,11 @@ struct __align__(8) SmemTail {
     int mt[kMaxE];  // 256-token blocks of each expert
 };
 
-constexpr size_t kSmemBytes =
-    1024 + (size_t)kStages * kStageBytes + 2 * kXchFloats * 4 + sizeof(SmemTail);
+template <class C>
+constexpr size_t smem_bytes() {
+    return 1024 + (size_t)C::kStages * C::kStageBytes + 2 * kXchFloats * 4 +
+           sizeof(SmemTail<C::kStages>);
+}
 
 struct Tile {
     int e, row0, row_end, n0;
@@ -87,8 +103,8 @@ struct Tile {
 
 // Tiles run expert by expert, then weight-column block, then token block, so the pairs running
 // together share each weight block through L2.
-template <int KIND>
-__device__ __forceinline__ Tile decode(const SmemTail& st, int E, int tile) {
+template <int KIND, int PAIR_TOK, class ST>
+__device__ __forceinline__ Tile decode(const ST& st, int E, int tile) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -102,25 +118,27 @@ __device__ __forceinline__ Tile decode(const SmemTail& st, int E, int tile) {
     const int nb = local / m, mb = local - nb * m;
     Tile t;
     t.e = lo;
-    t.row0 = st.off[lo] + mb * kPairTok;
+    t.row0 = st.off[lo] + mb * PAIR_TOK;
     t.row_end = st.off[lo + 1];
     t.n0 = nb * Shape<KIND>::kCols;
     return t;
 }
 
-// The MMA's N: the tile's tokens (at most 256) rounded up to 16, so each CTA's half is a whole
-// number of 8-row swizzle atoms.
+// The MMA's N: the tile's tokens (at most a pair tile) rounded up to 16, so each CTA's half is
+// a whole number of 8-row swizzle atoms.
+template <class C>
 __device__ __forceinline__ int tile_n(const Tile& t) {
     int n = t.row_end - t.row0;
-    if (n > kPairTok) n = kPairTok;
+    if (n > C::kPairTok) n = C::kPairTok;
     if (n < 1) n = 1;
     return (n + 15) & ~15;
 }
 
-// Token box i has 128 >> i rows; the smallest that holds `half` rows.
+// Token box i has kHalfTok >> i rows; the smallest that holds `half` rows.
+template <class C>
 __device__ __forceinline__ int box_index(int half) {
     int i = 0;
-    while (i < kBoxes - 1 && (kHalfTok >> (i + 1)) >= half) ++i;
+    while (i < C::kBoxes - 1 && (C::kHalfTok >> (i + 1)) >= half) ++i;
     return i;
 }
 
@@ -140,7 +158,7 @@ __device__ __forceinline__ bool epilogue_any(bool v) {
     return r != 0;
 }
 
-template <int KIND>
+template <int KIND, class C>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm_swap_pair(const __grid_constant__ CUtensorMap tmW,
                               const __grid_constant__ CUtensorMap tmX0,
@@ -148,12 +166,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                               const __grid_constant__ CUtensorMap tmX2,
                               const __grid_constant__ CUtensorMap tmX3,
                               const __grid_constant__ CUtensorMap tmX4, const Params p) {
+    constexpr int kStages = C::kStages;
+    constexpr int kStageBytes = C::kStageBytes;
+    constexpr int kHalfTok = C::kHalfTok;
+    constexpr int kPairTok = C::kPairTok;
+    constexpr uint32_t kAccCols = C::kAccCols;
+    constexpr uint32_t kTmemCols = C::kTmemCols;
+    using ST = SmemTail<kStages>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     float* xch = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);
-    SmemTail& st =
-        *reinterpret_cast<SmemTail*>(smem + (size_t)kStages * kStageBytes + 2 * kXchFloats * 4);
+    ST& st = *reinterpret_cast<ST*>(smem + (size_t)kStages * kStageBytes + 2 * kXchFloats * 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
     const uint32_t rank = cta_rank();
@@ -235,14 +259,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             for (int tile = pair0; tile < total && ok; tile += npairs) {
-                const Tile t = decode<KIND>(st, E, tile);
-                const int half = tile_n(t) >> 1;
-                const int bi = box_index(half);
+                const Tile t = decode<KIND, kPairTok>(st, E, tile);
+                const int half = tile_n<C>(t) >> 1;
+                const int bi = box_index<C>(half);
                 const CUtensorMap* tmX = bi == 0   ? &tmX0
                                          : bi == 1 ? &tmX1
                                          : bi == 2 ? &tmX2
                                          : bi == 3 ? &tmX3
-                                                   : &tmX4;
+                                                   : &tmX4;  // (only with five boxes)
                 const uint32_t stage_bytes = kABytes + (uint32_t)(kHalfTok >> bi) * kTileK * 2;
                 const int tok0 = t.row0 + (int)rank * half;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
@@ -276,9 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0, it = 0;
             bool ok = true, issued = false;
             for (int tile = pair0; tile < total && ok; tile += npairs, ++it) {
-                const Tile t = decode<KIND>(st, E, tile);
+                const Tile t = decode<KIND, kPairTok>(st, E, tile);
                 // M = 256 across the pair, N = the tile's tokens, A MN-major, B K-major
-                const uint32_t idesc = idesc_bf16_f32_ab(2 * 128, tile_n(t), true, false);
+                const uint32_t idesc = idesc_bf16_f32_ab(2 * 128, tile_n<C>(t), true, false);
                 const uint32_t acc = it & 1u;
                 if (!mbar_wait(&st.tempty[acc], ((it >> 1) & 1u) ^ 1u, abort_flag, kWaitLimitNs)) {
                     ok = false;
@@ -329,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tempty_leader0 = mapa(smem_u32(&st.tempty[0]), 0);
         const uint32_t tempty_leader1 = mapa(smem_u32(&st.tempty[1]), 0);
         for (int tile = pair0; tile < total; tile += npairs, ++it) {
-            const Tile t = decode<KIND>(st, E, tile);
+            const Tile t = decode<KIND, kPairTok>(st, E, tile);
             const uint32_t acc = it & 1u;
             const bool ok = mbar_wait(&st.tfull[acc], (it >> 1) & 1u, abort_flag, kWaitLimitNs);
             if (!ok && lane == 0) {
@@ -413,12 +437,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc_2sm(tmem_base, kTmemCols);
 }
 
-template <int KIND>
+template <int KIND, class C>
 cudaError_t launch_swap_pair_kind(const GroupedGemmArgs& a, cudaStream_t s) {
+    constexpr size_t kSmemBytes = smem_bytes<C>();
+    constexpr int kBoxes = C::kBoxes;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_grouped_gemm_swap_pair<KIND>,
+        attr_err = cudaFuncSetAttribute(tc_grouped_gemm_swap_pair<KIND, C>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)kSmemBytes);
     });
@@ -437,14 +463,15 @@ cudaError_t launch_swap_pair_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     if (!(a.packed ? encode_tensor_map_bf16(&tmW, a.b, 3, pk_dims, pk_str, pk_box)
                    : encode_tensor_map_bf16(&tmW, a.b, 3, w_dims, w_str, w_box)))
         return cudaErrorInvalidValue;
-    CUtensorMap tmX[kBoxes];
+    CUtensorMap tmX[5];
     const cuuint64_t x_dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.R};
     const cuuint64_t x_str[1] = {(cuuint64_t)a.K * 2};
     for (int i = 0; i < kBoxes; ++i) {
-        const cuuint32_t x_box[2] = {kTileK, (cuuint32_t)(kHalfTok >> i)};
+        const cuuint32_t x_box[2] = {kTileK, (cuuint32_t)(C::kHalfTok >> i)};
         if (!encode_tensor_map_bf16(&tmX[i], a.a, 2, x_dims, x_str, x_box))
             return cudaErrorInvalidValue;
     }
+    for (int i = kBoxes; i < 5; ++i) tmX[i] = tmX[kBoxes - 1];  // not selected
 
     Params p;
     p.offsets = a.offsets;
@@ -470,12 +497,13 @@ cudaError_t launch_swap_pair_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     if (dev < 0 || dev >= 64) dev = 0;
     if (max_clusters[dev] == 0)
         max_clusters[dev] =
-            max_pair_clusters(tc_grouped_gemm_swap_pair<KIND>, kThreads, kSmemBytes);
-    const long long tiles_ub = ((long long)(a.R + kPairTok - 1) / kPairTok + groups) * p.n_tiles;
+            max_pair_clusters(tc_grouped_gemm_swap_pair<KIND, C>, kThreads, kSmemBytes);
+    const long long tiles_ub =
+        ((long long)(a.R + C::kPairTok - 1) / C::kPairTok + groups) * p.n_tiles;
     long long clusters = max_clusters[dev];
     if (tiles_ub < clusters) clusters = tiles_ub;
     if (clusters < 1) clusters = 1;
-    return launch_kernel_ex(tc_grouped_gemm_swap_pair<KIND>, dim3((unsigned)(2 * clusters)),
+    return launch_kernel_ex(tc_grouped_gemm_swap_pair<KIND, C>, dim3((unsigned)(2 * clusters)),
                             dim3(kThreads), kSmemBytes, s, 2, tmW, tmX[0], tmX[1], tmX[2], tmX[3],
                             tmX[4], p);
 }
@@ -483,8 +511,8 @@ cudaError_t launch_swap_pair_kind(const GroupedGemmArgs& a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_grouped_gemm_bf16_swap_pair(const GroupedGemmArgs& a, cudaStream_t s) {
-    return a.kind == kGateUp ? launch_swap_pair_kind<kGateUp>(a, s)
-                             : launch_swap_pair_kind<kDown>(a, s);
+    return a.kind == kGateUp ? launch_swap_pair_kind<kGateUp, PairWide>(a, s)
+                             : launch_swap_pair_kind<kDown, PairWide>(a, s);
 }
 
 }  // namespace rdg
