@@ -213,6 +213,12 @@ def host_inputs(cfg, dev_inputs):
 
 
 # ------------------------------------------------------------------------------------------------
+# source file of each grouped GEMM kernel (traffic.json is keyed by it)
+GEMM_SOURCES = {"tc_grouped_gemm": "gemm_tc.cu", "tc_grouped_gemm_2sm": "gemm_tc_2sm.cu",
+                "tc_grouped_gemm_swap": "gemm_tc_swap.cu",
+                "tc_grouped_gemm_swap_pair": "gemm_tc_swap_pair.cu"}
+
+
 def traffic_for(kernel_file: str, workload: str):
     """DRAM bytes per launch of the kernel on this workload from the committed ncu summary, if it
     was taken on the current source of the kernel (matching sha256), else None."""
@@ -608,8 +614,9 @@ def run_ours(args, rank, world):
         sh_ms = statistics.mean(per_stage["shared_gate_up"]) + statistics.mean(
             per_stage["shared_down"])
     ach = gu_flops / (gu_ms * 1e-3) / 1e12
-    traffic, _ = traffic_for("gemm_tc.cu", cfg.name)
-    roof = {"bound": "tensor", "kernel": "tc_grouped_gemm<gate_up>", "achieved": round(ach, 1),
+    gu_kernel = moe.moe_gemm_kernel_name(moe.W_GATE_UP, R, E)
+    traffic, _ = traffic_for(GEMM_SOURCES.get(gu_kernel, ""), cfg.name)
+    roof = {"bound": "tensor", "kernel": f"{gu_kernel}<gate_up>", "achieved": round(ach, 1),
             "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
             "frac": round(ach / pk["bf16_tflops"], 4), "traffic": traffic,
             "peak_source": f"{pk_src} bf16_tflops (burst)",

@@ -304,6 +304,17 @@ size_t moe_forward_workspace_size(int T, int d, int E, int k, int I, int Is, moe
  */
 int moe_forward_kernel_count(moe_dtype dt, int T, int k, int Is);
 
+/*
+ * Name of the grouped GEMM kernel moe_gate_up / moe_down (and the GEMM steps of moe_forward
+ * and moe_experts) launch for bf16 layers of these sizes: R routed rows over E experts
+ * (grouped = 0: one group without offsets, as for a shared expert). One of
+ * "tc_grouped_gemm" (128-row tiles), "tc_grouped_gemm_2sm" (256-row tiles on CTA pairs),
+ * "tc_grouped_gemm_swap" (weights as the MMA M side, small batches),
+ * "tc_grouped_gemm_swap_pair" (weights as the M side of CTA pairs); "none" for R <= 0 or an
+ * unknown kind. A static string; for diagnostics and benchmarks.
+ */
+const char* moe_gemm_kernel_name(moe_weight_kind kind, int R, int E, int grouped);
+
 /* ============================== training: backward pass ==============================
  * [EP-intro] / [EP-dispatch]: the routing weights multiply the expert outputs, so a training
  * step differentiates the layer with respect to x, the expert weights, the routing weights and,

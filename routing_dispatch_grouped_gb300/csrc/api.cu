@@ -388,6 +388,17 @@ int moe_forward_kernel_count(moe_dtype dt, int T, int k, int Is) {
     return front + 2 + (Is > 0 ? 2 : 0) + 1;
 }
 
+const char* moe_gemm_kernel_name(moe_weight_kind kind, int R, int E, int grouped) {
+    if (R <= 0 || E < 1 || (kind != MOE_W_GATE_UP && kind != MOE_W_DOWN)) return "none";
+    switch (pick_grouped_gemm_bf16(kind == MOE_W_GATE_UP ? kGateUp : kDown, R,
+                                   grouped ? E : 1, false)) {
+        case kPickRows: return "tc_grouped_gemm";
+        case kPick2sm: return "tc_grouped_gemm_2sm";
+        case kPickSwapPair: return "tc_grouped_gemm_swap_pair";
+        default: return "tc_grouped_gemm_swap";
+    }
+}
+
 // moe_forward, and with train = true moe_forward_train
 static moe_status forward_impl(const void* x, const float* logits, moe_dtype dt, int T, int d,
                                int E, int k, int I, moe_score_fn score_fn, unsigned flags,

@@ -524,8 +524,11 @@ cudaError_t launch_grouped_gemm_bf16_swap(const GroupedGemmArgs& a, cudaStream_t
 // workload). Small batches (at most kSmallBatchRows routed rows): both run here with 32-token
 // tiles, which stream weights without fetching 128- or 256-row token tiles.
 // CTA pairs take the rest of the large batches:
-//   - gate_up of a single dense group (the shared expert): 256-row tiles (gemm_tc_2sm.cu);
-//     routed gate_up measured faster on the 128-row kernel (Mixtral, gpt-oss, Scout);
+//   - gate_up of a single dense group (the shared expert), and of routed experts averaging at
+//     least 512 rows: 256-row tiles (gemm_tc_2sm.cu), measured in one process against the
+//     128-row kernel: Mixtral 1.149-1.157 ms vs 1.179, Scout 1.647 vs 1.659; at about 256 rows
+//     per expert (gpt-oss) the 256-row padding costs more (1.03 vs 0.98) and the 128-row
+//     kernel runs;
 //   - down of a single dense group: 256-row tiles (gemm_tc_2sm.cu), faster than the weights-
 //     as-M pair on Scout's shared expert (0.76-0.81 ms against 0.93);
 //   - routed down: weights as the M = 256 side, tokens as N padded to 16 (gemm_tc_swap_pair.cu),
@@ -533,16 +536,24 @@ cudaError_t launch_grouped_gemm_bf16_swap(const GroupedGemmArgs& a, cudaStream_t
 //     0.58 and 0.56), Mixtral (0.59-0.60 against 0.61-0.62 and 0.65) and Scout's routed
 //     experts (0.82-0.84 against 0.85-0.87 and 1.01).
 // Small batches (at most kSmallBatchRows routed rows) run here.
-cudaError_t launch_grouped_gemm_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
-    const int groups = a.offsets ? a.E : 1;
+GemmPick pick_grouped_gemm_bf16(GemmKind kind, int R, int groups, bool special_epilogue) {
     // training (saved accumulators) and MX layers (h rounded to MXFP8) use the 128-row kernel
-    if (a.kind == kGateUp && (a.ab || a.mx_h)) return launch_grouped_gemm_bf16_rows(a, s);
-    if (a.R > kSmallBatchRows) {
-        if (groups == 1) return launch_grouped_gemm_bf16_2sm(a, s);
-        return a.kind == kGateUp ? launch_grouped_gemm_bf16_rows(a, s)
-                                 : launch_grouped_gemm_bf16_swap_pair(a, s);
+    if (kind == kGateUp && special_epilogue) return kPickRows;
+    if (R > kSmallBatchRows) {
+        if (groups == 1) return kPick2sm;
+        if (kind == kDown) return kPickSwapPair;
+        return (long long)R >= 512ll * groups ? kPick2sm : kPickRows;
     }
-    return launch_grouped_gemm_bf16_swap(a, s);
+    return kPickSwap;
+}
+
+cudaError_t launch_grouped_gemm_bf16(const GroupedGemmArgs& a, cudaStream_t s) {
+    switch (pick_grouped_gemm_bf16(a.kind, a.R, a.offsets ? a.E : 1, a.ab || a.mx_h)) {
+        case kPickRows: return launch_grouped_gemm_bf16_rows(a, s);
+        case kPick2sm: return launch_grouped_gemm_bf16_2sm(a, s);
+        case kPickSwapPair: return launch_grouped_gemm_bf16_swap_pair(a, s);
+        default: return launch_grouped_gemm_bf16_swap(a, s);
+    }
 }
 
 }  // namespace rdg

@@ -413,8 +413,11 @@ struct GroupedGemmArgs {
 };
 // Batches with at most this many routed rows use the small-batch (decode) GEMM configuration.
 constexpr int kSmallBatchRows = 512;
-// bf16 tensor-core path; picks one of the kernels below.
+// bf16 tensor-core path; picks one of the kernels below (pick_grouped_gemm_bf16).
 cudaError_t launch_grouped_gemm_bf16(const GroupedGemmArgs& a, cudaStream_t s);
+enum GemmPick { kPickRows = 0, kPick2sm = 1, kPickSwap = 2, kPickSwapPair = 3 };
+// special_epilogue: gate_up storing the training accumulators or rounding h to MXFP8
+GemmPick pick_grouped_gemm_bf16(GemmKind kind, int R, int groups, bool special_epilogue);
 // tokens as the MMA M side (128-row tiles; gemm_tc.cu)
 cudaError_t launch_grouped_gemm_bf16_rows(const GroupedGemmArgs& a, cudaStream_t s);
 // 256-row tiles on CTA pairs with tcgen05.mma.cta_group::2 (gemm_tc_2sm.cu)

@@ -43,6 +43,7 @@ SIGNATURES = {
                          _P, _P, _S, _P]),
     "moe_forward_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_forward_kernel_count": (_I, [_I, _I, _I, _I]),
+    "moe_gemm_kernel_name": (ctypes.c_char_p, [_I, _I, _I, _I]),
     "moe_gate_up_train": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _U, _P, _P, _P, _S,
                                _P]),
     "moe_combine_backward": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P]),
@@ -302,6 +303,12 @@ def moe_forward_workspace_size(T, d, E, k, I, Is, dtype) -> int:
 
 def moe_forward_kernel_count(T, k, Is, dtype=torch.bfloat16) -> int:
     return lib().moe_forward_kernel_count(BF16 if dtype == torch.bfloat16 else F32, T, k, Is)
+
+
+def moe_gemm_kernel_name(kind, R, E, grouped=True) -> str:
+    """The grouped GEMM kernel a bf16 gate_up (kind W_GATE_UP) or down (W_DOWN) call of R rows
+    over E experts launches."""
+    return lib().moe_gemm_kernel_name(kind, R, E, 1 if grouped else 0).decode()
 
 
 def moe_forward(x, logits, w_gate_up, w_down, k, score_fn=SOFTMAX, flags=RENORMALIZE,

@@ -226,3 +226,22 @@ def test_weight_grad_validation(L):
     assert b(*bad) == 2                                      # bf16 weight gradients of fp32 layers
     bad = list(args); bad[10] = 1 | 32
     assert b(*bad) == 1                                      # unknown flag
+
+
+def test_gemm_kernel_choice(L):
+    name = moe.moe_gemm_kernel_name
+    # experts averaging >= 512 rows (Mixtral, Scout): gate_up on 256-row CTA pairs
+    assert name(moe.W_GATE_UP, 8192, 8) == "tc_grouped_gemm_2sm"
+    assert name(moe.W_GATE_UP, 16384, 16) == "tc_grouped_gemm_2sm"
+    # about 256 rows per expert (gpt-oss): 128-row tiles
+    assert name(moe.W_GATE_UP, 32768, 128) == "tc_grouped_gemm"
+    # routed down above the small-batch size: weights as the M side of CTA pairs
+    for R, E in ((8192, 8), (32768, 128), (1024, 128)):
+        assert name(moe.W_DOWN, R, E) == "tc_grouped_gemm_swap_pair"
+    # one dense group (shared expert): 256-row CTA pairs for both
+    assert name(moe.W_GATE_UP, 16384, 1, False) == "tc_grouped_gemm_2sm"
+    assert name(moe.W_DOWN, 16384, 1, False) == "tc_grouped_gemm_2sm"
+    # at most 512 routed rows (decode chain): swapped operands
+    assert name(moe.W_GATE_UP, 512, 128) == "tc_grouped_gemm_swap"
+    assert name(moe.W_DOWN, 8, 128) == "tc_grouped_gemm_swap"
+    assert name(moe.W_DOWN, 0, 8) == "none" and name(7, 100, 8) == "none"
