@@ -215,6 +215,9 @@ GEMM_SHAPES = [
     # more than 512 rows: routed down with the weights as the M side of CTA pairs; the experts'
     # last token tiles (5, 44, 17, 100, 250 rows) take the 8-, 32-, 16-, 64- and 128-row boxes
     ([5, 300, 0, 17, 100, 250], 320, 256),
+    # experts averaging >= 512 rows: gate_up on 256-row CTA pairs, with empty experts and tails
+    # that leave the second CTA of a pair without rows (90, 1700 = 6 x 256 + 164)
+    ([0, 1700, 0, 90, 900], 256, 320),
 ]
 
 
