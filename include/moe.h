@@ -297,6 +297,25 @@ moe_status moe_forward(const void* x, const float* logits, moe_dtype dt, int T, 
 size_t moe_forward_workspace_size(int T, int d, int E, int k, int I, int Is, moe_dtype dt);
 
 /*
+ * moe_forward_host - moe_forward for a caller whose activations live in host memory: x_host
+ *   (dt [T, d]) and logits_host (float [T, E]) are copied to the device, the layer runs as in
+ *   moe_forward, and the output is copied back to out_host (dt [T, d]), all enqueued on
+ *   `stream` (cudaMemcpyAsync, one per buffer; the call does not wait for them). The host
+ *   buffers should be page-locked (pinned): pageable memory works, but then the copies block
+ *   the calling thread. The router's ids and weights stay in the workspace. Weights, flags and
+ *   errors as moe_forward; workspace: moe_forward_host_workspace_size(...) bytes, 256-byte
+ *   aligned (the forward workspace followed by device copies of x, logits, out, ids and
+ *   weights).
+ */
+size_t moe_forward_host_workspace_size(int T, int d, int E, int k, int I, int Is, moe_dtype dt);
+moe_status moe_forward_host(const void* x_host, const float* logits_host, moe_dtype dt, int T,
+                            int d, int E, int k, int I, moe_score_fn score_fn, unsigned flags,
+                            const void* w_gate_up, const void* w_down,
+                            const void* w_shared_gate_up, const void* w_shared_down, int Is,
+                            void* out_host, void* workspace, size_t ws_bytes,
+                            moe_stream_t stream);
+
+/*
  * Number of kernels moe_forward enqueues for these sizes (dispatch, experts and combine
  * kernels included; the status-word clear is a memset, not counted). 0 for T == 0. Batches
  * with T*k <= 1024 route and build the dispatch indices in one fused launch; decode batches

@@ -592,6 +592,66 @@ moe_status moe_forward_train(const void* x, const float* logits, moe_dtype dt, i
                         workspace, ws_bytes, stream, true);
 }
 
+// moe_forward_host: the forward workspace, then device staging for x, logits, out, ids, weights
+struct HostLayout {
+    size_t fwd, x, logits, out, ids, w, total;
+};
+static HostLayout host_layout(int T, int d, int E, int k, int I, int Is, moe_dtype dt) {
+    HostLayout L;
+    const size_t b = dt == MOE_BF16 ? 2 : 4;
+    L.fwd = forward_layout(T, d, E, k, I, Is, dt).total;
+    size_t o = round_up(L.fwd, 256);
+    auto take = [&](size_t n) {
+        const size_t at = o;
+        o += round_up(n, 256);
+        return at;
+    };
+    L.x = take((size_t)T * d * b);
+    L.logits = take((size_t)T * E * 4);
+    L.out = take((size_t)T * d * b);
+    L.ids = take((size_t)T * k * 4);
+    L.w = take((size_t)T * k * 4);
+    L.total = o;
+    return L;
+}
+
+size_t moe_forward_host_workspace_size(int T, int d, int E, int k, int I, int Is, moe_dtype dt) {
+    if (T < 0 || d < 1 || E < 1 || k < 1 || I < 1 || Is < 0 || !dtype_ok(dt)) return 0;
+    return host_layout(T, d, E, k, I, Is, dt).total;
+}
+
+moe_status moe_forward_host(const void* x_host, const float* logits_host, moe_dtype dt, int T,
+                            int d, int E, int k, int I, moe_score_fn score_fn, unsigned flags,
+                            const void* w_gate_up, const void* w_down,
+                            const void* w_shared_gate_up, const void* w_shared_down, int Is,
+                            void* out_host, void* workspace, size_t ws_bytes,
+                            moe_stream_t stream) {
+    moe_status st = check_tek(T, E, k);
+    if (st != MOE_OK) return st;
+    if (!dtype_ok(dt) || d < 1 || I < 1 || Is < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x_host || !logits_host || !out_host) return MOE_ERR_INVALID_ARG;
+    const HostLayout L = host_layout(T, d, E, k, I, Is, dt);
+    if (!workspace || !aligned256(workspace) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t b = dt == MOE_BF16 ? 2 : 4;
+    if ((st = launch_status(cudaMemcpyAsync(ws + L.x, x_host, (size_t)T * d * b,
+                                            cudaMemcpyHostToDevice, s))) != MOE_OK)
+        return st;
+    if ((st = launch_status(cudaMemcpyAsync(ws + L.logits, logits_host, (size_t)T * E * 4,
+                                            cudaMemcpyHostToDevice, s))) != MOE_OK)
+        return st;
+    if ((st = forward_impl(ws + L.x, reinterpret_cast<const float*>(ws + L.logits), dt, T, d, E,
+                           k, I, score_fn, flags, w_gate_up, w_down, w_shared_gate_up,
+                           w_shared_down, Is, reinterpret_cast<int32_t*>(ws + L.ids),
+                           reinterpret_cast<float*>(ws + L.w), ws + L.out, workspace, L.fwd,
+                           stream, false)) != MOE_OK)
+        return st;
+    return launch_status(
+        cudaMemcpyAsync(out_host, ws + L.out, (size_t)T * d * b, cudaMemcpyDeviceToHost, s));
+}
+
 size_t moe_forward_train_workspace_size(int T, int d, int E, int k, int I, int Is,
                                         moe_dtype dt) {
     if (T < 0 || d < 1 || E < 1 || k < 1 || I < 1 || Is < 0 || !dtype_ok(dt)) return 0;

@@ -42,6 +42,9 @@ SIGNATURES = {
     "moe_forward": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P, _P,
                          _P, _P, _S, _P]),
     "moe_forward_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
+    "moe_forward_host": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P,
+                              _P, _S, _P]),
+    "moe_forward_host_workspace_size": (_S, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_forward_kernel_count": (_I, [_I, _I, _I, _I]),
     "moe_gemm_kernel_name": (ctypes.c_char_p, [_I, _I, _I, _I]),
     "moe_gate_up_train": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _U, _P, _P, _P, _S,
@@ -336,6 +339,38 @@ def moe_forward(x, logits, w_gate_up, w_down, k, score_fn=SOFTMAX, flags=RENORMA
         _p(w_shared_gate_up), _p(w_shared_down), Is, _p(ids), _p(w), _p(out), _p(ws), ws.numel(),
         _stream(stream)))
     return out, ids, w, ws
+
+
+def moe_forward_host_workspace_size(T, d, E, k, I, Is, dtype) -> int:
+    return lib().moe_forward_host_workspace_size(T, d, E, k, I, Is,
+                                                 BF16 if dtype == torch.bfloat16 else F32)
+
+
+def moe_forward_host(x_host, logits_host, w_gate_up, w_down, k, score_fn=SOFTMAX,
+                     flags=RENORMALIZE, w_shared_gate_up=None, w_shared_down=None, out=None,
+                     workspace=None, stream=None, device=None):
+    """The whole layer on host activations (CPU tensors, pinned for asynchronous copies): x and
+    logits are copied in and the output copied back by the library on `stream`. Returns
+    (out_host, workspace); synchronise the stream before reading out_host."""
+    if x_host.is_cuda or logits_host.is_cuda:
+        raise ValueError("moe_forward_host takes host tensors")
+    x_host, logits_host = x_host.contiguous(), logits_host.contiguous()
+    T, d = x_host.shape
+    E, _, I, pk = _w_dims(w_gate_up, W_GATE_UP)
+    flags |= pk
+    Is = 0
+    if w_shared_gate_up is not None:
+        Is = (w_shared_gate_up.N if isinstance(w_shared_gate_up, PackedWeights)
+              else w_shared_gate_up.shape[-1] // 2)
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    out = out if out is not None else torch.empty(T, d, dtype=x_host.dtype).pin_memory()
+    ws = workspace if workspace is not None else _workspace(
+        moe_forward_host_workspace_size(T, d, E, k, I, Is, x_host.dtype), dev)
+    _check("moe_forward_host", lib().moe_forward_host(
+        _p(x_host), _p(logits_host), _dt(x_host), T, d, E, k, I, score_fn, flags,
+        _p(w_gate_up), _p(w_down), _p(w_shared_gate_up), _p(w_shared_down), Is, _p(out), _p(ws),
+        ws.numel(), _stream(stream)))
+    return out, ws
 
 
 def moe_read_device_status(workspace, stream=None) -> int:

@@ -245,3 +245,21 @@ def test_gemm_kernel_choice(L):
     assert name(moe.W_GATE_UP, 512, 128) == "tc_grouped_gemm_swap"
     assert name(moe.W_DOWN, 8, 128) == "tc_grouped_gemm_swap"
     assert name(moe.W_DOWN, 0, 8) == "none" and name(7, 100, 8) == "none"
+
+
+def test_forward_host_validation(L):
+    f = L.moe_forward_host
+    sz = L.moe_forward_host_workspace_size(64, 128, 8, 2, 256, 0, 1)
+    assert sz > L.moe_forward_workspace_size(64, 128, 8, 2, 256, 0, 1)
+    args = [FAKE, FAKE, 1, 64, 128, 8, 2, 256, 0, 1, FAKE, FAKE, None, None, 0, FAKE, 0x100000,
+            sz, NULL]
+    bad = list(args); bad[0] = None
+    assert f(*bad) == 1                                            # no host x
+    bad = list(args); bad[15] = None
+    assert f(*bad) == 1                                            # no host out
+    bad = list(args); bad[17] = sz - 256
+    assert f(*bad) == 3                                            # short workspace
+    bad = list(args); bad[3] = 0
+    assert f(*bad) == 0                                            # T = 0: nothing enqueued
+    bad = list(args); bad[6] = 9
+    assert f(*bad) == 1                                            # k > E

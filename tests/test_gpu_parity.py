@@ -359,6 +359,27 @@ def test_forward_256_experts_matches_oracle():
     assert err_rms(f64(out), ref["out"]) <= TOL[cfg.dtype]
 
 
+@pytest.mark.parametrize("name,T", [("mixtral_8x7b", 600), ("decode", 8), ("llama4_scout", 300)])
+def test_forward_host_equals_forward(name, T):
+    """moe_forward_host (host activations, copies enqueued by the library) returns exactly what
+    moe_forward returns on the same inputs: the chain, the one-kernel decode layer and a shared
+    expert."""
+    cfg = _cfg(name, T)
+    inp = synth.make_inputs(cfg, DEV)
+    flags = (moe.RENORMALIZE if cfg.renormalize else 0) | (moe.SCALE_INPUT if cfg.scale_input
+                                                           else 0)
+    out, _, _, ws = moe.moe_forward(inp["x"], inp["logits"], inp["w_gate_up"], inp["w_down"],
+                                    cfg.k, cfg.score_fn, flags, inp["w_shared_gate_up"],
+                                    inp["w_shared_down"])
+    xh, lh = inp["x"].cpu().pin_memory(), inp["logits"].cpu().pin_memory()
+    outh, hws = moe.moe_forward_host(xh, lh, inp["w_gate_up"], inp["w_down"], cfg.k,
+                                     cfg.score_fn, flags, inp["w_shared_gate_up"],
+                                     inp["w_shared_down"])
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(hws) == 0
+    assert torch.equal(outh, out.cpu())
+
+
 def test_forward_fused_combine_weight_matches():
     cfg = _cfg("gpt_oss_120b", 300)
     inp = synth.make_inputs(cfg, DEV)
