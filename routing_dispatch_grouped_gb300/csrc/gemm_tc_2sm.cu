@@ -13,8 +13,14 @@
 //     receives its own 128 rows x all 256 columns, so the epilogue of each CTA is the 1-SM one.
 //   - A stage is 32 KB per CTA instead of 48 KB, so six stages fit in shared memory and the
 //     loads in flight cover about half as much again of MMA time.
+// gate_up tails: an expert's last tile of at most 128 rows would leave most of an M = 256 MMA
+// empty. It runs instead with the operands' roles swapped (as gemm_tc_swap_pair.cu does): the
+// weights are the M = 256 side (CTA r: the gate and up columns of h columns n0 + 64 r .. + 63,
+// in the stage's weight half) and the tail's tokens the N side (rounded up to 16, half in each
+// CTA, fetched with an 8- to 64-row box into the stage's token half); the up half of the
+// accumulator reaches the gate lanes through shared memory in the epilogue.
 // Synchronisation: both CTAs' copies complete on the leader's stage barrier (armed by the leader
-// for the 64 KB of both), the leader's commits arrive on the stage and accumulator barriers of
+// for the bytes of both), the leader's commits arrive on the stage and accumulator barriers of
 // both CTAs, and the epilogue warps of both CTAs release an accumulator on the leader's barrier.
 // Every mbarrier wait is bounded in time as in the 1-SM kernels.
 #include <mutex>
@@ -34,6 +40,9 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr int kPairRows = 2 * kTileM;            // 256 rows per pair tile
 constexpr int kBandTiles = 8;                    // row tiles per band of the tile order
+constexpr int kTailRows = 128;                   // gate_up tails of at most this many rows swap
+constexpr int kTailBoxes = 4;                    // token boxes of 64 >> i rows for swapped tails
+constexpr int kXchFloats = 32 * 64;              // one exchange buffer: 32 tokens x 64 columns
 
 struct PairParams {
     const int32_t* offsets;
@@ -48,6 +57,7 @@ struct PairParams {
     int row_scale;
     int packed, nb, nbh, kpad;
     int band_m;    // groups of at least this many row tiles run in bands (see decode_pair)
+    int swap_tails;  // gate_up: run tails of <= kTailRows rows with the weights as M
 };
 
 struct __align__(8) SmemTail {
@@ -64,15 +74,18 @@ struct __align__(8) SmemTail {
     int mt[kMaxE];  // 256-row blocks of each expert
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kStages * kStageBytes + sizeof(SmemTail);
+constexpr size_t kSmemBytes =
+    1024 + (size_t)kStages * kStageBytes + 2 * kXchFloats * 4 + sizeof(SmemTail);
 
 struct PairTile {
     int e, row0, row_end, n0;  // row0: this CTA's first row
+    int tile_row0;             // the pair tile's first row
+    int tail_n;                // > 0: a swapped tail of tail_n tokens (rounded up to 16)
 };
 
 __device__ __forceinline__ PairTile decode_pair(const SmemTail& st, int E, int n_tile,
                                                 int n_tiles, int band_m, int tile,
-                                                uint32_t rank) {
+                                                uint32_t rank, int swap_tails) {
     int lo = 0, hi = E - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -97,21 +110,49 @@ __device__ __forceinline__ PairTile decode_pair(const SmemTail& st, int E, int n
     const int nb = r / bm, mb = first_m + (r - (r / bm) * bm);
     PairTile t;
     t.e = lo;
-    t.row0 = st.off[lo] + mb * kPairRows + (int)rank * kTileM;
+    t.tile_row0 = st.off[lo] + mb * kPairRows;
+    t.row0 = t.tile_row0 + (int)rank * kTileM;
     t.row_end = st.off[lo + 1];
     t.n0 = nb * n_tile;
+    const int rows = t.row_end - t.tile_row0;
+    t.tail_n = (swap_tails && rows <= kTailRows) ? ((rows + 15) & ~15) : 0;
     return t;
 }
 
 
+// Barrier among the 128 epilogue threads (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// The same barrier, returning to every epilogue thread whether any of them passed `v` true, so
+// the four epilogue warps leave their loop together (none is left at a named barrier).
+__device__ __forceinline__ bool epilogue_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, 1, 128, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm_2sm(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const PairParams p) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmW1,
+                        const __grid_constant__ CUtensorMap tmX0,
+                        const __grid_constant__ CUtensorMap tmX1,
+                        const __grid_constant__ CUtensorMap tmX2,
+                        const __grid_constant__ CUtensorMap tmX3, const PairParams p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + (size_t)kStages * kStageBytes);
+    float* xch = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);
+    SmemTail& st = *reinterpret_cast<SmemTail*>(smem + (size_t)kStages * kStageBytes +
+                                                2 * kXchFloats * 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = p.E;
     const uint32_t rank = cta_rank();
@@ -166,21 +207,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             tma_prefetch_desc(&tmA);
             tma_prefetch_desc(&tmB);
+            if (p.swap_tails) {
+                tma_prefetch_desc(&tmW1);
+                tma_prefetch_desc(&tmX0);
+                tma_prefetch_desc(&tmX1);
+                tma_prefetch_desc(&tmX2);
+                tma_prefetch_desc(&tmX3);
+            }
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             for (int tile = pair0; tile < total && ok; tile += npairs) {
-                const PairTile t = decode_pair(st, E, p.n_tile, p.n_tiles, p.band_m, tile, rank);
+                const PairTile t =
+                    decode_pair(st, E, p.n_tile, p.n_tiles, p.band_m, tile, rank, p.swap_tails);
+                // a swapped tail: this CTA's half of the tail's tokens through the smallest of
+                // the 64/32/16/8-row boxes that holds it (both CTAs pick the same box)
+                uint32_t stage_bytes = kStageBytes;
+                const CUtensorMap* tmT = &tmX0;
+                int tok0 = 0;
+                if (t.tail_n) {
+                    const int half = t.tail_n >> 1;
+                    int bi = 0;
+                    while (bi < kTailBoxes - 1 && (64 >> (bi + 1)) >= half) ++bi;
+                    tmT = bi == 0 ? &tmX0 : bi == 1 ? &tmX1 : bi == 2 ? &tmX2 : &tmX3;
+                    stage_bytes = kBBytes + (uint32_t)(64 >> bi) * kTileK * 2;
+                    tok0 = t.tile_row0 + (int)rank * half;
+                }
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait(&st.empty[stage], phase ^ 1u, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     // the leader's stage barrier counts the bytes of both CTAs
-                    if (leader) mbar_arrive_expect_tx(&st.full[stage], 2 * kStageBytes);
+                    if (leader) mbar_arrive_expect_tx(&st.full[stage], 2 * stage_bytes);
                     const uint32_t bar = mapa(smem_u32(&st.full[stage]), 0);
                     const uint32_t a_dst = smem_u32(smem + (size_t)stage * kStageBytes);
                     const uint32_t b_dst = a_dst + kABytes;
                     const int kc = kb * kTileK;
+                    if (t.tail_n) {
+                        tma_load_2d_pair(a_dst, tmT, bar, kc, tok0);
+                        // the gate block and the up block of h columns n0 + 64 rank .. + 63
+                        if (p.packed) {
+                            const int g = t.e * p.nb + (t.n0 >> 6) + (int)rank;
+                            tma_load_3d_pair(b_dst, &tmW1, bar, 0, kc, g);
+                            tma_load_3d_pair(b_dst + kBBlockBytes, &tmW1, bar, 0, kc, g + p.nbh);
+                        } else {
+                            const int c0 = t.n0 + 64 * (int)rank;
+                            tma_load_3d_pair(b_dst, &tmB, bar, c0, kc, t.e);
+                            tma_load_3d_pair(b_dst + kBBlockBytes, &tmB, bar, p.N + c0, kc, t.e);
+                        }
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
                     tma_load_2d_pair(a_dst, &tmA, bar, kc, t.row0);
                     // this CTA's two 64-column weight blocks: gate_up = gate (rank 0) or up
                     // (rank 1) of h columns n0 .. n0+127; down = output columns
@@ -216,6 +296,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0, it = 0;
             bool ok = true, issued = false;
             for (int tile = pair0; tile < total && ok; tile += npairs, ++it) {
+                const PairTile t =
+                    decode_pair(st, E, p.n_tile, p.n_tiles, p.band_m, tile, rank, p.swap_tails);
+                // a swapped tail: M = 256 weight columns, N = the tail's tokens, A MN-major,
+                // B K-major (the same two shared-memory operands, roles exchanged). The choice
+                // is made once per tile: the issue loop below has no branch.
+                const bool tail = t.tail_n != 0;
+                const uint32_t idesc_t =
+                    tail ? idesc_bf16_f32_ab(2 * kTileM, t.tail_n, true, false) : idesc;
+                // A and B: offset of the operand in the stage, bytes per K=16 step, LBO
+                const uint32_t a_off = tail ? (uint32_t)kABytes : 0u, b_off = tail ? 0u : kABytes;
+                const uint32_t a_step = tail ? 2048u : 32u, b_step = tail ? 32u : 2048u;
+                const uint32_t a_lbo = tail ? (uint32_t)kBBlockBytes : 16u;
+                const uint32_t b_lbo = tail ? 16u : (uint32_t)kBBlockBytes;
                 const uint32_t acc = it & 1u;
                 if (!mbar_wait(&st.tempty[acc], ((it >> 1) & 1u) ^ 1u, abort_flag, kWaitLimitNs)) {
                     ok = false;
@@ -229,17 +322,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = smem_u32(smem + (size_t)stage * kStageBytes);
-                    const uint32_t b_addr = a_addr + kABytes;
+                    const uint32_t st_addr = smem_u32(smem + (size_t)stage * kStageBytes);
+                    const uint64_t adesc0 = smem_desc(st_addr + a_off, a_lbo, 1024);
+                    const uint64_t bdesc0 = smem_desc(st_addr + b_off, b_lbo, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < kTileK / 16; ++kk) {
-                        // each CTA's operands sit at these offsets of its own shared memory:
-                        // A 128 rows K-major (+32 B per K step), B 128 columns MN-major in two
-                        // 64-column blocks 8 KB apart (+2 KB per K step)
-                        const uint64_t adesc = smem_desc(a_addr + kk * 32, 16, 1024);
-                        const uint64_t bdesc = smem_desc(b_addr + kk * 2048, kBBlockBytes, 1024);
-                        umma_bf16_2sm(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < kTileK / 16; ++kk)
+                        umma_bf16_2sm(d_tmem, adesc0 + (uint64_t)((a_step >> 4) * kk),
+                                      bdesc0 + (uint64_t)((b_step >> 4) * kk), idesc_t,
+                                      (kb | kk) != 0 ? 1u : 0u);
                     issued = true;
                     umma_commit_2sm(&st.empty[stage]);
                     if (++stage == kStages) {
@@ -262,20 +352,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ================= epilogue (warps 2..5, both CTAs) =================
         const int q = warp & 3;
-        uint32_t it = 0;
+        uint32_t it = 0, xbuf = 0;
         const uint32_t tempty_leader0 = mapa(smem_u32(&st.tempty[0]), 0);
         const uint32_t tempty_leader1 = mapa(smem_u32(&st.tempty[1]), 0);
         for (int tile = pair0; tile < total; tile += npairs, ++it) {
-            const PairTile t = decode_pair(st, E, p.n_tile, p.n_tiles, p.band_m, tile, rank);
+            const PairTile t =
+                decode_pair(st, E, p.n_tile, p.n_tiles, p.band_m, tile, rank, p.swap_tails);
             const uint32_t acc = it & 1u;
-            if (!mbar_wait(&st.tfull[acc], (it >> 1) & 1u, abort_flag, kWaitLimitNs)) {
-                if (lane == 0) {
-                    st.abort = 1;
-                    set_status(p.status, MOE_ERR_TIMEOUT);
-                }
-                break;
+            const bool ok = mbar_wait(&st.tfull[acc], (it >> 1) & 1u, abort_flag, kWaitLimitNs);
+            if (!ok && lane == 0) {
+                st.abort = 1;
+                set_status(p.status, MOE_ERR_TIMEOUT);
             }
+            // the four epilogue warps leave together, so none is left at a named barrier
+            if (epilogue_any(!ok || *abort_flag != 0)) break;
             tc_fence_after();
+            if (KIND == kGateUp && t.tail_n) {
+                // swapped tail: lanes 0..63 hold the gate of h columns n0 + 64 rank .. + 63,
+                // lanes 64..127 their up; accumulator column j is the tail's token j. The up
+                // warps pass their values to the gate warps through shared memory, 32 tokens at
+                // a time (double-buffered).
+                const uint32_t tb = tmem_base + acc * kTileN + ((uint32_t)(q * 32) << 16);
+                const bool is_gate = q < 2;
+                const int hc = (q & 1) * 32 + lane;
+                const int col = t.n0 + 64 * (int)rank + hc;
+                const bool col_ok = col < p.N;
+                const int n_valid = t.row_end - t.tile_row0;
+                __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 1
+                for (int c = 0; c * 32 < n_valid; ++c, xbuf ^= 1u) {
+                    const int tok0 = t.tile_row0 + c * 32;
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(tb + c * 32, v);
+                    tmem_ld_wait();
+                    float* xb = xch + xbuf * kXchFloats;
+                    if (!is_gate) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) xb[j * 64 + hc] = __uint_as_float(v[j]);
+                    }
+                    float my_s = 1.0f;
+                    if (p.row_scale && tok0 + lane < t.row_end)
+                        my_s = __ldg(p.topk_weights + __ldg(p.sorted_to_slot + tok0 + lane));
+                    epilogue_sync();
+                    if (is_gate) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const float sj = __shfl_sync(0xFFFFFFFFu, my_s, j);
+                            const float gj = __uint_as_float(v[j]) * sj;
+                            const float uj = xb[j * 64 + hc] * sj;
+                            if (tok0 + j < t.row_end && col_ok)
+                                out[(size_t)(tok0 + j) * p.N + col] =
+                                    __float2bfloat16_rn(silu(gj) * uj);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
+                continue;
+            }
             const int row = t.row0 + q * 32 + lane;
             const bool row_ok = row < t.row_end;
             float s = 1.0f;
@@ -375,6 +510,21 @@ cudaError_t launch_pair_kind(const GroupedGemmArgs& a, cudaStream_t s) {
         !(a.packed ? encode_tensor_map_bf16(&tmB, a.b, 3, pk_dims, pk_str, pk_box)
                    : encode_tensor_map_bf16(&tmB, a.b, 3, b_dims, b_str, b_box)))
         return cudaErrorInvalidValue;
+    // swapped gate_up tails: single packed weight blocks and token boxes of 64/32/16/8 rows
+    // (down never has them: its maps stand in)
+    CUtensorMap tmW1 = tmB, tmX[kTailBoxes];
+    for (int i = 0; i < kTailBoxes; ++i) tmX[i] = tmA;
+    const bool tails = KIND == kGateUp;
+    if (tails) {
+        const cuuint32_t pk1_box[3] = {64, kTileK, 1};
+        if (a.packed && !encode_tensor_map_bf16(&tmW1, a.b, 3, pk_dims, pk_str, pk1_box))
+            return cudaErrorInvalidValue;
+        for (int i = 0; i < kTailBoxes; ++i) {
+            const cuuint32_t x_box[2] = {kTileK, (cuuint32_t)(64 >> i)};
+            if (!encode_tensor_map_bf16(&tmX[i], a.a, 2, a_dims, a_str, x_box))
+                return cudaErrorInvalidValue;
+        }
+    }
 
     PairParams p;
     p.offsets = a.offsets;
@@ -389,6 +539,7 @@ cudaError_t launch_pair_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     p.n_tile = (KIND == kGateUp) ? 128 : 256;
     p.n_tiles = (a.N + p.n_tile - 1) / p.n_tile;
     p.k_blocks = (a.K + kTileK - 1) / kTileK;
+    p.swap_tails = tails ? 1 : 0;
     p.row_scale = (KIND == kGateUp) ? (a.scale_rows ? 1 : 0) : (a.weight_rows ? 1 : 0);
     p.packed = a.packed ? 1 : 0;
     p.nb = g.nb;
@@ -415,7 +566,8 @@ cudaError_t launch_pair_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     if (pair_ub < clusters) clusters = pair_ub;
     if (clusters < 1) clusters = 1;
     return launch_kernel_ex(tc_grouped_gemm_2sm<KIND>, dim3((unsigned)(2 * clusters)),
-                            dim3(kThreads), kSmemBytes, s, 2, tmA, tmB, p);
+                            dim3(kThreads), kSmemBytes, s, 2, tmA, tmB, tmW1, tmX[0], tmX[1],
+                            tmX[2], tmX[3], p);
 }
 
 }  // namespace
