@@ -291,7 +291,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc = idesc_bf16_f32_ab(128, 256, kMN, kMN);
         uint32_t stage = 0, phase = 0, it = 0;
         bool ok = true, issued = false;
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+        if (MODE != kModeWgrad) {
+            // dgrad: nothing to fix up in shared memory, so one thread waits and issues (a
+            // warp-wide wait and shuffle per stage only lengthen the issue path)
+            if (lane == 0) {
+                for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+                    const Tile t = decode_tile<MODE>(st, p, tile);
+                    const uint32_t acc = it & 1u;
+                    if (!mbar_wait(&st.tempty[acc], ((it >> 1) & 1u) ^ 1u, abort_flag,
+                                   kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + acc * 256;
+                    for (int kb = 0; kb < t.kbs; ++kb) {
+                        if (!mbar_wait(&st.full[stage], phase, abort_flag, kWaitLimitNs)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a_addr = smem_u32(smem + (size_t)stage * kStageBytes);
+                        const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            // K-major: 128-byte rows, 8-row groups 1 KB apart, +32 B per step
+                            umma_bf16(d_tmem, smem_desc(a_addr + kk * 32, 16, 1024),
+                                      smem_desc(b_addr + kk * 32, 16, 1024), idesc,
+                                      (kb | kk) != 0 ? 1u : 0u);
+                        issued = true;
+                        umma_commit(&st.empty[stage]);
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                    }
+                    if (ok) umma_commit(&st.tfull[acc]);
+                }
+            }
+        }
+        for (int tile = blockIdx.x; MODE == kModeWgrad && tile < total && ok;
+             tile += gridDim.x, ++it) {
             const Tile t = decode_tile<MODE>(st, p, tile);
             const uint32_t acc = it & 1u;
             bool w_ok = true;
