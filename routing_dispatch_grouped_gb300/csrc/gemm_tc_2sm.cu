@@ -120,24 +120,6 @@ __device__ __forceinline__ PairTile decode_pair(const SmemTail& st, int E, int n
 }
 
 
-// Barrier among the 128 epilogue threads (id 1; id 0 is __syncthreads).
-__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// The same barrier, returning to every epilogue thread whether any of them passed `v` true, so
-// the four epilogue warps leave their loop together (none is left at a named barrier).
-__device__ __forceinline__ bool epilogue_any(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, 1, 128, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm_2sm(const __grid_constant__ CUtensorMap tmA,

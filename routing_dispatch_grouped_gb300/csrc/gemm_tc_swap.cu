@@ -129,26 +129,6 @@ __device__ __forceinline__ uint32_t idesc_swap(int n_tok) {
 }
 
 
-// Barrier among the 128 epilogue threads only (id 1; id 0 is __syncthreads).
-__device__ __forceinline__ void epilogue_sync() {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-
-// Same barrier, returning to every epilogue thread whether any of them passed `v` true, so all
-// four epilogue warps take the same branch.
-__device__ __forceinline__ bool epilogue_any(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, 1, 128, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-
 // Token box i has max(16, TOK >> i) rows; pick the smallest that holds n_tok rows.
 template <int TOK>
 __device__ __forceinline__ int token_box(int n_tok) {

@@ -142,22 +142,6 @@ __device__ __forceinline__ int box_index(int half) {
     return i;
 }
 
-__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// Barrier among the 128 epilogue threads that returns whether any of them passed `v` true.
-__device__ __forceinline__ bool epilogue_any(bool v) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred pi, po;\n\t"
-        "setp.ne.u32 pi, %1, 0;\n\t"
-        "bar.red.or.pred po, 1, 128, pi;\n\t"
-        "selp.u32 %0, 1, 0, po;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)v)
-        : "memory");
-    return r != 0;
-}
-
 template <int KIND, class C>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_gemm_swap_pair(const __grid_constant__ CUtensorMap tmW,

@@ -222,6 +222,25 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Named barrier 1 among the 128 threads of the four epilogue warps of the tcgen05 GEMMs (id 0
+// is __syncthreads; no other warp of those kernels uses id 1).
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// The same barrier, returning to every epilogue thread whether any of them passed `v` true, so
+// the four epilogue warps take the same branch (and none is left at a named barrier).
+__device__ __forceinline__ bool epilogue_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.or.pred po, 1, 128, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
 // Shared-memory matrix descriptor for tcgen05.mma (sm_100 family): start address, leading and
 // stride byte offsets (all >> 4), descriptor version 1 (bit 46), swizzle mode in bits 61-63
 // (2 = 128-byte swizzle). Tiles are 1024-byte aligned, so the base-offset field stays 0.
