@@ -504,11 +504,10 @@ cudaError_t launch_grouped_gemm_bf16_swap(const GroupedGemmArgs& a, cudaStream_t
 // workload). Small batches (at most kSmallBatchRows routed rows): both run here with 32-token
 // tiles, which stream weights without fetching 128- or 256-row token tiles.
 // CTA pairs take the rest of the large batches:
-//   - gate_up of a single dense group (the shared expert), and of routed experts averaging at
-//     least 512 rows: 256-row tiles (gemm_tc_2sm.cu), measured in one process against the
-//     128-row kernel: Mixtral 1.149-1.157 ms vs 1.179, Scout 1.647 vs 1.659; at about 256 rows
-//     per expert (gpt-oss) the 256-row padding costs more (1.03 vs 0.98) and the 128-row
-//     kernel runs;
+//   - gate_up: 256-row tiles (gemm_tc_2sm.cu), an expert's tail of at most 128 rows run with
+//     the weights as M; measured in one process against the 128-row kernel: Mixtral 1.15 ms vs
+//     1.18, Scout routed 1.65 vs 1.66-1.70, gpt-oss 0.961 vs 0.970 (before the swapped tails
+//     the 256-row padding made gpt-oss slower, 1.03 vs 0.98);
 //   - down of a single dense group: 256-row tiles (gemm_tc_2sm.cu), faster than the weights-
 //     as-M pair on Scout's shared expert (0.76-0.81 ms against 0.93);
 //   - routed down: weights as the M = 256 side, tokens as N padded to 16 (gemm_tc_swap_pair.cu),
@@ -521,8 +520,7 @@ GemmPick pick_grouped_gemm_bf16(GemmKind kind, int R, int groups, bool special_e
     if (kind == kGateUp && special_epilogue) return kPickRows;
     if (R > kSmallBatchRows) {
         if (groups == 1) return kPick2sm;
-        if (kind == kDown) return kPickSwapPair;
-        return (long long)R >= 512ll * groups ? kPick2sm : kPickRows;
+        return kind == kDown ? kPickSwapPair : kPick2sm;
     }
     return kPickSwap;
 }

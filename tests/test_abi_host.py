@@ -230,11 +230,9 @@ def test_weight_grad_validation(L):
 
 def test_gemm_kernel_choice(L):
     name = moe.moe_gemm_kernel_name
-    # experts averaging >= 512 rows (Mixtral, Scout): gate_up on 256-row CTA pairs
-    assert name(moe.W_GATE_UP, 8192, 8) == "tc_grouped_gemm_2sm"
-    assert name(moe.W_GATE_UP, 16384, 16) == "tc_grouped_gemm_2sm"
-    # about 256 rows per expert (gpt-oss): 128-row tiles
-    assert name(moe.W_GATE_UP, 32768, 128) == "tc_grouped_gemm"
+    # routed gate_up above the small-batch size: 256-row CTA pairs (tails swapped)
+    for R, E in ((8192, 8), (16384, 16), (32768, 128), (1024, 128)):
+        assert name(moe.W_GATE_UP, R, E) == "tc_grouped_gemm_2sm"
     # routed down above the small-batch size: weights as the M side of CTA pairs
     for R, E in ((8192, 8), (32768, 128), (1024, 128)):
         assert name(moe.W_DOWN, R, E) == "tc_grouped_gemm_swap_pair"
