@@ -243,6 +243,11 @@ def test_gemm_kernel_choice(L):
     assert name(moe.W_GATE_UP, 512, 128) == "tc_grouped_gemm_swap"
     assert name(moe.W_DOWN, 8, 128) == "tc_grouped_gemm_swap"
     assert name(moe.W_DOWN, 0, 8) == "none" and name(7, 100, 8) == "none"
+    # the small-batch boundary: at most 512 routed rows stay on the swapped-operand kernel
+    assert name(moe.W_GATE_UP, 512, 8) == "tc_grouped_gemm_swap"
+    assert name(moe.W_GATE_UP, 513, 8) == "tc_grouped_gemm_2sm"
+    assert name(moe.W_DOWN, 512, 8) == "tc_grouped_gemm_swap"
+    assert name(moe.W_DOWN, 513, 8) == "tc_grouped_gemm_swap_pair"
 
 
 def test_forward_host_validation(L):
