@@ -327,10 +327,12 @@ int moe_forward_kernel_count(moe_dtype dt, int T, int k, int Is);
  * Name of the grouped GEMM kernel moe_gate_up / moe_down (and the GEMM steps of moe_forward
  * and moe_experts) launch for bf16 layers of these sizes: R routed rows over E experts
  * (grouped = 0: one group without offsets, as for a shared expert). One of
- * "tc_grouped_gemm" (128-row tiles), "tc_grouped_gemm_2sm" (256-row tiles on CTA pairs),
- * "tc_grouped_gemm_swap" (weights as the MMA M side, small batches),
- * "tc_grouped_gemm_swap_pair" (weights as the M side of CTA pairs); "none" for R <= 0 or an
- * unknown kind. A static string; for diagnostics and benchmarks.
+ * "tc_grouped_gemm_2sm" (256-row tiles on CTA pairs; gate_up tails of at most 128 rows with
+ * the weights as the M side), "tc_grouped_gemm_swap" (weights as the MMA M side, at most 512
+ * rows), "tc_grouped_gemm_swap_pair" (weights as the M side of CTA pairs: routed down);
+ * "none" for R <= 0 or an unknown kind. (The training and MX forms of gate_up run the 128-row
+ * kernel "tc_grouped_gemm", whose epilogue keeps the accumulators or rounds h to MXFP8.) A
+ * static string; for diagnostics and benchmarks.
  */
 const char* moe_gemm_kernel_name(moe_weight_kind kind, int R, int E, int grouped);
 
