@@ -13,9 +13,13 @@
 // array and must be serialised by the caller.
 //
 // Host code cannot pass the array's name to a kernel (on the host it names a stand-in, not
-// device memory), so the first call on each device looks up its device address with
-// cudaGetSymbolAddress while that device is current and caches it; that first call on a device
-// should come before any stream capture.
+// device memory), so the first call in each CUDA context looks up its device address with
+// cudaGetSymbolAddress while that context is current and caches it; that first call should
+// come before any stream capture. The module, and so the array, is loaded once per context:
+// a caller that makes its own (non-primary) context current on a device gets that context's
+// copy, not the primary context's. The cache is keyed on the context's unique id (cuCtxGetId),
+// which a context created after cudaDeviceReset does not share with the one it replaces, so a
+// reset context is looked up again instead of reusing a stale address.
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -27,24 +31,89 @@ constexpr size_t kNoallocScratchInts = MOE_DISPATCH_NOALLOC_MAX_SCRATCH_INTS;
 
 static __device__ __align__(256) int32_t g_dispatch_scratch[kNoallocScratchInts];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-int32_t* g_scratch_addr[kMaxDevices] = {nullptr};
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Device address of g_dispatch_scratch on the current device (looked up once per device).
-cudaError_t scratch_on_current_device(int32_t** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+struct CtxFns {
+    CtxGetCurrentFn get_current = nullptr;
+    CtxGetIdFn get_id = nullptr;
+};
+
+// The two driver calls, resolved through the runtime (the library links no libcuda).
+const CtxFns& ctx_fns() {
+    static CtxFns f;
+    static std::once_flag once;
+    std::call_once(once, [] {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+            f.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            f.get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    return f;
+}
+
+// Unique id of the current context; 0 with *has == false when none is current yet.
+cudaError_t current_ctx_id(unsigned long long* id, bool* has) {
+    const CtxFns& f = ctx_fns();
+    if (!f.get_current || !f.get_id) return cudaErrorNotSupported;
+    CUcontext ctx = nullptr;
+    if (f.get_current(&ctx) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+    *has = ctx != nullptr;
+    *id = 0;
+    if (ctx && f.get_id(ctx, id) != CUDA_SUCCESS) return cudaErrorDeviceUninitialized;
+    return cudaSuccess;
+}
+
+constexpr int kMaxContexts = 64;
+std::mutex g_mu;
+struct CachedAddr {
+    unsigned long long ctx_id;
+    int32_t* addr;
+};
+CachedAddr g_cache[kMaxContexts];
+int g_cached = 0;
+
+// Device address of g_dispatch_scratch in the current context (looked up once per context).
+cudaError_t scratch_in_current_context(int32_t** out) {
+    unsigned long long id = 0;
+    bool has = false;
+    cudaError_t e = current_ctx_id(&id, &has);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (has)
+        for (int i = 0; i < g_cached; ++i)
+            if (g_cache[i].ctx_id == id) {
+                *out = g_cache[i].addr;
+                return cudaSuccess;
+            }
+    // not cached (or no context yet: the runtime makes the device's primary context current
+    // inside this call)
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
+    if (e != cudaSuccess) return e;
+    if (!has) {
+        e = current_ctx_id(&id, &has);
         if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = static_cast<int32_t*>(p);
+        if (!has) return cudaErrorDeviceUninitialized;
+        for (int i = 0; i < g_cached; ++i)
+            if (g_cache[i].ctx_id == id) {
+                g_cache[i].addr = static_cast<int32_t*>(p);
+                *out = g_cache[i].addr;
+                return cudaSuccess;
+            }
     }
-    *out = g_scratch_addr[dev];
+    // a full table drops its oldest entry (it is looked up again if that context comes back)
+    if (g_cached == kMaxContexts) {
+        for (int i = 1; i < kMaxContexts; ++i) g_cache[i - 1] = g_cache[i];
+        --g_cached;
+    }
+    g_cache[g_cached++] = {id, static_cast<int32_t*>(p)};
+    *out = static_cast<int32_t*>(p);
     return cudaSuccess;
 }
 
@@ -76,7 +145,7 @@ extern "C" moe_status moe_dispatch_noalloc(const int32_t* topk_ids, const void* 
     if (dispatch_scratch_bytes(T * k, E) > kNoallocScratchInts * sizeof(int32_t))
         return MOE_ERR_UNSUPPORTED;
     int32_t* scratch = nullptr;
-    if (scratch_on_current_device(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+    if (scratch_in_current_context(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
     const size_t row_bytes = (size_t)d * (dt == MOE_BF16 ? 2 : 4);
     const cudaError_t e =
         launch_dispatch(topk_ids, x, row_bytes, T, E, k, counts, offsets, sorted_to_slot,
