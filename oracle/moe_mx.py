@@ -131,16 +131,14 @@ def mx_weights(w, axis):
     return quantize_mx(np.asarray(w, dtype=np.float64), E2M1, axis=axis)
 
 
-def mx_swiglu_ffn(xq, wgu, wd, row_scale=None, h_fp32=None):
+def mx_swiglu_ffn(xq, wgu, wd, row_scale=None):
     """One expert on MXFP8 rows xq (already dequantized values) with dequantized MXFP4 weights
-    wgu [d, 2I], wd [I, d]: h = SiLU(s g) (s u) quantised to MXFP8 along I, y = h_q . wd.
-    h_fp32, when given, replaces the float64 h before quantisation (to quantise the value a
-    device computed in fp32)."""
+    wgu [d, 2I], wd [I, d]: h = SiLU(s g) (s u) quantised to MXFP8 along I, y = h_q . wd."""
     I = wgu.shape[1] // 2
     acc = xq @ wgu
     s = np.ones(len(xq)) if row_scale is None else np.asarray(row_scale, dtype=np.float64)
     g, u = s[:, None] * acc[:, :I], s[:, None] * acc[:, I:]
-    h = g / (1.0 + np.exp(-g)) * u if h_fp32 is None else np.asarray(h_fp32, dtype=np.float64)
+    h = g / (1.0 + np.exp(-g)) * u
     hq = fake_quant(h, E4M3, axis=-1)
     return hq @ wd, h, hq
 

@@ -139,13 +139,14 @@ def permute_rows(x, sorted_to_slot, k: int):
 # ----------------------------------------------------------------------------------------------
 # Step 3: per-expert gated feed-forward (gate/up projection, SwiGLU, down projection)
 # ----------------------------------------------------------------------------------------------
-def swiglu_ffn(xrows, w_gate_up, w_down, round_h: bool):
-    """y = (SiLU(x @ W_gate) * (x @ W_up)) @ W_down for a block of rows of one expert.
+def swiglu_activation(xrows, w_gate_up, round_h: bool):
+    """h = SiLU(x @ W_gate) * (x @ W_up) for a block of rows of one expert: the first half of
+    the gated feed-forward, the value the down projection reads.
 
     w_gate_up is [d, 2I] with gate = columns [0, I) and up = columns [I, 2I) (the packed
-    layout and chunk order of "Packed strategies"); w_down is [I, d]. SiLU(z) = z * sigmoid(z).
-    round_h: store the activation as bf16 (round to nearest even) before the down projection,
-    the one intermediate rounding a bf16 layer fixes.
+    layout and chunk order of "Packed strategies"). SiLU(z) = z * sigmoid(z).
+    round_h: store the activation as bf16 (round to nearest even), the one intermediate
+    rounding a bf16 layer fixes.
     """
     x = np.asarray(xrows, dtype=np.float64)
     wgu = np.asarray(w_gate_up, dtype=np.float64)
@@ -155,11 +156,23 @@ def swiglu_ffn(xrows, w_gate_up, w_down, round_h: bool):
     h = gate / (1.0 + np.exp(-gate)) * up
     if round_h:
         h = round_bf16(h)
-    return h @ np.asarray(w_down, dtype=np.float64)
+    return h
 
 
-def experts(x_sorted, offsets, w_gate_up, w_down, round_h: bool, row_scale=None):
-    """Run expert e on its rows [offsets[e], offsets[e+1]); returns y_sorted float64 [R, d].
+def swiglu_ffn(xrows, w_gate_up, w_down, round_h: bool, return_h: bool = False):
+    """y = (SiLU(x @ W_gate) * (x @ W_up)) @ W_down for a block of rows of one expert
+    (``swiglu_activation`` then the down projection; w_down is [I, d]).
+    return_h: also return the activation h, as (y, h).
+    """
+    h = swiglu_activation(xrows, w_gate_up, round_h)
+    y = h @ np.asarray(w_down, dtype=np.float64)
+    return (y, h) if return_h else y
+
+
+def experts(x_sorted, offsets, w_gate_up, w_down, round_h: bool, row_scale=None,
+            return_h: bool = False):
+    """Run expert e on its rows [offsets[e], offsets[e+1]); returns y_sorted float64 [R, d]
+    (with return_h, the pair (y_sorted, h) with h [R, I] the activation of every row).
 
     w_gate_up[e] / w_down[e] are read one expert at a time, so any indexable of per-expert
     arrays works (e.g. one that widens bf16 blocks to float64 on access).
@@ -172,11 +185,20 @@ def experts(x_sorted, offsets, w_gate_up, w_down, round_h: bool, row_scale=None)
         xs = xs * np.asarray(row_scale, dtype=np.float64)[:, None]
     R, d = xs.shape   # the layer maps hidden size d back to d
     y = np.zeros((R, d), dtype=np.float64)
+    h = None
     E = len(offsets) - 1
     for e in range(E):
         a, b = int(offsets[e]), int(offsets[e + 1])
         if b > a:  # an expert with no rows does no work (uneven or empty slices)
-            y[a:b] = swiglu_ffn(xs[a:b], w_gate_up[e], w_down[e], round_h)
+            y[a:b], he = swiglu_ffn(xs[a:b], w_gate_up[e], w_down[e], round_h, return_h=True)
+            if return_h:
+                if h is None:
+                    h = np.zeros((R, he.shape[1]), dtype=np.float64)
+                h[a:b] = he
+    if return_h:
+        if h is None:   # no rows at all: the width comes from the down projection
+            h = np.zeros((R, np.asarray(w_down[0]).shape[0]), dtype=np.float64)
+        return y, h
     return y
 
 
@@ -221,14 +243,14 @@ def forward(x, logits, w_gate_up, w_down, k: int, score_fn: int = SOFTMAX,
     counts, offsets, s2p, p2s = dispatch(ids, E)
     xs = permute_rows(x, s2p, k)
     scale = w.reshape(-1)[s2p] if scale_input else None
-    y = experts(xs, offsets, w_gate_up, w_down, round_h, row_scale=scale)
-    ys = None
+    y, h = experts(xs, offsets, w_gate_up, w_down, round_h, row_scale=scale, return_h=True)
+    ys = hs = None
     if w_shared_gate_up is not None:
-        ys = swiglu_ffn(x, w_shared_gate_up, w_shared_down, round_h)
+        ys, hs = swiglu_ffn(x, w_shared_gate_up, w_shared_down, round_h, return_h=True)
     out = combine(y, p2s, None if scale_input else w, k, ys)
     return dict(topk_ids=ids, topk_weights=w, counts=counts, offsets=offsets,
-                sorted_to_slot=s2p, slot_to_sorted=p2s, x_sorted=xs, y_sorted=y,
-                y_shared=ys, out=out)
+                sorted_to_slot=s2p, slot_to_sorted=p2s, x_sorted=xs, h=h, y_sorted=y,
+                h_shared=hs, y_shared=ys, out=out)
 
 
 def token_outputs(tokens, x, ids, weights, w_gate_up, w_down, scale_input: bool = False,

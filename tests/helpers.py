@@ -3,6 +3,8 @@ error measures the parity bar is written in, and the seeded inputs of each workl
 import numpy as np
 import torch
 
+from routing_dispatch_grouped_gb300 import moe
+
 # Parity bar. Outputs: max-abs error over the tensor <= TOL * rms(reference) (2e-2 for bf16
 # layers, 1e-4 for fp32 layers). Router weights (fp32, from fp32 logits): relative error
 # <= 2e-6, the fp32 rounding of l_j - max (<= 2^-24 |l_j - max|, |l_j - max| < 16 here) plus a few
@@ -36,6 +38,24 @@ class Expertwise:
         return self.t[e].detach().to("cpu", torch.float64).numpy()
 
 
+class HostMX:
+    """Expert weights [E, K, N] as the MX oracle's dequantized MXFP4 values (blocks of 32 along
+    K), quantised on the host from the bf16 values one expert at a time (cached)."""
+
+    def __init__(self, t: torch.Tensor):
+        self.t = t
+        self.cache = {}
+
+    def __len__(self):
+        return self.t.shape[0]
+
+    def __getitem__(self, e):
+        from oracle import moe_mx as M
+        if e not in self.cache:
+            self.cache[e] = M.fake_quant(f64(self.t[e]), M.E2M1, axis=0)
+        return self.cache[e]
+
+
 def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().to("cpu", torch.float64).numpy()
 
@@ -59,3 +79,46 @@ def bits(t: torch.Tensor) -> np.ndarray:
     if t.element_size() == 2:
         return bits16(t)
     return t.detach().contiguous().view(torch.int32).cpu().numpy()
+
+
+def mx_weight_views(mx):
+    """The stored codes unpacked to one E2M1 code per element, uint8 [E, K, cols], and the
+    E8M0 scales, uint8 [E, ceil(K / 32), cols], in the logical column order (numpy, on the
+    host; for tests)."""
+    gu = mx.kind == moe.W_GATE_UP
+    cols = 2 * mx.N if gu else mx.N
+    nbh = (mx.N + 63) // 64
+    NB = 2 * nbh if gu else nbh
+    KB = (mx.K + 31) // 32
+    raw = mx.data.cpu().numpy()
+    ncode = mx.E * NB * KB * 1024
+    cb = raw[:ncode].reshape(mx.E, NB, KB, 1024)
+    sb = raw[ncode:ncode + mx.E * NB * KB * 64].reshape(mx.E, NB, KB, 64)
+    m = np.arange(64)[:, None]
+    kk = np.arange(32)[None, :]
+    mt, r16 = m // 16, m % 16
+    hi, lq = r16 // 8, r16 % 8
+    ks, kx = kk // 16, kk % 16
+    kh, bit = kx // 8, kx % 2
+    lane = lq * 4 + (kx % 8) // 2
+    byte = (((ks * 4 + mt) * 32 + lane) * 4 + hi + 2 * kh)      # [64, 32]
+    nib = (cb[..., byte] >> (4 * bit)) & 15                      # [E, NB, KB, 64, 32]
+    # logical column of (nb, m)
+    nb = np.arange(NB)[:, None]
+    if gu:
+        up = nb >= nbh
+        c = (nb - np.where(up, nbh, 0)) * 64 + np.arange(64)[None, :]
+        col = np.where(c < mx.N, c + np.where(up, mx.N, 0), -1)
+    else:
+        c = nb * 64 + np.arange(64)[None, :]
+        col = np.where(c < mx.N, c, -1)
+    codes = np.zeros((mx.E, KB * 32, cols), dtype=np.uint8)
+    scales = np.zeros((mx.E, KB, cols), dtype=np.uint8)
+    for b in range(NB):
+        ok = col[b] >= 0
+        cs = col[b][ok]
+        # nib[:, b] is [E, KB, 64, 32] -> rows kb*32 + kk
+        blk = nib[:, b][:, :, ok, :]                               # [E, KB, n, 32]
+        codes[:, :, cs] = blk.transpose(0, 1, 3, 2).reshape(mx.E, KB * 32, len(cs))
+        scales[:, :, cs] = sb[:, b][:, :, ok]
+    return codes[:, :mx.K], scales

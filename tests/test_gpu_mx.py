@@ -13,7 +13,7 @@ import torch
 
 from oracle import moe_mx as M
 from routing_dispatch_grouped_gb300 import moe, synth
-from tests.helpers import Expertwise, err_rms, f64
+from tests.helpers import HostMX, err_rms, f64, mx_weight_views
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -47,7 +47,7 @@ def test_weight_quantisation_bit_exact(kind, E, K, N):
     mx = moe.quantize_weights_mx(w, kind)
     deq = moe.dequantize_weights_mx(mx)
     torch.cuda.synchronize()
-    got, scales = mx.views()
+    got, scales = mx_weight_views(mx)
     rc, rs = M.quantize_mx(f64(w), M.E2M1, axis=1)
     assert np.array_equal(scales, rs)
     assert np.array_equal(got, rc)
@@ -98,13 +98,15 @@ def test_mx_layer_matches_oracle(case):
                                          msgu, msdn)
     torch.cuda.synchronize()
     assert moe.moe_read_device_status(ws) == 0
-    deq_gu, deq_dn = moe.dequantize_weights_mx(mgu), moe.dequantize_weights_mx(mdn)
+    # the oracle's weights are quantised on the host from the bf16 weights, one expert at a
+    # time; the device quantiser is checked against them separately (bit for bit, below)
+    hgu, hdn = HostMX(inp["w_gate_up"]), HostMX(inp["w_down"])
     sh = {}
     if Is:
-        sh = dict(wsgu_deq=f64(moe.dequantize_weights_mx(msgu)[0]),
-                  wsd_deq=f64(moe.dequantize_weights_mx(msdn)[0]))
-    ref = M.mx_forward(f64(inp["x"]), inp["logits"].cpu().numpy(), Expertwise(deq_gu),
-                       Expertwise(deq_dn), k, fn, renorm, scale, **sh)
+        sh = dict(wsgu_deq=HostMX(inp["w_shared_gate_up"][None])[0],
+                  wsd_deq=HostMX(inp["w_shared_down"][None])[0])
+    ref = M.mx_forward(f64(inp["x"]), inp["logits"].cpu().numpy(), hgu, hdn, k, fn, renorm,
+                       scale, **sh)
     assert np.array_equal(ids.cpu().numpy(), ref["topk_ids"])
     v = moe.forward_workspace_views(ws, T, d, E, k, I, Is, bf16, mx=True)
     fused = moe.moe_forward_kernel_count(T, k, Is) == 1
@@ -124,3 +126,13 @@ def test_mx_layer_matches_oracle(case):
                   + 2.0 ** -9 * np.abs(hr).max())
     e = err_rms(f64(out), ref["out"])
     assert e <= 2e-2, e
+    # the weights the layer ran on: the device's dequantized MXFP4 values equal the host
+    # quantisation of this workload's own bf16 weights
+    pairs = [(mgu, hgu), (mdn, hdn)]
+    if Is:
+        pairs += [(msgu, HostMX(inp["w_shared_gate_up"][None])),
+                  (msdn, HostMX(inp["w_shared_down"][None]))]
+    for mx_w, host in pairs:
+        deq = moe.dequantize_weights_mx(mx_w)
+        for ex in range(len(host)):
+            assert np.array_equal(f64(deq[ex]), host[ex]), ex

@@ -218,6 +218,10 @@ GEMM_SHAPES = [
     # experts averaging >= 512 rows: gate_up on 256-row CTA pairs, with empty experts and tails
     # that leave the second CTA of a pair without rows (90, 1700 = 6 x 256 + 164)
     ([0, 1700, 0, 90, 900], 256, 320),
+    # more than 512 rows, experts ending on swapped gate_up tails: 600 = 2 x 256 + 88, exactly
+    # 128 (the largest swapped tail, through the 64-row box), 129 (one over: a half-empty pair
+    # tile), 300 = 256 + 44 and 17
+    ([600, 128, 129, 300, 17], 256, 320),
 ]
 
 
@@ -255,7 +259,7 @@ def test_grouped_gemm_matches_oracle(dtype, shape):
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-@pytest.mark.parametrize("counts", [[100, 200, 1], [900, 700], [1100]])
+@pytest.mark.parametrize("counts", [[100, 200, 1], [900, 700], [1100], [600, 128, 129, 300, 17]])
 def test_grouped_gemm_row_scale_and_weight(dtype, counts):
     d, I = 256, 256
     offsets, xs, wgu, wd = _gemm_case(counts, d, I, dtype, seed=9)

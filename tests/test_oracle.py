@@ -204,6 +204,26 @@ def test_ffn_hand_case():
         assert np.max(np.abs(y[0] - np.array(c["y"]))) <= c["tol"]
 
 
+def test_activation_hand_case():
+    """The activation alone on the same hand case: gate = [40, -50, 50], up = [5, 13, 1], so
+    h = [200, SiLU(-50) * 13 (about -2.5e-20), 50] (the fixture's derivation)."""
+    c = _golden()["ffn"]
+    x, wgu = np.array([c["x"]], float), np.array(c["w_gate_up"], float)
+    for round_h in (False, True):
+        h = o.swiglu_activation(x, wgu, round_h)
+        assert h.shape == (1, 3)
+        assert h[0, 0] == 200.0 and h[0, 2] == 50.0
+        assert -1e-18 < h[0, 1] < 0
+    # experts() hands back the same activation, row by row, for rows split over two experts
+    offsets = np.array([0, 1, 2])
+    xs = np.array([c["x"], [0.5, -1.0]], float)
+    y, h = o.experts(xs, offsets, [wgu, wgu * 0.5], [np.array(c["w_down"], float)] * 2, False,
+                     return_h=True)
+    assert np.array_equal(h[0], o.swiglu_activation(xs[:1], wgu, False)[0])
+    assert np.array_equal(h[1], o.swiglu_activation(xs[1:], wgu * 0.5, False)[0])
+    assert np.max(np.abs(y[0] - np.array(c["y"]))) <= c["tol"]
+
+
 def _dense_swiglu_loops(x, wgu, wd):
     """Textbook dense SwiGLU MLP as plain triple loops."""
     n, d = len(x), len(x[0])
