@@ -183,8 +183,11 @@ size_t moe_dispatch_workspace_size(int T, int E, int k);
  *   ceil(T*k / 256) * E > MOE_DISPATCH_NOALLOC_MAX_SCRATCH_INTS, return MOE_ERR_UNSUPPORTED
  *   before anything is enqueued; use moe_dispatch for those.
  *   No cudaMalloc, cudaFree or other allocating call is made.
- *   The first call on each device looks up the array's device address (cudaGetSymbolAddress,
- *   with that device current) and caches it; make that first call before any stream capture.
+ *   The first call in each CUDA context looks up the array's device address
+ *   (cudaGetSymbolAddress, with that context current) and caches it per context, keyed on the
+ *   context's unique id: a non-primary context on a device has its own copy of the array and
+ *   gets its own address, and a context created after cudaDeviceReset is looked up afresh.
+ *   Make the first call in a context before any stream capture.
  *   All calls share the array and it keeps the last call's contents (the kernels overwrite
  *   every entry before reading it). Calls whose kernels overlap on the GPU, e.g. on two
  *   streams, race on it: serialise them. There is no status word: an expert id outside [0, E)
@@ -549,6 +552,19 @@ moe_status moe_read_device_status(const void* workspace, moe_stream_t stream);
 
 /* Static text for a status code. */
 const char* moe_status_string(moe_status status);
+
+/*
+ * moe_debug_set_gemm_stall_ns - test hook for the bounded-wait path of the tcgen05 kernels
+ * (no counterpart on the pages: it exists to show that an expired device wait ends the kernel
+ * cleanly). From the next launch on, the 128-row gate_up kernel (the one moe_gate_up_train,
+ * moe_forward_train and the MX layer run) makes its MMA issuer first wait `ns` nanoseconds on
+ * a barrier that nothing completes. When that wait runs out the kernel takes the path of any
+ * expired wait: it records MOE_ERR_TIMEOUT in the call's status word, stops its other roles,
+ * lets its own copies land, frees its tensor memory and returns; the stream goes on and the
+ * context stays usable. Its outputs are then unspecified. 0 (the default) turns the hook off.
+ * Process-wide and read at launch: set it only while no other thread launches these kernels.
+ */
+void moe_debug_set_gemm_stall_ns(uint32_t ns);
 
 #ifdef __cplusplus
 }

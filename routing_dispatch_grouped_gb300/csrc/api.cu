@@ -2,6 +2,7 @@
 // Every check runs before anything is enqueued (Expert parallelism page, "Overriding the
 // plans": errors are raised before any work). No call allocates, frees or synchronises, except
 // moe_read_device_status, which exists to synchronise.
+#include <atomic>
 #include <mutex>
 
 #include "moe_internal.cuh"
@@ -28,9 +29,19 @@ int device_sm_count() {
     return cache[dev];
 }
 
+namespace {
+std::atomic<uint32_t> g_gemm_stall_ns{0};
+}
+
+uint32_t debug_gemm_stall_ns() { return g_gemm_stall_ns.load(std::memory_order_relaxed); }
+
 }  // namespace rdg
 
 using namespace rdg;
+
+extern "C" void moe_debug_set_gemm_stall_ns(uint32_t ns) {
+    g_gemm_stall_ns.store(ns, std::memory_order_relaxed);
+}
 
 namespace {
 

@@ -278,11 +278,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 st.abort = 1;
                 set_status(p.status, MOE_ERR_TIMEOUT);
             }
-            if (*abort_flag) {
-                // let every copy this thread started land before shared memory is released
-                for (int s = 0; s < kStages; ++s)
-                    if (armed[s]) mbar_wait(&st.full[s], armed_phase[s], nullptr, kWaitLimitNs);
-            }
+            // let every copy this thread started land before shared memory is released (after
+            // an abort elsewhere nothing else waits for them)
+            for (int s = 0; s < kStages; ++s)
+                if (armed[s]) mbar_wait(&st.full[s], armed_phase[s], nullptr, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp == 1) {

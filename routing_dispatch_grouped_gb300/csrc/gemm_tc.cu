@@ -54,6 +54,8 @@ struct TcParams {
     int nb, nbh, kpad;
     __nv_bfloat16* ab;  // gate_up for training: [g | u] before the row scale, [R, 2N]
     int mx_h;           // gate_up: round h to MXFP8 (32-column blocks) before storing it
+    uint32_t stall_ns;  // test hook: the MMA issuer first waits this long on a barrier that
+                        // nothing completes, then gives up as on an expired wait (0 = off)
 };
 
 struct __align__(8) SmemTail {
@@ -62,6 +64,7 @@ struct __align__(8) SmemTail {
     uint64_t tfull[2];
     uint64_t tempty[2];
     uint64_t drain;
+    uint64_t never;  // completed by nothing: the stall_ns test hook waits on it
     uint32_t tmem_base;
     int abort;
     int total_tiles;
@@ -123,6 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&st.tempty[a], 4);
         }
         mbar_init(&st.drain, 1);
+        mbar_init(&st.never, 1);
         st.abort = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -194,11 +198,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 st.abort = 1;
                 set_status(p.status, MOE_ERR_TIMEOUT);
             }
-            if (*abort_flag) {
-                // let every copy this thread started land before shared memory is released
-                for (int s = 0; s < kStages; ++s)
-                    if (armed[s]) mbar_wait(&st.full[s], armed_phase[s], nullptr, kWaitLimitNs);
-            }
+            // let every copy this thread started land before shared memory is released: after
+            // an abort elsewhere nothing else waits for them (on the normal path they have
+            // landed already, as the MMA issuer waited for each stage)
+            for (int s = 0; s < kStages; ++s)
+                if (armed[s]) mbar_wait(&st.full[s], armed_phase[s], nullptr, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp == 6) {
@@ -260,10 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 st.abort = 1;
                 set_status(p.status, MOE_ERR_TIMEOUT);
             }
-            if (*abort_flag) {
-                for (int s = 0; s < kStages; ++s)
-                    if (armed[s]) mbar_wait(&st.full[s], armed_phase[s], nullptr, kWaitLimitNs);
-            }
+            for (int s = 0; s < kStages; ++s)
+                if (armed[s]) mbar_wait(&st.full[s], armed_phase[s], nullptr, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -272,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, true);
             uint32_t stage = 0, phase = 0, it = 0;
             bool ok = true, issued = false;
+            if (p.stall_ns != 0 && !mbar_wait(&st.never, 0, nullptr, p.stall_ns)) ok = false;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
                 const uint32_t acc = it & 1u;
                 if (!mbar_wait(&st.tempty[acc], ((it >> 1) & 1u) ^ 1u, abort_flag, kWaitLimitNs)) {
@@ -540,6 +543,7 @@ cudaError_t launch_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     p.kpad = g.kpad;
     p.ab = static_cast<__nv_bfloat16*>(a.ab);
     p.mx_h = a.mx_h ? 1 : 0;
+    p.stall_ns = debug_gemm_stall_ns();
 
     // upper bound on tiles: sum_e ceil(n_e / 128) <= R / 128 + groups
     const long long m_ub = (long long)(a.R + kTileM - 1) / kTileM + groups;

@@ -198,6 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             uint32_t stage = 0, phase = 0;
             bool ok = true;
+            uint32_t armed_mask = 0, armed_par = 0;  // leader: stages armed, their phase
             for (int tile = pair0; tile < total && ok; tile += npairs) {
                 const PairTile t =
                     decode_pair(st, E, p.n_tile, p.n_tiles, p.band_m, tile, rank, p.swap_tails);
@@ -220,7 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     // the leader's stage barrier counts the bytes of both CTAs
-                    if (leader) mbar_arrive_expect_tx(&st.full[stage], 2 * stage_bytes);
+                    if (leader) {
+                        mbar_arrive_expect_tx(&st.full[stage], 2 * stage_bytes);
+                        armed_mask |= 1u << stage;
+                        armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+                    }
                     const uint32_t bar = mapa(smem_u32(&st.full[stage]), 0);
                     const uint32_t a_dst = smem_u32(smem + (size_t)stage * kStageBytes);
                     const uint32_t b_dst = a_dst + kABytes;
@@ -268,6 +273,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 st.abort = 1;
                 set_status(p.status, MOE_ERR_TIMEOUT);
             }
+            // the leader's stage barriers count both CTAs' copies: let every armed stage land
+            // before shared memory is released (after an abort nothing else waits for them;
+            // on the normal path they have landed already)
+            if (leader)
+                for (int s = 0; s < kStages; ++s)
+                    if ((armed_mask >> s) & 1u)
+                        mbar_wait(&st.full[s], (armed_par >> s) & 1u, nullptr, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp == 1) {

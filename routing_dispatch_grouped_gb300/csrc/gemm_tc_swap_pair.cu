@@ -222,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tmX4);
             uint32_t stage = 0, phase = 0;
             bool ok = true;
+            uint32_t armed_mask = 0, armed_par = 0;  // leader: stages armed, their phase
             // this CTA's weight blocks at (tile, kb): coordinates of their copies
             auto weight_blocks = [&](const Tile& t, int kc, auto&& op) {
                 if (p.packed) {
@@ -259,7 +260,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     // the leader's stage barrier counts the bytes of both CTAs (same boxes)
-                    if (leader) mbar_arrive_expect_tx(&st.full[stage], 2 * stage_bytes);
+                    if (leader) {
+                        mbar_arrive_expect_tx(&st.full[stage], 2 * stage_bytes);
+                        armed_mask |= 1u << stage;
+                        armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+                    }
                     const uint32_t bar = mapa(smem_u32(&st.full[stage]), 0);
                     const uint32_t a_dst = smem_u32(smem + (size_t)stage * kStageBytes);
                     weight_blocks(t, kb * kTileK, [&](int j, int c0, int c1, int c2) {
@@ -276,6 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 st.abort = 1;
                 set_status(p.status, MOE_ERR_TIMEOUT);
             }
+            // the leader's stage barriers count both CTAs' copies: let every armed stage land
+            // before shared memory is released (after an abort nothing else waits for them;
+            // on the normal path they have landed already)
+            if (leader)
+                for (int s = 0; s < kStages; ++s)
+                    if ((armed_mask >> s) & 1u)
+                        mbar_wait(&st.full[s], (armed_par >> s) & 1u, nullptr, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp == 1) {

@@ -454,6 +454,8 @@ bool encode_tensor_map_f32(CUtensorMap* m, const void* base, int rank, const cuu
 cudaError_t launch_grouped_gemm_f32(const GroupedGemmArgs& a, cudaStream_t s);
 
 int device_sm_count();
+// Stall of the 128-row gate_up kernel's test hook (moe_debug_set_gemm_stall_ns; 0 = off).
+uint32_t debug_gemm_stall_ns();
 
 // ---------------------------------------------------------------------------------------------
 // MX formats (mx.cu): MXFP4 expert weights, MXFP8 activations

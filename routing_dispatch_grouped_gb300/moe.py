@@ -73,6 +73,7 @@ SIGNATURES = {
                             _P, _S, _P]),
     "moe_read_device_status": (_I, [_P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
+    "moe_debug_set_gemm_stall_ns": (None, [ctypes.c_uint32]),
 }
 
 _lib = None
@@ -687,48 +688,6 @@ class MxWeights:
     def data_ptr(self):
         return self.data.data_ptr()
 
-    def views(self):
-        """The stored codes unpacked to one E2M1 code per element, uint8 [E, K, cols], and the
-        E8M0 scales, uint8 [E, ceil(K / 32), cols], in the logical column order (numpy, on the
-        host; for tests)."""
-        import numpy as np
-        gu = self.kind == W_GATE_UP
-        cols = 2 * self.N if gu else self.N
-        nbh = (self.N + 63) // 64
-        NB = 2 * nbh if gu else nbh
-        KB = (self.K + 31) // 32
-        raw = self.data.cpu().numpy()
-        ncode = self.E * NB * KB * 1024
-        cb = raw[:ncode].reshape(self.E, NB, KB, 1024)
-        sb = raw[ncode:ncode + self.E * NB * KB * 64].reshape(self.E, NB, KB, 64)
-        m = np.arange(64)[:, None]
-        kk = np.arange(32)[None, :]
-        mt, r16 = m // 16, m % 16
-        hi, lq = r16 // 8, r16 % 8
-        ks, kx = kk // 16, kk % 16
-        kh, bit = kx // 8, kx % 2
-        lane = lq * 4 + (kx % 8) // 2
-        byte = (((ks * 4 + mt) * 32 + lane) * 4 + hi + 2 * kh)      # [64, 32]
-        nib = (cb[..., byte] >> (4 * bit)) & 15                      # [E, NB, KB, 64, 32]
-        # logical column of (nb, m)
-        nb = np.arange(NB)[:, None]
-        if gu:
-            up = nb >= nbh
-            c = (nb - np.where(up, nbh, 0)) * 64 + np.arange(64)[None, :]
-            col = np.where(c < self.N, c + np.where(up, self.N, 0), -1)
-        else:
-            c = nb * 64 + np.arange(64)[None, :]
-            col = np.where(c < self.N, c, -1)
-        codes = np.zeros((self.E, KB * 32, cols), dtype=np.uint8)
-        scales = np.zeros((self.E, KB, cols), dtype=np.uint8)
-        for b in range(NB):
-            ok = col[b] >= 0
-            cs = col[b][ok]
-            # nib[:, b] is [E, KB, 64, 32] -> rows kb*32 + kk
-            blk = nib[:, b][:, :, ok, :]                               # [E, KB, n, 32]
-            codes[:, :, cs] = blk.transpose(0, 1, 3, 2).reshape(self.E, KB * 32, len(cs))
-            scales[:, :, cs] = sb[:, b][:, :, ok]
-        return codes[:, :self.K], scales
 
 def quantize_weights_mx(w: torch.Tensor, kind: int, stream=None) -> MxWeights:
     """bf16 gate_up ([E, d, 2I] or [d, 2I]) or down ([E, I, d] or [I, d]) weights to MXFP4."""
