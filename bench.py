@@ -4,7 +4,13 @@ A step is one pass of the whole layer over one batch: route, dispatch, gate_up G
 down GEMM (and the shared expert's two GEMMs when the workload has one), combine - the same
 C-ABI calls moe_forward makes, issued one by one so CUDA events between them time each kernel
 family on the stream it runs on. Inputs are seeded synthetic tensors resident in HBM before the
-timed region; the weights alone (GBs) exceed the 129 MB L2, so no flush is inserted.
+timed region; a 256 MB write (twice the L2) precedes every timed step, outside its events, so
+no step finds the previous step's weights or activations in L2.
+
+The headline line is the Mixtral-shaped layer (the default --config); `per_config` adds, from
+the same run, every other workload: gpt-oss-shaped, Llama-4-Scout-shaped with its shared expert,
+the decode batches T = 1, 8 and 64 (µs per layer against HBM bandwidth) and the tiny fp32 layer,
+each with its stage times, the roofline of its dominant kernel and its own CPU-oracle sample.
 
 e2e: the same metric through moe_forward with host buffers: every step copies x and the logits
 from pinned host memory, runs the layer, and copies the output back.
@@ -48,6 +54,8 @@ def parse():
                     help="override the expert count (smaller cases for profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-sample", type=int, default=None, help="tokens in the CPU sample")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time the selected workload only (no per_config object)")
     return ap.parse_args()
 
 
@@ -252,6 +260,339 @@ def shard_tokens(T: int, rank: int, world: int):
     return a, min(T, a + per)
 
 
+def decode_name(T):
+    return f"decode_T{T}"
+
+
+def workload_config(name, T=None, E=None):
+    """The synth workload of a bench name (decode_T<n> = the decode shape at T = n)."""
+    from routing_dispatch_grouped_gb300 import synth
+    if name.startswith("decode_T"):
+        T = int(name[len("decode_T"):]) if T is None else T
+        name = "decode"
+    cfg = synth.CONFIGS[name]
+    if T is not None:
+        cfg = cfg.with_T(T)
+    if E is not None:
+        cfg = dataclasses.replace(cfg, E=E, name=f"{cfg.name}@E{E}")
+    return cfg
+
+
+def fp32_alu_peak_tflops(sm_max_mhz):
+    """FP32 FMA peak of the GPU: 152 SMs x 128 FP32 lanes x 2 FLOP per FMA x the maximum SM
+    clock (the tiny fp32 layer runs on the FP32 pipes)."""
+    return 152 * 128 * 2 * sm_max_mhz * 1e6 / 1e12
+
+
+class Layer:
+    """One workload on the device: inputs, packed weights, workspaces and the timed forms."""
+
+    def __init__(self, cfg, dev, steps, warmup, world):
+        import torch
+
+        from routing_dispatch_grouped_gb300 import moe, synth
+        self.cfg, self.dev, self.steps, self.warmup, self.world = cfg, dev, steps, warmup, world
+        self.moe = moe
+        self.inp = synth.make_inputs(cfg, dev)
+        T, d, E, k, I, Is = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.I_shared
+        # expert weights are repacked once, as at model load (moe_pack_weights); bf16 layers
+        self.packed = cfg.dtype == torch.bfloat16
+        self.wts = {}
+        for n_ in ("w_gate_up", "w_down", "w_shared_gate_up", "w_shared_down"):
+            w_ = self.inp[n_]
+            if w_ is not None and self.packed:
+                w_ = moe.pack_weights(w_, moe.W_GATE_UP if "gate_up" in n_ else moe.W_DOWN)
+            self.wts[n_] = w_
+        torch.cuda.synchronize()
+        self.flags = (moe.RENORMALIZE if cfg.renormalize else 0) | (
+            moe.SCALE_INPUT if cfg.scale_input else 0)
+        dt = cfg.dtype
+        self.stream = torch.cuda.current_stream(dev)
+        self.ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+        self.w = torch.empty(T, k, dtype=torch.float32, device=dev)
+        self.out = torch.empty(T, d, dtype=dt, device=dev)
+        self.ws = torch.empty(moe.moe_forward_workspace_size(T, d, E, k, I, Is, dt),
+                              dtype=torch.uint8, device=dev)
+        self.v = moe.forward_workspace_views(self.ws, T, d, E, k, I, Is, dt)
+        self.dws = torch.empty(moe.moe_dispatch_workspace_size(T, E, k), dtype=torch.uint8,
+                               device=dev)
+        self.gws = torch.empty(256, dtype=torch.uint8, device=dev)
+        # between timed steps: write a buffer twice the L2 size so no step finds the previous
+        # step's weights or activations cached (decode touches less than the L2 holds)
+        self.l2_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.stages = ["route", "dispatch", "gate_up", "down"] + (
+            ["shared_gate_up", "shared_down"] if Is else []) + ["combine"]
+
+    def flush_l2(self):
+        self.l2_buf.fill_(1)
+
+    def events(self, n):
+        import torch
+        return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def step(self, ev=None):
+        """The layer as its separate C-ABI calls, with an event after each."""
+        moe, cfg, inp, v, wts, st = self.moe, self.cfg, self.inp, self.v, self.wts, self.stream
+
+        def mark(i):
+            if ev is not None:
+                ev[i].record(st)
+        k, E, Is = cfg.k, cfg.E, cfg.I_shared
+        mark(0)
+        moe.moe_route(inp["logits"], k, cfg.score_fn, cfg.renormalize, self.ids, self.w, st)
+        mark(1)
+        disp = {n: v[n] for n in ("counts", "offsets", "sorted_to_slot", "slot_to_sorted",
+                                  "x_sorted")}
+        moe.moe_dispatch(self.ids, E, x=inp["x"], workspace=self.dws, out=disp, stream=st)
+        mark(2)
+        moe.moe_gate_up(v["x_sorted"], v["offsets"], wts["w_gate_up"], v["sorted_to_slot"],
+                        self.w, cfg.scale_input, h=v["h"], workspace=self.gws, stream=st)
+        mark(3)
+        moe.moe_down(v["h"], v["offsets"], wts["w_down"], y_sorted=v["y_sorted"],
+                     workspace=self.gws, stream=st)
+        mark(4)
+        i = 5
+        if Is:
+            sgu, sdn = wts["w_shared_gate_up"], wts["w_shared_down"]
+            moe.moe_gate_up(inp["x"], None, sgu if self.packed else sgu.unsqueeze(0),
+                            h=v["h_shared"], workspace=self.gws, stream=st)
+            mark(i)
+            moe.moe_down(v["h_shared"], None, sdn if self.packed else sdn.unsqueeze(0),
+                         y_sorted=v["y_shared"], workspace=self.gws, stream=st)
+            mark(i + 1)
+            i += 2
+        moe.moe_combine(v["y_sorted"], v["slot_to_sorted"], k, cfg.dtype,
+                        topk_weights=None if cfg.scale_input else self.w,
+                        y_shared=v["y_shared"] if Is else None, out=self.out, stream=st)
+        mark(i)
+
+    def fwd(self, st_):
+        cfg, wts = self.cfg, self.wts
+        self.moe.moe_forward(self.inp["x"], self.inp["logits"], wts["w_gate_up"], wts["w_down"],
+                             cfg.k, cfg.score_fn, self.flags, wts["w_shared_gate_up"],
+                             wts["w_shared_down"], out=self.out, topk_ids=self.ids,
+                             topk_weights=self.w, workspace=self.ws, stream=st_)
+
+    def timed(self, fn):
+        """Mean ms of fn() over the timed steps, each between its own events, L2 flushed
+        before each (max over ranks)."""
+        import torch
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        self.barrier()
+        evs = [self.events(2) for _ in range(self.steps)]
+        for a_, b_ in evs:
+            self.flush_l2()
+            a_.record(self.stream)
+            fn()
+            b_.record(self.stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)
+        return reduce_max(ms, self.dev) if self.world > 1 else ms
+
+    def run_staged(self):
+        import torch
+        moe = self.moe
+        for _ in range(max(self.warmup, 3)):
+            self.step()
+        torch.cuda.synchronize()
+        assert moe.moe_read_device_status(self.gws) == 0
+        assert moe.moe_read_device_status(self.dws) == 0
+        nev = len(self.stages) + 1
+        events = [self.events(nev) for _ in range(self.steps)]
+        self.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(self.dev.index) as clocks:
+            for s_ in range(self.steps):
+                self.flush_l2()
+                self.step(events[s_])
+            torch.cuda.synchronize()
+        self.barrier()
+        per_stage = {name: [] for name in self.stages}
+        step_ms = []
+        for ev in events:
+            for i, name in enumerate(self.stages):
+                per_stage[name].append(ev[i].elapsed_time(ev[i + 1]))
+            step_ms.append(ev[0].elapsed_time(ev[-1]))
+        self.per_stage = per_stage
+        self.staged_ms = statistics.mean(step_ms)
+        if self.world > 1:
+            self.staged_ms = reduce_max(self.staged_ms, self.dev)
+        self.staged_clocks = clocks.summary()
+
+    def run_graph(self):
+        """moe_forward captured once as a CUDA graph and replayed: the headline timed region."""
+        import torch
+        dev, stream = self.dev, self.stream
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            self.fwd(cap)  # first call on this stream outside capture
+            torch.cuda.current_stream().synchronize()
+            with torch.cuda.graph(graph, stream=cap):
+                self.fwd(cap)
+        stream.wait_stream(cap)
+        for _ in range(max(self.warmup, 3)):
+            graph.replay()
+        torch.cuda.synchronize()
+        self.barrier()
+        torch.cuda.synchronize()
+        g_ev = [self.events(2) for _ in range(self.steps)]
+        with ClockSampler(dev.index) as gclocks:
+            for a_, b_ in g_ev:
+                self.flush_l2()
+                a_.record(stream)
+                graph.replay()
+                b_.record(stream)
+            torch.cuda.synchronize()
+        ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in g_ev)
+        self.graph_ms = reduce_max(ms, dev) if self.world > 1 else ms
+        self.graph_clocks = gclocks.summary()
+        assert self.moe.moe_read_device_status(self.ws) == 0
+        del graph
+
+    def run_e2e(self):
+        import torch
+        cfg, moe, wts = self.cfg, self.moe, self.wts
+        T, d, E, k, I, Is = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.I_shared
+        self.x_h = self.inp["x"].cpu().pin_memory()
+        self.lg_h = self.inp["logits"].cpu().pin_memory()
+        self.out_h = torch.empty(T, d, dtype=cfg.dtype).pin_memory()
+        hws = torch.empty(moe.moe_forward_host_workspace_size(T, d, E, k, I, Is, cfg.dtype),
+                          dtype=torch.uint8, device=self.dev)
+
+        def e2e_step():
+            # moe_forward_host: the library copies x and logits in and the output back on the
+            # stream, around the same chain
+            moe.moe_forward_host(self.x_h, self.lg_h, wts["w_gate_up"], wts["w_down"], k,
+                                 cfg.score_fn, self.flags, wts["w_shared_gate_up"],
+                                 wts["w_shared_down"], out=self.out_h, workspace=hws,
+                                 stream=self.stream, device=self.dev)
+
+        self.e2e_ms = self.timed(e2e_step)
+        del hws
+
+    def e2e_entry(self):
+        T = self.cfg.T
+        return {"value": round(T * self.world / (self.e2e_ms * 1e-3), 1), "unit": "tokens/s",
+                "ms_per_step": round(self.e2e_ms, 4),
+                "h2d_bytes_per_step": self.x_h.numel() * self.x_h.element_size()
+                + self.lg_h.numel() * self.lg_h.element_size(),
+                "d2h_bytes_per_step": self.out_h.numel() * self.out_h.element_size(),
+                "path": "moe_forward_host: pinned host x and logits in, the layer, out back to "
+                        "pinned host memory, all enqueued by the library on the timed stream"}
+
+    def roofline(self):
+        """Roofline of the dominant kernel: the gate_up grouped GEMM (2/3 of the expert FLOPs)
+        for prefill layers; the whole layer against HBM for decode batches; the FP32 pipes for
+        the fp32 layer."""
+        import torch
+        cfg, moe, v = self.cfg, self.moe, self.v
+        T, d, E, k, I, Is = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.I_shared
+        R = T * k
+        pk, pk_src = peaks()
+        ps = self.per_stage
+        gu_ms = statistics.mean(ps["gate_up"])
+        dn_ms = statistics.mean(ps["down"])
+        gu_flops, dn_flops = 4.0 * d * I * R, 2.0 * d * I * R
+        sh_flops, sh_ms = 0.0, 0.0
+        if Is:
+            sh_flops = 6.0 * d * Is * T
+            sh_ms = statistics.mean(ps["shared_gate_up"]) + statistics.mean(ps["shared_down"])
+        self.experts_ms = gu_ms + dn_ms + sh_ms
+        self.expert_tflops = (gu_flops + dn_flops + sh_flops) / (self.experts_ms * 1e-3) / 1e12
+        ach = gu_flops / (gu_ms * 1e-3) / 1e12
+        if cfg.dtype != torch.bfloat16:
+            peak = fp32_alu_peak_tflops(pk.get("sm_max_mhz", 2070.0))
+            return {"bound": "alu", "kernel": "simt_grouped_gemm<gate_up>",
+                    "achieved": round(ach, 3), "peak": round(peak, 1), "unit": "TFLOP/s",
+                    "frac": round(ach / peak, 5), "traffic": None,
+                    "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 FLOP x max SM clock",
+                    "note": "correctness workload (0.1 GFLOP): launch-bound, no target"}
+        gu_kernel = moe.moe_gemm_kernel_name(moe.W_GATE_UP, R, E)
+        traffic, _ = traffic_for(GEMM_SOURCES.get(gu_kernel, ""), cfg.name)
+        roof = {"bound": "tensor", "kernel": f"{gu_kernel}<gate_up>", "achieved": round(ach, 1),
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(ach / pk["bf16_tflops"], 4), "traffic": traffic,
+                "peak_source": f"{pk_src} bf16_tflops (burst)",
+                "frac_of_sustained": round(ach / pk.get("bf16_tflops_sustained",
+                                                        pk["bf16_tflops"]), 4),
+                "algorithmic_flops": gu_flops,
+                "time": "gate_up stage of the staged loop (events around the call, L2 flushed)"}
+        if cfg.name.startswith("decode"):
+            # decode streams weights: the bound is HBM. Algorithmic bytes of one layer = the
+            # distinct experts' weights (3 d I bf16 each) + x, logits, ids/weights and out,
+            # over the whole layer's replay time (the fused kernel, or the chain)
+            n_touched = int((v["counts"] > 0).sum().item())
+            layer_bytes = (n_touched * 3.0 * d * I * 2 + T * d * 2 * 2 + T * E * 4 + T * k * 8)
+            ach_gbs = layer_bytes / (self.graph_ms * 1e-3) / 1e9
+            fused = moe.moe_forward_kernel_count(T, k, Is, cfg.dtype) == 1
+            traffic, _ = traffic_for("decode_fused.cu", cfg.name) if fused else (None, None)
+            roof = {"bound": "hbm",
+                    "kernel": ("decode layer: decode_fused_kernel (route, dispatch, experts, "
+                               "combine)" if fused else
+                               "decode layer: route/dispatch chain + grouped GEMMs + combine"),
+                    "achieved": round(ach_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(ach_gbs / pk["hbm_gbs"], 4), "traffic": traffic,
+                    "peak_source": f"{pk_src} hbm_gbs",
+                    "algorithmic_bytes": int(layer_bytes), "distinct_experts": n_touched,
+                    "time": "whole-layer graph replay (per-step events, L2 flushed between "
+                            "steps)"}
+        return roof
+
+    def kernels(self):
+        cfg = self.cfg
+        return self.moe.moe_forward_kernel_count(cfg.T, cfg.k, cfg.I_shared, cfg.dtype)
+
+
+# the workload statement's 60% bars (SURVEY-style targets), by bench name
+TARGETS = {"mixtral_8x7b": ("experts_ms", 2.49), "gpt_oss_120b": ("experts_ms", 1.40),
+           "llama4_scout": ("experts_ms", 7.10), "decode_T1": ("us_per_layer", 18.8),
+           "decode_T8": ("us_per_layer", 121.0), "decode_T64": ("us_per_layer", 296.0)}
+PER_CONFIG = ["tiny_fp32", "mixtral_8x7b", "gpt_oss_120b", "llama4_scout", "decode_T1",
+              "decode_T8", "decode_T64"]
+
+
+def config_entry(L, name, cpu):
+    """The per_config object of one workload (staged stages, graph-replayed layer, e2e,
+    roofline of its dominant kernel, CPU oracle sample)."""
+    cfg = L.cfg
+    roof = L.roofline()
+    ent = {"workload": cfg.name, "T": cfg.T, "d": cfg.d, "E": cfg.E, "k": cfg.k, "I": cfg.I,
+           "I_shared": cfg.I_shared,
+           "dtype": "bf16" if L.packed else "f32",
+           "tokens_per_s": round(cfg.T * L.world / (L.graph_ms * 1e-3), 1),
+           "ms_per_step": round(L.graph_ms, 4), "us_per_layer": round(L.graph_ms * 1e3, 2),
+           "experts_ms": round(L.experts_ms, 4),
+           "expert_gemm_tflops": round(L.expert_tflops, 1),
+           "stages_ms": {n: round(statistics.mean(vv), 4) for n, vv in L.per_stage.items()},
+           "roofline": roof, "e2e": L.e2e_entry(), "gpu_launches_per_step": L.kernels(),
+           "clocks": L.graph_clocks}
+    tgt = TARGETS.get(name)
+    if tgt is not None:
+        key, bar = tgt
+        ent["target"] = {"quantity": key, "bar": bar, "met": ent[key] <= bar}
+    if cpu is not None:
+        ent["cpu_baseline"] = cpu
+    return ent
+
+
+def cpu_sample_entry(cfg, L, n):
+    n = min(n, cfg.T)
+    hi = host_inputs(cfg, L.inp)
+    secs = cpu_oracle_run(cfg, hi, n)
+    return {"value": round(n / secs, 2), "unit": "tokens/s", "cores": blas_threads(),
+            "kind": "oracle",
+            "sample": f"first {n} of {cfg.T} tokens, whole layer, float64 numpy ({secs:.1f} s)"}
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -259,189 +600,25 @@ def run_ours(args, rank, world):
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    cfg = synth.CONFIGS[args.config]
-    if args.T is not None:
-        cfg = cfg.with_T(args.T)
-    if args.E is not None:
-        cfg = dataclasses.replace(cfg, E=args.E, name=f"{cfg.name}@E{args.E}")
+    cfg = workload_config(args.config, args.T, args.E)
     moe.lib()
-    inp = synth.make_inputs(cfg, dev)
+    L = Layer(cfg, dev, args.steps, args.warmup, world)
     T, d, E, k, I, Is = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.I_shared
-    # expert weights are repacked once, as at model load (moe_pack_weights); bf16 layers only
-    packed = cfg.dtype == torch.bfloat16
-    wts = {}
-    for n_ in ("w_gate_up", "w_down", "w_shared_gate_up", "w_shared_down"):
-        w_ = inp[n_]
-        if w_ is not None and packed:
-            w_ = moe.pack_weights(w_, moe.W_GATE_UP if "gate_up" in n_ else moe.W_DOWN)
-        wts[n_] = w_
-    torch.cuda.synchronize()
     R = T * k
-    flags = (moe.RENORMALIZE if cfg.renormalize else 0) | (moe.SCALE_INPUT if cfg.scale_input
-                                                           else 0)
     dt = cfg.dtype
-    stream = torch.cuda.current_stream(dev)
+    inp, wts, stream, flags = L.inp, L.wts, L.stream, L.flags
+    ids, w, out = L.ids, L.w, L.out
+    flush_l2 = L.flush_l2
 
-    # buffers (outside the timed region)
-    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
-    w = torch.empty(T, k, dtype=torch.float32, device=dev)
-    out = torch.empty(T, d, dtype=dt, device=dev)
-    ws = torch.empty(moe.moe_forward_workspace_size(T, d, E, k, I, Is, dt), dtype=torch.uint8,
-                     device=dev)
-    v = moe.forward_workspace_views(ws, T, d, E, k, I, Is, dt)
-    dws = torch.empty(moe.moe_dispatch_workspace_size(T, E, k), dtype=torch.uint8, device=dev)
-    gws = torch.empty(256, dtype=torch.uint8, device=dev)
-    disp_out = {n: v[n] for n in ("counts", "offsets", "sorted_to_slot", "slot_to_sorted",
-                                  "x_sorted")}
-
-    # between timed steps: write a buffer twice the L2 size so no step finds the previous
-    # step's weights or activations cached (decode touches less than the L2 holds)
-    l2_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    def flush_l2():
-        l2_buf.fill_(1)
-
-    stages = ["route", "dispatch", "gate_up", "down"] + (["shared_gate_up", "shared_down"]
-                                                         if Is else []) + ["combine"]
-
-    def step(ev=None):
-        def mark(i):
-            if ev is not None:
-                ev[i].record(stream)
-        mark(0)
-        moe.moe_route(inp["logits"], k, cfg.score_fn, cfg.renormalize, ids, w, stream)
-        mark(1)
-        moe.moe_dispatch(ids, E, x=inp["x"], workspace=dws, out=disp_out, stream=stream)
-        mark(2)
-        moe.moe_gate_up(v["x_sorted"], v["offsets"], wts["w_gate_up"], v["sorted_to_slot"], w,
-                        cfg.scale_input, h=v["h"], workspace=gws, stream=stream)
-        mark(3)
-        moe.moe_down(v["h"], v["offsets"], wts["w_down"], y_sorted=v["y_sorted"],
-                     workspace=gws, stream=stream)
-        mark(4)
-        i = 5
-        if Is:
-            sgu, sdn = wts["w_shared_gate_up"], wts["w_shared_down"]
-            moe.moe_gate_up(inp["x"], None, sgu if packed else sgu.unsqueeze(0),
-                            h=v["h_shared"], workspace=gws, stream=stream)
-            mark(i)
-            moe.moe_down(v["h_shared"], None, sdn if packed else sdn.unsqueeze(0),
-                         y_sorted=v["y_shared"], workspace=gws, stream=stream)
-            mark(i + 1)
-            i += 2
-        moe.moe_combine(v["y_sorted"], v["slot_to_sorted"], k, dt,
-                        topk_weights=None if cfg.scale_input else w,
-                        y_shared=v["y_shared"] if Is else None, out=out, stream=stream)
-        mark(i)
-
-    nev = len(stages) + 1
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
-    assert moe.moe_read_device_status(gws) == 0 and moe.moe_read_device_status(dws) == 0
-
-    import torch.distributed as dist
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)]
-              for _ in range(args.steps)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(dev.index) as clocks:
-        for s in range(args.steps):
-            flush_l2()
-            step(events[s])
-        torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    per_stage = {name: [] for name in stages}
-    step_ms = []
-    for ev in events:
-        for i, name in enumerate(stages):
-            per_stage[name].append(ev[i].elapsed_time(ev[i + 1]))
-        step_ms.append(ev[0].elapsed_time(ev[-1]))
-    ms_per_step = statistics.mean(step_ms)
-    if world > 1:
-        ms_per_step = reduce_max(ms_per_step, dev)
-
+    L.run_staged()
     # the product call: moe_forward issued from the host every step ...
-    def fwd(st_):
-        moe.moe_forward(inp["x"], inp["logits"], wts["w_gate_up"], wts["w_down"], k,
-                        cfg.score_fn, flags, wts["w_shared_gate_up"], wts["w_shared_down"],
-                        out=out, topk_ids=ids, topk_weights=w, workspace=ws, stream=st_)
-
-    for _ in range(3):
-        fwd(stream)
-    f_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)]
-    for a_, b_ in f_ev:
-        flush_l2()
-        a_.record(stream)
-        fwd(stream)
-        b_.record(stream)
-    torch.cuda.synchronize()
-    forward_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in f_ev)
-
+    forward_ms = L.timed(lambda: L.fwd(stream))
     # ... and captured once as a CUDA graph and replayed (no host launch cost; the form a
     # decode loop runs in). This is the timed region of the headline value.
-    graph = torch.cuda.CUDAGraph()
-    cap = torch.cuda.Stream(dev)
-    cap.wait_stream(stream)
-    with torch.cuda.stream(cap):
-        fwd(cap)  # first call on this stream outside capture
-        torch.cuda.current_stream().synchronize()
-        with torch.cuda.graph(graph, stream=cap):
-            fwd(cap)
-    stream.wait_stream(cap)
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    g_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)]
-    with ClockSampler(dev.index) as gclocks:
-        for a_, b_ in g_ev:
-            flush_l2()
-            a_.record(stream)
-            graph.replay()
-            b_.record(stream)
-        torch.cuda.synchronize()
-    graph_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in g_ev)
-    if world > 1:
-        graph_ms = reduce_max(graph_ms, dev)
-    assert moe.moe_read_device_status(ws) == 0
-
+    L.run_graph()
+    graph_ms = L.graph_ms
     # end to end through moe_forward with host buffers
-    x_h = inp["x"].cpu().pin_memory()
-    lg_h = inp["logits"].cpu().pin_memory()
-    out_h = torch.empty(T, d, dtype=dt).pin_memory()
-    hws = torch.empty(moe.moe_forward_host_workspace_size(T, d, E, k, I, Is, dt),
-                      dtype=torch.uint8, device=dev)
-
-    def e2e_step():
-        # moe_forward_host: the library copies x and logits in and the output back on the
-        # stream, around the same chain
-        moe.moe_forward_host(x_h, lg_h, wts["w_gate_up"], wts["w_down"], k, cfg.score_fn, flags,
-                             wts["w_shared_gate_up"], wts["w_shared_down"], out=out_h,
-                             workspace=hws, stream=stream, device=dev)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    x_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)]
-    for a_, b_ in x_ev:
-        flush_l2()
-        a_.record(stream)
-        e2e_step()
-        b_.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in x_ev)
-    if world > 1:
-        e2e_ms = reduce_max(e2e_ms, dev)
+    L.run_e2e()
 
     # the router from hidden states (logits = x W_r + b and the top-k in one kernel): the step
     # before the layer, timed on its own (not part of the layer's timed region above)
@@ -449,20 +626,9 @@ def run_ours(args, rank, world):
     b_r = synth.router_bias(cfg, device=dev)
     b_r = None if b_r is None else b_r.to(torch.float32).contiguous()
     lg_r = torch.empty(T, E, dtype=torch.float32, device=dev)
-    for _ in range(3):
-        moe.moe_route_hidden(inp["x"], w_r, k, cfg.score_fn, cfg.renormalize, bias=b_r,
-                             logits=lg_r, topk_ids=ids, topk_weights=w, stream=stream)
-    r_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)]
-    for a_, b_ in r_ev:
-        flush_l2()
-        a_.record(stream)
-        moe.moe_route_hidden(inp["x"], w_r, k, cfg.score_fn, cfg.renormalize, bias=b_r,
-                             logits=lg_r, topk_ids=ids, topk_weights=w, stream=stream)
-        b_.record(stream)
-    torch.cuda.synchronize()
-    router_hidden_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in r_ev)
-
+    router_hidden_ms = L.timed(lambda: moe.moe_route_hidden(
+        inp["x"], w_r, k, cfg.score_fn, cfg.renormalize, bias=b_r, logits=lg_r, topk_ids=ids,
+        topk_weights=w, stream=stream))
     # training step of the same layer (not part of the headline value): moe_forward_train, which
     # keeps what the backward reads, then moe_backward (dx, both weight gradients in fp32, the
     # routing-weight and logit gradients), each step with its own events, L2 flushed before it
@@ -601,45 +767,7 @@ def run_ours(args, rank, world):
                "time": "per-step events around moe_forward_mx, L2 flushed before each step"}
         del mxw, mws
 
-    # roofline of the dominant kernel (the gate_up grouped GEMM: 2/3 of the expert FLOPs)
-    pk, pk_src = peaks()
-    gu_ms = statistics.mean(per_stage["gate_up"])
-    dn_ms = statistics.mean(per_stage["down"])
-    gu_flops = 4.0 * d * I * R
-    dn_flops = 2.0 * d * I * R
-    sh_flops, sh_ms = 0.0, 0.0
-    if Is:
-        sh_flops = 6.0 * d * Is * T
-        sh_ms = statistics.mean(per_stage["shared_gate_up"]) + statistics.mean(
-            per_stage["shared_down"])
-    ach = gu_flops / (gu_ms * 1e-3) / 1e12
-    gu_kernel = moe.moe_gemm_kernel_name(moe.W_GATE_UP, R, E)
-    traffic, _ = traffic_for(GEMM_SOURCES.get(gu_kernel, ""), cfg.name)
-    roof = {"bound": "tensor", "kernel": f"{gu_kernel}<gate_up>", "achieved": round(ach, 1),
-            "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-            "frac": round(ach / pk["bf16_tflops"], 4), "traffic": traffic,
-            "peak_source": f"{pk_src} bf16_tflops (burst)",
-            "frac_of_sustained": round(ach / pk.get("bf16_tflops_sustained",
-                                                    pk["bf16_tflops"]), 4)}
-    expert_tflops = (gu_flops + dn_flops + sh_flops) / ((gu_ms + dn_ms + sh_ms) * 1e-3) / 1e12
-    if cfg.name.startswith("decode"):
-        # decode streams weights: the bound is HBM. Algorithmic bytes of one layer = the
-        # distinct experts' weights (3 d I bf16 each) + x, logits, ids/weights and out, over
-        # the whole layer's replay time (both kernels of the fused path, or the chain).
-        n_touched = int((v["counts"] > 0).sum().item())
-        layer_bytes = (n_touched * 3.0 * d * I * 2 + T * d * 2 * 2 + T * E * 4 + T * k * 8)
-        ach_gbs = layer_bytes / (graph_ms * 1e-3) / 1e9
-        fused = moe.moe_forward_kernel_count(T, k, Is, dt) == 1
-        traffic, _ = traffic_for("decode_fused.cu", cfg.name) if fused else (None, None)
-        roof = {"bound": "hbm",
-                "kernel": ("decode layer: decode_fused_kernel (route, dispatch, experts, combine)" if fused
-                           else "decode layer: route/dispatch chain + grouped GEMMs + combine"),
-                "achieved": round(ach_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach_gbs / pk["hbm_gbs"], 4), "traffic": traffic,
-                "peak_source": f"{pk_src} hbm_gbs",
-                "algorithmic_bytes": int(layer_bytes), "distinct_experts": n_touched,
-                "time": "whole-layer graph replay (per-step events, L2 flushed between steps)"}
-
+    roof = L.roofline()
     tokens_per_s = T * world / (graph_ms * 1e-3)
     res = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s",
@@ -651,36 +779,51 @@ def run_ours(args, rank, world):
         "data": "synthetic (seeded counter-based generator; shapes of the workload)",
         "config": {"workload": cfg.name, "T": T, "d": d, "E": E, "k": k, "I": I,
                    "I_shared": Is, "seed": cfg.seed,
-                   "weights": "repacked once at load (moe_pack_weights)" if packed
+                   "weights": "repacked once at load (moe_pack_weights)" if L.packed
                    else "layout of the pages",
-                   "l2": "flushed before every timed step (256 MB write, outside the events)"},
+                   "l2": "flushed before every timed step (256 MB write, outside the events)",
+                   "headline": "value, roofline, e2e and cpu_baseline are this workload's; "
+                               "per_config holds every workload of the same run"},
         "roofline": roof,
-        "expert_gemm_tflops": round(expert_tflops, 1),
-        "stages_ms": {n: round(statistics.mean(vv), 4) for n, vv in per_stage.items()},
-        "staged_calls_ms_per_step": round(ms_per_step, 4),
+        "expert_gemm_tflops": round(L.expert_tflops, 1),
+        "experts_ms": round(L.experts_ms, 4),
+        "stages_ms": {n: round(statistics.mean(vv), 4) for n, vv in L.per_stage.items()},
+        "staged_calls_ms_per_step": round(L.staged_ms, 4),
         "forward_call_ms": round(forward_ms, 4),
         "router_from_hidden_ms": round(router_hidden_ms, 4),
         "training": bwd,
         "mx": mxr,
-        "e2e": {"value": round(T * world / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
-                "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": x_h.numel() * x_h.element_size()
-                + lg_h.numel() * lg_h.element_size(),
-                "d2h_bytes_per_step": out_h.numel() * out_h.element_size(),
-                "path": "moe_forward_host: pinned host x and logits in, the layer, out back to "
-                        "pinned host memory, all enqueued by the library on the timed stream"},
-        "gpu_launches": args.steps * moe.moe_forward_kernel_count(T, k, Is, dt),
-        "clocks": gclocks.summary(),
-        "clocks_staged": clocks.summary(),
+        "e2e": L.e2e_entry(),
+        "gpu_launches": args.steps * L.kernels(),
+        "clocks": L.graph_clocks,
+        "clocks_staged": L.staged_clocks,
     }
+    cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n = args.cpu_sample or default_sample(cfg)
-        hi = host_inputs(cfg, inp)
-        secs = cpu_oracle_run(cfg, hi, n)
-        res["cpu_baseline"] = {"value": round(n / secs, 2), "unit": "tokens/s",
-                               "cores": blas_threads(), "kind": "oracle",
-                               "sample": f"first {n} of {T} tokens, whole layer, float64 numpy "
-                                         f"({secs:.1f} s)"}
+        cpu = cpu_sample_entry(cfg, L, args.cpu_sample or default_sample(cfg))
+        res["cpu_baseline"] = cpu
+
+    if not args.no_per_config:
+        # every workload in the same run: the headline's own entry, then the others one at a
+        # time (each freed before the next is built)
+        per = {}
+        head = args.config if args.config.startswith("decode_T") or args.T is None else None
+        small = rank == 0 and world == 1 and not args.no_cpu_baseline
+        for name in PER_CONFIG:
+            if name == head and args.E is None:
+                per[name] = config_entry(L, name, cpu)
+                continue
+            c_ = workload_config(name)
+            Lc = Layer(c_, dev, args.steps, args.warmup, world)
+            Lc.run_staged()
+            Lc.run_graph()
+            Lc.run_e2e()
+            # a shorter CPU sample per extra workload (about a third of the headline's)
+            cs = cpu_sample_entry(c_, Lc, max(8, default_sample(c_) // 3)) if small else None
+            per[name] = config_entry(Lc, name, cs)
+            del Lc
+            torch.cuda.empty_cache()
+        res["per_config"] = per
     return res
 
 
@@ -690,12 +833,11 @@ def run_reference(args, rank, world):
 
     from routing_dispatch_grouped_gb300 import synth
 
-    cfg = synth.CONFIGS[args.config]
-    if args.T is not None:
-        cfg = cfg.with_T(args.T)
+    cfg = workload_config(args.config, args.T, args.E)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = host_inputs(cfg, synth.make_inputs(cfg, dev))
     n = args.cpu_sample or max(8, default_sample(cfg) // max(1, args.steps + args.warmup) * 2)
+    n = min(n, cfg.T)
     for _ in range(args.warmup):
         cpu_oracle_run(cfg, inp, n)
     secs = [cpu_oracle_run(cfg, inp, n) for _ in range(args.steps)]
