@@ -545,6 +545,58 @@ moe_status moe_forward_mx(const void* x, const float* logits, int T, int d, int 
                           moe_stream_t stream);
 
 /*
+ * MX on the block-scaled tensor cores ("Expert parallelism", the Mega MoE paragraph: FP8
+ * activations times FP4 weights with block scales on the newest GPUs). The same MX numerics as
+ * moe_forward_mx (x and h MXFP8, weights MXFP4, fp32 accumulation), computed by
+ * tcgen05.mma.kind::mxf8f6f4.block_scale: the tensor cores multiply the E4M3 and E2M1 codes and
+ * apply both E8M0 block scales themselves; nothing is dequantized.
+ *
+ * MX tensor-core weight buffer of one kind (gate_up: K = d, logical columns C = 2I, gate
+ * columns first; down: K = I, C = d), N (= I or d) and K multiples of 32, Kp = K rounded up to
+ * 128:
+ *   codes: for group e and logical column c, Kp / 2 bytes of E2M1 codes along K (element k in
+ *     the low nibble of byte k / 2 when k is even), at (e * C + c) * Kp / 2; zero past K;
+ *   scales, from sf_off = (E * C * Kp / 2) rounded up to 1024: 512-byte atoms, one per
+ *     (e, 128-column block cb, 128-element K chunk kc) at sf_off + ((e * CB + cb) * (Kp / 128)
+ *     + kc) * 512; byte 16 (n % 32) + 4 (n / 32) + j holds the scale (s + 127) of the block's
+ *     column n at K block 4 kc + j, 127 past the end of the columns or of K. Column blocks:
+ *     gate_up ceil(I / 128) for the gate half then as many for the up half (CB = 2 ceil(I/128));
+ *     down ceil(d / 128).
+ *   256-byte aligned; moe_mx_tc_weights_size(...) bytes (0: unsupported sizes).
+ */
+size_t moe_mx_tc_weights_size(moe_weight_kind kind, int E, int K, int N);
+/* bf16 weights in the pages' layout ([E, d, 2I] or [E, I, d]) -> MX tensor-core buffer (the
+ * same codes and scales moe_quantize_weights_mx decides, in this layout). */
+moe_status moe_quantize_weights_mx_tc(moe_weight_kind kind, const void* w, void* mx, int E,
+                                      int K, int N, moe_stream_t stream);
+/* MX tensor-core buffer -> bf16 weights [E, K, C] (exact). */
+moe_status moe_dequantize_weights_mx_tc(moe_weight_kind kind, const void* mx, void* w, int E,
+                                        int K, int N, moe_stream_t stream);
+/*
+ * moe_forward_mx_tc - the MX layer on the block-scaled tensor cores (moe_forward_mx's
+ *   arguments, weights in the MX tensor-core layout, d, I and Is multiples of 32; flags:
+ *   MOE_RENORMALIZE | MOE_SCALE_INPUT). Route, dispatch indices, one kernel that rounds each
+ *   token's x to MXFP8 once and writes it to every row it was sent to, the gate_up GEMM (h
+ *   rounded to MXFP8 in its epilogue), the down GEMM, the combine.
+ *   workspace: moe_forward_mx_tc_workspace_size(...) bytes, 256-byte aligned: the status word
+ *   (256 B), then, each rounded up to 256 bytes: counts [E], offsets [E+1], dispatch scratch,
+ *   sorted_to_slot [R], slot_to_sorted [R], x codes [Rp][d], x scale atoms [Rp/128][ceil(d/128)],
+ *   h codes [Rp][I], h scale atoms [Rp/128][ceil(I/128)], y_sorted fp32 [R][d], and with a
+ *   shared expert its x codes [Tp][d] and atoms, h codes [Tp][Is] and atoms, y fp32 [T][d].
+ *   Rp = R rounded up to 128 plus 128 E, Tp = T rounded up to 128; expert e's rows occupy padded
+ *   rows from poff[e] = sum over e' < e of ceil(count[e'] / 128) * 128; an atom's byte
+ *   16 (m % 32) + 4 (m / 32) + j holds the scale of row m of its 128-row block at K block j of
+ *   its 128-element chunk.
+ */
+size_t moe_forward_mx_tc_workspace_size(int T, int d, int E, int k, int I, int Is);
+moe_status moe_forward_mx_tc(const void* x, const float* logits, int T, int d, int E, int k,
+                             int I, moe_score_fn score_fn, unsigned flags,
+                             const void* w_gate_up_mx, const void* w_down_mx,
+                             const void* w_shared_gate_up_mx, const void* w_shared_down_mx,
+                             int Is, int32_t* topk_ids, float* topk_weights, void* out,
+                             void* workspace, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * moe_read_device_status - synchronise `stream`, then return the status word the kernels of
  * the last call that used `workspace` left there (MOE_OK if none). Diagnostics only.
  */

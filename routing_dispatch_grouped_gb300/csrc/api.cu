@@ -1062,6 +1062,199 @@ moe_status moe_forward_mx(const void* x, const float* logits, int T, int d, int 
                         topk_weights, out, workspace, ws_bytes, stream, false, true);
 }
 
+// ---- MX on the block-scaled tensor cores (weights in the MX tensor-core layout) ----
+size_t moe_mx_tc_weights_size(moe_weight_kind kind, int E, int K, int N) {
+    if ((kind != MOE_W_GATE_UP && kind != MOE_W_DOWN) || E < 1 || K < 1 || N < 1 || N % 32 ||
+        K % 32)
+        return 0;
+    return mx_tc_geom(kind == MOE_W_GATE_UP, K, N, E).total;
+}
+
+static moe_status check_mx_tc_weights(moe_weight_kind kind, const void* a, const void* b, int E,
+                                      int K, int N) {
+    if (kind != MOE_W_GATE_UP && kind != MOE_W_DOWN) return MOE_ERR_INVALID_ARG;
+    if (E < 1 || K < 1 || N < 1 || N % 32 != 0 || K % 32 != 0) return MOE_ERR_INVALID_ARG;
+    if (!a || !b || !aligned256(a) || !aligned256(b)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+moe_status moe_quantize_weights_mx_tc(moe_weight_kind kind, const void* w, void* mx, int E,
+                                      int K, int N, moe_stream_t stream) {
+    if (!aligned16(w)) return MOE_ERR_INVALID_ARG;
+    const moe_status st = check_mx_tc_weights(kind, mx, mx, E, K, N);
+    if (st != MOE_OK) return st;
+    if (!w) return MOE_ERR_INVALID_ARG;
+    return launch_status(launch_mx_tc_quant_weights(kind == MOE_W_GATE_UP, w, E, K, N, mx,
+                                                    (cudaStream_t)stream));
+}
+
+moe_status moe_dequantize_weights_mx_tc(moe_weight_kind kind, const void* mx, void* w, int E,
+                                        int K, int N, moe_stream_t stream) {
+    const moe_status st = check_mx_tc_weights(kind, mx, mx, E, K, N);
+    if (st != MOE_OK) return st;
+    if (!w || !aligned16(w)) return MOE_ERR_INVALID_ARG;
+    return launch_status(launch_mx_tc_dequant_weights(kind == MOE_W_GATE_UP, mx, E, K, N, w,
+                                                      (cudaStream_t)stream));
+}
+
+namespace {
+// moe_forward_mx_tc's workspace: status word, dispatch indices, then the padded MXFP8 rows
+// (x codes and scale atoms, h codes and scale atoms), y_sorted, and for a shared expert its own
+// x and h in the same form plus its y. Rp = R rounded up to 128 plus 128 per expert bounds the
+// padded rows (every expert's rows start at a multiple of 128).
+struct MxTcLayout {
+    size_t counts, offsets, chunk, s2p, p2s, xq, xsf, hq, hsf, y, sxq, ssf, shq, shsf, ysh,
+        total;
+    int Rp, Tp;
+};
+
+MxTcLayout mx_tc_layout(int T, int d, int E, int k, int I, int Is) {
+    const size_t R = (size_t)T * k;
+    MxTcLayout L;
+    L.Rp = (int)(round_up(R, 128) + 128 * (size_t)E);
+    L.Tp = (int)round_up((size_t)T, 128);
+    const size_t kcd = (d + 127) / 128, kci = (I + 127) / 128, kcs = (Is + 127) / 128;
+    size_t o = kStatusBytes;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = round_up(o + bytes, 256);
+        return at;
+    };
+    L.counts = take((size_t)E * 4);
+    L.offsets = take((size_t)(E + 1) * 4);
+    L.chunk = take(dispatch_scratch_bytes((int)R, E));
+    L.s2p = take(R * 4);
+    L.p2s = take(R * 4);
+    L.xq = take((size_t)L.Rp * d);
+    L.xsf = take((size_t)L.Rp / 128 * kcd * 512);
+    L.hq = take((size_t)L.Rp * I);
+    L.hsf = take((size_t)L.Rp / 128 * kci * 512);
+    L.y = take(R * (size_t)d * 4);
+    L.sxq = take(Is > 0 ? (size_t)L.Tp * d : 0);
+    L.ssf = take(Is > 0 ? (size_t)L.Tp / 128 * kcd * 512 : 0);
+    L.shq = take(Is > 0 ? (size_t)L.Tp * Is : 0);
+    L.shsf = take(Is > 0 ? (size_t)L.Tp / 128 * kcs * 512 : 0);
+    L.ysh = take(Is > 0 ? (size_t)T * d * 4 : 0);
+    L.total = o;
+    return L;
+}
+
+moe_status run_mx_tc_gemm(GemmKind kind, const void* a, const void* a_sf, const void* w,
+                          const int32_t* offsets, const int32_t* s2p, const float* tw,
+                          bool scale, int R, int Rp, int K, int N, int groups, void* out,
+                          void* h_sf, int* status, cudaStream_t s) {
+    MxTcGemmArgs g;
+    g.kind = kind;
+    g.a = a;
+    g.a_sf = a_sf;
+    g.b = w;
+    g.offsets = offsets;
+    g.sorted_to_slot = s2p;
+    g.topk_weights = tw;
+    g.scale_rows = scale;
+    g.R = R;
+    g.Rp = Rp;
+    g.K = K;
+    g.N = N;
+    g.groups = groups;
+    g.out = out;
+    g.h_sf = h_sf;
+    g.status = status;
+    return launch_status(launch_mx_tc_gemm(g, s));
+}
+}  // namespace
+
+size_t moe_forward_mx_tc_workspace_size(int T, int d, int E, int k, int I, int Is) {
+    if (T < 0 || d < 1 || E < 1 || k < 1 || I < 1 || Is < 0) return 0;
+    return mx_tc_layout(T, d, E, k, I, Is).total;
+}
+
+moe_status moe_forward_mx_tc(const void* x, const float* logits, int T, int d, int E, int k,
+                             int I, moe_score_fn score_fn, unsigned flags,
+                             const void* w_gate_up_mx, const void* w_down_mx,
+                             const void* w_shared_gate_up_mx, const void* w_shared_down_mx,
+                             int Is, int32_t* topk_ids, float* topk_weights, void* out,
+                             void* workspace, size_t ws_bytes, moe_stream_t stream) {
+    moe_status st = check_tek(T, E, k);
+    if (st != MOE_OK) return st;
+    if (score_fn != MOE_SCORE_SOFTMAX && score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+    if (flags & ~(unsigned)(MOE_RENORMALIZE | MOE_SCALE_INPUT)) return MOE_ERR_INVALID_ARG;
+    if (d < 1 || I < 1 || Is < 0 || d % 32 || I % 32 || Is % 32) return MOE_ERR_INVALID_ARG;
+    const bool shared = w_shared_gate_up_mx != nullptr || w_shared_down_mx != nullptr;
+    if (shared != (Is > 0)) return MOE_ERR_INVALID_ARG;
+    if (shared && (!w_shared_gate_up_mx || !w_shared_down_mx)) return MOE_ERR_INVALID_ARG;
+    if ((long long)T * k + 128ll * (E + 1) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!x || !logits || !w_gate_up_mx || !w_down_mx || !topk_ids || !topk_weights || !out)
+        return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, logits, topk_ids, topk_weights, out};
+    for (const void* q : ptrs)
+        if (!aligned16(q)) return MOE_ERR_INVALID_ARG;
+    const void* wptrs[] = {w_gate_up_mx, w_down_mx, w_shared_gate_up_mx, w_shared_down_mx};
+    for (const void* q : wptrs)
+        if (q && !aligned256(q)) return MOE_ERR_INVALID_ARG;
+    const MxTcLayout L = mx_tc_layout(T, d, E, k, I, Is);
+    if (!workspace || !aligned256(workspace) || ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* status = reinterpret_cast<int*>(ws);
+    int32_t* counts = reinterpret_cast<int32_t*>(ws + L.counts);
+    int32_t* offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+    int32_t* chunk = reinterpret_cast<int32_t*>(ws + L.chunk);
+    int32_t* s2p = reinterpret_cast<int32_t*>(ws + L.s2p);
+    int32_t* p2s = reinterpret_cast<int32_t*>(ws + L.p2s);
+    float* y = reinterpret_cast<float*>(ws + L.y);
+    float* ysh = reinterpret_cast<float*>(ws + L.ysh);
+    const int R = T * k;
+    const bool scale = (flags & MOE_SCALE_INPUT) != 0;
+    const bool renorm = (flags & MOE_RENORMALIZE) != 0;
+
+    if ((st = clear_status(workspace, s)) != MOE_OK) return st;
+    // route and the dispatch indices (no row copy: the next kernel writes the rows in MXFP8)
+    if (R <= kSmallDispatchMaxSlots) {
+        if ((st = launch_status(launch_route_dispatch_small(logits, T, E, k, (int)score_fn,
+                                                            renorm, topk_ids, topk_weights,
+                                                            counts, offsets, s2p, p2s, s))) !=
+            MOE_OK)
+            return st;
+    } else {
+        if ((st = launch_status(launch_route(logits, T, E, k, (int)score_fn, renorm, topk_ids,
+                                             topk_weights, s))) != MOE_OK)
+            return st;
+    }
+    PdlScope pdl(true);
+    if (R > kSmallDispatchMaxSlots &&
+        (st = launch_status(launch_dispatch(topk_ids, nullptr, 0, T, E, k, counts, offsets, s2p,
+                                            p2s, nullptr, chunk, status, s))) != MOE_OK)
+        return st;
+    // x to MXFP8 once per token, written to every padded row it was sent to (and to the shared
+    // expert's rows)
+    if ((st = launch_status(launch_mx_tc_quant_rows(
+             x, T, d, k, E, topk_ids, p2s, offsets, ws + L.xq, ws + L.xsf,
+             shared ? ws + L.sxq : nullptr, shared ? ws + L.ssf : nullptr, s))) != MOE_OK)
+        return st;
+    if ((st = run_mx_tc_gemm(kGateUp, ws + L.xq, ws + L.xsf, w_gate_up_mx, offsets, s2p,
+                             topk_weights, scale, R, L.Rp, d, I, E, ws + L.hq, ws + L.hsf,
+                             status, s)) != MOE_OK)
+        return st;
+    if ((st = run_mx_tc_gemm(kDown, ws + L.hq, ws + L.hsf, w_down_mx, offsets, nullptr, nullptr,
+                             false, R, L.Rp, I, d, E, y, nullptr, status, s)) != MOE_OK)
+        return st;
+    if (shared) {
+        if ((st = run_mx_tc_gemm(kGateUp, ws + L.sxq, ws + L.ssf, w_shared_gate_up_mx, nullptr,
+                                 nullptr, nullptr, false, T, L.Tp, d, Is, 1, ws + L.shq,
+                                 ws + L.shsf, status, s)) != MOE_OK)
+            return st;
+        if ((st = run_mx_tc_gemm(kDown, ws + L.shq, ws + L.shsf, w_shared_down_mx, nullptr,
+                                 nullptr, nullptr, false, T, L.Tp, Is, d, 1, ysh, nullptr, status,
+                                 s)) != MOE_OK)
+            return st;
+    }
+    return launch_status(launch_combine(y, p2s, scale ? nullptr : topk_weights,
+                                        shared ? ysh : nullptr, T, d, k, true, out, s));
+}
+
 moe_status moe_read_device_status(const void* workspace, moe_stream_t stream) {
     if (!workspace) return MOE_ERR_INVALID_ARG;
     int v = 0;

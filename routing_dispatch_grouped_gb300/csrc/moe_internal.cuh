@@ -489,6 +489,50 @@ cudaError_t launch_mx_dequant_weights(bool gate_up, const void* mx, int G, int K
 cudaError_t launch_mx_rows(const void* in, int R, int K, void* out, void* codes, void* scales,
                            cudaStream_t s);
 
+// MX tensor-core layout (gemm_mx_tc.cu): weights as K-major E2M1 codes [G][C][Kp / 2] (Kp = K
+// rounded up to 128) followed by 512-byte scale atoms [G][CB][KC]; activations as E4M3 codes
+// [Rp][K] with every expert's rows starting at a multiple of 128, and scale atoms
+// [Rp / 128][KC]. The block-scaled tcgen05 GEMM reads both.
+struct MxTcGeom {
+    int C;          // logical columns (2I or d)
+    int Kp;         // K rounded up to 128
+    int KC;         // Kp / 128
+    int cbh;        // 128-column scale blocks of a half (gate_up) or of all columns (down)
+    int CB;         // scale blocks per group
+    size_t sf_off;  // byte offset of the scale atoms
+    size_t total;   // buffer size
+};
+MxTcGeom mx_tc_geom(bool gate_up, int K, int N, int G);  // N = I (gate_up) or d (down)
+cudaError_t launch_mx_tc_quant_weights(bool gate_up, const void* w, int G, int K, int N, void* mx,
+                                       cudaStream_t s);
+cudaError_t launch_mx_tc_dequant_weights(bool gate_up, const void* mx, int G, int K, int N,
+                                         void* w, cudaStream_t s);
+// x [T, d] bf16 to the padded MXFP8 layout: each token's codes and scales go to the padded row
+// of each of its slots (topk_ids, slot_to_sorted, offsets of the dispatch) and, when codes_sh is
+// not null, to row t of the shared expert's single group.
+cudaError_t launch_mx_tc_quant_rows(const void* x, int T, int d, int k, int E,
+                                    const int32_t* topk_ids, const int32_t* slot_to_sorted,
+                                    const int32_t* offsets, void* codes, void* sf, void* codes_sh,
+                                    void* sf_sh, cudaStream_t s);
+struct MxTcGemmArgs {
+    GemmKind kind;
+    const void* a;     // E4M3 codes [Rp][K]
+    const void* a_sf;  // their scale atoms
+    const void* b;     // weights in the MX tensor-core layout
+    const int32_t* offsets;  // [groups + 1] or nullptr (one group of R rows)
+    const int32_t* sorted_to_slot;
+    const float* topk_weights;
+    bool scale_rows;   // gate_up: multiply each row's accumulators by its routing weight
+    int R, Rp, K, N, groups;
+    void* out;         // gate_up: h codes [Rp][N]; down: y fp32 [R][N]
+    void* h_sf;        // gate_up: h scale atoms [Rp / 128][ceil(N / 128)]
+    int* status;
+};
+cudaError_t launch_mx_tc_gemm(const MxTcGemmArgs& a, cudaStream_t s);
+// Tensor map of any element type with a 128-byte swizzle and zero fill outside the tensor.
+bool encode_tensor_map(CUtensorMap* m, CUtensorMapDataType type, int rank, const void* base,
+                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box);
+
 // ---------------------------------------------------------------------------------------------
 // backward pass (gemm_bwd.cu: tensor cores; backward.cu: fp32 layers and the small kernels)
 // ---------------------------------------------------------------------------------------------

@@ -71,6 +71,12 @@ SIGNATURES = {
     "moe_forward_mx_workspace_size": (_S, [_I, _I, _I, _I, _I, _I]),
     "moe_forward_mx": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P, _P, _P,
                             _P, _S, _P]),
+    "moe_mx_tc_weights_size": (_S, [_I, _I, _I, _I]),
+    "moe_quantize_weights_mx_tc": (_I, [_I, _P, _P, _I, _I, _I, _P]),
+    "moe_dequantize_weights_mx_tc": (_I, [_I, _P, _P, _I, _I, _I, _P]),
+    "moe_forward_mx_tc_workspace_size": (_S, [_I, _I, _I, _I, _I, _I]),
+    "moe_forward_mx_tc": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P, _P,
+                               _P, _P, _S, _P]),
     "moe_read_device_status": (_I, [_P, _P]),
     "moe_status_string": (ctypes.c_char_p, [_I]),
     "moe_debug_set_gemm_stall_ns": (None, [ctypes.c_uint32]),
@@ -132,8 +138,9 @@ class PackedWeights:
     """Expert weights repacked by moe_pack_weights (bf16): `data` is the packed buffer, kind is
     W_GATE_UP (logical [E, K=d, 2I], N = I) or W_DOWN (logical [E, K=I, N=d])."""
 
-    def __init__(self, data: torch.Tensor, kind: int, E: int, K: int, N: int):
+    def __init__(self, data: torch.Tensor, kind: int, E: int, K: int, N: int, tc=False):
         self.data, self.kind, self.E, self.K, self.N = data, kind, E, K, N
+        self.tc = tc  # True: the MX tensor-core layout (moe_quantize_weights_mx_tc)
 
     def data_ptr(self):
         return self.data.data_ptr()
@@ -682,8 +689,9 @@ class MxWeights:
     codes then the E8M0 scales; kind W_GATE_UP (logical [E, K=d, 2I], N = I) or W_DOWN
     ([E, K=I, N=d])."""
 
-    def __init__(self, data: torch.Tensor, kind: int, E: int, K: int, N: int):
+    def __init__(self, data: torch.Tensor, kind: int, E: int, K: int, N: int, tc=False):
         self.data, self.kind, self.E, self.K, self.N = data, kind, E, K, N
+        self.tc = tc  # True: the MX tensor-core layout (moe_quantize_weights_mx_tc)
 
     def data_ptr(self):
         return self.data.data_ptr()
@@ -706,6 +714,30 @@ def dequantize_weights_mx(mx: MxWeights, stream=None) -> torch.Tensor:
     cols = 2 * mx.N if mx.kind == W_GATE_UP else mx.N
     w = torch.empty(mx.E, mx.K, cols, dtype=torch.bfloat16, device=mx.data.device)
     _check("moe_dequantize_weights_mx", lib().moe_dequantize_weights_mx(
+        mx.kind, _p(mx.data), _p(w), mx.E, mx.K, mx.N, _stream(stream)))
+    return w
+
+
+def quantize_weights_mx_tc(w: torch.Tensor, kind: int, stream=None) -> MxWeights:
+    """bf16 gate_up ([E, d, 2I] or [d, 2I]) or down ([E, I, d] or [I, d]) weights to MXFP4 in
+    the MX tensor-core layout (the block-scaled GEMMs of moe_forward_mx_tc read it)."""
+    _need(w, "w")
+    w3 = w.unsqueeze(0) if w.dim() == 2 else w
+    E, K, C = w3.shape
+    N = C // 2 if kind == W_GATE_UP else C
+    n = lib().moe_mx_tc_weights_size(kind, E, K, N)
+    if n == 0:
+        raise MoEError("moe_mx_tc_weights_size", 1)
+    out = torch.empty(n, dtype=torch.uint8, device=w.device)
+    _check("moe_quantize_weights_mx_tc", lib().moe_quantize_weights_mx_tc(
+        kind, _p(w3), _p(out), E, K, N, _stream(stream)))
+    return MxWeights(out, kind, E, K, N, tc=True)
+
+
+def dequantize_weights_mx_tc(mx: MxWeights, stream=None) -> torch.Tensor:
+    cols = 2 * mx.N if mx.kind == W_GATE_UP else mx.N
+    w = torch.empty(mx.E, mx.K, cols, dtype=torch.bfloat16, device=mx.data.device)
+    _check("moe_dequantize_weights_mx_tc", lib().moe_dequantize_weights_mx_tc(
         mx.kind, _p(mx.data), _p(w), mx.E, mx.K, mx.N, _stream(stream)))
     return w
 
@@ -749,3 +781,65 @@ def moe_forward_mx(x, logits, w_gate_up: MxWeights, w_down: MxWeights, k, score_
         _p(w_shared_gate_up), _p(w_shared_down), Is, _p(ids), _p(w), _p(out), _p(ws), ws.numel(),
         _stream(stream)))
     return out, ids, w, ws
+
+
+def moe_forward_mx_tc_workspace_size(T, d, E, k, I, Is) -> int:
+    return lib().moe_forward_mx_tc_workspace_size(T, d, E, k, I, Is)
+
+
+def moe_forward_mx_tc(x, logits, w_gate_up: MxWeights, w_down: MxWeights, k, score_fn=SOFTMAX,
+                      flags=RENORMALIZE, w_shared_gate_up=None, w_shared_down=None, out=None,
+                      topk_ids=None, topk_weights=None, workspace=None, stream=None):
+    """The MX layer on the block-scaled tensor cores (weights from quantize_weights_mx_tc).
+    Returns (out, topk_ids, topk_weights, workspace)."""
+    _need(x, "x")
+    _need(logits, "logits")
+    T, d = x.shape
+    E, I = w_gate_up.E, w_gate_up.N
+    Is = w_shared_gate_up.N if w_shared_gate_up is not None else 0
+    dev = x.device
+    out = out if out is not None else torch.empty(T, d, dtype=x.dtype, device=dev)
+    ids = topk_ids if topk_ids is not None else torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = topk_weights if topk_weights is not None else torch.empty(T, k, dtype=torch.float32,
+                                                                  device=dev)
+    ws = workspace if workspace is not None else _workspace(
+        moe_forward_mx_tc_workspace_size(T, d, E, k, I, Is), dev)
+    _check("moe_forward_mx_tc", lib().moe_forward_mx_tc(
+        _p(x), _p(logits), T, d, E, k, I, score_fn, flags, _p(w_gate_up), _p(w_down),
+        _p(w_shared_gate_up), _p(w_shared_down), Is, _p(ids), _p(w), _p(out), _p(ws), ws.numel(),
+        _stream(stream)))
+    return out, ids, w, ws
+
+
+def mx_tc_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is):
+    """Views of what moe_forward_mx_tc leaves in its workspace (layout of include/moe.h):
+    indices, the padded MXFP8 rows of x and h (codes [Rp, K] uint8, scale atoms
+    [Rp / 128, ceil(K / 128), 512] uint8), y_sorted and the shared expert's."""
+    R = T * k
+    Rp = (R + 127) // 128 * 128 + 128 * E
+    Tp = (T + 127) // 128 * 128
+    kc = lambda K: (K + 127) // 128
+    sizes = [("counts", E * 4), ("offsets", (E + 1) * 4), ("chunk", (R + 255) // 256 * E * 4),
+             ("sorted_to_slot", R * 4), ("slot_to_sorted", R * 4), ("x_codes", Rp * d),
+             ("x_sf", Rp // 128 * kc(d) * 512), ("h_codes", Rp * I),
+             ("h_sf", Rp // 128 * kc(I) * 512), ("y_sorted", R * d * 4),
+             ("sx_codes", Tp * d if Is else 0), ("sx_sf", Tp // 128 * kc(d) * 512 if Is else 0),
+             ("sh_codes", Tp * Is if Is else 0), ("sh_sf", Tp // 128 * kc(Is) * 512 if Is else 0),
+             ("y_shared", T * d * 4 if Is else 0)]
+    v, o = {}, 256
+    for name, nbytes in sizes:
+        v[name] = ws[o:o + nbytes]
+        o = (o + nbytes + 255) // 256 * 256
+    out = {"counts": v["counts"].view(torch.int32), "offsets": v["offsets"].view(torch.int32),
+           "sorted_to_slot": v["sorted_to_slot"].view(torch.int32),
+           "slot_to_sorted": v["slot_to_sorted"].view(torch.int32),
+           "x_codes": v["x_codes"].view(Rp, d), "x_sf": v["x_sf"].view(Rp // 128, kc(d), 512),
+           "h_codes": v["h_codes"].view(Rp, I), "h_sf": v["h_sf"].view(Rp // 128, kc(I), 512),
+           "y_sorted": v["y_sorted"].view(torch.float32).view(R, d), "Rp": Rp, "Tp": Tp}
+    if Is:
+        out.update({"sx_codes": v["sx_codes"].view(Tp, d),
+                    "sx_sf": v["sx_sf"].view(Tp // 128, kc(d), 512),
+                    "sh_codes": v["sh_codes"].view(Tp, Is),
+                    "sh_sf": v["sh_sf"].view(Tp // 128, kc(Is), 512),
+                    "y_shared": v["y_shared"].view(torch.float32).view(T, d)})
+    return out
