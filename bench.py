@@ -551,6 +551,67 @@ class Layer:
         cfg = self.cfg
         return self.moe.moe_forward_kernel_count(cfg.T, cfg.k, cfg.I_shared, cfg.dtype)
 
+    def run_mx_tc(self):
+        """The MX layer on the block-scaled tensor cores (MXFP4 weights quantised once at load
+        into the tensor-core layout, x and h MXFP8): moe_forward_mx_tc timed whole, and its
+        x rounding and two GEMMs timed on their own; L2 flushed before each step."""
+        import torch
+        cfg, moe, inp = self.cfg, self.moe, self.inp
+        T, d, E, k, I, Is = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.I_shared
+        R = T * k
+        q = {n_: (moe.quantize_weights_mx_tc(inp[n_], moe.W_GATE_UP if "gate_up" in n_
+                                             else moe.W_DOWN) if inp[n_] is not None else None)
+             for n_ in ("w_gate_up", "w_down", "w_shared_gate_up", "w_shared_down")}
+        ws = torch.empty(moe.moe_forward_mx_tc_workspace_size(T, d, E, k, I, Is),
+                         dtype=torch.uint8, device=self.dev)
+        out = torch.empty_like(self.out)
+
+        def layer():
+            moe.moe_forward_mx_tc(inp["x"], inp["logits"], q["w_gate_up"], q["w_down"], k,
+                                  cfg.score_fn, self.flags, q["w_shared_gate_up"],
+                                  q["w_shared_down"], out=out, topk_ids=self.ids,
+                                  topk_weights=self.w, workspace=ws, stream=self.stream)
+
+        layer_ms = self.timed(layer)
+        assert moe.moe_read_device_status(ws) == 0
+        v = moe.mx_tc_workspace_views(ws, T, d, E, k, I, Is)
+        gws = torch.zeros(256, dtype=torch.uint8, device=self.dev)
+        rows_ms = self.timed(lambda: moe.mx_tc_rows(
+            inp["x"], self.ids, v["slot_to_sorted"], v["offsets"], E, v["x_codes"], v["x_sf"],
+            stream=self.stream))
+        gu_ms = self.timed(lambda: moe.moe_gate_up_mx_tc(
+            v["x_codes"], v["x_sf"], v["offsets"], q["w_gate_up"], R, v["h_codes"], v["h_sf"],
+            v["sorted_to_slot"], self.w, cfg.scale_input, gws, self.stream))
+        dn_ms = self.timed(lambda: moe.moe_down_mx_tc(
+            v["h_codes"], v["h_sf"], v["offsets"], q["w_down"], R, v["y_sorted"], gws,
+            self.stream))
+        assert moe.moe_read_device_status(gws) == 0
+        pk, pk_src = peaks()
+        fp8_peak = 2.0 * pk["bf16_tflops"]   # dense FP8 = 2 x bf16 (nominal 4.5 / 2.25 PFLOP/s)
+        gu_tf = 4.0 * d * I * R / (gu_ms * 1e-3) / 1e12
+        dn_tf = 2.0 * d * I * R / (dn_ms * 1e-3) / 1e12
+        wb = sum(v_.data.numel() for v_ in q.values() if v_ is not None)
+        bf = sum(inp[n_].numel() * 2 for n_ in q if inp[n_] is not None)
+        res = {"ms_per_step": round(layer_ms, 4),
+               "tokens_per_s": round(T * self.world / (layer_ms * 1e-3), 1),
+               "stages_ms": {"x_to_mxfp8_rows": round(rows_ms, 4), "gate_up": round(gu_ms, 4),
+                             "down": round(dn_ms, 4)},
+               "roofline": {"bound": "tensor", "kernel": "tc_mx_gemm<gate_up>",
+                            "achieved": round(gu_tf, 1), "peak": round(fp8_peak, 1),
+                            "unit": "TFLOP/s", "frac": round(gu_tf / fp8_peak, 4),
+                            "peak_source": f"{pk_src} bf16_tflops (burst) x 2, the nominal "
+                                           "FP8 / bf16 dense ratio"},
+               "down_tflops": round(dn_tf, 1),
+               "weight_bytes": wb, "weight_bytes_bf16": bf,
+               "path": "tcgen05.mma.kind::mxf8f6f4.block_scale: E4M3 x E2M1 codes with E8M0 "
+                       "block scales applied by the tensor cores (nothing dequantized)",
+               # route(+dispatch indices when R <= 1024), x rows, gate_up, down, combine; the
+               # dispatch's histogram, scan and rank above 1024 slots; two for a shared expert
+               "kernels_per_step": 5 + (2 if Is else 0) + (0 if R <= 1024 else 3),
+               "time": "events around each call, L2 flushed before each step"}
+        del q, ws, v
+        return res
+
 
 # the workload statement's 60% bars (SURVEY-style targets), by bench name
 TARGETS = {"mixtral_8x7b": ("experts_ms", 2.49), "gpt_oss_120b": ("experts_ms", 1.40),
@@ -766,6 +827,8 @@ def run_ours(args, rank, world):
                         "dequantized to bf16 (exact) for the bf16 tensor-core GEMMs"),
                "time": "per-step events around moe_forward_mx, L2 flushed before each step"}
         del mxw, mws
+        if d % 32 == 0 and I % 32 == 0 and Is % 32 == 0:
+            mxr = {"tensor_core": L.run_mx_tc(), "dequantized_or_decode": mxr}
 
     roof = L.roofline()
     tokens_per_s = T * world / (graph_ms * 1e-3)
@@ -812,15 +875,20 @@ def run_ours(args, rank, world):
         for name in PER_CONFIG:
             if name == head and args.E is None:
                 per[name] = config_entry(L, name, cpu)
+                if isinstance(mxr, dict) and "tensor_core" in mxr:
+                    per[name]["mx_tensor_core"] = mxr["tensor_core"]
                 continue
             c_ = workload_config(name)
             Lc = Layer(c_, dev, args.steps, args.warmup, world)
             Lc.run_staged()
             Lc.run_graph()
             Lc.run_e2e()
+            mx_tc = Lc.run_mx_tc() if Lc.packed and not name.startswith("decode") else None
             # a shorter CPU sample per extra workload (about a third of the headline's)
             cs = cpu_sample_entry(c_, Lc, max(8, default_sample(c_) // 3)) if small else None
             per[name] = config_entry(Lc, name, cs)
+            if mx_tc is not None:
+                per[name]["mx_tensor_core"] = mx_tc
             del Lc
             torch.cuda.empty_cache()
         res["per_config"] = per

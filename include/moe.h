@@ -588,6 +588,28 @@ moe_status moe_dequantize_weights_mx_tc(moe_weight_kind kind, const void* mx, vo
  *   16 (m % 32) + 4 (m / 32) + j holds the scale of row m of its 128-row block at K block j of
  *   its 128-element chunk.
  */
+/*
+ * The steps of moe_forward_mx_tc on their own (buffers in the layouts described above; Rp =
+ * R rounded up to 128 plus 128 E with offsets, R rounded up to 128 for one group without):
+ *   moe_mx_tc_rows: x [T, d] bf16 to MXFP8, written to the padded row of each routed slot
+ *     (codes [Rp][d], scale atoms; needs topk_ids, slot_to_sorted and offsets from
+ *     moe_dispatch) and/or to row t of one unpermuted group (codes_sh [Tp][d], atoms).
+ *   moe_gate_up_mx_tc: h (codes [Rp][I] and atoms) from x codes/atoms and the gate_up weights
+ *     (flags: MOE_SCALE_INPUT, which needs sorted_to_slot and topk_weights).
+ *   moe_down_mx_tc: y_sorted fp32 [R][d] (unpadded sorted rows) from h codes/atoms.
+ *   offsets NULL: one group (E = 1). workspace: >= 256 bytes, 256-byte aligned (status word).
+ */
+moe_status moe_mx_tc_rows(const void* x, int T, int d, int k, int E, const int32_t* topk_ids,
+                          const int32_t* slot_to_sorted, const int32_t* offsets, void* codes,
+                          void* sf, void* codes_sh, void* sf_sh, moe_stream_t stream);
+moe_status moe_gate_up_mx_tc(const void* x_codes, const void* x_sf, const int32_t* offsets,
+                             const int32_t* sorted_to_slot, const float* topk_weights, int R,
+                             int d, int E, int I, const void* w_gate_up_mx, unsigned flags,
+                             void* h_codes, void* h_sf, void* workspace, size_t ws_bytes,
+                             moe_stream_t stream);
+moe_status moe_down_mx_tc(const void* h_codes, const void* h_sf, const int32_t* offsets, int R,
+                          int I, int E, int d, const void* w_down_mx, float* y_sorted,
+                          void* workspace, size_t ws_bytes, moe_stream_t stream);
 size_t moe_forward_mx_tc_workspace_size(int T, int d, int E, int k, int I, int Is);
 moe_status moe_forward_mx_tc(const void* x, const float* logits, int T, int d, int E, int k,
                              int I, moe_score_fn score_fn, unsigned flags,

@@ -1164,6 +1164,71 @@ moe_status run_mx_tc_gemm(GemmKind kind, const void* a, const void* a_sf, const 
 }
 }  // namespace
 
+moe_status moe_mx_tc_rows(const void* x, int T, int d, int k, int E, const int32_t* topk_ids,
+                          const int32_t* slot_to_sorted, const int32_t* offsets, void* codes,
+                          void* sf, void* codes_sh, void* sf_sh, moe_stream_t stream) {
+    moe_status st = check_tek(T, E, k);
+    if (st != MOE_OK) return st;
+    if (d < 32 || d % 32) return MOE_ERR_INVALID_ARG;
+    if ((codes == nullptr) != (sf == nullptr) || (codes_sh == nullptr) != (sf_sh == nullptr))
+        return MOE_ERR_INVALID_ARG;
+    if (codes && (!topk_ids || !slot_to_sorted || !offsets)) return MOE_ERR_INVALID_ARG;
+    if (!codes && !codes_sh) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    const void* ptrs[] = {x, codes, sf, codes_sh, sf_sh};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    if (!x) return MOE_ERR_INVALID_ARG;
+    return launch_status(launch_mx_tc_quant_rows(x, T, d, codes ? k : 0, E, topk_ids,
+                                                 slot_to_sorted, codes ? offsets : nullptr,
+                                                 codes, sf, codes_sh, sf_sh,
+                                                 (cudaStream_t)stream));
+}
+
+static moe_status mx_tc_gemm_entry(GemmKind kind, const void* a, const void* a_sf,
+                                   const int32_t* offsets, const int32_t* s2p, const float* tw,
+                                   bool scale, int R, int K, int E, int N, const void* w,
+                                   void* out, void* h_sf, void* workspace, size_t ws_bytes,
+                                   moe_stream_t stream) {
+    if (R < 0 || E < 1 || E > kMaxE || K < 32 || N < 32 || K % 32 || N % 32)
+        return MOE_ERR_INVALID_ARG;
+    if (offsets == nullptr && E != 1) return MOE_ERR_INVALID_ARG;
+    if (scale && (s2p == nullptr || tw == nullptr)) return MOE_ERR_INVALID_ARG;
+    if ((long long)R + 128ll * (E + 1) >= (1ll << 31)) return MOE_ERR_UNSUPPORTED;
+    if (workspace == nullptr || !aligned256(workspace) || ws_bytes < kStatusBytes)
+        return MOE_ERR_WORKSPACE;
+    if (R == 0) return MOE_OK;
+    if (!a || !a_sf || !w || !out || (kind == kGateUp && !h_sf)) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {a, a_sf, out, h_sf, offsets};
+    for (const void* q : ptrs)
+        if (q && !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    if (!aligned256(w)) return MOE_ERR_INVALID_ARG;
+    const int Rp = (int)(round_up((size_t)R, 128) + (offsets ? 128 * (size_t)E : 0));
+    cudaStream_t s = (cudaStream_t)stream;
+    moe_status st = clear_status(workspace, s);
+    if (st != MOE_OK) return st;
+    return run_mx_tc_gemm(kind, a, a_sf, w, offsets, s2p, tw, scale, R, Rp, K, N, E, out, h_sf,
+                          reinterpret_cast<int*>(workspace), s);
+}
+
+moe_status moe_gate_up_mx_tc(const void* x_codes, const void* x_sf, const int32_t* offsets,
+                             const int32_t* sorted_to_slot, const float* topk_weights, int R,
+                             int d, int E, int I, const void* w_gate_up_mx, unsigned flags,
+                             void* h_codes, void* h_sf, void* workspace, size_t ws_bytes,
+                             moe_stream_t stream) {
+    if (flags & ~(unsigned)MOE_SCALE_INPUT) return MOE_ERR_INVALID_ARG;
+    return mx_tc_gemm_entry(kGateUp, x_codes, x_sf, offsets, sorted_to_slot, topk_weights,
+                            (flags & MOE_SCALE_INPUT) != 0, R, d, E, I, w_gate_up_mx, h_codes,
+                            h_sf, workspace, ws_bytes, stream);
+}
+
+moe_status moe_down_mx_tc(const void* h_codes, const void* h_sf, const int32_t* offsets, int R,
+                          int I, int E, int d, const void* w_down_mx, float* y_sorted,
+                          void* workspace, size_t ws_bytes, moe_stream_t stream) {
+    return mx_tc_gemm_entry(kDown, h_codes, h_sf, offsets, nullptr, nullptr, false, R, I, E, d,
+                            w_down_mx, y_sorted, nullptr, workspace, ws_bytes, stream);
+}
+
 size_t moe_forward_mx_tc_workspace_size(int T, int d, int E, int k, int I, int Is) {
     if (T < 0 || d < 1 || E < 1 || k < 1 || I < 1 || Is < 0) return 0;
     return mx_tc_layout(T, d, E, k, I, Is).total;

@@ -31,18 +31,19 @@
 //   K-block scales of row r + 32 c; the MMA reads row m's scale at column m / 32, byte j (the
 //   scale-factor id of its K step).
 //
-// Structure (one CTA per SM, 224 threads, tiles expert-major, then N block, then M block):
+// Structure (one CTA per SM, 352 threads, tiles expert-major, then N block, then M block):
 //   warp 0      A producer: one 128 x 128-byte FP8 box (128B swizzle) and the A scale atom per
 //               stage; arms the stage barrier for all of the stage's bytes.
-//   warp 6      B producer: two 128-column x 128-element FP4 boxes (TMA type 16U4_ALIGN16B: each
+//   warp 10     B producer: two 128-column x 128-element FP4 boxes (TMA type 16U4_ALIGN16B: each
 //               16 codes land in 16 bytes, the layout the MMA reads 4-bit operands in) and the
 //               two B scale atoms.
 //   warp 1      allocates 512 TMEM columns (accumulator 0..255, scale atoms from 256), one lane
 //               copies each stage's scale atoms into TMEM and issues 4 MMAs (M=128, N=256, K=32)
 //               per stage.
-//   warps 2..5  epilogue over their 32 TMEM lanes.
-// The accumulator is single-buffered (the scale columns take the room of a second one): the
-// epilogue of a tile runs before the next tile's MMAs. Every mbarrier wait is bounded in time;
+//   warps 2..9  epilogue, two warps per TMEM lane quarter, each over half of the columns.
+// The accumulator is single-buffered (the scale columns take the room of a second one), so each
+// epilogue warp first loads its 128 accumulator columns into registers and releases the
+// accumulator: the next tile's MMAs then overlap the SwiGLU, the MXFP8 rounding and the stores. Every mbarrier wait is bounded in time;
 // on expiry the kernel records MOE_ERR_TIMEOUT, lets its own copies and MMAs finish, frees TMEM
 // and returns.
 #include <mutex>
@@ -65,7 +66,7 @@ constexpr int kBBoxTxBytes = 128 * 128 / 2;
 constexpr int kStageTxBytes = kABytes + 2 * kBBoxTxBytes;  // 32 KB
 constexpr int kAtom = 512;                           // one scale atom
 constexpr int kSfStageBytes = 3 * kAtom;             // A atom + two B atoms
-constexpr int kThreads = 224;
+constexpr int kThreads = 352;  // 11 warps: A loads, MMA, 8 epilogue, B loads
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfCol0 = 256;                    // first TMEM column of the scale atoms
 constexpr uint32_t kSfColsPerStage = 16;             // A: +0..3, B: +4..11
@@ -175,6 +176,46 @@ __host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t sf_id) {
            ((uint32_t)(M >> 4) << 24) | (sf_id << 29);
 }
 
+// One MX block of h (32 columns from col0) from its gate and up accumulators: SwiGLU in
+// fp32 (accumulators times the row scale s), rounded to MXFP8; stores the 32 codes of a valid
+// row and returns the scale byte (127 for a block past the end of the columns).
+__device__ __forceinline__ uint32_t h_block_mxfp8(const uint32_t (&g)[32], const uint32_t (&u)[32],
+                                                  float s, int col0, int N, bool row_ok,
+                                                  uint8_t* hrow) {
+    if (col0 >= N) return 127u;
+    float hv[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        hv[i] = silu(__uint_as_float(g[i]) * s) * (__uint_as_float(u[i]) * s);
+        amax = fmaxf(amax, fabsf(hv[i]));
+    }
+    const int se = mx_scale_exp(amax, 8);
+    const float inv = pow2_f32(-se);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        w[i] = e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv) |
+               (e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv) << 16);
+    if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(hrow + col0);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    return (uint32_t)(se + 127);
+}
+
+// 32 fp32 accumulator columns from col0 of one output row (N a multiple of 32).
+__device__ __forceinline__ void store_y_block(const uint32_t (&y)[32], int col0, int N,
+                                              float* yrow) {
+    if (col0 >= N) return;
+    float4* dst = reinterpret_cast<float4*>(yrow + col0);
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+        dst[v] = make_float4(__uint_as_float(y[4 * v]), __uint_as_float(y[4 * v + 1]),
+                             __uint_as_float(y[4 * v + 2]), __uint_as_float(y[4 * v + 3]));
+}
+
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_mx_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -194,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&st.empty[s], 1);
         }
         mbar_init(&st.tfull, 1);
-        mbar_init(&st.tempty, 4);
+        mbar_init(&st.tempty, 8);
         mbar_init(&st.drain, 1);
         st.abort = 0;
         fence_barrier_init();
@@ -230,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int total = st.total_tiles;
     volatile int* abort_flag = &st.abort;
 
-    if (warp == 0 || warp == 6) {
-        // ================= TMA producers: warp 0 A codes + A scales, warp 6 B codes + scales
+    if (warp == 0 || warp == 10) {
+        // ================= TMA producers: warp 0 A codes + A scales, warp 10 B codes + scales
         if (lane == 0) {
             const bool a_side = warp == 0;
             if (a_side) tma_prefetch_desc(&tmA);
@@ -353,8 +394,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ================= epilogue (warps 2..5) =================
-        const int q = warp & 3;  // TMEM lane quarter of this warp
+        // ================= epilogue (warps 2..9) =================
+        // Two warps per TMEM lane quarter, each owning half of the tile's columns (gate_up: 64
+        // h columns, i.e. their 64 gate and 64 up accumulator columns; down: 128 output
+        // columns). A warp loads its 128 accumulator columns into registers and releases the
+        // accumulator at once, so the next tile's MMAs run while it computes and stores.
+        const int q = warp & 3;          // TMEM lane quarter of this warp
+        const int hf = (warp - 2) >> 2;  // which half of the columns
         uint32_t it = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
             const Tile t = decode_tile(st, E, p.n_tile, tile);
@@ -369,73 +415,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int m = q * 32 + lane;
             const bool row_ok = m < t.rows;
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16);
+            uint32_t a0[32], a1[32], a2[32], a3[32];
+            if (KIND == kGateUp) {
+                tmem_ld_32x32b_x32(tbase + hf * 64, a0);
+                tmem_ld_32x32b_x32(tbase + hf * 64 + 32, a1);
+                tmem_ld_32x32b_x32(tbase + 128 + hf * 64, a2);
+                tmem_ld_32x32b_x32(tbase + 128 + hf * 64 + 32, a3);
+            } else {
+                tmem_ld_32x32b_x32(tbase + hf * 128, a0);
+                tmem_ld_32x32b_x32(tbase + hf * 128 + 32, a1);
+                tmem_ld_32x32b_x32(tbase + hf * 128 + 64, a2);
+                tmem_ld_32x32b_x32(tbase + hf * 128 + 96, a3);
+            }
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&st.tempty);
             if (KIND == kGateUp) {
                 float s = 1.0f;
                 if (p.row_scale && row_ok)
                     s = __ldg(p.topk_weights + __ldg(p.sorted_to_slot + t.row0 + m));
                 uint8_t* hc = static_cast<uint8_t*>(p.out) + (size_t)(t.prow0 + m) * p.N;
-                uint32_t sf_word = 0;
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t g[32], u[32];
-                    tmem_ld_32x32b_x32(tbase + c * 32, g);
-                    tmem_ld_32x32b_x32(tbase + 128 + c * 32, u);
-                    tmem_ld_wait();
-                    const int col0 = t.n0 + c * 32;
-                    uint32_t sc = 127;  // past the end: scale 2^0 for zero codes
-                    if (col0 < p.N) {
-                        float hv[32];
-                        float amax = 0.0f;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            hv[i] = silu(__uint_as_float(g[i]) * s) * (__uint_as_float(u[i]) * s);
-                            amax = fmaxf(amax, fabsf(hv[i]));
-                        }
-                        const int se = mx_scale_exp(amax, 8);
-                        const float inv = pow2_f32(-se);
-                        uint32_t w[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            w[i] = e4m3x2(hv[4 * i] * inv, hv[4 * i + 1] * inv) |
-                                   (e4m3x2(hv[4 * i + 2] * inv, hv[4 * i + 3] * inv) << 16);
-                        if (row_ok) {
-                            uint4* dst = reinterpret_cast<uint4*>(hc + col0);
-                            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-                        }
-                        sc = (uint32_t)(se + 127);
-                    }
-                    sf_word |= sc << (8 * c);
-                }
+                const int col0 = t.n0 + hf * 64;
+                const uint32_t sc0 = h_block_mxfp8(a0, a2, s, col0, p.N, row_ok, hc);
+                const uint32_t sc1 = h_block_mxfp8(a1, a3, s, col0 + 32, p.N, row_ok, hc);
                 if (row_ok) {
-                    // the four scales of this row's 128-column chunk: one word of the h atom
+                    // this warp's two of the four scales of the row's 128-column chunk
                     const int hkc = (p.N + 127) >> 7;
                     uint8_t* atom = p.h_sf + ((size_t)(t.prow0 >> 7) * hkc + (t.n0 >> 7)) * kAtom;
-                    *reinterpret_cast<uint32_t*>(atom + 16 * lane + 4 * q) = sf_word;
+                    *reinterpret_cast<uint16_t*>(atom + 16 * lane + 4 * q + 2 * hf) =
+                        (uint16_t)(sc0 | (sc1 << 8));
                 }
-            } else {
-                float* out = static_cast<float*>(p.out);
-#pragma unroll 1
-                for (int c = 0; c < 8; ++c) {
-                    uint32_t y[32];
-                    tmem_ld_32x32b_x32(tbase + c * 32, y);
-                    tmem_ld_wait();
-                    const int col0 = t.n0 + c * 32;
-                    if (row_ok && col0 < p.N) {
-                        float4* dst = reinterpret_cast<float4*>(out + (size_t)(t.row0 + m) * p.N + col0);
-#pragma unroll
-                        for (int v = 0; v < 8; ++v)
-                            if (col0 + v * 4 < p.N)
-                                dst[v] = make_float4(__uint_as_float(y[4 * v]),
-                                                     __uint_as_float(y[4 * v + 1]),
-                                                     __uint_as_float(y[4 * v + 2]),
-                                                     __uint_as_float(y[4 * v + 3]));
-                    }
-                }
+            } else if (row_ok) {
+                float* yr = static_cast<float*>(p.out) + (size_t)(t.row0 + m) * p.N;
+                const int col0 = t.n0 + hf * 128;
+                store_y_block(a0, col0, p.N, yr);
+                store_y_block(a1, col0 + 32, p.N, yr);
+                store_y_block(a2, col0 + 64, p.N, yr);
+                store_y_block(a3, col0 + 96, p.N, yr);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&st.tempty);
         }
     }
 

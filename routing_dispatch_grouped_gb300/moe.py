@@ -74,6 +74,10 @@ SIGNATURES = {
     "moe_mx_tc_weights_size": (_S, [_I, _I, _I, _I]),
     "moe_quantize_weights_mx_tc": (_I, [_I, _P, _P, _I, _I, _I, _P]),
     "moe_dequantize_weights_mx_tc": (_I, [_I, _P, _P, _I, _I, _I, _P]),
+    "moe_mx_tc_rows": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_gate_up_mx_tc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _U, _P, _P, _P, _S,
+                               _P]),
+    "moe_down_mx_tc": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _S, _P]),
     "moe_forward_mx_tc_workspace_size": (_S, [_I, _I, _I, _I, _I, _I]),
     "moe_forward_mx_tc": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P, _P,
                                _P, _P, _S, _P]),
@@ -843,3 +847,35 @@ def mx_tc_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is):
                     "sh_sf": v["sh_sf"].view(Tp // 128, kc(Is), 512),
                     "y_shared": v["y_shared"].view(torch.float32).view(T, d)})
     return out
+
+
+def mx_tc_rows(x, topk_ids, slot_to_sorted, offsets, E, codes, sf, codes_sh=None, sf_sh=None,
+               stream=None):
+    """x [T, d] bf16 to MXFP8 in the padded tensor-core layout (see moe_mx_tc_rows)."""
+    T, d = x.shape
+    k = topk_ids.shape[1] if topk_ids is not None else 1
+    _check("moe_mx_tc_rows", lib().moe_mx_tc_rows(
+        _p(x), T, d, k, E, _p(topk_ids), _p(slot_to_sorted), _p(offsets), _p(codes), _p(sf),
+        _p(codes_sh), _p(sf_sh), _stream(stream)))
+
+
+def moe_gate_up_mx_tc(x_codes, x_sf, offsets, w_gate_up: MxWeights, R, h_codes, h_sf,
+                      sorted_to_slot=None, topk_weights=None, scale_input=False,
+                      workspace=None, stream=None):
+    d, E, I = w_gate_up.K, w_gate_up.E, w_gate_up.N
+    ws = workspace if workspace is not None else _workspace(256, x_codes.device)
+    _check("moe_gate_up_mx_tc", lib().moe_gate_up_mx_tc(
+        _p(x_codes), _p(x_sf), _p(offsets), _p(sorted_to_slot), _p(topk_weights), R, d, E, I,
+        _p(w_gate_up), SCALE_INPUT if scale_input else 0, _p(h_codes), _p(h_sf), _p(ws),
+        ws.numel(), _stream(stream)))
+    return ws
+
+
+def moe_down_mx_tc(h_codes, h_sf, offsets, w_down: MxWeights, R, y_sorted, workspace=None,
+                   stream=None):
+    I, E, d = w_down.K, w_down.E, w_down.N
+    ws = workspace if workspace is not None else _workspace(256, h_codes.device)
+    _check("moe_down_mx_tc", lib().moe_down_mx_tc(
+        _p(h_codes), _p(h_sf), _p(offsets), R, I, E, d, _p(w_down), _p(y_sorted), _p(ws),
+        ws.numel(), _stream(stream)))
+    return ws

@@ -178,3 +178,80 @@ def test_mx_tc_layer_matches_oracle(case):
         assert err_rms(f64(v["y_shared"]), ref["y_shared"]) <= 2e-2
     e = err_rms(f64(out), ref["out"])
     assert e <= 2e-2, e
+
+
+@pytest.mark.parametrize("name", ["mixtral_8x7b"])
+def test_mx_tc_full_size(name):
+    """The Mixtral-shaped workload the benchmark times the MX layer on, at full size, every
+    token, against the MX oracle's whole layer (x codes and scales bit for bit, h within one
+    E4M3 step where rounding midpoints straddle, y_sorted and the output within the bar). The
+    oracle quantises every expert's weights block by block in plain numpy (about a minute
+    here; the 128-expert and Scout shapes would take several), so the other shapes are
+    covered at reduced sizes above."""
+    cfg = synth.CONFIGS[name]
+    T, d, E, k, I, Is = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I, cfg.I_shared
+    inp = synth.make_inputs(cfg, DEV)
+    q = lambda w, kind: moe.quantize_weights_mx_tc(w, kind) if w is not None else None
+    mgu, mdn = q(inp["w_gate_up"], moe.W_GATE_UP), q(inp["w_down"], moe.W_DOWN)
+    msgu, msdn = q(inp["w_shared_gate_up"], moe.W_GATE_UP), q(inp["w_shared_down"], moe.W_DOWN)
+    flags = (moe.RENORMALIZE if cfg.renormalize else 0) | (moe.SCALE_INPUT if cfg.scale_input
+                                                           else 0)
+    out, ids, w, ws = moe.moe_forward_mx_tc(inp["x"], inp["logits"], mgu, mdn, k, cfg.score_fn,
+                                            flags, msgu, msdn)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    del mgu, mdn, msgu, msdn
+    sh = {}
+    if Is:
+        sh = dict(wsgu_deq=HostMX(inp["w_shared_gate_up"][None])[0],
+                  wsd_deq=HostMX(inp["w_shared_down"][None])[0])
+    ref = M.mx_forward(f64(inp["x"]), inp["logits"].cpu().numpy(), HostMX(inp["w_gate_up"]),
+                       HostMX(inp["w_down"]), k, cfg.score_fn, cfg.renormalize,
+                       cfg.scale_input, **sh)
+    assert np.array_equal(ids.cpu().numpy(), ref["topk_ids"])
+    v = moe.mx_tc_workspace_views(ws, T, d, E, k, I, Is)
+    prow = _padded_rows(ref["counts"])
+    xq, _, _ = decode_rows(v["x_codes"], v["x_sf"], prow, d)
+    assert np.array_equal(xq, ref["x_sorted"])
+    hg, _, _ = decode_rows(v["h_codes"], v["h_sf"], prow, I)
+    hr = ref["hq"]
+    off = np.abs(hg - hr) > 0
+    assert off.mean() <= 2e-3, off.mean()
+    assert np.all(np.abs(hg - hr)[off] <= 2.0 ** -3 * np.maximum(np.abs(hg), np.abs(hr))[off]
+                  + 2.0 ** -9 * np.abs(hr).max())
+    assert err_rms(f64(v["y_sorted"]), ref["y_sorted"]) <= 2e-2
+    if Is:
+        assert err_rms(f64(v["y_shared"]), ref["y_shared"]) <= 2e-2
+    e = err_rms(f64(out), ref["out"])
+    assert e <= 2e-2, e
+
+
+def test_mx_tc_steps_equal_the_layer():
+    """The step entry points (rows, gate_up, down) give the layer's own intermediates, bit for
+    bit, when called one by one on its dispatch."""
+    cfg = synth.MoEConfig("steps", 300, 512, 8, 2, 384, bf16, bias="normal0.5")
+    T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
+    inp = synth.make_inputs(cfg, DEV)
+    mgu = moe.quantize_weights_mx_tc(inp["w_gate_up"], moe.W_GATE_UP)
+    mdn = moe.quantize_weights_mx_tc(inp["w_down"], moe.W_DOWN)
+    out, ids, w, ws = moe.moe_forward_mx_tc(inp["x"], inp["logits"], mgu, mdn, k)
+    torch.cuda.synchronize()
+    v = moe.mx_tc_workspace_views(ws, T, d, E, k, I, 0)
+    R, Rp = T * k, v["Rp"]
+    xc = torch.zeros_like(v["x_codes"])
+    xs = torch.zeros_like(v["x_sf"])
+    hc = torch.zeros_like(v["h_codes"])
+    hs = torch.zeros_like(v["h_sf"])
+    y = torch.zeros_like(v["y_sorted"])
+    moe.mx_tc_rows(inp["x"], ids, v["slot_to_sorted"], v["offsets"], E, xc, xs)
+    g = moe.moe_gate_up_mx_tc(xc, xs, v["offsets"], mgu, R, hc, hs)
+    moe.moe_down_mx_tc(hc, hs, v["offsets"], mdn, R, y, g)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(g) == 0
+    counts = v["counts"].cpu().numpy()
+    prow = _padded_rows(counts)
+    assert torch.equal(xc[prow], v["x_codes"][prow])
+    assert torch.equal(hc[prow], v["h_codes"][prow])
+    assert torch.equal(y, v["y_sorted"])
+    a_ref, a_got = decode_rows(v["h_codes"], v["h_sf"], prow, I)[0], decode_rows(hc, hs, prow, I)[0]
+    assert np.array_equal(a_ref, a_got)
