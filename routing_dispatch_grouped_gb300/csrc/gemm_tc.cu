@@ -481,12 +481,14 @@ bool encode_tensor_map_bf16(CUtensorMap* m, const void* base, int rank, const cu
 }
 
 bool encode_tensor_map(CUtensorMap* m, CUtensorMapDataType type, int rank, const void* base,
-                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
+                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                       bool swizzle128) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint32_t elem[3] = {1, 1, 1};
     return fn(m, type, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, elem,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -529,9 +529,12 @@ struct MxTcGemmArgs {
     int* status;
 };
 cudaError_t launch_mx_tc_gemm(const MxTcGemmArgs& a, cudaStream_t s);
-// Tensor map of any element type with a 128-byte swizzle and zero fill outside the tensor.
+// Tensor map of any element type with a 128-byte swizzle (or none) and zero fill outside the
+// tensor.
 bool encode_tensor_map(CUtensorMap* m, CUtensorMapDataType type, int rank, const void* base,
-                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box);
+                       const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box,
+                       bool swizzle128 = true);
+
 
 // ---------------------------------------------------------------------------------------------
 // backward pass (gemm_bwd.cu: tensor cores; backward.cu: fp32 layers and the small kernels)
