@@ -266,3 +266,82 @@ def test_forward_host_validation(L):
     assert f(*bad) == 0                                            # T = 0: nothing enqueued
     bad = list(args); bad[6] = 9
     assert f(*bad) == 1                                            # k > E
+
+
+def test_mx_tc_weights_size_follows_the_layout(L):
+    """moe_mx_tc_weights_size: codes (K padded to 128, two per byte) then 512-byte scale atoms
+    from a 1024-byte boundary, as include/moe.h states; 0 for sizes the layout cannot hold."""
+    for kind, E, K, N in ((0, 3, 256, 160), (1, 2, 288, 96), (0, 128, 2880, 2880),
+                          (1, 8, 14336, 4096)):
+        C = 2 * N if kind == 0 else N
+        Kp = (K + 127) // 128 * 128
+        cbh = (N + 127) // 128
+        CB = 2 * cbh if kind == 0 else cbh
+        sf_off = (E * C * Kp // 2 + 1023) // 1024 * 1024
+        assert L.moe_mx_tc_weights_size(kind, E, K, N) == sf_off + E * CB * (Kp // 128) * 512
+    assert L.moe_mx_tc_weights_size(0, 2, 256, 48) == 0      # N not a multiple of 32
+    assert L.moe_mx_tc_weights_size(1, 2, 200, 64) == 0      # K not a multiple of 32
+    assert L.moe_mx_tc_weights_size(5, 2, 256, 64) == 0      # unknown kind
+
+
+def test_mx_tc_validation(L):
+    q = L.moe_quantize_weights_mx_tc
+    assert q(0, FAKE, FAKE, 2, 200, 64, NULL) == 1            # K % 32
+    assert q(0, FAKE, FAKE + 16, 2, 256, 64, NULL) == 1       # buffer not 256-byte aligned
+    assert q(0, NULL, FAKE, 2, 256, 64, NULL) == 1            # no weights
+    f = L.moe_forward_mx_tc
+    need = L.moe_forward_mx_tc_workspace_size(100, 256, 8, 2, 128, 0)
+    ok = [FAKE, FAKE, 100, 256, 8, 2, 128, 0, 1, FAKE, FAKE, NULL, NULL, 0, FAKE, FAKE, FAKE,
+          FAKE, need, NULL]
+
+    def call(**ch):
+        a = list(ok)
+        names = ["x", "logits", "T", "d", "E", "k", "I", "fn", "flags", "wgu", "wdn", "wsgu",
+                 "wsdn", "Is", "ids", "w", "out", "ws", "ws_bytes", "stream"]
+        for k_, v in ch.items():
+            a[names.index(k_)] = v
+        return f(*a)
+
+    assert call(d=240) == 1                  # d % 32
+    assert call(I=100) == 1                  # I % 32
+    assert call(flags=4) == 1                # the combine weight is not fused on this path
+    assert call(fn=3) == 1                   # bad score function
+    assert call(k=9) == 1                    # k > E
+    assert call(E=300, k=2) == 2             # E > 256
+    assert call(wsgu=FAKE) == 1              # a shared expert without Is
+    assert call(Is=64) == 1                  # Is without shared weights
+    assert call(wgu=FAKE + 16) == 1          # weights not 256-byte aligned
+    assert call(x=MIS) == 1                  # misaligned activations
+    assert call(ws_bytes=need - 1) == 3      # workspace too small
+    assert call(T=0, x=NULL, logits=NULL) == 0   # empty batch: nothing to do
+    g = L.moe_gate_up_mx_tc
+    # (x_codes, x_sf, offsets, s2p, w, R, d, E, I, w_gate_up, flags, h_codes, h_sf, ws, bytes, st)
+    assert g(FAKE, FAKE, NULL, NULL, NULL, 100, 256, 4, 128, FAKE, 0, FAKE, FAKE, FAKE, 256,
+             NULL) == 1                      # no offsets with E > 1
+    assert g(FAKE, FAKE, FAKE, NULL, NULL, 100, 256, 4, 128, FAKE, 2, FAKE, FAKE, FAKE, 256,
+             NULL) == 1                      # scaled input without the routing weights
+    assert g(FAKE, FAKE, FAKE, NULL, NULL, 100, 256, 4, 128, FAKE, 0, FAKE, FAKE, FAKE, 255,
+             NULL) == 3                      # no room for the status word
+    assert g(FAKE, FAKE, FAKE, NULL, NULL, 0, 256, 4, 128, FAKE, 0, FAKE, FAKE, FAKE, 256,
+             NULL) == 0                      # no rows
+    r = L.moe_mx_tc_rows
+    # (x, T, d, k, E, ids, s2p, offsets, codes, sf, codes_sh, sf_sh, stream)
+    assert r(FAKE, 10, 200, 2, 8, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, NULL, NULL) == 1  # d % 32
+    assert r(FAKE, 10, 256, 2, 8, FAKE, FAKE, FAKE, FAKE, NULL, NULL, NULL, NULL) == 1  # no sf
+    assert r(FAKE, 10, 256, 2, 8, NULL, FAKE, FAKE, FAKE, FAKE, NULL, NULL, NULL) == 1  # no ids
+    assert r(NULL, 0, 256, 2, 8, FAKE, FAKE, FAKE, FAKE, FAKE, NULL, NULL, NULL) == 0   # T = 0
+
+
+def test_mx_tc_workspace_views_fit_the_workspace(L):
+    """The binding's views of moe_forward_mx_tc's workspace follow the library's layout: every
+    view ends inside the size the library asks for."""
+    import torch
+    for (T, d, E, k, I, Is) in ((100, 256, 8, 2, 128, 0), (4096, 4096, 8, 2, 14336, 0),
+                                (96, 256, 4, 1, 384, 192), (1, 1024, 32, 8, 384, 0)):
+        n = L.moe_forward_mx_tc_workspace_size(T, d, E, k, I, Is)
+        ws = torch.empty(n, dtype=torch.uint8)
+        v = moe.mx_tc_workspace_views(ws, T, d, E, k, I, Is)
+        for name, t in v.items():
+            if isinstance(t, torch.Tensor):
+                end = t.data_ptr() + t.numel() * t.element_size() - ws.data_ptr()
+                assert end <= n, (name, end, n)

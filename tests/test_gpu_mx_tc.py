@@ -124,6 +124,10 @@ CASES = [  # (name, T, d, E, k, I, score fn, renorm, scaled input, shared I, bia
     ("several_row_tiles", 700, 512, 4, 2, 256, o.SOFTMAX, True, False, 0, "none"),
     ("decode_T1", 1, 1024, 32, 8, 384, o.SOFTMAX, True, False, 0, "none"),
     ("down_ragged_d", 64, 416, 8, 2, 128, o.SOFTMAX, False, False, 0, "none"),
+    # most experts receive no rows (no tiles, nothing written for them)
+    ("empty_experts", 20, 256, 16, 1, 128, o.SOFTMAX, False, False, 0, "none"),
+    # one expert owning every row: several row tiles of one group
+    ("one_expert", 300, 256, 1, 1, 256, o.SOFTMAX, True, False, 0, "none"),
 ]
 
 
@@ -255,3 +259,14 @@ def test_mx_tc_steps_equal_the_layer():
     assert torch.equal(y, v["y_sorted"])
     a_ref, a_got = decode_rows(v["h_codes"], v["h_sf"], prow, I)[0], decode_rows(hc, hs, prow, I)[0]
     assert np.array_equal(a_ref, a_got)
+
+
+def test_mx_tc_empty_batch_is_a_noop():
+    cfg = synth.MoEConfig("empty", 8, 256, 4, 2, 128, bf16)
+    inp = synth.make_inputs(cfg, DEV)
+    mgu = moe.quantize_weights_mx_tc(inp["w_gate_up"], moe.W_GATE_UP)
+    mdn = moe.quantize_weights_mx_tc(inp["w_down"], moe.W_DOWN)
+    x0, lg0 = inp["x"][:0], inp["logits"][:0]
+    out, ids, w, ws = moe.moe_forward_mx_tc(x0, lg0, mgu, mdn, cfg.k)
+    torch.cuda.synchronize()
+    assert out.shape == (0, cfg.d) and ids.shape == (0, cfg.k)
