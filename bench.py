@@ -588,6 +588,13 @@ class Layer:
         assert moe.moe_read_device_status(gws) == 0
         pk, pk_src = peaks()
         fp8_peak = 2.0 * pk["bf16_tflops"]   # dense FP8 = 2 x bf16 (nominal 4.5 / 2.25 PFLOP/s)
+        # DRAM traffic of the gate_up launch: captured on the Mixtral shape cut to E=4, T=2048
+        # (a few GB on the device); its weights, x and h all grow in proportion to E and T, so
+        # the full Mixtral launch is that capture x (E/4)(T/2048) when both ratios agree
+        traffic = None
+        small, _ = traffic_for("gemm_mx_tc.cu", "mixtral_8x7b@T2048@E4")
+        if small is not None and cfg.name == "mixtral_8x7b":
+            traffic = int(small * (E / 4))
         gu_tf = 4.0 * d * I * R / (gu_ms * 1e-3) / 1e12
         dn_tf = 2.0 * d * I * R / (dn_ms * 1e-3) / 1e12
         wb = sum(v_.data.numel() for v_ in q.values() if v_ is not None)
@@ -599,6 +606,9 @@ class Layer:
                "roofline": {"bound": "tensor", "kernel": "tc_mx_gemm<gate_up>",
                             "achieved": round(gu_tf, 1), "peak": round(fp8_peak, 1),
                             "unit": "TFLOP/s", "frac": round(gu_tf / fp8_peak, 4),
+                            "traffic": traffic,
+                            "traffic_source": "ncu on E=4, T=2048 scaled x2 (weights, x and h "
+                                              "all double)" if traffic is not None else None,
                             "peak_source": f"{pk_src} bf16_tflops (burst) x 2, the nominal "
                                            "FP8 / bf16 dense ratio"},
                "down_tflops": round(dn_tf, 1),

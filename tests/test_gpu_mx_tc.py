@@ -270,3 +270,26 @@ def test_mx_tc_empty_batch_is_a_noop():
     out, ids, w, ws = moe.moe_forward_mx_tc(x0, lg0, mgu, mdn, cfg.k)
     torch.cuda.synchronize()
     assert out.shape == (0, cfg.d) and ids.shape == (0, cfg.k)
+
+
+def test_mx_tc_mixtral_cut_to_4_experts():
+    """The Mixtral shape with 4 experts and 2048 tokens: inputs larger than the L2 (0.24 GB of
+    MXFP4 weights), a few GB on the device; the case the kernel's profile summary is taken on.
+    Routing, x codes and scales bit for bit, the output within the bar."""
+    import dataclasses
+    cfg = dataclasses.replace(synth.CONFIGS["mixtral_8x7b"].with_T(2048), E=4)
+    T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
+    inp = synth.make_inputs(cfg, DEV)
+    mgu = moe.quantize_weights_mx_tc(inp["w_gate_up"], moe.W_GATE_UP)
+    mdn = moe.quantize_weights_mx_tc(inp["w_down"], moe.W_DOWN)
+    out, ids, w, ws = moe.moe_forward_mx_tc(inp["x"], inp["logits"], mgu, mdn, k)
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    ref = M.mx_forward(f64(inp["x"]), inp["logits"].cpu().numpy(), HostMX(inp["w_gate_up"]),
+                       HostMX(inp["w_down"]), k)
+    assert np.array_equal(ids.cpu().numpy(), ref["topk_ids"])
+    v = moe.mx_tc_workspace_views(ws, T, d, E, k, I, 0)
+    xq, _, _ = decode_rows(v["x_codes"], v["x_sf"], _padded_rows(ref["counts"]), d)
+    assert np.array_equal(xq, ref["x_sorted"])
+    assert err_rms(f64(v["y_sorted"]), ref["y_sorted"]) <= 2e-2
+    assert err_rms(f64(out), ref["out"]) <= 2e-2
