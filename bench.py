@@ -589,12 +589,12 @@ class Layer:
         pk, pk_src = peaks()
         fp8_peak = 2.0 * pk["bf16_tflops"]   # dense FP8 = 2 x bf16 (nominal 4.5 / 2.25 PFLOP/s)
         # DRAM traffic of the gate_up launch: captured on the Mixtral shape cut to E=4, T=2048
-        # (a few GB on the device); its weights, x and h all grow in proportion to E and T, so
-        # the full Mixtral launch is that capture x (E/4)(T/2048) when both ratios agree
+        # (a few GB on the device). The full Mixtral launch (E=8, T=4096) doubles each part of
+        # it: the weights (with E) and the x and h rows (with T), so the capture is scaled x2
         traffic = None
         small, _ = traffic_for("gemm_mx_tc.cu", "mixtral_8x7b@T2048@E4")
         if small is not None and cfg.name == "mixtral_8x7b":
-            traffic = int(small * (E / 4))
+            traffic = int(small * 2)
         gu_tf = 4.0 * d * I * R / (gu_ms * 1e-3) / 1e12
         dn_tf = 2.0 * d * I * R / (dn_ms * 1e-3) / 1e12
         wb = sum(v_.data.numel() for v_ in q.values() if v_ is not None)
