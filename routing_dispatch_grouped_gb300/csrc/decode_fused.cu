@@ -143,7 +143,8 @@ struct Ctx {
     int nA;                  // gate_up items of the current wave
     int slot_off;            // partial slot offset of the current wave (see the schedule)
     int W, nq;               // waves, touched experts
-    int ready_q;             // touched expert whose h this warp has seen complete (-1: none)
+    int ready_q;             // touched expert whose h blocks ready_mask covers (-1: none)
+    uint64_t ready_mask;     // h blocks of ready_q this warp has seen stored (all ones: every)
     int dumps;               // hand-overs so far
 };
 
@@ -680,20 +681,39 @@ __device__ void group_b(Ctx& c, const Params& p, int q, int i0, int kc0, int kc1
             for (int j = 0; j < 4; ++j) acc[mt][n][j] = 0.0f;
     for (int i = first_owned(i0, c.warp); i < i0 + (kc1 - kc0); i += kStages) {
         if (c.ready_q != q) {
-            // every h block of the expert must be stored (bounded wait; the launch is
-            // cooperative); lane j watches block j, j + 32, ...
-            for (int jb = c.lane; jb < p.nbh; jb += 32) {
-                const uint64_t t0 = globaltimer_ns();
-                while (ld_acquire(p.hflag + q * p.nbh + jb) == 0) {
-                    if (c.flags[0] || globaltimer_ns() - t0 > kWaitLimitNs) {
-                        set_status(p.status, MOE_ERR_TIMEOUT);
-                        c.flags[0] = 1;
-                        break;
+            c.ready_q = q;
+            c.ready_mask = 0;
+        }
+        // the h blocks this item reads must be stored (bounded wait; the launch is
+        // cooperative): an item covers K rows [K_item kc, K_item kc + K_item) of h (256 rows,
+        // or 30 MX blocks = 960 rows), i.e. its 64-column blocks K_item / 64 * kc onwards, so
+        // the item waits for those and not for the rest of the expert's h. Lane j watches
+        // block j of the range (the whole expert, lanes j, j + 32, ..., when it has more than
+        // 64 blocks and no mask covers them).
+        {
+            constexpr int kBlocksPerItem = (MX ? kMxKbB * 32 : kKcB) / 64;
+            static_assert((MX ? kMxKbB * 32 : kKcB) % 64 == 0, "items cover whole h blocks");
+            const int kc = kc0 + (i - i0);
+            const bool masked = p.nbh <= 64;
+            const int jb_lo = masked ? kBlocksPerItem * kc : 0;
+            const int jb_hi = masked ? min(p.nbh, jb_lo + kBlocksPerItem) : p.nbh;
+            const uint64_t need =
+                masked ? (((jb_hi - jb_lo) >= 64 ? ~0ull : ((1ull << (jb_hi - jb_lo)) - 1)) << jb_lo)
+                       : ~0ull;
+            if ((c.ready_mask & need) != need) {
+                for (int jb = jb_lo + c.lane; jb < jb_hi; jb += 32) {
+                    const uint64_t t0 = globaltimer_ns();
+                    while (ld_acquire(p.hflag + q * p.nbh + jb) == 0) {
+                        if (c.flags[0] || globaltimer_ns() - t0 > kWaitLimitNs) {
+                            set_status(p.status, MOE_ERR_TIMEOUT);
+                            c.flags[0] = 1;
+                            break;
+                        }
                     }
                 }
+                __syncwarp();
+                c.ready_mask |= need;
             }
-            __syncwarp();
-            c.ready_q = q;
         }
         if (MX)
             item_b_mx<NTILE>(c, p, i, kc0 + (i - i0), hrow, hsc, acc);
@@ -1185,6 +1205,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     c.W = W;
     c.nq = nq;
     c.ready_q = -1;
+    c.ready_mask = 0;
     c.dumps = 0;
     const bool epilogue = warp == kEpilogueWarp;
 
