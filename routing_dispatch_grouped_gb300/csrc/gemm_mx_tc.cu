@@ -43,9 +43,9 @@
 //   warps 2..9  epilogue, two warps per TMEM lane quarter, each over half of the columns.
 // The accumulator is single-buffered (the scale columns take the room of a second one), so each
 // epilogue warp first loads its 128 accumulator columns into registers and releases the
-// accumulator: the next tile's MMAs then overlap the SwiGLU, the MXFP8 rounding and the stores. Every mbarrier wait is bounded in time;
-// on expiry the kernel records MOE_ERR_TIMEOUT, lets its own copies and MMAs finish, frees TMEM
-// and returns.
+// accumulator: the next tile's MMAs then overlap the SwiGLU, the MXFP8 rounding and the
+// stores. Every mbarrier wait is bounded in time; on expiry the kernel records MOE_ERR_TIMEOUT,
+// lets its own copies and MMAs finish, frees TMEM and returns.
 #include <mutex>
 
 #include "mx_tc.cuh"
