@@ -293,3 +293,33 @@ def test_mx_tc_mixtral_cut_to_4_experts():
     assert np.array_equal(xq, ref["x_sorted"])
     assert err_rms(f64(v["y_sorted"]), ref["y_sorted"]) <= 2e-2
     assert err_rms(f64(out), ref["out"]) <= 2e-2
+
+
+def test_mx_tc_is_deterministic_and_replays_in_a_graph():
+    """Every sum of the tensor-core MX layer has a fixed order: two calls give the same bits, and
+    the call captured once in a CUDA graph (no host synchronisation inside) replays to them."""
+    cfg = synth.MoEConfig("graph", 600, 512, 8, 2, 384, bf16, bias="normal0.5")
+    inp = synth.make_inputs(cfg, DEV)
+    mgu = moe.quantize_weights_mx_tc(inp["w_gate_up"], moe.W_GATE_UP)
+    mdn = moe.quantize_weights_mx_tc(inp["w_down"], moe.W_DOWN)
+    out1, ids, w, ws = moe.moe_forward_mx_tc(inp["x"], inp["logits"], mgu, mdn, cfg.k)
+    out2 = torch.empty_like(out1)
+    moe.moe_forward_mx_tc(inp["x"], inp["logits"], mgu, mdn, cfg.k, out=out2, topk_ids=ids,
+                          topk_weights=w, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+    out3 = torch.zeros_like(out1)
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            moe.moe_forward_mx_tc(inp["x"], inp["logits"], mgu, mdn, cfg.k, out=out3,
+                                  topk_ids=ids, topk_weights=w, workspace=ws, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(2):
+        out3.zero_()
+        graph.replay()
+    torch.cuda.synchronize()
+    assert moe.moe_read_device_status(ws) == 0
+    assert torch.equal(out1.view(torch.int16), out3.view(torch.int16))
