@@ -469,8 +469,8 @@ class Layer:
                           dtype=torch.uint8, device=self.dev)
 
         def e2e_step():
-            # moe_forward_host: the library copies x and logits in and the output back on the
-            # stream, around the same chain
+            # moe_forward_host: the kernels read the pinned x and logits and write the pinned
+            # output in place
             moe.moe_forward_host(self.x_h, self.lg_h, wts["w_gate_up"], wts["w_down"], k,
                                  cfg.score_fn, self.flags, wts["w_shared_gate_up"],
                                  wts["w_shared_down"], out=self.out_h, workspace=hws,
@@ -486,8 +486,9 @@ class Layer:
                 "h2d_bytes_per_step": self.x_h.numel() * self.x_h.element_size()
                 + self.lg_h.numel() * self.lg_h.element_size(),
                 "d2h_bytes_per_step": self.out_h.numel() * self.out_h.element_size(),
-                "path": "moe_forward_host: pinned host x and logits in, the layer, out back to "
-                        "pinned host memory, all enqueued by the library on the timed stream"}
+                "path": "moe_forward_host on pinned host x, logits and out: the kernels read x "
+                        "and the logits and write out across NVLink-C2C (x staged by one copy "
+                        "when a shared expert runs), all on the timed stream"}
 
     def roofline(self):
         """Roofline of the dominant kernel: the gate_up grouped GEMM (2/3 of the expert FLOPs)

@@ -301,14 +301,17 @@ size_t moe_forward_workspace_size(int T, int d, int E, int k, int I, int Is, moe
 
 /*
  * moe_forward_host - moe_forward for a caller whose activations live in host memory: x_host
- *   (dt [T, d]) and logits_host (float [T, E]) are copied to the device, the layer runs as in
- *   moe_forward, and the output is copied back to out_host (dt [T, d]), all enqueued on
- *   `stream` (cudaMemcpyAsync, one per buffer; the call does not wait for them). The host
- *   buffers should be page-locked (pinned): pageable memory works, but then the copies block
- *   the calling thread. The router's ids and weights stay in the workspace. Weights, flags and
- *   errors as moe_forward; workspace: moe_forward_host_workspace_size(...) bytes, 256-byte
- *   aligned (the forward workspace followed by device copies of x, logits, out, ids and
- *   weights).
+ *   (dt [T, d]), logits_host (float [T, E]) and out_host (dt [T, d]). All work is enqueued on
+ *   `stream`; the call does not wait for it, so synchronise the stream before reading out_host.
+ *   A buffer that is page-locked and mapped (cudaHostAlloc, cudaMallocHost, cudaHostRegister;
+ *   reached over NVLink-C2C on a Grace-Blackwell node) is used in place: the route kernel reads
+ *   the logits, the dispatch (or the one-kernel decode layer) reads x and the combine writes
+ *   out there, with no staging copy. Any other buffer goes through the workspace with one
+ *   cudaMemcpyAsync (pageable memory makes that copy block the calling thread). With a shared
+ *   expert (Is > 0) x is always staged, since its gate_up loads x with TMA. The router's ids
+ *   and weights stay in the workspace. Weights, flags and errors as moe_forward; workspace:
+ *   moe_forward_host_workspace_size(...) bytes, 256-byte aligned (the forward workspace
+ *   followed by device room for x, logits, out, ids and weights).
  */
 size_t moe_forward_host_workspace_size(int T, int d, int E, int k, int I, int Is, moe_dtype dt);
 moe_status moe_forward_host(const void* x_host, const float* logits_host, moe_dtype dt, int T,

@@ -631,6 +631,17 @@ size_t moe_forward_host_workspace_size(int T, int d, int E, int k, int I, int Is
     return host_layout(T, d, E, k, I, Is, dt).total;
 }
 
+// Device address of a page-locked, mapped host buffer (one the GPU reaches over NVLink-C2C),
+// or nullptr for pageable or device memory and on a failed query.
+static void* mapped_host_address(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 moe_status moe_forward_host(const void* x_host, const float* logits_host, moe_dtype dt, int T,
                             int d, int E, int k, int I, moe_score_fn score_fn, unsigned flags,
                             const void* w_gate_up, const void* w_down,
@@ -647,18 +658,32 @@ moe_status moe_forward_host(const void* x_host, const float* logits_host, moe_dt
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     cudaStream_t s = (cudaStream_t)stream;
     const size_t b = dt == MOE_BF16 ? 2 : 4;
-    if ((st = launch_status(cudaMemcpyAsync(ws + L.x, x_host, (size_t)T * d * b,
-                                            cudaMemcpyHostToDevice, s))) != MOE_OK)
+    // A page-locked buffer is used in place: the route kernel reads the logits, the dispatch
+    // (or the decode kernel) reads x and the combine writes out across NVLink-C2C, each once
+    // and in token order, so no staging copy runs for it. x is staged whenever a shared
+    // expert runs: its gate_up loads x through TMA, which is kept to device memory.
+    const void* x_dev = Is == 0 ? mapped_host_address(x_host) : nullptr;
+    const void* logits_dev = mapped_host_address(logits_host);
+    void* out_dev = mapped_host_address(out_host);
+    if (!x_dev) {
+        if ((st = launch_status(cudaMemcpyAsync(ws + L.x, x_host, (size_t)T * d * b,
+                                                cudaMemcpyHostToDevice, s))) != MOE_OK)
+            return st;
+        x_dev = ws + L.x;
+    }
+    if (!logits_dev) {
+        if ((st = launch_status(cudaMemcpyAsync(ws + L.logits, logits_host, (size_t)T * E * 4,
+                                                cudaMemcpyHostToDevice, s))) != MOE_OK)
+            return st;
+        logits_dev = ws + L.logits;
+    }
+    if ((st = forward_impl(x_dev, static_cast<const float*>(logits_dev), dt, T, d, E, k, I,
+                           score_fn, flags, w_gate_up, w_down, w_shared_gate_up, w_shared_down,
+                           Is, reinterpret_cast<int32_t*>(ws + L.ids),
+                           reinterpret_cast<float*>(ws + L.w), out_dev ? out_dev : ws + L.out,
+                           workspace, L.fwd, stream, false)) != MOE_OK)
         return st;
-    if ((st = launch_status(cudaMemcpyAsync(ws + L.logits, logits_host, (size_t)T * E * 4,
-                                            cudaMemcpyHostToDevice, s))) != MOE_OK)
-        return st;
-    if ((st = forward_impl(ws + L.x, reinterpret_cast<const float*>(ws + L.logits), dt, T, d, E,
-                           k, I, score_fn, flags, w_gate_up, w_down, w_shared_gate_up,
-                           w_shared_down, Is, reinterpret_cast<int32_t*>(ws + L.ids),
-                           reinterpret_cast<float*>(ws + L.w), ws + L.out, workspace, L.fwd,
-                           stream, false)) != MOE_OK)
-        return st;
+    if (out_dev) return MOE_OK;
     return launch_status(
         cudaMemcpyAsync(out_host, ws + L.out, (size_t)T * d * b, cudaMemcpyDeviceToHost, s));
 }

@@ -361,8 +361,8 @@ def moe_forward_host_workspace_size(T, d, E, k, I, Is, dtype) -> int:
 def moe_forward_host(x_host, logits_host, w_gate_up, w_down, k, score_fn=SOFTMAX,
                      flags=RENORMALIZE, w_shared_gate_up=None, w_shared_down=None, out=None,
                      workspace=None, stream=None, device=None):
-    """The whole layer on host activations (CPU tensors, pinned for asynchronous copies): x and
-    logits are copied in and the output copied back by the library on `stream`. Returns
+    """The whole layer on host activations (CPU tensors): pinned ones are read and written in
+    place by the kernels, pageable ones copied in and out by the library on `stream`. Returns
     (out_host, workspace); synchronise the stream before reading out_host."""
     if x_host.is_cuda or logits_host.is_cuda:
         raise ValueError("moe_forward_host takes host tensors")

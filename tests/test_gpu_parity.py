@@ -363,11 +363,15 @@ def test_forward_256_experts_matches_oracle():
     assert err_rms(f64(out), ref["out"]) <= TOL[cfg.dtype]
 
 
-@pytest.mark.parametrize("name,T", [("mixtral_8x7b", 600), ("decode", 8), ("llama4_scout", 300)])
-def test_forward_host_equals_forward(name, T):
-    """moe_forward_host (host activations, copies enqueued by the library) returns exactly what
-    moe_forward returns on the same inputs: the chain, the one-kernel decode layer and a shared
-    expert."""
+@pytest.mark.parametrize("name,T,mem", [("mixtral_8x7b", 600, "pinned"), ("decode", 8, "pinned"),
+                                        ("llama4_scout", 300, "pinned"),
+                                        ("mixtral_8x7b", 600, "pageable"),
+                                        ("decode", 8, "pageable"), ("mixtral_8x7b", 600, "mixed")])
+def test_forward_host_equals_forward(name, T, mem):
+    """moe_forward_host (host activations) returns exactly what moe_forward returns on the same
+    inputs: the chain, the one-kernel decode layer and a shared expert. Page-locked buffers are
+    read and written in place by the kernels; pageable ones go through the library's staging
+    copies; "mixed" has x page-locked and the logits and out pageable."""
     cfg = _cfg(name, T)
     inp = synth.make_inputs(cfg, DEV)
     flags = (moe.RENORMALIZE if cfg.renormalize else 0) | (moe.SCALE_INPUT if cfg.scale_input
@@ -375,10 +379,15 @@ def test_forward_host_equals_forward(name, T):
     out, _, _, ws = moe.moe_forward(inp["x"], inp["logits"], inp["w_gate_up"], inp["w_down"],
                                     cfg.k, cfg.score_fn, flags, inp["w_shared_gate_up"],
                                     inp["w_shared_down"])
-    xh, lh = inp["x"].cpu().pin_memory(), inp["logits"].cpu().pin_memory()
+    xh, lh = inp["x"].cpu(), inp["logits"].cpu()
+    outh = torch.empty(cfg.T, cfg.d, dtype=cfg.dtype)
+    if mem in ("pinned", "mixed"):
+        xh = xh.pin_memory()
+    if mem == "pinned":
+        lh, outh = lh.pin_memory(), outh.pin_memory()
     outh, hws = moe.moe_forward_host(xh, lh, inp["w_gate_up"], inp["w_down"], cfg.k,
                                      cfg.score_fn, flags, inp["w_shared_gate_up"],
-                                     inp["w_shared_down"])
+                                     inp["w_shared_down"], out=outh)
     torch.cuda.synchronize()
     assert moe.moe_read_device_status(hws) == 0
     assert torch.equal(outh, out.cpu())
