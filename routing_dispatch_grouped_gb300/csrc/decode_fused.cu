@@ -41,7 +41,20 @@
 //     At the end of an output block it either writes bf16 out (sole contributor) or leaves
 //     the block's per-token partial; the last contributor sums them in block order, one
 //     rounding.
-// While a block waits, its producer keeps streaming down weights. The launch is cooperative,
+// While a block waits, its producer keeps streaming down weights.
+//
+// Owner layout (bf16, when every touched h block can have a block of its own and at least one
+// block is left over: T = 1 at the decode shape). Block g streams the gate_up items of h
+// block g, then, through the same ring, the down weight rows of those 64 h columns for every
+// output column (items of four [64 K][64 column] boxes, 256 output columns each). Its
+// epilogue warp stores h as above, and also keeps it in shared memory, so the consumer warps
+// multiply the down items by it at once: h crosses no SM and no flag is waited on. Each
+// consumer writes its item's weighted sums per token row as an fp32 partial and bumps the
+// 256-column group's counter. The remaining blocks then sum, per 64 output columns and per
+// token, the partials of its k slots (slot order) and the expert's h blocks (block order), and
+// store bf16 out: one rounding, in a fixed order.
+//
+// The launch is cooperative,
 // so every block is resident and the waits end. Every sum runs in an order fixed by the sizes
 // alone: results do not depend on timing. The counters are zeroed by the caller's memset of
 // the workspace head that precedes the launch.
@@ -87,7 +100,7 @@ constexpr size_t kOffOut = kOffRed + kRedFloats * 4;
 constexpr size_t kOffLists = kOffOut + kOutFloats * 4;
 constexpr size_t kListInts = 3 * kMaxE + 2 * kDecodeFusedMaxRows;
 constexpr size_t kOffBars = kOffLists + kListInts * 4;
-constexpr size_t kSmemBytes = kOffBars + (2 * kStages + 2) * 8 + 64 + 1024;  // + align slack
+constexpr size_t kSmemBytes = kOffBars + (2 * kStages + 3) * 8 + 64 + 1024;  // + align slack
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a block may use");
 
 struct Params {
@@ -106,6 +119,10 @@ struct Params {
     int* cnt_a;              // [R * nbh] contributors arrived, per h block
     int* hflag;              // [R * nbh] h block stored
     int* cnt_b;              // [nbd] per output block
+    // owner layout (see the schedule): down partials [nbh][R][d] (weighted, fp32; null when
+    // the layout cannot occur) and, per 256 output columns, the owners done with them
+    float* part_c;
+    int* cnt_c;
     int* status;
     int T, d, E, k, I, R;
     int score_fn, renorm;
@@ -144,6 +161,9 @@ struct Ctx {
     int slot_off;            // partial slot offset of the current wave (see the schedule)
     int W, nq;               // waves, touched experts
     int ready_q;             // touched expert whose h blocks ready_mask covers (-1: none)
+    bool owner;              // owner layout: h stays in this block (h_s), no flags
+    __nv_bfloat16* h_s;      // [rows of the block's expert][64]: its h block
+    uint64_t* h_full;        // h_s written
     uint64_t ready_mask;     // h blocks of ready_q this warp has seen stored (all ones: every)
     int dumps;               // hand-overs so far
 };
@@ -337,10 +357,12 @@ __device__ __forceinline__ void item_b(Ctx& c, const Params& p, int i, int kc,
     release_stage(c);
 }
 
-__device__ __forceinline__ void store_h(const Params& p, const Ctx& c, int row, int hc, float g,
-                                        float u) {
+__device__ __forceinline__ __nv_bfloat16 store_h(const Params& p, const Ctx& c, int row, int hc,
+                                                 float g, float u) {
     const float s = p.scale_input ? c.s_w[row] : 1.0f;
-    p.h[(size_t)row * p.I + hc] = __float2bfloat16_rn(silu(g * s) * (u * s));
+    const __nv_bfloat16 v = __float2bfloat16_rn(silu(g * s) * (u * s));
+    p.h[(size_t)row * p.I + hc] = v;
+    return v;
 }
 
 // MX layers: h rounded to MXFP8 (blocks of 32 along I). Called by all 32 lanes of the epilogue
@@ -737,6 +759,151 @@ __device__ void group_b(Ctx& c, const Params& p, int q, int i0, int kc0, int kc1
     }
 }
 
+// ---- owner layout: down partials of the block's own h block ----
+// Item g4 of h block (q, jb): W_down rows [64 jb, 64 jb + 64) x output columns
+// [256 g4, 256 g4 + 256), four [64 K][64 column] boxes; h block from h_s as the B side. Each
+// token row's sums, times its routing weight, go to part_c[jb][row], then the group's counter
+// is bumped (release) for the summing blocks.
+template <int NTILE>
+__device__ void owner_down(Ctx& c, const Params& p, int q, int jb, int i0, int n4) {
+    const int row0 = c.s_off[q], tq = c.s_tq[q];
+    bool have_h = false;
+    uint32_t b[4][NTILE][2];
+    for (int g4 = (c.warp - i0 % kStages + kStages) % kStages; g4 < n4; g4 += kStages) {
+        const int i = i0 + g4;
+        if (!have_h) {
+            if (!mbar_wait(c.h_full, 0u, c.flags, kWaitLimitNs)) {
+                set_status(p.status, MOE_ERR_TIMEOUT);
+                c.flags[0] = 1;
+            }
+            // B fragments: lane l holds token row 8 n + l/4, h columns 16 ks + 2 (l%4) (+8)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+                for (int n = 0; n < NTILE; ++n) {
+                    const int r = 8 * n + (c.lane >> 2);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int kk = 16 * ks + 8 * hh + 2 * (c.lane & 3);
+                        b[ks][n][hh] =
+                            r < tq ? *reinterpret_cast<const uint32_t*>(c.h_s + r * 64 + kk) : 0u;
+                    }
+                }
+            have_h = true;
+        }
+        float acc[16][NTILE][4];
+#pragma unroll
+        for (int m = 0; m < 16; ++m)
+#pragma unroll
+            for (int n = 0; n < NTILE; ++n)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[m][n][j] = 0.0f;
+        if (take_stage(c, p, i)) {
+            const uint32_t stage = c.stage0 + (uint32_t)c.warp * kStageBytes;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks)
+#pragma unroll
+                    for (int mt = 0; mt < 4; ++mt)
+                        mma_step<NTILE>(stage + (uint32_t)j * 8192u, 16 * ks, 16 * mt, c.lane,
+                                        b[ks], acc[4 * j + mt]);
+        }
+        release_stage(c);
+        // C fragment: m = output column 16 m + l/4 (+8), n = token row 8 n + 2 (l%4) (+1)
+#pragma unroll
+        for (int n = 0; n < NTILE; ++n)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const int r = 8 * n + 2 * (c.lane & 3) + (jj & 1);
+                if (r >= tq) continue;
+                const float wgt = p.scale_input ? 1.0f : c.s_w[row0 + r];
+                float* dst = p.part_c + ((size_t)jb * p.R + row0 + r) * p.d;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) {
+                    const int col = 256 * g4 + 16 * m + (c.lane >> 2) + ((jj & 2) ? 8 : 0);
+                    if (col < p.d) __stcg(dst + col, wgt * acc[m][n][jj]);
+                }
+            }
+        __syncwarp();
+        if (c.lane == 0)
+            asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.cnt_c + g4) : "memory");
+    }
+}
+
+// Owner layout, the blocks past the owners: output block cb (64 columns) of every token is
+// the sum over its k slots (slot order) and the expert's h blocks (jb order) of part_c, taken
+// once all owners are done with its 256-column group. 224 threads (the consumer warps and the
+// epilogue warp): thread (grp, c4) sums terms grp, grp + 14, ... of four columns; the 14
+// partial sums are then added in group order.
+__device__ void owner_reduce(const Params& p, volatile int* flags, float* red, const int* s_p2s,
+                             int tid, int first_cb, int stride, int owners) {
+    constexpr int kGroups = 14;
+    const int c4 = tid & 15, grp = tid >> 4;
+    const int terms = p.k * p.nbh;
+    float4* red4 = reinterpret_cast<float4*>(red);
+    for (int cb = first_cb; cb < p.nbd; cb += stride) {
+        if (tid == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire(p.cnt_c + (cb >> 2)) < owners) {
+                if (flags[0] || globaltimer_ns() - t0 > kWaitLimitNs) {
+                    set_status(p.status, MOE_ERR_TIMEOUT);
+                    flags[0] = 1;
+                    break;
+                }
+            }
+        }
+        asm volatile("bar.sync 1, 224;" ::: "memory");
+        if (flags[0]) return;
+        const int col = cb * 64 + 4 * c4;
+        for (int t = 0; t < p.T; ++t) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (col < p.d) {
+                for (int m0 = grp; m0 < terms; m0 += 8 * kGroups) {
+                    float4 v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int m = m0 + u * kGroups;
+                        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (m < terms) {
+                            const int j = m / p.nbh, jb = m - j * p.nbh;
+                            const int pos = s_p2s[t * p.k + j];
+                            v[u] = __ldcg(reinterpret_cast<const float4*>(
+                                p.part_c + ((size_t)jb * p.R + pos) * p.d + col));
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        acc.x += v[u].x;
+                        acc.y += v[u].y;
+                        acc.z += v[u].z;
+                        acc.w += v[u].w;
+                    }
+                }
+            }
+            red4[grp * 16 + c4] = acc;
+            asm volatile("bar.sync 1, 224;" ::: "memory");
+            if (tid < 16 && col < p.d) {
+                float4 s4 = red4[c4];
+                for (int g = 1; g < kGroups; ++g) {
+                    const float4 v = red4[g * 16 + c4];
+                    s4.x += v.x;
+                    s4.y += v.y;
+                    s4.z += v.z;
+                    s4.w += v.w;
+                }
+                __nv_bfloat162 lo = __floats2bfloat162_rn(s4.x, s4.y);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(s4.z, s4.w);
+                uint2 packed;
+                packed.x = *reinterpret_cast<uint32_t*>(&lo);
+                packed.y = *reinterpret_cast<uint32_t*>(&hi);
+                *reinterpret_cast<uint2*>(p.out + (size_t)t * p.d + col) = packed;
+            }
+            asm volatile("bar.sync 1, 224;" ::: "memory");
+        }
+    }
+}
+
 // ================= epilogue side (one warp) =================
 
 // h of group g (rows of expert q at row0, h block jb) from the partials of its contributors,
@@ -797,17 +964,27 @@ __device__ void epi_a(Ctx& c, const Params& p, int q, int jb, int g, int b_first
                     if (whole) uu += rr[64];
                 }
                 if (whole) {
-                    if (p.mx)
+                    if (p.mx) {
                         store_h_mx(p, c, row0 + pass * kPass + t, jb * 64 + col, v, uu,
                                    jb * 64 + col < p.I);
-                    else if (jb * 64 + col < p.I)
-                        store_h(p, c, row0 + pass * kPass + t, jb * 64 + col, v, uu);
+                    } else {
+                        const __nv_bfloat16 hv =
+                            jb * 64 + col < p.I
+                                ? store_h(p, c, row0 + pass * kPass + t, jb * 64 + col, v, uu)
+                                : __float2bfloat16_rn(0.0f);
+                        if (c.owner) c.h_s[(pass * kPass + t) * 64 + col] = hv;
+                    }
                 } else {
                     __stcg(part + (size_t)(pass * kPass + t) * 128 + col, v);
                 }
             }
             epi_give(c);
         }
+    }
+    if (c.owner) {  // the down partials of this h block are computed in this block
+        __syncwarp();
+        if (c.lane == 0) mbar_arrive(c.h_full);
+        return;
     }
     bool stored = whole;
     if (!whole && epi_arrive_last(c, p.cnt_a + g, contributors(c.nA, c.GA, b_first, b_last))) {
@@ -930,7 +1107,8 @@ __device__ __forceinline__ void by_rows(int tq, F&& f) {
 template <bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
-                    const __grid_constant__ CUtensorMap tmD, Params p, int vpl) {
+                    const __grid_constant__ CUtensorMap tmD,
+                    const __grid_constant__ CUtensorMap tmO, Params p, int vpl) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -939,35 +1117,27 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     int* s_tq = s_off + kMaxE;
     int* s_tok = s_tq + kMaxE;
     float* s_w = reinterpret_cast<float*>(s_tok + kDecodeFusedMaxRows);
+    // slot -> sorted row, for the owner layout's summing blocks: the last 1 KB of the stage
+    // ring, which the routing scratch (at its start) does not reach and the summing blocks
+    // never fill with copies
+    int* s_p2s = reinterpret_cast<int*>(smem + (size_t)kStages * kStageBytes) -
+                 kDecodeFusedMaxRows;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
     uint64_t* empty = full + kStages;
     uint64_t* red_full = empty + kStages;
     uint64_t* red_empty = red_full + 1;
-    volatile int* flags = reinterpret_cast<volatile int*>(red_empty + 1);
+    uint64_t* h_full = red_empty + 1;
+    volatile int* flags = reinterpret_cast<volatile int*>(h_full + 1);
     // flags: [0] a wait timed out (every bounded wait gives up at once after that; the status
     // word says so and the results are void), [2] number of touched experts.
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
-        }
-        mbar_init(red_full, kConsumerWarps);
-        mbar_init(red_empty, 1);
-        fence_barrier_init();
-        for (int f = 0; f < 4; ++f) flags[f] = 0;
-    }
-    if (!MX && warp == kProducerWarp && lane == 0) {  // MX items are plain bulk copies
-        tma_prefetch_desc(&tmGU);
-        tma_prefetch_desc(&tmD);
-    }
-    float* outacc = reinterpret_cast<float*>(smem + kOffOut);
-    for (int i = threadIdx.x; i < kOutFloats; i += blockDim.x) outacc[i] = 0.0f;
     griddep_wait();
 
     // ---- router top-k and dispatch indices, in every block (scratch in the stage buffers,
     // which no copy uses yet). Same warp router and counting sort as the stand-alone kernels.
+    // Warp w routes tokens w, w + 8, ... at once (the logits load heads the critical path);
+    // the set-up below runs beside it.
     const int R = p.R, E = p.E, nch = (R + 31) / 32;
     int* ids_s = reinterpret_cast<int*>(smem);
     float* w_s = reinterpret_cast<float*>(ids_s + kDecodeFusedMaxRows);
@@ -975,7 +1145,6 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     int* cnt_s = rank_s + kDecodeFusedMaxRows;
     int* off_s = cnt_s + kMaxE;
     int* chunk_s = off_s + kMaxE + 32;  // [chunk of 32 slots][E]: counts, then bases
-    for (int i = threadIdx.x; i < nch * E; i += blockDim.x) chunk_s[i] = 0;
     for (int t = warp; t < p.T; t += kWarps) {
         const float* row = p.logits + (size_t)t * E;
         int id;
@@ -991,6 +1160,25 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
             w_s[t * p.k + lane] = wt;
         }
     }
+    if (warp == kEpilogueWarp && lane == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(red_full, kConsumerWarps);
+        mbar_init(red_empty, 1);
+        mbar_init(h_full, 1);
+        fence_barrier_init();
+        for (int f = 0; f < 4; ++f) flags[f] = 0;
+    }
+    if (!MX && warp == kProducerWarp && lane == 0) {  // MX items are plain bulk copies
+        tma_prefetch_desc(&tmGU);
+        tma_prefetch_desc(&tmD);
+        tma_prefetch_desc(&tmO);
+    }
+    float* outacc = reinterpret_cast<float*>(smem + kOffOut);
+    for (int i = threadIdx.x; i < kOutFloats; i += blockDim.x) outacc[i] = 0.0f;
+    for (int i = threadIdx.x; i < nch * E; i += blockDim.x) chunk_s[i] = 0;
     __syncthreads();
     for (int ch = warp; ch < nch; ch += kWarps) {
         const int s = ch * 32 + lane;
@@ -1053,6 +1241,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
         const int pos = off_s[e] + chunk_s[(s >> 5) * E + e] + rank_s[s];
         s_tok[pos] = s / p.k;
         s_w[pos] = w_s[s];
+        s_p2s[s] = pos;
         if (writer) {
             p.topk_ids[s] = e;
             p.topk_w[s] = w_s[s];
@@ -1080,10 +1269,18 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     // sums, h flagged as soon as it is stored) and blocks [ngA, G) take the down items,
     // prefetching them while the gate_up items stream.
     const int ngA = nq * p.nbh;
+    // Owner layout (bf16, one wave, an SM for every touched h block and at least one left
+    // over): block g < ngA streams the gate_up items of h block g and then the down weight
+    // rows of those 64 h columns, all output columns (n4 items of four 64-column boxes), and
+    // multiplies them by h from its own shared memory; blocks [ngA, G) sum the resulting
+    // partials per output block. No h or partial crosses SMs before the final sums.
+    const bool owner = !MX && W == 1 && ngA < G && p.part_c != nullptr;
+    const int n4 = (p.nbd + 3) / 4;
     const bool whole_groups = W == 1 && ngA < G &&
-                              (long long)p.nbd * nq * p.nkb * 4 <= 5ll * p.nka * (G - ngA);
+                              (owner || (long long)p.nbd * nq * p.nkb * 4 <=
+                                            5ll * p.nka * (G - ngA));
     const int GA = whole_groups ? ngA : G;
-    const int B0 = whole_groups ? ngA : 0, GB = G - B0;
+    const int B0 = owner ? G : whole_groups ? ngA : 0, GB = G - B0;
     const int ba = b < GA ? b : GA;            // gate_up range index (GA: empty)
     const int bb = b >= B0 ? b - B0 : GB;      // down range index (GB: empty)
     auto wave_a = [&](int w, int& q_lo, int& n) {
@@ -1149,6 +1346,22 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                     }
                 }
             }
+            if (owner && ba < GA) {
+                // the down weight rows of this block's h block: output columns 256 g4 ..
+                const int q = ba / p.nbh, jb = ba % p.nbh, e = s_eq[q];
+                for (int g4 = 0; ok && g4 < n4; ++g4) {
+                    uint32_t dst;
+                    uint64_t* bar;
+                    if (!(ok = next_stage(dst, bar, kStageBytes))) break;
+                    if (p.packed) {
+                        tma_load_3d_hint(dst, &tmO, bar, 0, 64 * jb, e * p.dn_nb + 4 * g4, pol);
+                    } else {
+                        for (int j = 0; j < 4; ++j)
+                            tma_load_3d_hint(dst + 8192u * j, &tmO, bar, 64 * (4 * g4 + j),
+                                             64 * jb, e, pol);
+                    }
+                }
+            }
             for (int w = 0; ok && w < W; ++w) {
                 const int q_lo = range_lo(nq, w, W);
                 const int perC = (range_lo(nq, w + 1, W) - q_lo) * p.nkb, n = p.nbd * perC;
@@ -1207,6 +1420,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     c.ready_q = -1;
     c.ready_mask = 0;
     c.dumps = 0;
+    c.owner = owner;
+    c.h_s = reinterpret_cast<__nv_bfloat16*>(outacc);  // the combine accumulator is unused
+    c.h_full = h_full;
     const bool epilogue = warp == kEpilogueWarp;
 
     // consumers (warp w: the items of stage w) and the epilogue warp walk the same groups
@@ -1234,6 +1450,20 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
             u += kc1 - kc0;
             i0 += kc1 - kc0;
         }
+    }
+    if (owner) {
+        if (b < ngA) {
+            if (!epilogue) {
+                const int q = b / p.nbh, jb = b % p.nbh;
+                by_rows(s_tq[q], [&](auto tag) {
+                    owner_down<decltype(tag)::value>(c, p, q, jb, i0, n4);
+                });
+            }
+        } else {
+            const int tid = (warp < kProducerWarp ? warp : warp - 1) * 32 + lane;
+            owner_reduce(p, flags, c.red, s_p2s, tid, b - ngA, G - ngA, ngA);
+        }
+        return;
     }
     for (int w = 0; w < W; ++w) {
         const WaveB v = wave_b(c, p, w);
@@ -1279,7 +1509,7 @@ DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I, bool mx) {
         L.nkb = (I + kKcB - 1) / kKcB;
     }
     auto up = [](size_t v) { return (v + 255) / 256 * 256; };
-    L.counter_bytes = up((2 * R * L.nbh + L.nbd) * 4);
+    L.counter_bytes = up((2 * R * L.nbh + L.nbd + (L.nbd + 3) / 4) * 4);
     // partial slots: contributor block b of group g writes slot b + g (unique: a block's groups
     // are consecutive and the next block starts at or after its last one)
     // (gate_up slot b + g + w G and down slot b + c + w (G + nbd) for wave w: unique across
@@ -1288,6 +1518,12 @@ DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I, bool mx) {
     L.part_b = up(((size_t)kDecodeWaves * kDecodeFusedMaxGrid + R * L.nbh) * T * 128 * 4);
     L.part_bytes = L.part_b + up((size_t)kDecodeWaves * (kDecodeFusedMaxGrid + L.nbd) * T *
                                  64 * 4);
+    // owner layout (bf16; it needs fewer touched h blocks than SMs): [nbh][R][d] fp32
+    L.part_c = 0;
+    if (!mx && L.nbh < kDecodeFusedMaxGrid) {
+        L.part_c = L.part_bytes;
+        L.part_bytes += up((size_t)L.nbh * R * d * 4);
+    }
     return L;
 }
 
@@ -1307,7 +1543,7 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
 
     const DecodeFusedLayout L = decode_fused_layout(a.T, a.d, a.k, a.I, a.mx);
     const int R = a.T * a.k;
-    CUtensorMap tmGU = {}, tmD = {};  // MX: unused (items are plain bulk copies)
+    CUtensorMap tmGU = {}, tmD = {}, tmO = {};  // MX: unused (items are plain bulk copies)
     const cuuint32_t box_a[3] = {64, kKcA, 1}, box_b[3] = {64, kKcB, 1};
     bool ok = true;
     if (a.mx) {
@@ -1318,15 +1554,20 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
         const cuuint64_t gu_str[2] = {128, (cuuint64_t)gg.kpad * 128};
         const cuuint64_t dn_dims[3] = {64, (cuuint64_t)gd.kpad, (cuuint64_t)a.E * gd.nb};
         const cuuint64_t dn_str[2] = {128, (cuuint64_t)gd.kpad * 128};
+        // owner layout: 64 K rows of four consecutive 64-column blocks
+        const cuuint32_t box_o[3] = {64, 64, 4};
         ok = encode_tensor_map_bf16(&tmGU, a.w_gate_up, 3, gu_dims, gu_str, box_a) &&
-             encode_tensor_map_bf16(&tmD, a.w_down, 3, dn_dims, dn_str, box_b);
+             encode_tensor_map_bf16(&tmD, a.w_down, 3, dn_dims, dn_str, box_b) &&
+             encode_tensor_map_bf16(&tmO, a.w_down, 3, dn_dims, dn_str, box_o);
     } else {
         const cuuint64_t gu_dims[3] = {2 * (cuuint64_t)a.I, (cuuint64_t)a.d, (cuuint64_t)a.E};
         const cuuint64_t gu_str[2] = {4 * (cuuint64_t)a.I, 4 * (cuuint64_t)a.I * a.d};
         const cuuint64_t dn_dims[3] = {(cuuint64_t)a.d, (cuuint64_t)a.I, (cuuint64_t)a.E};
         const cuuint64_t dn_str[2] = {2 * (cuuint64_t)a.d, 2 * (cuuint64_t)a.d * a.I};
+        const cuuint32_t box_o[3] = {64, 64, 1};  // owner layout: four loads per item
         ok = encode_tensor_map_bf16(&tmGU, a.w_gate_up, 3, gu_dims, gu_str, box_a) &&
-             encode_tensor_map_bf16(&tmD, a.w_down, 3, dn_dims, dn_str, box_b);
+             encode_tensor_map_bf16(&tmD, a.w_down, 3, dn_dims, dn_str, box_b) &&
+             encode_tensor_map_bf16(&tmO, a.w_down, 3, dn_dims, dn_str, box_o);
     }
     if (!ok) return cudaErrorInvalidValue;
 
@@ -1345,6 +1586,8 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
     p.cnt_a = a.counters;
     p.hflag = a.counters + (size_t)R * L.nbh;
     p.cnt_b = a.counters + (size_t)2 * R * L.nbh;
+    p.cnt_c = p.cnt_b + L.nbd;
+    p.part_c = (!a.mx && L.part_c) ? reinterpret_cast<float*>(parts + L.part_c) : nullptr;
     p.part_a = reinterpret_cast<float*>(parts + L.part_a);
     p.part_b = reinterpret_cast<float*>(parts + L.part_b);
     p.status = a.status;
@@ -1397,8 +1640,8 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return a.mx ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<true>, tmGU, tmD, p, vpl)
-                : cudaLaunchKernelEx(&cfg, decode_fused_kernel<false>, tmGU, tmD, p, vpl);
+    return a.mx ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<true>, tmGU, tmD, tmO, p, vpl)
+                : cudaLaunchKernelEx(&cfg, decode_fused_kernel<false>, tmGU, tmD, tmO, p, vpl);
 }
 
 }  // namespace rdg

@@ -361,6 +361,7 @@ struct DecodeFusedLayout {
     int nbh, nka, nbd, nkb;  // h blocks, gate_up K chunks, output blocks, down K chunks
     size_t counter_bytes;    // int counters
     size_t part_a, part_b, part_bytes;  // partial sums: offsets and total size
+    size_t part_c;                      // owner-layout down partials (0: none)
 };
 DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I, bool mx = false);
 struct DecodeFusedArgs {

@@ -401,7 +401,8 @@ def forward_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is, dtype, mx=False
     nchunks = (R + 255) // 256
     # decode batches run the one-kernel layer, whose counters follow the status word
     fused = dtype == torch.bfloat16 and Is == 0 and 1 <= T <= 16 and R <= 256
-    fcnt = (2 * R * ((I + 63) // 64) + (d + 63) // 64) * 4 if fused else 0
+    nbd = (d + 63) // 64
+    fcnt = (2 * R * ((I + 63) // 64) + nbd + (nbd + 3) // 4) * 4 if fused else 0
     sizes = [("fused_counters", fcnt), ("counts", E * 4), ("offsets", (E + 1) * 4), ("chunk", nchunks * E * 4),
              ("sorted_to_slot", R * 4), ("slot_to_sorted", R * 4), ("x_sorted", R * d * b),
              ("h", R * I * b), ("y_sorted", R * d * 4), ("h_shared", T * Is * b),

@@ -106,10 +106,12 @@ def test_decode_fused_combine_weight_flag():
     assert err_rms(f64(out), ref["out"]) <= TOL[cfg.dtype]
 
 
-def test_decode_fused_is_deterministic_and_replays_in_a_graph():
+@pytest.mark.parametrize("name", ["decode_T8", "decode_T1", "crowded"])
+def test_decode_fused_is_deterministic_and_replays_in_a_graph(name):
     """Every partial sum is reduced in a fixed order, so repeated calls give the same bits, and
-    the launch captures into a CUDA graph."""
-    cfg = CASES["decode_T8"]
+    the launch captures into a CUDA graph. T=1 and the crowded case run the layout where each
+    touched h block has a block of its own; T=8 the stream-K layout."""
+    cfg = CASES[name]
     inp = synth.make_inputs(cfg, DEV)
     wgu, wd = _weights(inp, True)
     out, ids, w, ws = moe.moe_forward(inp["x"], inp["logits"], wgu, wd, cfg.k)
