@@ -43,16 +43,19 @@
 //     rounding.
 // While a block waits, its producer keeps streaming down weights.
 //
-// Owner layout (bf16, when every touched h block can have a block of its own and at least one
-// block is left over: T = 1 at the decode shape). Block g streams the gate_up items of h
-// block g, then, through the same ring, the down weight rows of those 64 h columns for every
+// Owner layout (bf16 weights, while the final sums below come to at most two units per block;
+// otherwise, and for the MX layer, the stream-K layout above). Every block owns whole
+// h blocks: h block b while there are fewer h blocks than blocks (T = 1 at the decode shape),
+// else an equal contiguous share (4 or 5 at T = 8). For each of them it streams the gate_up
+// items, then, through the same ring, the down weight rows of those 64 h columns for every
 // output column (items of four [64 K][64 column] boxes, 256 output columns each). Its
 // epilogue warp stores h as above, and also keeps it in shared memory, so the consumer warps
 // multiply the down items by it at once: h crosses no SM and no flag is waited on. Each
 // consumer writes its item's weighted sums per token row as an fp32 partial and bumps the
-// 256-column group's counter. The remaining blocks then sum, per 64 output columns and per
-// token, the partials of its k slots (slot order) and the expert's h blocks (block order), and
-// store bf16 out: one rounding, in a fixed order.
+// 256-column group's counter. Then, per (64 output columns, token), the blocks past the owners
+// (or all blocks, once their own h blocks are done) sum the partials of the token's rows
+// (sorted row order) and h blocks (block order) and store bf16 out: one rounding, in a fixed
+// order.
 //
 // The launch is cooperative,
 // so every block is resident and the waits end. Every sum runs in an order fixed by the sizes
@@ -100,7 +103,7 @@ constexpr size_t kOffOut = kOffRed + kRedFloats * 4;
 constexpr size_t kOffLists = kOffOut + kOutFloats * 4;
 constexpr size_t kListInts = 3 * kMaxE + 2 * kDecodeFusedMaxRows;
 constexpr size_t kOffBars = kOffLists + kListInts * 4;
-constexpr size_t kSmemBytes = kOffBars + (2 * kStages + 3) * 8 + 64 + 1024;  // + align slack
+constexpr size_t kSmemBytes = kOffBars + (2 * kStages + 4) * 8 + 64 + 1024;  // + align slack
 static_assert(kSmemBytes <= 232448, "exceeds the 227 KB of shared memory a block may use");
 
 struct Params {
@@ -765,14 +768,15 @@ __device__ void group_b(Ctx& c, const Params& p, int q, int i0, int kc0, int kc1
 // token row's sums, times its routing weight, go to part_c[jb][row], then the group's counter
 // is bumped (release) for the summing blocks.
 template <int NTILE>
-__device__ void owner_down(Ctx& c, const Params& p, int q, int jb, int i0, int n4) {
+__device__ void owner_down(Ctx& c, const Params& p, int q, int jb, int i0, int n4,
+                           uint32_t hphase) {
     const int row0 = c.s_off[q], tq = c.s_tq[q];
     bool have_h = false;
     uint32_t b[4][NTILE][2];
     for (int g4 = (c.warp - i0 % kStages + kStages) % kStages; g4 < n4; g4 += kStages) {
         const int i = i0 + g4;
         if (!have_h) {
-            if (!mbar_wait(c.h_full, 0u, c.flags, kWaitLimitNs)) {
+            if (!mbar_wait(c.h_full, hphase, c.flags, kWaitLimitNs)) {
                 set_status(p.status, MOE_ERR_TIMEOUT);
                 c.flags[0] = 1;
             }
@@ -831,76 +835,88 @@ __device__ void owner_down(Ctx& c, const Params& p, int q, int jb, int i0, int n
     }
 }
 
-// Owner layout, the blocks past the owners: output block cb (64 columns) of every token is
-// the sum over its k slots (slot order) and the expert's h blocks (jb order) of part_c, taken
-// once all owners are done with its 256-column group. 224 threads (the consumer warps and the
-// epilogue warp): thread (grp, c4) sums terms grp, grp + 14, ... of four columns; the 14
-// partial sums are then added in group order.
-__device__ void owner_reduce(const Params& p, volatile int* flags, float* red, const int* s_p2s,
-                             int tid, int first_cb, int stride, int owners) {
+// Owner layout, the summing step: unit u = (output block cb = u / T, token t = u % T) is the
+// sum over the token's rows (ascending sorted row: an expert appears once per token) and each
+// row's h blocks (block order) of part_c, taken once every h block's owner is done with the
+// 256-column group of cb. 224 threads (the consumer warps and the epilogue warp): thread
+// (grp, c4) sums terms grp, grp + 14, ... of four columns; the 14 partial sums are then added
+// in group order. Units first, first + stride, ...
+__device__ void owner_reduce(const Params& p, volatile int* flags, float* red, const int* s_tok,
+                             int tid, int first, int stride, int owners) {
     constexpr int kGroups = 14;
     const int c4 = tid & 15, grp = tid >> 4;
     const int terms = p.k * p.nbh;
     float4* red4 = reinterpret_cast<float4*>(red);
-    for (int cb = first_cb; cb < p.nbd; cb += stride) {
-        if (tid == 0) {
-            const uint64_t t0 = globaltimer_ns();
-            while (ld_acquire(p.cnt_c + (cb >> 2)) < owners) {
-                if (flags[0] || globaltimer_ns() - t0 > kWaitLimitNs) {
-                    set_status(p.status, MOE_ERR_TIMEOUT);
-                    flags[0] = 1;
-                    break;
+    int* rows = reinterpret_cast<int*>(red4 + kGroups * 16);  // the token's sorted rows
+    for (int u = first; u < p.nbd * p.T; u += stride) {
+        const int cb = u / p.T, t = u - cb * p.T;
+        // every warp of the block is done with its own items (the epilogue warp with the last
+        // hand-over in this buffer) and with the previous unit's sums
+        asm volatile("bar.sync 1, 224;" ::: "memory");
+        if (tid < 32) {
+            if (tid == 0) {
+                const uint64_t t0 = globaltimer_ns();
+                while (ld_acquire(p.cnt_c + (cb >> 2)) < owners) {
+                    if (flags[0] || globaltimer_ns() - t0 > kWaitLimitNs) {
+                        set_status(p.status, MOE_ERR_TIMEOUT);
+                        flags[0] = 1;
+                        break;
+                    }
                 }
+            }
+            int n = 0;
+            for (int r0 = 0; r0 < p.R; r0 += 32) {
+                const bool mine = r0 + tid < p.R && s_tok[r0 + tid] == t;
+                const unsigned m = __ballot_sync(0xFFFFFFFFu, mine);
+                if (mine) rows[n + __popc(m & ((1u << tid) - 1u))] = r0 + tid;
+                n += __popc(m);
             }
         }
         asm volatile("bar.sync 1, 224;" ::: "memory");
         if (flags[0]) return;
         const int col = cb * 64 + 4 * c4;
-        for (int t = 0; t < p.T; ++t) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (col < p.d) {
-                for (int m0 = grp; m0 < terms; m0 += 8 * kGroups) {
-                    float4 v[8];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (col < p.d) {
+            for (int m0 = grp; m0 < terms; m0 += 8 * kGroups) {
+                float4 v[8];
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int m = m0 + u * kGroups;
-                        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (m < terms) {
-                            const int j = m / p.nbh, jb = m - j * p.nbh;
-                            const int pos = s_p2s[t * p.k + j];
-                            v[u] = __ldcg(reinterpret_cast<const float4*>(
-                                p.part_c + ((size_t)jb * p.R + pos) * p.d + col));
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        acc.x += v[u].x;
-                        acc.y += v[u].y;
-                        acc.z += v[u].z;
-                        acc.w += v[u].w;
+                for (int x = 0; x < 8; ++x) {
+                    const int m = m0 + x * kGroups;
+                    v[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (m < terms) {
+                        const int j = m / p.nbh, jb = m - j * p.nbh;
+                        v[x] = __ldcg(reinterpret_cast<const float4*>(
+                            p.part_c + ((size_t)jb * p.R + rows[j]) * p.d + col));
                     }
                 }
-            }
-            red4[grp * 16 + c4] = acc;
-            asm volatile("bar.sync 1, 224;" ::: "memory");
-            if (tid < 16 && col < p.d) {
-                float4 s4 = red4[c4];
-                for (int g = 1; g < kGroups; ++g) {
-                    const float4 v = red4[g * 16 + c4];
-                    s4.x += v.x;
-                    s4.y += v.y;
-                    s4.z += v.z;
-                    s4.w += v.w;
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                    acc.x += v[x].x;
+                    acc.y += v[x].y;
+                    acc.z += v[x].z;
+                    acc.w += v[x].w;
                 }
-                __nv_bfloat162 lo = __floats2bfloat162_rn(s4.x, s4.y);
-                __nv_bfloat162 hi = __floats2bfloat162_rn(s4.z, s4.w);
-                uint2 packed;
-                packed.x = *reinterpret_cast<uint32_t*>(&lo);
-                packed.y = *reinterpret_cast<uint32_t*>(&hi);
-                *reinterpret_cast<uint2*>(p.out + (size_t)t * p.d + col) = packed;
             }
-            asm volatile("bar.sync 1, 224;" ::: "memory");
         }
+        red4[grp * 16 + c4] = acc;
+        asm volatile("bar.sync 1, 224;" ::: "memory");
+        if (tid < 16 && col < p.d) {
+            float4 s4 = red4[c4];
+            for (int g = 1; g < kGroups; ++g) {
+                const float4 v = red4[g * 16 + c4];
+                s4.x += v.x;
+                s4.y += v.y;
+                s4.z += v.z;
+                s4.w += v.w;
+            }
+            __nv_bfloat162 lo = __floats2bfloat162_rn(s4.x, s4.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(s4.z, s4.w);
+            uint2 packed;
+            packed.x = *reinterpret_cast<uint32_t*>(&lo);
+            packed.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(p.out + (size_t)t * p.d + col) = packed;
+        }
+        asm volatile("bar.sync 1, 224;" ::: "memory");
     }
 }
 
@@ -1117,17 +1133,12 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     int* s_tq = s_off + kMaxE;
     int* s_tok = s_tq + kMaxE;
     float* s_w = reinterpret_cast<float*>(s_tok + kDecodeFusedMaxRows);
-    // slot -> sorted row, for the owner layout's summing blocks: the last 1 KB of the stage
-    // ring, which the routing scratch (at its start) does not reach and the summing blocks
-    // never fill with copies
-    int* s_p2s = reinterpret_cast<int*>(smem + (size_t)kStages * kStageBytes) -
-                 kDecodeFusedMaxRows;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBars);
     uint64_t* empty = full + kStages;
     uint64_t* red_full = empty + kStages;
     uint64_t* red_empty = red_full + 1;
-    uint64_t* h_full = red_empty + 1;
-    volatile int* flags = reinterpret_cast<volatile int*>(h_full + 1);
+    uint64_t* h_full = red_empty + 1;  // [2]: one per h buffer (owner layout)
+    volatile int* flags = reinterpret_cast<volatile int*>(h_full + 2);
     // flags: [0] a wait timed out (every bounded wait gives up at once after that; the status
     // word says so and the results are void), [2] number of touched experts.
 
@@ -1167,7 +1178,8 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
         }
         mbar_init(red_full, kConsumerWarps);
         mbar_init(red_empty, 1);
-        mbar_init(h_full, 1);
+        mbar_init(&h_full[0], 1);
+        mbar_init(&h_full[1], 1);
         fence_barrier_init();
         for (int f = 0; f < 4; ++f) flags[f] = 0;
     }
@@ -1241,7 +1253,6 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
         const int pos = off_s[e] + chunk_s[(s >> 5) * E + e] + rank_s[s];
         s_tok[pos] = s / p.k;
         s_w[pos] = w_s[s];
-        s_p2s[s] = pos;
         if (writer) {
             p.topk_ids[s] = e;
             p.topk_w[s] = w_s[s];
@@ -1269,18 +1280,23 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     // sums, h flagged as soon as it is stored) and blocks [ngA, G) take the down items,
     // prefetching them while the gate_up items stream.
     const int ngA = nq * p.nbh;
-    // Owner layout (bf16, one wave, an SM for every touched h block and at least one left
-    // over): block g < ngA streams the gate_up items of h block g and then the down weight
-    // rows of those 64 h columns, all output columns (n4 items of four 64-column boxes), and
-    // multiplies them by h from its own shared memory; blocks [ngA, G) sum the resulting
-    // partials per output block. No h or partial crosses SMs before the final sums.
-    const bool owner = !MX && W == 1 && ngA < G && p.part_c != nullptr;
+    // Owner layout (bf16 weights, one wave): block b owns whole h blocks [ob_lo, ob_hi): h
+    // block b alone while there are fewer h blocks than blocks, else an equal contiguous share.
+    // For each owned h block it streams the gate_up items and then the down weight rows of
+    // those 64 h columns for all output columns (n4 items of four 64-column boxes), and
+    // multiplies them by h kept in its own shared memory. The weighted partials are then summed
+    // per (output block, token) by the blocks past the owners (fewer h blocks than blocks) or by
+    // every block once its own h blocks are done. No h crosses SMs.
+    // (Taken while the final sums are at most two (output block, token) units per block; past
+    // that, as at T = 16 on the decode shape, the stream-K layout measured faster.)
+    const bool owner = !MX && W == 1 && p.part_c != nullptr && p.nbd * p.T <= 2 * G;
     const int n4 = (p.nbd + 3) / 4;
+    const int ob_lo = ngA <= G ? min(b, ngA) : (int)((long long)ngA * b / G);
+    const int ob_hi = ngA <= G ? min(b + 1, ngA) : (int)((long long)ngA * (b + 1) / G);
     const bool whole_groups = W == 1 && ngA < G &&
-                              (owner || (long long)p.nbd * nq * p.nkb * 4 <=
-                                            5ll * p.nka * (G - ngA));
+                              (long long)p.nbd * nq * p.nkb * 4 <= 5ll * p.nka * (G - ngA);
     const int GA = whole_groups ? ngA : G;
-    const int B0 = owner ? G : whole_groups ? ngA : 0, GB = G - B0;
+    const int B0 = whole_groups ? ngA : 0, GB = G - B0;
     const int ba = b < GA ? b : GA;            // gate_up range index (GA: empty)
     const int bb = b >= B0 ? b - B0 : GB;      // down range index (GB: empty)
     auto wave_a = [&](int w, int& q_lo, int& n) {
@@ -1310,7 +1326,50 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                 ++i;
                 return true;
             };
-            for (int w = 0; ok && w < W; ++w) {
+            if (owner) {
+                // per owned h block j: its gate_up items, and the down items of h block j - 1
+                // behind them, so the ring streams while the epilogue warp finishes h
+                for (int j = 0; ok && j <= ob_hi - ob_lo; ++j) {
+                    if (j < ob_hi - ob_lo) {
+                        const int g = ob_lo + j;
+                        const int q = g / p.nbh, jb = g % p.nbh, e = s_eq[q];
+                        for (int kc = 0; ok && kc < p.nka; ++kc) {
+                            uint32_t dst;
+                            uint64_t* bar;
+                            if (!(ok = next_stage(dst, bar, kStageBytes))) break;
+                            if (p.packed) {
+                                tma_load_3d_hint(dst, &tmGU, bar, 0, kc * kKcA,
+                                                 e * p.gu_nb + jb, pol);
+                                tma_load_3d_hint(dst + kBoxBytesA, &tmGU, bar, 0, kc * kKcA,
+                                                 e * p.gu_nb + p.nbh + jb, pol);
+                            } else {
+                                tma_load_3d_hint(dst, &tmGU, bar, 64 * jb, kc * kKcA, e, pol);
+                                tma_load_3d_hint(dst + kBoxBytesA, &tmGU, bar, p.I + 64 * jb,
+                                                 kc * kKcA, e, pol);
+                            }
+                        }
+                    }
+                    if (j >= 1) {
+                        // the down weight rows of h block j - 1: output columns 256 g4 ..
+                        const int g = ob_lo + j - 1;
+                        const int q = g / p.nbh, jb = g % p.nbh, e = s_eq[q];
+                        for (int g4 = 0; ok && g4 < n4; ++g4) {
+                            uint32_t dst;
+                            uint64_t* bar;
+                            if (!(ok = next_stage(dst, bar, kStageBytes))) break;
+                            if (p.packed) {
+                                tma_load_3d_hint(dst, &tmO, bar, 0, 64 * jb,
+                                                 e * p.dn_nb + 4 * g4, pol);
+                            } else {
+                                for (int x = 0; x < 4; ++x)
+                                    tma_load_3d_hint(dst + 8192u * x, &tmO, bar,
+                                                     64 * (4 * g4 + x), 64 * jb, e, pol);
+                            }
+                        }
+                    }
+                }
+            }
+            for (int w = 0; !owner && ok && w < W; ++w) {
                 int q_lo, n;
                 wave_a(w, q_lo, n);
                 const int lo = ba < GA ? range_lo(n, ba, GA) : 0;
@@ -1346,23 +1405,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                     }
                 }
             }
-            if (owner && ba < GA) {
-                // the down weight rows of this block's h block: output columns 256 g4 ..
-                const int q = ba / p.nbh, jb = ba % p.nbh, e = s_eq[q];
-                for (int g4 = 0; ok && g4 < n4; ++g4) {
-                    uint32_t dst;
-                    uint64_t* bar;
-                    if (!(ok = next_stage(dst, bar, kStageBytes))) break;
-                    if (p.packed) {
-                        tma_load_3d_hint(dst, &tmO, bar, 0, 64 * jb, e * p.dn_nb + 4 * g4, pol);
-                    } else {
-                        for (int j = 0; j < 4; ++j)
-                            tma_load_3d_hint(dst + 8192u * j, &tmO, bar, 64 * (4 * g4 + j),
-                                             64 * jb, e, pol);
-                    }
-                }
-            }
-            for (int w = 0; ok && w < W; ++w) {
+            for (int w = 0; !owner && ok && w < W; ++w) {
                 const int q_lo = range_lo(nq, w, W);
                 const int perC = (range_lo(nq, w + 1, W) - q_lo) * p.nkb, n = p.nbd * perC;
                 const int lo = bb < GB ? range_lo(n, bb, GB) : 0;
@@ -1421,12 +1464,53 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     c.ready_mask = 0;
     c.dumps = 0;
     c.owner = owner;
-    c.h_s = reinterpret_cast<__nv_bfloat16*>(outacc);  // the combine accumulator is unused
+    // owner layout: two h buffers in the (then unused) combine accumulator
+    __nv_bfloat16* const h_buf = reinterpret_cast<__nv_bfloat16*>(outacc);
+    c.h_s = h_buf;
     c.h_full = h_full;
     const bool epilogue = warp == kEpilogueWarp;
 
     // consumers (warp w: the items of stage w) and the epilogue warp walk the same groups
     int i0 = 0;  // block-local index of the next item
+    if (owner) {
+        // the producer's order: gate_up of h block j (h into buffer j & 1), then the down
+        // items of h block j - 1 (h from buffer (j - 1) & 1, its barrier's use (j - 1) >> 1)
+        const int n_own = ob_hi - ob_lo;
+        for (int j = 0; j <= n_own; ++j) {
+            if (j < n_own) {
+                const int g = ob_lo + j, q = g / p.nbh, jb = g % p.nbh;
+                c.h_s = h_buf + (j & 1) * kDecodeFusedMaxTokens * 64;
+                c.h_full = &h_full[j & 1];
+                if (epilogue)
+                    by_rows(s_tq[q], [&](auto tag) {
+                        epi_a<decltype(tag)::value>(c, p, q, jb, g, b, b);
+                    });
+                else
+                    by_rows(s_tq[q], [&](auto tag) {
+                        group_a<decltype(tag)::value, false>(c, p, q, i0, 0, p.nka);
+                    });
+                i0 += p.nka;
+            }
+            if (j >= 1) {
+                const int g = ob_lo + j - 1, q = g / p.nbh, jb = g % p.nbh;
+                c.h_s = h_buf + ((j - 1) & 1) * kDecodeFusedMaxTokens * 64;
+                c.h_full = &h_full[(j - 1) & 1];
+                if (!epilogue)
+                    by_rows(s_tq[q], [&](auto tag) {
+                        owner_down<decltype(tag)::value>(c, p, q, jb, i0, n4,
+                                                         (uint32_t)((j - 1) >> 1) & 1u);
+                    });
+                i0 += n4;
+            }
+        }
+        const int tid = (warp < kProducerWarp ? warp : warp - 1) * 32 + lane;
+        if (ngA < G) {
+            if (b >= ngA) owner_reduce(p, flags, c.red, s_tok, tid, b - ngA, G - ngA, ngA);
+        } else {
+            owner_reduce(p, flags, c.red, s_tok, tid, b, G, ngA);
+        }
+        return;
+    }
     for (int w = 0; w < W; ++w) {
         int q_lo, n;
         wave_a(w, q_lo, n);
@@ -1450,20 +1534,6 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
             u += kc1 - kc0;
             i0 += kc1 - kc0;
         }
-    }
-    if (owner) {
-        if (b < ngA) {
-            if (!epilogue) {
-                const int q = b / p.nbh, jb = b % p.nbh;
-                by_rows(s_tq[q], [&](auto tag) {
-                    owner_down<decltype(tag)::value>(c, p, q, jb, i0, n4);
-                });
-            }
-        } else {
-            const int tid = (warp < kProducerWarp ? warp : warp - 1) * 32 + lane;
-            owner_reduce(p, flags, c.red, s_p2s, tid, b - ngA, G - ngA, ngA);
-        }
-        return;
     }
     for (int w = 0; w < W; ++w) {
         const WaveB v = wave_b(c, p, w);
@@ -1518,7 +1588,7 @@ DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I, bool mx) {
     L.part_b = up(((size_t)kDecodeWaves * kDecodeFusedMaxGrid + R * L.nbh) * T * 128 * 4);
     L.part_bytes = L.part_b + up((size_t)kDecodeWaves * (kDecodeFusedMaxGrid + L.nbd) * T *
                                  64 * 4);
-    // owner layout (bf16; it needs fewer touched h blocks than SMs): [nbh][R][d] fp32
+    // owner layout (bf16): the down partials [nbh][R][d] fp32
     L.part_c = 0;
     if (!mx && L.nbh < kDecodeFusedMaxGrid) {
         L.part_c = L.part_bytes;
