@@ -4,6 +4,8 @@
 // moe_read_device_status, which exists to synchronise.
 #include <atomic>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "moe_internal.cuh"
 
@@ -17,16 +19,29 @@ PdlScope::PdlScope(bool on) : prev(t_pdl) { t_pdl = on; }
 PdlScope::~PdlScope() { t_pdl = prev; }
 
 int device_sm_count() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-    if (cache[dev] == 0) {
-        int n = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
             n = 148;
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
+}
+
+cudaError_t ensure_max_dynamic_smem(const void* fn, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static std::set<std::pair<const void*, int>> done;  // (kernel, device)
+    std::lock_guard<std::mutex> lock(mu);
+    if (done.count({fn, dev})) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.insert({fn, dev});
+    return e;
 }
 
 namespace {

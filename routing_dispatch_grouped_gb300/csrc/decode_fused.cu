@@ -61,7 +61,6 @@
 // so every block is resident and the waits end. Every sum runs in an order fixed by the sizes
 // alone: results do not depend on timing. The counters are zeroed by the caller's memset of
 // the workspace head that precedes the launch.
-#include <mutex>
 
 #include "mx.cuh"
 #include "route_warp.cuh"
@@ -1651,18 +1650,11 @@ DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I, bool mx) {
 }
 
 cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(decode_fused_kernel<false>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kSmemBytes);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(decode_fused_kernel<true>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    {
+        const cudaError_t e = ensure_max_dynamic_smem(
+            a.mx ? decode_fused_kernel<true> : decode_fused_kernel<false>, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+    }
 
     const DecodeFusedLayout L = decode_fused_layout(a.T, a.d, a.k, a.I, a.mx);
     const int R = a.T * a.k;

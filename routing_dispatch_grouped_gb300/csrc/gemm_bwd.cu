@@ -24,7 +24,6 @@
 //
 // Every mbarrier wait is bounded in time; on expiry the kernel records MOE_ERR_TIMEOUT, drains
 // its own copies and MMAs, frees TMEM and returns.
-#include <mutex>
 
 #include "moe_internal.cuh"
 
@@ -651,13 +650,7 @@ namespace {
 
 template <int MODE>
 cudaError_t set_smem_attr() {
-    static std::once_flag once;
-    static cudaError_t err = cudaSuccess;
-    std::call_once(once, [] {
-        err = cudaFuncSetAttribute(tc_bwd_gemm<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)Layout<MODE>::bytes);
-    });
-    return err;
+    return ensure_max_dynamic_smem(tc_bwd_gemm<MODE>, (int)Layout<MODE>::bytes);
 }
 
 template <int MODE>

@@ -46,7 +46,6 @@
 // accumulator: the next tile's MMAs then overlap the SwiGLU, the MXFP8 rounding and the
 // stores. Every mbarrier wait is bounded in time; on expiry the kernel records MOE_ERR_TIMEOUT,
 // lets its own copies and MMAs finish, frees TMEM and returns.
-#include <mutex>
 
 #include "mx_tc.cuh"
 
@@ -673,14 +672,10 @@ cudaError_t launch_mx_tc_quant_rows(const void* x, int T, int d, int k, int E,
 namespace {
 template <int KIND>
 cudaError_t launch_mx_tc_kind(const MxTcGemmArgs& a, cudaStream_t s) {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_mx_gemm<KIND>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    {
+        const cudaError_t e = ensure_max_dynamic_smem(tc_mx_gemm<KIND>, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+    }
     const bool gu = KIND == kGateUp;
     const MxTcGeom wg = mx_tc_geom(gu, a.K, a.N, a.groups);
     const int KC = (a.K + 127) / 128;

@@ -508,14 +508,10 @@ namespace {
 
 template <int KIND>
 cudaError_t launch_kind(const GroupedGemmArgs& a, cudaStream_t s) {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_grouped_gemm<KIND>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    {
+        const cudaError_t e = ensure_max_dynamic_smem(tc_grouped_gemm<KIND>, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+    }
 
     CUtensorMap tmA, tmB;
     const cuuint64_t a_dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.R};

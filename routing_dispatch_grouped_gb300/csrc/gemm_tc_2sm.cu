@@ -23,7 +23,8 @@
 // for the bytes of both), the leader's commits arrive on the stage and accumulator barriers of
 // both CTAs, and the epilogue warps of both CTAs release an accumulator on the leader's barrier.
 // Every mbarrier wait is bounded in time as in the 1-SM kernels.
-#include <mutex>
+
+#include <atomic>
 
 #include "pair.cuh"
 
@@ -478,14 +479,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int KIND>
 cudaError_t launch_pair_kind(const GroupedGemmArgs& a, cudaStream_t s) {
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_grouped_gemm_2sm<KIND>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    {
+        const cudaError_t e = ensure_max_dynamic_smem(tc_grouped_gemm_2sm<KIND>, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+    }
 
     const int groups = a.offsets ? a.E : 1;
     CUtensorMap tmA, tmB;
@@ -549,14 +546,17 @@ cudaError_t launch_pair_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     }
 
     // clusters that can be resident at once (SMs pair up within a GPC)
-    static int max_clusters[64] = {0};
+    static std::atomic<int> max_clusters[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
-    if (max_clusters[dev] == 0)
-        max_clusters[dev] = max_pair_clusters(tc_grouped_gemm_2sm<KIND>, kThreads, kSmemBytes);
+    int mc = max_clusters[dev].load(std::memory_order_relaxed);
+    if (mc == 0) {
+        mc = max_pair_clusters(tc_grouped_gemm_2sm<KIND>, kThreads, kSmemBytes);
+        max_clusters[dev].store(mc, std::memory_order_relaxed);
+    }
     const long long pair_ub = ((long long)(a.R + kPairRows - 1) / kPairRows + groups) * p.n_tiles;
-    long long clusters = max_clusters[dev];
+    long long clusters = mc;
     if (pair_ub < clusters) clusters = pair_ub;
     if (clusters < 1) clusters = 1;
     return launch_kernel_ex(tc_grouped_gemm_2sm<KIND>, dim3((unsigned)(2 * clusters)),

@@ -26,7 +26,6 @@
 // Tiles are enumerated on the device from the offsets: expert, then weight-column block, then
 // token block, so CTAs running together share weight blocks through L2. Waits are bounded as
 // in gemm_tc.cu.
-#include <mutex>
 
 #include "moe_internal.cuh"
 
@@ -427,14 +426,11 @@ template <int KIND, class C>
 cudaError_t launch_swap_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     constexpr int kTok = C::kTok;
     constexpr size_t kSmemBytes = smem_bytes<C>();
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_grouped_gemm_swap<KIND, C>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    {
+        const cudaError_t e =
+            ensure_max_dynamic_smem(tc_grouped_gemm_swap<KIND, C>, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+    }
 
     const int groups = a.offsets ? a.E : 1;
     CUtensorMap tmW, tmX;

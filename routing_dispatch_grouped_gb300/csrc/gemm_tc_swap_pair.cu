@@ -23,7 +23,8 @@
 // both CTAs' copies complete on the leader's stage barrier, the leader's commits are multicast
 // to both CTAs, both CTAs' epilogue warps release an accumulator on the leader's barrier, and
 // every wait is bounded in time.
-#include <mutex>
+
+#include <atomic>
 
 #include "pair.cuh"
 
@@ -437,14 +438,11 @@ template <int KIND, class C>
 cudaError_t launch_swap_pair_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     constexpr size_t kSmemBytes = smem_bytes<C>();
     constexpr int kBoxes = C::kBoxes;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(tc_grouped_gemm_swap_pair<KIND, C>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kSmemBytes);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    {
+        const cudaError_t e =
+            ensure_max_dynamic_smem(tc_grouped_gemm_swap_pair<KIND, C>, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+    }
 
     const int groups = a.offsets ? a.E : 1;
     CUtensorMap tmW;
@@ -487,16 +485,18 @@ cudaError_t launch_swap_pair_kind(const GroupedGemmArgs& a, cudaStream_t s) {
     p.nbh = g.nbh;
     p.kpad = g.kpad;
 
-    static int max_clusters[64] = {0};
+    static std::atomic<int> max_clusters[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) dev = 0;
-    if (max_clusters[dev] == 0)
-        max_clusters[dev] =
-            max_pair_clusters(tc_grouped_gemm_swap_pair<KIND, C>, kThreads, kSmemBytes);
+    int mc = max_clusters[dev].load(std::memory_order_relaxed);
+    if (mc == 0) {
+        mc = max_pair_clusters(tc_grouped_gemm_swap_pair<KIND, C>, kThreads, kSmemBytes);
+        max_clusters[dev].store(mc, std::memory_order_relaxed);
+    }
     const long long tiles_ub =
         ((long long)(a.R + C::kPairTok - 1) / C::kPairTok + groups) * p.n_tiles;
-    long long clusters = max_clusters[dev];
+    long long clusters = mc;
     if (tiles_ub < clusters) clusters = tiles_ub;
     if (clusters < 1) clusters = 1;
     return launch_kernel_ex(tc_grouped_gemm_swap_pair<KIND, C>, dim3((unsigned)(2 * clusters)),

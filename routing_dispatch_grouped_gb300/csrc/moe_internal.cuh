@@ -455,6 +455,14 @@ bool encode_tensor_map_f32(CUtensorMap* m, const void* base, int rank, const cuu
 cudaError_t launch_grouped_gemm_f32(const GroupedGemmArgs& a, cudaStream_t s);
 
 int device_sm_count();
+// Lets kernel `fn` take `bytes` of dynamic shared memory on the current device. The attribute
+// belongs to each device's copy of the module, so it is set the first time each device
+// launches the kernel (a process-wide once would leave every other device without it).
+cudaError_t ensure_max_dynamic_smem(const void* fn, int bytes);
+template <typename K>
+cudaError_t ensure_max_dynamic_smem(K* kernel, int bytes) {
+    return ensure_max_dynamic_smem(reinterpret_cast<const void*>(kernel), bytes);
+}
 // Stall of the 128-row gate_up kernel's test hook (moe_debug_set_gemm_stall_ns; 0 = off).
 uint32_t debug_gemm_stall_ns();
 

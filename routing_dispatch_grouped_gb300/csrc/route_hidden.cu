@@ -22,7 +22,6 @@
 //     memory within the cluster) and selects.
 // Either way every logit's summation order is fixed by the sizes, so results do not depend on
 // timing.
-#include <mutex>
 
 #include "route_warp.cuh"
 
@@ -378,13 +377,10 @@ cudaError_t launch_mma(const void* x, const float* w_router, const float* bias, 
                        int E, int k, int score_fn, int renorm, float* logits, int32_t* ids,
                        float* weights, cudaStream_t s) {
     using S = MmaShape<EPAD>;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(route_hidden_mma_kernel<EPAD>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kSmem);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    {
+        const cudaError_t e = ensure_max_dynamic_smem(route_hidden_mma_kernel<EPAD>, (int)S::kSmem);
+        if (e != cudaSuccess) return e;
+    }
     return launch_kernel(route_hidden_mma_kernel<EPAD>, dim3((T + 63) / 64), dim3(256), S::kSmem,
                          s, static_cast<const __nv_bfloat16*>(x), w_router, bias, T, d, E, k,
                          score_fn, renorm, logits, ids, weights);
@@ -397,14 +393,8 @@ cudaError_t launch_shape(const void* x, bool bf16, const float* w_router, const 
     using S = RhShape<VPL, KS>;
     auto kern = bf16 ? route_hidden_kernel<VPL, true, KS> : route_hidden_kernel<VPL, false, KS>;
     if (S::kSmem > 48 * 1024) {
-        static std::once_flag once[2];
-        static cudaError_t attr_err[2] = {cudaSuccess, cudaSuccess};
-        const int which = bf16 ? 1 : 0;
-        std::call_once(once[which], [&] {
-            attr_err[which] = cudaFuncSetAttribute(
-                kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)S::kSmem);
-        });
-        if (attr_err[which] != cudaSuccess) return attr_err[which];
+        const cudaError_t e = ensure_max_dynamic_smem(kern, (int)S::kSmem);
+        if (e != cudaSuccess) return e;
     }
     const int groups = (T + S::kTok - 1) / S::kTok;
     const int cl = KS > 1 ? kCluster : 1;
