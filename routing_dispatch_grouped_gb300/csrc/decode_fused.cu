@@ -43,8 +43,8 @@
 //     rounding.
 // While a block waits, its producer keeps streaming down weights.
 //
-// Owner layout (bf16 weights, while the final sums below come to at most two units per block;
-// otherwise, and for the MX layer, the stream-K layout above). Every block owns whole
+// Owner layout (while the final sums below come to at most two units per block; otherwise the
+// stream-K layout above). Every block owns whole
 // h blocks: h block b while there are fewer h blocks than blocks (T = 1 at the decode shape),
 // else an equal contiguous share (4 or 5 at T = 8). For each of them it streams the gate_up
 // items, then, through the same ring, the down weight rows of those 64 h columns for every
@@ -92,6 +92,12 @@ constexpr int kMxKbB = 30;
 constexpr uint32_t kMxUpCodes = 15 * 1024;     // up codes after the gate codes (gate_up item)
 constexpr uint32_t kMxScales = 30 * 1024;      // scales after the codes
 constexpr uint32_t kMxUpScales = kMxScales + 15 * 64;
+// owner layout, MX: a down item holds the 64 h rows (two 32-row K blocks) of up to 14 output
+// column blocks: codes [column block][K block][1 KB], then scales [column block][K block][64]
+constexpr int kMxOwnCb = 14;
+constexpr uint32_t kMxOwnScales = kMxOwnCb * 2 * 1024;
+static_assert(kMxOwnScales + kMxOwnCb * 2 * 64 <= kStageBytes, "owner MX item exceeds a stage");
+constexpr int kMxHsScales = kDecodeFusedMaxTokens * 64;  // h_s (MX): codes, then 2 scales a row
 static_assert(kMxUpScales + 15 * 64 <= kStageBytes && kMxScales + 30 * 64 <= kStageBytes,
               "MX items exceed a stage");
 constexpr int kDecodeWaves = 1;                 // expert waves (gate_up of wave w + 1 hides the
@@ -371,8 +377,8 @@ __device__ __forceinline__ __nv_bfloat16 store_h(const Params& p, const Ctx& c, 
 // warp together, lane l holding column hc of the same 32-column block of one row (valid: hc < I):
 // the block's largest magnitude is a warp maximum. Stores the E4M3 code and scale the down items
 // read, and the rounded value into h.
-__device__ __forceinline__ void store_h_mx(const Params& p, const Ctx& c, int row, int hc,
-                                           float g, float u, bool valid) {
+__device__ __forceinline__ uint32_t store_h_mx(const Params& p, const Ctx& c, int row, int hc,
+                                               float g, float u, bool valid) {
     const float s = p.scale_input ? c.s_w[row] : 1.0f;
     const float hv = valid ? silu(g * s) * (u * s) : 0.0f;
     float amax = fabsf(hv);
@@ -385,6 +391,7 @@ __device__ __forceinline__ void store_h_mx(const Params& p, const Ctx& c, int ro
         p.h[(size_t)row * p.I + hc] = __float2bfloat16_rn(e4m3x2_to_f32(code).x * pow2_f32(se));
         if (c.lane == 0) p.h_scales[(size_t)row * p.kbi + hc / 32] = (uint8_t)(se + 127);
     }
+    return (valid ? code : 0u) | ((uint32_t)(se + 127) << 8);
 }
 
 // First item of [i0, ...) that warp w owns (item i belongs to warp i % kStages).
@@ -834,6 +841,105 @@ __device__ void owner_down(Ctx& c, const Params& p, int q, int jb, int i0, int n
     }
 }
 
+// Owner layout, MX: down item g4 of h block (q, jb) holds W_down's two 32-row K blocks of the
+// 64 h rows (one when I ends inside them) for output column blocks [14 g4, 14 g4 + 14). The B
+// side is the h block's MXFP8 codes and scales from h_s; per K block the partial sums are
+// added times the weight column's and the token's scales, as in the stream-K items.
+template <int NTILE>
+__device__ void owner_down_mx(Ctx& c, const Params& p, int q, int jb, int i0, int n4,
+                              uint32_t hphase) {
+    const int row0 = c.s_off[q], tq = c.s_tq[q];
+    const int nkb = min(2, p.kbi - 2 * jb);
+    const uint8_t* hb = reinterpret_cast<const uint8_t*>(c.h_s);
+    bool have_h = false;
+    uint32_t b[2][2][NTILE][2];
+    float sxc[2][NTILE][2];
+    for (int g4 = (c.warp - i0 % kStages + kStages) % kStages; g4 < n4; g4 += kStages) {
+        const int i = i0 + g4;
+        if (!have_h) {
+            if (!mbar_wait(c.h_full, hphase, c.flags, kWaitLimitNs)) {
+                set_status(p.status, MOE_ERR_TIMEOUT);
+                c.flags[0] = 1;
+            }
+            // lane l: B codes of token row 8 n + l/4 at h columns 32 kb + 16 ks + 8 h + 2 (l%4),
+            // and the K block scales of its C fragment's token rows 8 n + 2 (l%4) + {0, 1}
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                for (int n = 0; n < NTILE; ++n) {
+                    const int r = 8 * n + (c.lane >> 2);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int kk = 32 * kb + 16 * (j >> 1) + 8 * (j & 1) + 2 * (c.lane & 3);
+                        const uint32_t w =
+                            r < tq ? *reinterpret_cast<const unsigned short*>(hb + r * 64 + kk) : 0u;
+                        b[kb][j >> 1][n][j & 1] = e4m3x2_f16x2(w);
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int rt = 8 * n + 2 * (c.lane & 3) + jj;
+                        sxc[kb][n][jj] = rt < tq ? e8m0_f32(hb[kMxHsScales + rt * 2 + kb]) : 0.0f;
+                    }
+                }
+            have_h = true;
+        }
+        const int cb0 = g4 * kMxOwnCb, ncb = min(kMxOwnCb, p.nbd - cb0);
+        const bool taken = take_stage(c, p, i);
+        const uint32_t stage = c.stage0 + (uint32_t)c.warp * kStageBytes;
+        for (int cbl = 0; cbl < ncb; ++cbl) {
+            float acc[4][NTILE][4];
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+                for (int n = 0; n < NTILE; ++n)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) acc[mt][n][j] = 0.0f;
+            if (taken) {
+                for (int kb = 0; kb < nkb; ++kb) {
+#pragma unroll
+                    for (int mt = 0; mt < 4; ++mt) {
+                        float part[NTILE][4];
+#pragma unroll
+                        for (int n = 0; n < NTILE; ++n)
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) part[n][j] = 0.0f;
+#pragma unroll
+                        for (int ks = 0; ks < 2; ++ks) {
+                            uint32_t a[4];
+                            mx_a(stage + (uint32_t)cbl * 2048u, kb, ks, mt, c.lane, a);
+                            mma_f16<NTILE>(a, b[kb][ks], part);
+                        }
+                        const uint32_t scl = stage + kMxOwnScales + (uint32_t)(cbl * 2 + kb) * 64u +
+                                             mt * 16 + (c.lane >> 2);
+                        mx_rescale<NTILE>(part, e8m0_f32(lds8(scl)), e8m0_f32(lds8(scl + 8)),
+                                          sxc[kb], acc[mt]);
+                    }
+                }
+            }
+            // C fragment: m = output column 16 mt + l/4 (+8), n = token row 8 n + 2 (l%4) (+1)
+#pragma unroll
+            for (int n = 0; n < NTILE; ++n)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int r = 8 * n + 2 * (c.lane & 3) + (jj & 1);
+                    if (r >= tq) continue;
+                    const float wgt = p.scale_input ? 1.0f : c.s_w[row0 + r];
+                    float* dst = p.part_c + ((size_t)jb * p.R + row0 + r) * p.d;
+#pragma unroll
+                    for (int mt = 0; mt < 4; ++mt) {
+                        const int col = 64 * (cb0 + cbl) + 16 * mt + (c.lane >> 2) +
+                                        ((jj & 2) ? 8 : 0);
+                        if (col < p.d) __stcg(dst + col, wgt * acc[mt][n][jj]);
+                    }
+                }
+        }
+        release_stage(c);
+        __syncwarp();
+        if (c.lane == 0)
+            asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.cnt_c + g4) : "memory");
+    }
+}
+
 // Owner layout, the summing step: unit u = (output block cb = u / T, token t = u % T) is the
 // sum over the token's rows (ascending sorted row: an expert appears once per token) and each
 // row's h blocks (block order) of part_c, taken once every h block's owner is done with the
@@ -841,7 +947,7 @@ __device__ void owner_down(Ctx& c, const Params& p, int q, int jb, int i0, int n
 // (grp, c4) sums terms grp, grp + 14, ... of four columns; the 14 partial sums are then added
 // in group order. Units first, first + stride, ...
 __device__ void owner_reduce(const Params& p, volatile int* flags, float* red, const int* s_tok,
-                             int tid, int first, int stride, int owners) {
+                             int tid, int first, int stride, int owners, int cb_per_group) {
     constexpr int kGroups = 14;
     const int c4 = tid & 15, grp = tid >> 4;
     const int terms = p.k * p.nbh;
@@ -855,7 +961,7 @@ __device__ void owner_reduce(const Params& p, volatile int* flags, float* red, c
         if (tid < 32) {
             if (tid == 0) {
                 const uint64_t t0 = globaltimer_ns();
-                while (ld_acquire(p.cnt_c + (cb >> 2)) < owners) {
+                while (ld_acquire(p.cnt_c + cb / cb_per_group) < owners) {
                     if (flags[0] || globaltimer_ns() - t0 > kWaitLimitNs) {
                         set_status(p.status, MOE_ERR_TIMEOUT);
                         flags[0] = 1;
@@ -980,8 +1086,14 @@ __device__ void epi_a(Ctx& c, const Params& p, int q, int jb, int g, int b_first
                 }
                 if (whole) {
                     if (p.mx) {
-                        store_h_mx(p, c, row0 + pass * kPass + t, jb * 64 + col, v, uu,
-                                   jb * 64 + col < p.I);
+                        const uint32_t cs = store_h_mx(p, c, row0 + pass * kPass + t,
+                                                       jb * 64 + col, v, uu, jb * 64 + col < p.I);
+                        if (c.owner) {
+                            uint8_t* hb = reinterpret_cast<uint8_t*>(c.h_s);
+                            const int r = pass * kPass + t;
+                            hb[r * 64 + col] = (uint8_t)(cs & 0xFFu);
+                            if ((col & 31) == 0) hb[kMxHsScales + r * 2 + (col >> 5)] = (uint8_t)(cs >> 8);
+                        }
                     } else {
                         const __nv_bfloat16 hv =
                             jb * 64 + col < p.I
@@ -1341,8 +1453,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     // every block once its own h blocks are done. No h crosses SMs.
     // (Taken while the final sums are at most two (output block, token) units per block; past
     // that, as at T = 16 on the decode shape, the stream-K layout measured faster.)
-    const bool owner = !MX && W == 1 && p.part_c != nullptr && p.nbd * p.T <= 2 * G;
-    const int n4 = (p.nbd + 3) / 4;
+    const bool owner = W == 1 && p.part_c != nullptr && p.nbd * p.T <= 2 * G;
+    const int cb_per_item = MX ? kMxOwnCb : 4;  // output column blocks per owner down item
+    const int n4 = (p.nbd + cb_per_item - 1) / cb_per_item;
     const int ob_lo = ngA <= G ? min(b, ngA) : (int)((long long)ngA * b / G);
     const int ob_hi = ngA <= G ? min(b + 1, ngA) : (int)((long long)ngA * (b + 1) / G);
     const bool whole_groups = W == 1 && ngA < G &&
@@ -1388,6 +1501,20 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                         for (int kc = 0; ok && kc < p.nka; ++kc) {
                             uint32_t dst;
                             uint64_t* bar;
+                            if (MX) {
+                                const int kb0 = kc * kMxKbA, nk = min(kMxKbA, p.kbd - kb0);
+                                const size_t bg = ((size_t)e * p.gu_nb + jb) * p.kbd + kb0;
+                                const size_t bu = ((size_t)e * p.gu_nb + p.nbh + jb) * p.kbd + kb0;
+                                if (!(ok = next_stage(dst, bar, (uint32_t)nk * 2 * (1024 + 64))))
+                                    break;
+                                bulk_load(dst, p.mx_gu + bg * 1024, nk * 1024, bar, pol);
+                                bulk_load(dst + kMxUpCodes, p.mx_gu + bu * 1024, nk * 1024, bar, pol);
+                                bulk_load(dst + kMxScales, p.mx_gu + p.mx_gu_scales + bg * 64,
+                                          nk * 64, bar, pol);
+                                bulk_load(dst + kMxUpScales, p.mx_gu + p.mx_gu_scales + bu * 64,
+                                          nk * 64, bar, pol);
+                                continue;
+                            }
                             if (!(ok = next_stage(dst, bar, kStageBytes))) break;
                             if (p.packed) {
                                 tma_load_3d_hint(dst, &tmGU, bar, 0, kc * kKcA,
@@ -1408,6 +1535,24 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                         for (int g4 = 0; ok && g4 < n4; ++g4) {
                             uint32_t dst;
                             uint64_t* bar;
+                            if (MX) {
+                                // K blocks 2 jb, 2 jb + 1 (those below I) of 14 column blocks
+                                const int cb0 = g4 * kMxOwnCb, ncb = min(kMxOwnCb, p.nbd - cb0);
+                                const int nkb = min(2, p.kbi - 2 * jb);
+                                if (!(ok = next_stage(dst, bar,
+                                                      (uint32_t)(ncb * nkb * (1024 + 64)))))
+                                    break;
+                                for (int cbl = 0; cbl < ncb; ++cbl) {
+                                    const size_t bd =
+                                        ((size_t)e * p.dn_nb + cb0 + cbl) * p.kbi + 2 * jb;
+                                    bulk_load(dst + (uint32_t)cbl * 2048u, p.mx_dn + bd * 1024,
+                                              nkb * 1024, bar, pol);
+                                    bulk_load(dst + kMxOwnScales + (uint32_t)cbl * 128u,
+                                              p.mx_dn + p.mx_dn_scales + bd * 64, nkb * 64, bar,
+                                              pol);
+                                }
+                                continue;
+                            }
                             if (!(ok = next_stage(dst, bar, kStageBytes))) break;
                             if (p.packed) {
                                 tma_load_3d_hint(dst, &tmO, bar, 0, 64 * jb,
@@ -1539,7 +1684,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                     });
                 else
                     by_rows(s_tq[q], [&](auto tag) {
-                        group_a<decltype(tag)::value, false>(c, p, q, i0, 0, p.nka);
+                        group_a<decltype(tag)::value, MX>(c, p, q, i0, 0, p.nka);
                     });
                 i0 += p.nka;
             }
@@ -1549,17 +1694,22 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                 c.h_full = &h_full[(j - 1) & 1];
                 if (!epilogue)
                     by_rows(s_tq[q], [&](auto tag) {
-                        owner_down<decltype(tag)::value>(c, p, q, jb, i0, n4,
-                                                         (uint32_t)((j - 1) >> 1) & 1u);
+                        if (MX)
+                            owner_down_mx<decltype(tag)::value>(c, p, q, jb, i0, n4,
+                                                                (uint32_t)((j - 1) >> 1) & 1u);
+                        else
+                            owner_down<decltype(tag)::value>(c, p, q, jb, i0, n4,
+                                                             (uint32_t)((j - 1) >> 1) & 1u);
                     });
                 i0 += n4;
             }
         }
         const int tid = (warp < kProducerWarp ? warp : warp - 1) * 32 + lane;
         if (ngA < G) {
-            if (b >= ngA) owner_reduce(p, flags, c.red, s_tok, tid, b - ngA, G - ngA, ngA);
+            if (b >= ngA)
+                owner_reduce(p, flags, c.red, s_tok, tid, b - ngA, G - ngA, ngA, cb_per_item);
         } else {
-            owner_reduce(p, flags, c.red, s_tok, tid, b, G, ngA);
+            owner_reduce(p, flags, c.red, s_tok, tid, b, G, ngA, cb_per_item);
         }
         return;
     }
@@ -1640,9 +1790,9 @@ DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I, bool mx) {
     L.part_b = up(((size_t)kDecodeWaves * kDecodeFusedMaxGrid + R * L.nbh) * T * 128 * 4);
     L.part_bytes = L.part_b + up((size_t)kDecodeWaves * (kDecodeFusedMaxGrid + L.nbd) * T *
                                  64 * 4);
-    // owner layout (bf16): the down partials [nbh][R][d] fp32
+    // owner layout: the down partials [nbh][R][d] fp32
     L.part_c = 0;
-    if (!mx && L.nbh < kDecodeFusedMaxGrid) {
+    if (L.nbh < kDecodeFusedMaxGrid) {
         L.part_c = L.part_bytes;
         L.part_bytes += up((size_t)L.nbh * R * d * 4);
     }
@@ -1702,7 +1852,7 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
     p.hflag = a.counters + (size_t)R * L.nbh;
     p.cnt_b = a.counters + (size_t)2 * R * L.nbh;
     p.cnt_c = p.cnt_b + L.nbd;
-    p.part_c = (!a.mx && L.part_c) ? reinterpret_cast<float*>(parts + L.part_c) : nullptr;
+    p.part_c = L.part_c ? reinterpret_cast<float*>(parts + L.part_c) : nullptr;
     p.part_a = reinterpret_cast<float*>(parts + L.part_a);
     p.part_b = reinterpret_cast<float*>(parts + L.part_b);
     p.status = a.status;

@@ -414,8 +414,11 @@ def forward_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is, dtype, mx=False
     v = views
     if mx and fused:
         # the one-kernel layer on MX weights: its partial sums, then h's MXFP8 codes and scales
-        part_b = ((512 + R * ((I + 63) // 64)) * T * 128 * 4 + 255) // 256 * 256
-        part = part_b + ((512 + (d + 63) // 64) * T * 64 * 4 + 255) // 256 * 256
+        nbh = (I + 63) // 64
+        part_b = ((512 + R * nbh) * T * 128 * 4 + 255) // 256 * 256
+        part = part_b + ((512 + nbd) * T * 64 * 4 + 255) // 256 * 256
+        if nbh < 512:  # the owner layout's down partials [nbh][R][d] fp32
+            part += (nbh * R * d * 4 + 255) // 256 * 256
         o = (o + part + 255) // 256 * 256
         views["h_codes"] = ws[o:o + R * I]
         o = (o + R * I + 255) // 256 * 256
