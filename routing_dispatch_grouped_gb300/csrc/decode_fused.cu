@@ -1231,7 +1231,9 @@ __device__ __forceinline__ void by_rows(int tq, F&& f) {
         f(NtTag<2>{});
 }
 
-template <bool MX>
+// OWNER: the owner layout (chosen on the host from the sizes alone, so that each instantiation
+// holds one layout's code)
+template <bool MX, bool OWNER>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                     const __grid_constant__ CUtensorMap tmD,
@@ -1452,8 +1454,9 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     // per (output block, token) by the blocks past the owners (fewer h blocks than blocks) or by
     // every block once its own h blocks are done. No h crosses SMs.
     // (Taken while the final sums are at most two (output block, token) units per block; past
-    // that, as at T = 16 on the decode shape, the stream-K layout measured faster.)
-    const bool owner = W == 1 && p.part_c != nullptr && p.nbd * p.T <= 2 * G;
+    // that, as at T = 16 on the decode shape, the stream-K layout measured faster. The host
+    // picks the instantiation: see launch_decode_fused.)
+    constexpr bool owner = OWNER;
     const int cb_per_item = MX ? kMxOwnCb : 4;  // output column blocks per owner down item
     const int n4 = (p.nbd + cb_per_item - 1) / cb_per_item;
     const int ob_lo = ngA <= G ? min(b, ngA) : (int)((long long)ngA * b / G);
@@ -1800,13 +1803,22 @@ DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I, bool mx) {
 }
 
 cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
+    const DecodeFusedLayout L = decode_fused_layout(a.T, a.d, a.k, a.I, a.mx);
+    // one block per SM (its shared memory allows no more), all resident: cooperative launch.
+    // It is the first kernel of the layer, so it follows the caller's work in stream order.
+    int grid = device_sm_count();
+    if (grid > kDecodeFusedMaxGrid) grid = kDecodeFusedMaxGrid;
+    // the owner layout while its final sums come to at most two (output block, token) units
+    // per block (and its partial region exists)
+    const bool owner = L.part_c != 0 && (long long)L.nbd * a.T <= 2ll * grid;
+    using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, Params, int);
+    const Kern kern = a.mx ? (owner ? decode_fused_kernel<true, true> : decode_fused_kernel<true, false>)
+                           : (owner ? decode_fused_kernel<false, true>
+                                    : decode_fused_kernel<false, false>);
     {
-        const cudaError_t e = ensure_max_dynamic_smem(
-            a.mx ? decode_fused_kernel<true> : decode_fused_kernel<false>, (int)kSmemBytes);
+        const cudaError_t e = ensure_max_dynamic_smem(kern, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
     }
-
-    const DecodeFusedLayout L = decode_fused_layout(a.T, a.d, a.k, a.I, a.mx);
     const int R = a.T * a.k;
     CUtensorMap tmGU = {}, tmD = {}, tmO = {};  // MX: unused (items are plain bulk copies)
     const cuuint32_t box_a[3] = {64, kKcA, 1}, box_b[3] = {64, kKcB, 1};
@@ -1891,10 +1903,6 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
     }
     const int vpl = a.E <= 32 ? 1 : a.E <= 64 ? 2 : a.E <= 128 ? 4 : 8;
 
-    // one block per SM (its shared memory allows no more), all resident: cooperative launch.
-    // It is the first kernel of the layer, so it follows the caller's work in stream order.
-    int grid = device_sm_count();
-    if (grid > kDecodeFusedMaxGrid) grid = kDecodeFusedMaxGrid;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
     cfg.blockDim = dim3(kThreads);
@@ -1905,8 +1913,7 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return a.mx ? cudaLaunchKernelEx(&cfg, decode_fused_kernel<true>, tmGU, tmD, tmO, p, vpl)
-                : cudaLaunchKernelEx(&cfg, decode_fused_kernel<false>, tmGU, tmD, tmO, p, vpl);
+    return cudaLaunchKernelEx(&cfg, kern, tmGU, tmD, tmO, p, vpl);
 }
 
 }  // namespace rdg
