@@ -1793,9 +1793,10 @@ DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I, bool mx) {
     L.part_b = up(((size_t)kDecodeWaves * kDecodeFusedMaxGrid + R * L.nbh) * T * 128 * 4);
     L.part_bytes = L.part_b + up((size_t)kDecodeWaves * (kDecodeFusedMaxGrid + L.nbd) * T *
                                  64 * 4);
-    // owner layout: the down partials [nbh][R][d] fp32
+    // owner layout: the down partials [nbh][R][d] fp32 (only where the layout can be taken on
+    // any grid: at most two (output block, token) summing units per block of the largest grid)
     L.part_c = 0;
-    if (L.nbh < kDecodeFusedMaxGrid) {
+    if (L.nbh < kDecodeFusedMaxGrid && (long long)L.nbd * T <= 2ll * kDecodeFusedMaxGrid) {
         L.part_c = L.part_bytes;
         L.part_bytes += up((size_t)L.nbh * R * d * 4);
     }

@@ -417,7 +417,7 @@ def forward_workspace_views(ws: torch.Tensor, T, d, E, k, I, Is, dtype, mx=False
         nbh = (I + 63) // 64
         part_b = ((512 + R * nbh) * T * 128 * 4 + 255) // 256 * 256
         part = part_b + ((512 + nbd) * T * 64 * 4 + 255) // 256 * 256
-        if nbh < 512:  # the owner layout's down partials [nbh][R][d] fp32
+        if nbh < 512 and nbd * T <= 1024:  # the owner layout's down partials [nbh][R][d]
             part += (nbh * R * d * 4 + 255) // 256 * 256
         o = (o + part + 255) // 256 * 256
         views["h_codes"] = ws[o:o + R * I]
