@@ -13,8 +13,11 @@
 //
 // Every block first routes all tokens and builds the dispatch indices in shared memory (the
 // same warp router and counting sort as the stand-alone kernels, so the ids and the order
-// agree bit for bit); block 0 also writes them out. Then:
-// Work items are 32 KB weight chunks:
+// agree bit for bit; with at most 32 slots one warp builds the same indices by votes); block 0
+// also writes them out. Then the work takes one of two layouts, picked on the host from the
+// sizes (one kernel instantiation each).
+//
+// Stream-K layout. Work items are 32 KB weight chunks:
 //   gate_up item (q, jb, kc): K rows [128 kc, 128 kc + 128) of gate columns [64 jb, 64 jb + 64)
 //     of the q-th touched expert and the same rows of the matching up columns. Items are
 //     ordered (q, jb, kc); a group (q, jb) is one 64-column block of h.
@@ -43,22 +46,22 @@
 //     rounding.
 // While a block waits, its producer keeps streaming down weights.
 //
-// Owner layout (while the final sums below come to at most two units per block; otherwise the
-// stream-K layout above). Every block owns whole
-// h blocks: h block b while there are fewer h blocks than blocks (T = 1 at the decode shape),
-// else an equal contiguous share (4 or 5 at T = 8). For each of them it streams the gate_up
-// items, then, through the same ring, the down weight rows of those 64 h columns for every
-// output column (items of four [64 K][64 column] boxes, 256 output columns each). Its
-// epilogue warp stores h as above, and also keeps it in shared memory, so the consumer warps
-// multiply the down items by it at once: h crosses no SM and no flag is waited on. Each
-// consumer writes its item's weighted sums per token row as an fp32 partial and bumps the
-// 256-column group's counter. Then, per (64 output columns, token), the blocks past the owners
-// (or all blocks, once their own h blocks are done) sum the partials of the token's rows
-// (sorted row order) and h blocks (block order) and store bf16 out: one rounding, in a fixed
-// order.
+// Owner layout (taken while the final sums below come to at most two units per block). Every
+// block owns whole h blocks: h block b while there are fewer h blocks than blocks (T = 1 at the
+// decode shape), else an equal contiguous share (4 or 5 at T = 8). For each of them it streams
+// the gate_up items, then, through the same ring, the down weight rows of those 64 h columns for
+// every output column: bf16 items of four [64 K][64 column] boxes (256 output columns), MX
+// items of both 32-row K blocks of 14 output column blocks. The gate_up items of the next owned
+// h block are streamed ahead of the down items of the current one, so the ring keeps streaming
+// while h is finished. The epilogue warp stores h as above and also keeps it in shared memory
+// (two buffers, one mbarrier each), so the consumer warps multiply the down items by it at
+// once: h crosses no SM and no flag is waited on. Each consumer writes its item's weighted sums
+// per token row as an fp32 partial and bumps the item's counter. Then, per (64 output columns,
+// token), the blocks past the owners (or all blocks, once their own h blocks are done) sum the
+// partials of the token's rows (sorted row order) and h blocks (block order) and store bf16
+// out: one rounding, in a fixed order.
 //
-// The launch is cooperative,
-// so every block is resident and the waits end. Every sum runs in an order fixed by the sizes
+// The launch is cooperative, so every block is resident and the waits end. Every sum runs in an order fixed by the sizes
 // alone: results do not depend on timing. The counters are zeroed by the caller's memset of
 // the workspace head that precedes the launch.
 
