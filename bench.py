@@ -458,6 +458,56 @@ class Layer:
         assert self.moe.moe_read_device_status(self.ws) == 0
         del graph
 
+    def run_mx_decode(self):
+        """moe_forward_mx on MXFP4 weights (the one-kernel decode layer) captured as a CUDA graph
+        and replayed with L2 flushed, as the bf16 layer is timed: µs per layer and the touched
+        experts' MX bytes (codes and scales) per second."""
+        import torch
+        cfg, moe, dev, stream = self.cfg, self.moe, self.dev, self.stream
+        T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
+        mgu = moe.quantize_weights_mx(self.inp["w_gate_up"], moe.W_GATE_UP)
+        mdn = moe.quantize_weights_mx(self.inp["w_down"], moe.W_DOWN)
+        ws = torch.empty(moe.moe_forward_mx_workspace_size(T, d, E, k, I, 0), dtype=torch.uint8,
+                         device=dev)
+        out, ids, w = torch.empty_like(self.out), torch.empty_like(self.ids), torch.empty_like(self.w)
+
+        def fwd(s_):
+            moe.moe_forward_mx(self.inp["x"], self.inp["logits"], mgu, mdn, k, cfg.score_fn,
+                               self.flags, out=out, topk_ids=ids, topk_weights=w, workspace=ws,
+                               stream=s_)
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            fwd(cap)
+            torch.cuda.current_stream().synchronize()
+            with torch.cuda.graph(graph, stream=cap):
+                fwd(cap)
+        stream.wait_stream(cap)
+        for _ in range(max(self.warmup, 3)):
+            graph.replay()
+        torch.cuda.synchronize()
+        evs = [self.events(2) for _ in range(self.steps)]
+        for a_, b_ in evs:
+            self.flush_l2()
+            a_.record(stream)
+            graph.replay()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        assert moe.moe_read_device_status(ws) == 0
+        ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)
+        ms = reduce_max(ms, dev) if self.world > 1 else ms
+        distinct = int(torch.unique(ids).numel())
+        touched = (mgu.data.numel() + mdn.data.numel()) * distinct // E
+        del graph
+        return {"us_per_layer": round(ms * 1e3, 2), "distinct_experts": distinct,
+                "weight_bytes_touched": touched,
+                "weight_gbs": round(touched / (ms * 1e-3) / 1e9, 1),
+                "path": "moe_forward_mx: one cooperative kernel streaming the touched experts' "
+                        "MXFP4 codes and scales (x and h rounded to MXFP8 in the kernel)",
+                "time": "CUDA-graph replay, events on the launching stream, L2 flushed before "
+                        "every replay"}
+
     def run_e2e(self):
         import torch
         cfg, moe, wts = self.cfg, self.moe, self.wts
@@ -888,6 +938,8 @@ def run_ours(args, rank, world):
                 per[name] = config_entry(L, name, cpu)
                 if isinstance(mxr, dict) and "tensor_core" in mxr:
                     per[name]["mx_tensor_core"] = mxr["tensor_core"]
+                if name.startswith("decode") and moe.moe_forward_kernel_count(T, k, Is, dt) == 1:
+                    per[name]["mx_decode"] = L.run_mx_decode()
                 continue
             c_ = workload_config(name)
             Lc = Layer(c_, dev, args.steps, args.warmup, world)
@@ -900,6 +952,9 @@ def run_ours(args, rank, world):
             per[name] = config_entry(Lc, name, cs)
             if mx_tc is not None:
                 per[name]["mx_tensor_core"] = mx_tc
+            if (name.startswith("decode") and Lc.packed and
+                    moe.moe_forward_kernel_count(c_.T, c_.k, c_.I_shared, c_.dtype) == 1):
+                per[name]["mx_decode"] = Lc.run_mx_decode()
             del Lc
             torch.cuda.empty_cache()
         res["per_config"] = per
