@@ -90,14 +90,15 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // MX weights (MXFP4 codes in 1 KB blocks of 64 columns x 32 K rows, 64 scale bytes each): a
 // gate_up item is up to 15 K blocks of its gate and up column blocks, a down item up to 30 K
 // blocks of one output column block; codes, then scales, within the 32 KB stage.
-constexpr int kMxKbA = 15;
+constexpr int kMxKbA = 15;  // at most; the launch picks 15 (T = 1) or 11 (Params::kba)
 constexpr int kMxKbB = 30;
 constexpr uint32_t kMxUpCodes = 15 * 1024;     // up codes after the gate codes (gate_up item)
 constexpr uint32_t kMxScales = 30 * 1024;      // scales after the codes
 constexpr uint32_t kMxUpScales = kMxScales + 15 * 64;
-// owner layout, MX: a down item holds the 64 h rows (two 32-row K blocks) of up to 14 output
-// column blocks: codes [column block][K block][1 KB], then scales [column block][K block][64]
-constexpr int kMxOwnCb = 14;
+// owner layout, MX: a down item holds the 64 h rows (two 32-row K blocks) of up to 6 output
+// column blocks (six items cover the decode shape's 32, one per consumer warp): codes [column
+// block][K block][1 KB], then scales [column block][K block][64]
+constexpr int kMxOwnCb = 6;
 constexpr uint32_t kMxOwnScales = kMxOwnCb * 2 * 1024;
 static_assert(kMxOwnScales + kMxOwnCb * 2 * 64 <= kStageBytes, "owner MX item exceeds a stage");
 constexpr int kMxHsScales = kDecodeFusedMaxTokens * 64;  // h_s (MX): codes, then 2 scales a row
@@ -148,6 +149,7 @@ struct Params {
     uint8_t* h_codes;
     uint8_t* h_scales;
     int kbd, kbi;            // 32-row K blocks of d and I
+    int kba;                 // MX gate_up items: 32-row K blocks per item (<= kMxKbA)
     int mx;
 };
 
@@ -519,7 +521,7 @@ __device__ __forceinline__ void item_a_mx(Ctx& c, const Params& p, int i, int kc
                                           const unsigned int* const (&rows)[NTILE],
                                           float (&acc)[8][NTILE][4]) {
     const uint32_t stage = c.stage0 + (uint32_t)c.warp * kStageBytes;
-    const int kb0 = kc * kMxKbA, nk = min(kMxKbA, p.kbd - kb0);
+    const int kb0 = kc * p.kba, nk = min(p.kba, p.kbd - kb0);
     // x words two K blocks ahead of the math (the first two before the stage wait)
     uint32_t w0[NTILE][4], w1[NTILE][4], w2[NTILE][4];
     mx_x_load<NTILE>(rows, kb0, p.d, c.lane, w0);
@@ -1508,7 +1510,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                             uint32_t dst;
                             uint64_t* bar;
                             if (MX) {
-                                const int kb0 = kc * kMxKbA, nk = min(kMxKbA, p.kbd - kb0);
+                                const int kb0 = kc * p.kba, nk = min(p.kba, p.kbd - kb0);
                                 const size_t bg = ((size_t)e * p.gu_nb + jb) * p.kbd + kb0;
                                 const size_t bu = ((size_t)e * p.gu_nb + p.nbh + jb) * p.kbd + kb0;
                                 if (!(ok = next_stage(dst, bar, (uint32_t)nk * 2 * (1024 + 64))))
@@ -1585,7 +1587,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                     if (MX) {
                         // K blocks [15 kc, ...) of the gate and up column blocks: runs of 1 KB
                         // code blocks and 64 B scale blocks
-                        const int kb0 = kc * kMxKbA, nk = min(kMxKbA, p.kbd - kb0);
+                        const int kb0 = kc * p.kba, nk = min(p.kba, p.kbd - kb0);
                         const size_t bg = ((size_t)e * p.gu_nb + jb) * p.kbd + kb0;
                         const size_t bu = ((size_t)e * p.gu_nb + p.nbh + jb) * p.kbd + kb0;
                         if (!(ok = next_stage(dst, bar, (uint32_t)nk * 2 * (1024 + 64)))) break;
@@ -1769,6 +1771,10 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
 
 }  // namespace
 
+// MX gate_up items: 32-row K blocks per item. At T = 1 fewer, larger items measured faster; from
+// T = 2 up, 11 (more items to share among the consumer warps).
+static int mx_kba(int T) { return T == 1 ? kMxKbA : 11; }
+
 bool decode_fused_applies(moe_dtype dt, int T, int k, int Is) {
     return dt == MOE_BF16 && Is == 0 && T >= 1 && T <= kDecodeFusedMaxTokens &&
            T * k <= kDecodeFusedMaxRows;
@@ -1780,7 +1786,7 @@ DecodeFusedLayout decode_fused_layout(int T, int d, int k, int I, bool mx) {
     L.nbh = (I + 63) / 64;
     L.nbd = (d + 63) / 64;
     if (mx) {  // items of up to 15 (gate_up) / 30 (down) 32-row K blocks
-        L.nka = ((d + 31) / 32 + kMxKbA - 1) / kMxKbA;
+        L.nka = ((d + 31) / 32 + mx_kba(T) - 1) / mx_kba(T);
         L.nkb = ((I + 31) / 32 + kMxKbB - 1) / kMxKbB;
     } else {
         L.nka = (d + kKcA - 1) / kKcA;
@@ -1894,6 +1900,7 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
     p.h_codes = p.h_scales = nullptr;
     p.kbd = (a.d + 31) / 32;
     p.kbi = (a.I + 31) / 32;
+    p.kba = mx_kba(a.T);
     if (a.mx) {
         const MxGeom gg = mx_geom(true, a.d, a.I, a.E), gd = mx_geom(false, a.I, a.d, a.E);
         p.mx_gu = static_cast<const uint8_t*>(a.w_gate_up);
