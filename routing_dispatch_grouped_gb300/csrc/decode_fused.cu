@@ -1227,18 +1227,23 @@ struct NtTag {
     static constexpr int value = N;
 };
 
-// Run a group with one MMA n-tile per 8 of its rows.
-template <typename F>
+// Run a group with one MMA n-tile per 8 of its rows (SMALL: at most 8 tokens, so one n-tile
+// always and only that form is compiled).
+template <bool SMALL, typename F>
 __device__ __forceinline__ void by_rows(int tq, F&& f) {
-    if (tq <= kPass)
+    if constexpr (SMALL) {
         f(NtTag<1>{});
-    else
-        f(NtTag<2>{});
+    } else {
+        if (tq <= kPass)
+            f(NtTag<1>{});
+        else
+            f(NtTag<2>{});
+    }
 }
 
-// OWNER: the owner layout (chosen on the host from the sizes alone, so that each instantiation
-// holds one layout's code)
-template <bool MX, bool OWNER>
+// OWNER: the owner layout; SMALL: at most 8 tokens. Both are chosen on the host from the sizes
+// alone, so that each instantiation holds only the code its batches run.
+template <bool MX, bool OWNER, bool SMALL>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                     const __grid_constant__ CUtensorMap tmD,
@@ -1677,7 +1682,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
 
     // consumers (warp w: the items of stage w) and the epilogue warp walk the same groups
     int i0 = 0;  // block-local index of the next item
-    if (owner) {
+    if constexpr (OWNER) {
         // the producer's order: gate_up of h block j (h into buffer j & 1), then the down
         // items of h block j - 1 (h from buffer (j - 1) & 1, its barrier's use (j - 1) >> 1)
         const int n_own = ob_hi - ob_lo;
@@ -1687,11 +1692,11 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                 c.h_s = h_buf + (j & 1) * kDecodeFusedMaxTokens * 64;
                 c.h_full = &h_full[j & 1];
                 if (epilogue)
-                    by_rows(s_tq[q], [&](auto tag) {
+                    by_rows<SMALL>(s_tq[q], [&](auto tag) {
                         epi_a<decltype(tag)::value>(c, p, q, jb, g, b, b);
                     });
                 else
-                    by_rows(s_tq[q], [&](auto tag) {
+                    by_rows<SMALL>(s_tq[q], [&](auto tag) {
                         group_a<decltype(tag)::value, MX>(c, p, q, i0, 0, p.nka);
                     });
                 i0 += p.nka;
@@ -1701,7 +1706,7 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
                 c.h_s = h_buf + ((j - 1) & 1) * kDecodeFusedMaxTokens * 64;
                 c.h_full = &h_full[(j - 1) & 1];
                 if (!epilogue)
-                    by_rows(s_tq[q], [&](auto tag) {
+                    by_rows<SMALL>(s_tq[q], [&](auto tag) {
                         if (MX)
                             owner_down_mx<decltype(tag)::value>(c, p, q, jb, i0, n4,
                                                                 (uint32_t)((j - 1) >> 1) & 1u);
@@ -1719,52 +1724,52 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
         } else {
             owner_reduce(p, flags, c.red, s_tok, tid, b, G, ngA, cb_per_item);
         }
-        return;
-    }
-    for (int w = 0; w < W; ++w) {
-        int q_lo, n;
-        wave_a(w, q_lo, n);
-        c.nA = n;
-        c.slot_off = w * G;
-        const int hi = ba < GA ? range_lo(n, ba + 1, GA) : 0;
-        for (int u = ba < GA ? range_lo(n, ba, GA) : 0; u < hi;) {
-            const int gl = u / p.nka, kc0 = u % p.nka;  // group within the wave, K chunk
-            const int kc1 = min(p.nka, kc0 + (hi - u));
-            const int g = q_lo * p.nbh + gl, q = g / p.nbh, jb = g % p.nbh;
-            if (epilogue) {
-                const int bf = block_of(n, gl * p.nka, GA);
-                const int bl = block_of(n, (gl + 1) * p.nka - 1, GA);
-                by_rows(s_tq[q],
-                        [&](auto tag) { epi_a<decltype(tag)::value>(c, p, q, jb, g, bf, bl); });
-            } else {
-                by_rows(s_tq[q], [&](auto tag) {
-                    group_a<decltype(tag)::value, MX>(c, p, q, i0, kc0, kc1);
-                });
-            }
-            u += kc1 - kc0;
-            i0 += kc1 - kc0;
-        }
-    }
-    for (int w = 0; w < W; ++w) {
-        const WaveB v = wave_b(c, p, w);
-        c.slot_off = w * (GB + p.nbd);
-        const int hi = bb < GB ? range_lo(v.n, bb + 1, GB) : 0;
-        for (int u = bb < GB ? range_lo(v.n, bb, GB) : 0; u < hi;) {
-            const int cb = u / v.perC;
-            const int c_end = min(hi, (cb + 1) * v.perC);
-            while (u < c_end) {
-                const int rem = u % v.perC, q = v.q_lo + rem / p.nkb, kc0 = rem % p.nkb;
-                const int kc1 = min(p.nkb, kc0 + (c_end - u));
-                if (epilogue)
-                    by_rows(s_tq[q], [&](auto tag) { epi_b<decltype(tag)::value>(c, p, q); });
-                else
-                    by_rows(s_tq[q], [&](auto tag) {
-                        group_b<decltype(tag)::value, MX>(c, p, q, i0, kc0, kc1);
+    } else {
+        for (int w = 0; w < W; ++w) {
+            int q_lo, n;
+            wave_a(w, q_lo, n);
+            c.nA = n;
+            c.slot_off = w * G;
+            const int hi = ba < GA ? range_lo(n, ba + 1, GA) : 0;
+            for (int u = ba < GA ? range_lo(n, ba, GA) : 0; u < hi;) {
+                const int gl = u / p.nka, kc0 = u % p.nka;  // group within the wave, K chunk
+                const int kc1 = min(p.nka, kc0 + (hi - u));
+                const int g = q_lo * p.nbh + gl, q = g / p.nbh, jb = g % p.nbh;
+                if (epilogue) {
+                    const int bf = block_of(n, gl * p.nka, GA);
+                    const int bl = block_of(n, (gl + 1) * p.nka - 1, GA);
+                    by_rows<SMALL>(s_tq[q],
+                            [&](auto tag) { epi_a<decltype(tag)::value>(c, p, q, jb, g, bf, bl); });
+                } else {
+                    by_rows<SMALL>(s_tq[q], [&](auto tag) {
+                        group_a<decltype(tag)::value, MX>(c, p, q, i0, kc0, kc1);
                     });
+                }
                 u += kc1 - kc0;
                 i0 += kc1 - kc0;
             }
-            if (epilogue) epi_flush(c, p, cb);
+        }
+        for (int w = 0; w < W; ++w) {
+            const WaveB v = wave_b(c, p, w);
+            c.slot_off = w * (GB + p.nbd);
+            const int hi = bb < GB ? range_lo(v.n, bb + 1, GB) : 0;
+            for (int u = bb < GB ? range_lo(v.n, bb, GB) : 0; u < hi;) {
+                const int cb = u / v.perC;
+                const int c_end = min(hi, (cb + 1) * v.perC);
+                while (u < c_end) {
+                    const int rem = u % v.perC, q = v.q_lo + rem / p.nkb, kc0 = rem % p.nkb;
+                    const int kc1 = min(p.nkb, kc0 + (c_end - u));
+                    if (epilogue)
+                        by_rows<SMALL>(s_tq[q], [&](auto tag) { epi_b<decltype(tag)::value>(c, p, q); });
+                    else
+                        by_rows<SMALL>(s_tq[q], [&](auto tag) {
+                            group_b<decltype(tag)::value, MX>(c, p, q, i0, kc0, kc1);
+                        });
+                    u += kc1 - kc0;
+                    i0 += kc1 - kc0;
+                }
+                if (epilogue) epi_flush(c, p, cb);
+            }
         }
     }
 }
@@ -1822,9 +1827,12 @@ cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s) {
     // per block (and its partial region exists)
     const bool owner = L.part_c != 0 && (long long)L.nbd * a.T <= 2ll * grid;
     using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, Params, int);
-    const Kern kern = a.mx ? (owner ? decode_fused_kernel<true, true> : decode_fused_kernel<true, false>)
-                           : (owner ? decode_fused_kernel<false, true>
-                                    : decode_fused_kernel<false, false>);
+    static const Kern kKern[2][2][2] = {
+        {{decode_fused_kernel<false, false, false>, decode_fused_kernel<false, false, true>},
+         {decode_fused_kernel<false, true, false>, decode_fused_kernel<false, true, true>}},
+        {{decode_fused_kernel<true, false, false>, decode_fused_kernel<true, false, true>},
+         {decode_fused_kernel<true, true, false>, decode_fused_kernel<true, true, true>}}};
+    const Kern kern = kKern[a.mx ? 1 : 0][owner ? 1 : 0][a.T <= kPass ? 1 : 0];
     {
         const cudaError_t e = ensure_max_dynamic_smem(kern, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
