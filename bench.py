@@ -458,23 +458,25 @@ class Layer:
         assert self.moe.moe_read_device_status(self.ws) == 0
         del graph
 
-    def run_mx_decode(self):
-        """moe_forward_mx on MXFP4 weights (the one-kernel decode layer) captured as a CUDA graph
-        and replayed with L2 flushed, as the bf16 layer is timed: µs per layer and the touched
-        experts' MX bytes (codes and scales) per second."""
+    def run_mx_decode(self, tc=False):
+        """The MX layer on MXFP4 weights captured as a CUDA graph and replayed with L2 flushed,
+        as the bf16 layer is timed: µs per layer and the touched experts' MX bytes (codes and
+        scales) per second. tc=False: moe_forward_mx (first-version layout, warp-level MMAs);
+        tc=True: moe_forward_mx_tc (tensor-core layout, block-scaled tcgen05 MMAs)."""
         import torch
         cfg, moe, dev, stream = self.cfg, self.moe, self.dev, self.stream
         T, d, E, k, I = cfg.T, cfg.d, cfg.E, cfg.k, cfg.I
-        mgu = moe.quantize_weights_mx(self.inp["w_gate_up"], moe.W_GATE_UP)
-        mdn = moe.quantize_weights_mx(self.inp["w_down"], moe.W_DOWN)
-        ws = torch.empty(moe.moe_forward_mx_workspace_size(T, d, E, k, I, 0), dtype=torch.uint8,
-                         device=dev)
+        quant = moe.quantize_weights_mx_tc if tc else moe.quantize_weights_mx
+        mgu = quant(self.inp["w_gate_up"], moe.W_GATE_UP)
+        mdn = quant(self.inp["w_down"], moe.W_DOWN)
+        size = moe.moe_forward_mx_tc_workspace_size if tc else moe.moe_forward_mx_workspace_size
+        ws = torch.empty(size(T, d, E, k, I, 0), dtype=torch.uint8, device=dev)
         out, ids, w = torch.empty_like(self.out), torch.empty_like(self.ids), torch.empty_like(self.w)
+        layer = moe.moe_forward_mx_tc if tc else moe.moe_forward_mx
 
         def fwd(s_):
-            moe.moe_forward_mx(self.inp["x"], self.inp["logits"], mgu, mdn, k, cfg.score_fn,
-                               self.flags, out=out, topk_ids=ids, topk_weights=w, workspace=ws,
-                               stream=s_)
+            layer(self.inp["x"], self.inp["logits"], mgu, mdn, k, cfg.score_fn, self.flags,
+                  out=out, topk_ids=ids, topk_weights=w, workspace=ws, stream=s_)
         graph = torch.cuda.CUDAGraph()
         cap = torch.cuda.Stream(dev)
         cap.wait_stream(stream)
@@ -500,11 +502,18 @@ class Layer:
         distinct = int(torch.unique(ids).numel())
         touched = (mgu.data.numel() + mdn.data.numel()) * distinct // E
         del graph
+        kernels = moe.moe_forward_mx_tc_kernel_count(T, d, k, I, 0) if tc else 1
+        path = ("moe_forward_mx_tc: one cooperative kernel, the touched experts' MXFP4 codes "
+                "times x and h in MXFP8 on the block-scaled tensor cores "
+                "(tcgen05.mma.kind::mxf8f6f4.block_scale, weights as M, tokens as N)"
+                if tc and kernels == 1 else
+                f"moe_forward_mx_tc: {kernels} kernels (block-scaled tensor-core GEMMs)" if tc else
+                "moe_forward_mx: one cooperative kernel streaming the touched experts' "
+                "MXFP4 codes and scales (x and h rounded to MXFP8 in the kernel)")
         return {"us_per_layer": round(ms * 1e3, 2), "distinct_experts": distinct,
                 "weight_bytes_touched": touched,
                 "weight_gbs": round(touched / (ms * 1e-3) / 1e9, 1),
-                "path": "moe_forward_mx: one cooperative kernel streaming the touched experts' "
-                        "MXFP4 codes and scales (x and h rounded to MXFP8 in the kernel)",
+                "path": path,
                 "time": "CUDA-graph replay, events on the launching stream, L2 flushed before "
                         "every replay"}
 
@@ -940,6 +949,8 @@ def run_ours(args, rank, world):
                     per[name]["mx_tensor_core"] = mxr["tensor_core"]
                 if name.startswith("decode") and moe.moe_forward_kernel_count(T, k, Is, dt) == 1:
                     per[name]["mx_decode"] = L.run_mx_decode()
+                if name.startswith("decode") and L.packed:
+                    per[name]["mx_tc_decode"] = L.run_mx_decode(tc=True)
                 continue
             c_ = workload_config(name)
             Lc = Layer(c_, dev, args.steps, args.warmup, world)
@@ -955,6 +966,8 @@ def run_ours(args, rank, world):
             if (name.startswith("decode") and Lc.packed and
                     moe.moe_forward_kernel_count(c_.T, c_.k, c_.I_shared, c_.dtype) == 1):
                 per[name]["mx_decode"] = Lc.run_mx_decode()
+            if name.startswith("decode") and Lc.packed:
+                per[name]["mx_tc_decode"] = Lc.run_mx_decode(tc=True)
             del Lc
             torch.cuda.empty_cache()
         res["per_config"] = per

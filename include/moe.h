@@ -581,11 +581,19 @@ moe_status moe_dequantize_weights_mx_tc(moe_weight_kind kind, const void* mx, vo
  *   MOE_RENORMALIZE | MOE_SCALE_INPUT). Route, dispatch indices, one kernel that rounds each
  *   token's x to MXFP8 once and writes it to every row it was sent to, the gate_up GEMM (h
  *   rounded to MXFP8 in its epilogue), the down GEMM, the combine.
+ *   Decode batches (no shared expert, T <= 16, T*k <= 256, d <= 2048, I <= 4096) run the whole
+ *   layer as one cooperative kernel instead (same arithmetic: the weights are the M side of the
+ *   block-scaled MMAs and the tokens the N side; h's 128-column blocks are owned by one SM each;
+ *   the weighted sums of each run of an expert's h blocks on one SM are fp32 partials, added
+ *   per token in a fixed order and rounded once). It writes the routed rows' x and h codes and
+ *   atoms as the steps do, but not y_sorted. moe_forward_mx_tc_kernel_count says which runs.
  *   workspace: moe_forward_mx_tc_workspace_size(...) bytes, 256-byte aligned: the status word
- *   (256 B), then, each rounded up to 256 bytes: counts [E], offsets [E+1], dispatch scratch,
- *   sorted_to_slot [R], slot_to_sorted [R], x codes [Rp][d], x scale atoms [Rp/128][ceil(d/128)],
- *   h codes [Rp][I], h scale atoms [Rp/128][ceil(I/128)], y_sorted fp32 [R][d], and with a
- *   shared expert its x codes [Tp][d] and atoms, h codes [Tp][Is] and atoms, y fp32 [T][d].
+ *   (256 B; the one-kernel layer keeps a counter at byte 128 of it), then, each rounded up to
+ *   256 bytes: counts [E], offsets [E+1], dispatch scratch, sorted_to_slot [R], slot_to_sorted
+ *   [R], x codes [Rp][d], x scale atoms [Rp/128][ceil(d/128)], h codes [Rp][I], h scale atoms
+ *   [Rp/128][ceil(I/128)], y_sorted fp32 [R][d], with a shared expert its x codes [Tp][d] and
+ *   atoms, h codes [Tp][Is] and atoms, y fp32 [T][d], and for decode batches the one-kernel
+ *   layer's fp32 partials [ceil(I/128)][R][d].
  *   Rp = R rounded up to 128 plus 128 E, Tp = T rounded up to 128; expert e's rows occupy padded
  *   rows from poff[e] = sum over e' < e of ceil(count[e'] / 128) * 128; an atom's byte
  *   16 (m % 32) + 4 (m / 32) + j holds the scale of row m of its 128-row block at K block j of
@@ -614,6 +622,9 @@ moe_status moe_down_mx_tc(const void* h_codes, const void* h_sf, const int32_t* 
                           int I, int E, int d, const void* w_down_mx, float* y_sorted,
                           void* workspace, size_t ws_bytes, moe_stream_t stream);
 size_t moe_forward_mx_tc_workspace_size(int T, int d, int E, int k, int I, int Is);
+/* Number of kernels moe_forward_mx_tc enqueues for these sizes (1: the one-kernel decode
+ * layer; the status-word clear is a memset, not counted). 0 for T == 0. */
+int moe_forward_mx_tc_kernel_count(int T, int d, int k, int I, int Is);
 moe_status moe_forward_mx_tc(const void* x, const float* logits, int T, int d, int E, int k,
                              int I, moe_score_fn score_fn, unsigned flags,
                              const void* w_gate_up_mx, const void* w_down_mx,

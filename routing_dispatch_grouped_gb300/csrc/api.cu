@@ -1144,7 +1144,7 @@ namespace {
 // padded rows (every expert's rows start at a multiple of 128).
 struct MxTcLayout {
     size_t counts, offsets, chunk, s2p, p2s, xq, xsf, hq, hsf, y, sxq, ssf, shq, shsf, ysh,
-        total;
+        part, total;
     int Rp, Tp;
 };
 
@@ -1175,6 +1175,8 @@ MxTcLayout mx_tc_layout(int T, int d, int E, int k, int I, int Is) {
     L.shq = take(Is > 0 ? (size_t)L.Tp * Is : 0);
     L.shsf = take(Is > 0 ? (size_t)L.Tp / 128 * kcs * 512 : 0);
     L.ysh = take(Is > 0 ? (size_t)T * d * 4 : 0);
+    // decode batches: the one-kernel layer's partial sums
+    L.part = take(decode_mx_tc_applies(T, d, k, I, Is) ? decode_mx_tc_part_bytes(T, d, k, I) : 0);
     L.total = o;
     return L;
 }
@@ -1274,6 +1276,13 @@ size_t moe_forward_mx_tc_workspace_size(int T, int d, int E, int k, int I, int I
     return mx_tc_layout(T, d, E, k, I, Is).total;
 }
 
+int moe_forward_mx_tc_kernel_count(int T, int d, int k, int I, int Is) {
+    if (T <= 0 || k <= 0 || d < 1 || I < 1 || Is < 0) return 0;
+    if (decode_mx_tc_applies(T, d, k, I, Is)) return 1;
+    const bool small = (long long)T * k <= kSmallDispatchMaxSlots;
+    return (small ? 1 : 1 + dispatch_kernel_count(false)) + 3 + (Is > 0 ? 2 : 0) + 1;
+}
+
 moe_status moe_forward_mx_tc(const void* x, const float* logits, int T, int d, int E, int k,
                              int I, moe_score_fn score_fn, unsigned flags,
                              const void* w_gate_up_mx, const void* w_down_mx,
@@ -1315,6 +1324,40 @@ moe_status moe_forward_mx_tc(const void* x, const float* logits, int T, int d, i
     const bool scale = (flags & MOE_SCALE_INPUT) != 0;
     const bool renorm = (flags & MOE_RENORMALIZE) != 0;
 
+    if (decode_mx_tc_applies(T, d, k, I, Is)) {
+        // decode: the whole layer in one cooperative kernel; its counter sits in the workspace
+        // head and is cleared with the status word
+        if ((st = launch_status(cudaMemsetAsync(workspace, 0, kStatusBytes, s))) != MOE_OK)
+            return st;
+        DecodeMxTcArgs a;
+        a.x = x;
+        a.logits = logits;
+        a.w_gate_up = w_gate_up_mx;
+        a.w_down = w_down_mx;
+        a.score_fn = (int)score_fn;
+        a.renorm = renorm;
+        a.scale_input = scale;
+        a.T = T;
+        a.d = d;
+        a.E = E;
+        a.k = k;
+        a.I = I;
+        a.topk_ids = topk_ids;
+        a.topk_weights = topk_weights;
+        a.counts = counts;
+        a.offsets = offsets;
+        a.sorted_to_slot = s2p;
+        a.slot_to_sorted = p2s;
+        a.x_codes = ws + L.xq;
+        a.x_sf = ws + L.xsf;
+        a.h_codes = ws + L.hq;
+        a.h_sf = ws + L.hsf;
+        a.partials = ws + L.part;
+        a.out = out;
+        a.done = reinterpret_cast<int*>(ws + kDecodeMxTcCounterByte);
+        a.status = status;
+        return launch_status(launch_decode_mx_tc(a, s));
+    }
     if ((st = clear_status(workspace, s)) != MOE_OK) return st;
     // route and the dispatch indices (no row copy: the next kernel writes the rows in MXFP8)
     if (R <= kSmallDispatchMaxSlots) {

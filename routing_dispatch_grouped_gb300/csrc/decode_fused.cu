@@ -66,7 +66,7 @@
 // the workspace head that precedes the launch.
 
 #include "mx.cuh"
-#include "route_warp.cuh"
+#include "decode_route.cuh"
 
 namespace rdg {
 namespace {
@@ -180,12 +180,6 @@ struct Ctx {
     uint64_t ready_mask;     // h blocks of ready_q this warp has seen stored (all ones: every)
     int dumps;               // hand-overs so far
 };
-
-__device__ __forceinline__ int ld_acquire(const int* ptr) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
-    return v;
-}
 
 // First item of block b's range when n items are split into G ranges, and the block whose
 // range holds item u.
@@ -1269,31 +1263,20 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     griddep_wait();
 
     // ---- router top-k and dispatch indices, in every block (scratch in the stage buffers,
-    // which no copy uses yet). Same warp router and counting sort as the stand-alone kernels.
-    // Warp w routes tokens w, w + 8, ... at once (the logits load heads the critical path);
-    // the set-up below runs beside it.
-    const int R = p.R, E = p.E, nch = (R + 31) / 32;
-    int* ids_s = reinterpret_cast<int*>(smem);
-    float* w_s = reinterpret_cast<float*>(ids_s + kDecodeFusedMaxRows);
-    int* rank_s = reinterpret_cast<int*>(w_s + kDecodeFusedMaxRows);
-    int* cnt_s = rank_s + kDecodeFusedMaxRows;
-    int* off_s = cnt_s + kMaxE;
-    int* chunk_s = off_s + kMaxE + 32;  // [chunk of 32 slots][E]: counts, then bases
-    for (int t = warp; t < p.T; t += kWarps) {
-        const float* row = p.logits + (size_t)t * E;
-        int id;
-        float wt;
-        switch (vpl) {
-            case 1: route_token_warp<1>(row, E, p.k, p.score_fn, p.renorm, lane, &id, &wt); break;
-            case 2: route_token_warp<2>(row, E, p.k, p.score_fn, p.renorm, lane, &id, &wt); break;
-            case 4: route_token_warp<4>(row, E, p.k, p.score_fn, p.renorm, lane, &id, &wt); break;
-            default: route_token_warp<8>(row, E, p.k, p.score_fn, p.renorm, lane, &id, &wt); break;
-        }
-        if (lane < p.k) {
-            ids_s[t * p.k + lane] = id;
-            w_s[t * p.k + lane] = wt;
-        }
-    }
+    // which no copy uses yet); the set-up below runs beside the routing.
+    const int R = p.R, E = p.E;
+    const DecodeRouteIO rio{p.logits, p.T, E, p.k, R, p.score_fn, p.renorm, p.topk_ids,
+                            p.topk_w, p.counts, p.offsets, p.s2p, p.p2s};
+    DecodeRouteSmem rsm;
+    rsm.eq = s_eq;
+    rsm.tq = s_tq;
+    rsm.offq = s_off;
+    rsm.tok = s_tok;
+    rsm.wrow = s_w;
+    rsm.pos = nullptr;
+    rsm.nq = flags + 2;
+    decode_route_scratch(rsm, smem);
+    decode_route_tokens<kWarps>(rio, rsm, vpl);
     if (warp == kEpilogueWarp && lane == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(&full[i], 1);
@@ -1313,135 +1296,8 @@ decode_fused_kernel(const __grid_constant__ CUtensorMap tmGU,
     }
     float* outacc = reinterpret_cast<float*>(smem + kOffOut);
     for (int i = threadIdx.x; i < kOutFloats; i += blockDim.x) outacc[i] = 0.0f;
-    for (int i = threadIdx.x; i < nch * E; i += blockDim.x) chunk_s[i] = 0;
     __syncthreads();
-    const bool writer = blockIdx.x == 0;
-    int nq = 0;
-    if (R <= 32) {
-        // at most 32 slots: warp 0 alone, by votes. Slot s's sorted row is the number of slots
-        // routed to a lower expert plus those of its own expert with a lower slot index (the
-        // counting sort's order), and the touched experts come out in ascending id order.
-        if (warp == 0) {
-            const bool act = lane < R;
-            const int e = act ? ids_s[lane] : -1;
-            const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
-            const int lead = (act && lane == __ffs(peers) - 1) ? 1 : 0;
-            int off = 0, qi = 0;
-            for (int j = 0; j < R; ++j) {
-                const int ej = __shfl_sync(0xFFFFFFFFu, e, j);
-                const int lj = __shfl_sync(0xFFFFFFFFu, lead, j);
-                off += ej < e ? 1 : 0;
-                qi += (lj && ej < e) ? 1 : 0;
-            }
-            if (act) {
-                const int pos = off + __popc(peers & ((1u << lane) - 1u));
-                s_tok[pos] = lane / p.k;
-                s_w[pos] = w_s[lane];
-                if (writer) {
-                    p.topk_ids[lane] = e;
-                    p.topk_w[lane] = w_s[lane];
-                    p.s2p[pos] = lane;
-                    p.p2s[lane] = pos;
-                }
-            }
-            if (lead) {
-                s_eq[qi] = e;
-                s_tq[qi] = __popc(peers);
-                s_off[qi] = off;
-            }
-            const unsigned lm = __ballot_sync(0xFFFFFFFFu, lead != 0);
-            if (lane == 0) flags[2] = __popc(lm);
-        }
-        if (writer) {
-            for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-                int cnt = 0, below = 0;
-                for (int s = 0; s < R; ++s) {
-                    const int v = ids_s[s];
-                    cnt += v == e ? 1 : 0;
-                    below += v < e ? 1 : 0;
-                }
-                if (e < E) p.counts[e] = cnt;
-                p.offsets[e] = below;
-            }
-        }
-        __syncthreads();
-        nq = flags[2];
-    } else {
-        for (int ch = warp; ch < nch; ch += kWarps) {
-            const int s = ch * 32 + lane;
-            const int e = s < R ? ids_s[s] : -1;
-            const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
-            if (e >= 0) {
-                rank_s[s] = __popc(peers & ((1u << lane) - 1u));
-                if (lane == __ffs(peers) - 1) chunk_s[ch * E + e] = __popc(peers);
-            }
-        }
-        __syncthreads();
-        for (int e = threadIdx.x; e < E; e += blockDim.x) {
-            int run = 0;
-            for (int ch = 0; ch < nch; ++ch) {
-                const int v = chunk_s[ch * E + e];
-                chunk_s[ch * E + e] = run;
-                run += v;
-            }
-            cnt_s[e] = run;
-        }
-        __syncthreads();
-        if (warp == 0) {
-            // exclusive scan of the counts, and the touched experts in ascending id order
-            const int per = (E + 31) / 32;
-            const int e0 = min(E, lane * per), e1 = min(E, e0 + per);
-            int run = 0;
-            for (int e = e0; e < e1; ++e) run += cnt_s[e];
-            int incl = run;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            int base = incl - run;
-            for (int e = e0; e < e1; ++e) {
-                off_s[e] = base;
-                base += cnt_s[e];
-            }
-            if (lane == 31) off_s[E] = incl;
-            int nt = 0;
-            for (int eb = 0; eb < E; eb += 32) {
-                const int e = eb + lane;
-                const int cnt = e < E ? cnt_s[e] : 0;
-                const unsigned m = __ballot_sync(0xFFFFFFFFu, cnt > 0);
-                if (cnt > 0) {
-                    const int q = nt + __popc(m & ((1u << lane) - 1u));
-                    s_eq[q] = e;
-                    s_tq[q] = cnt;
-                }
-                nt += __popc(m);
-            }
-            if (lane == 0) flags[2] = nt;
-        }
-        __syncthreads();
-        nq = flags[2];
-        for (int q = threadIdx.x; q < nq; q += blockDim.x) s_off[q] = off_s[s_eq[q]];
-        for (int s = threadIdx.x; s < R; s += blockDim.x) {
-            const int e = ids_s[s];
-            const int pos = off_s[e] + chunk_s[(s >> 5) * E + e] + rank_s[s];
-            s_tok[pos] = s / p.k;
-            s_w[pos] = w_s[s];
-            if (writer) {
-                p.topk_ids[s] = e;
-                p.topk_w[s] = w_s[s];
-                p.s2p[pos] = s;
-                p.p2s[s] = pos;
-            }
-        }
-        if (writer) {
-            for (int e = threadIdx.x; e <= E; e += blockDim.x) {
-                if (e < E) p.counts[e] = cnt_s[e];
-                p.offsets[e] = off_s[e];
-            }
-        }
-        __syncthreads();
-    }
+    const int nq = decode_dispatch(rio, rsm, blockIdx.x == 0);
     // the stage buffers are free for the copies again
 
     // Schedule. The touched experts form W waves; every block takes its stream-K share of the

@@ -132,17 +132,6 @@ __device__ __forceinline__ Tile decode_tile(const SmemTail& st, int E, int n_til
     return t;
 }
 
-// ---- block-scaled tcgen05 pieces (the rest in mx_tc.cuh) ----
-// 1D bulk copy global -> shared, completing on an mbarrier (both addresses 16-byte aligned,
-// size a multiple of 16).
-__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(dst),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
-        : "memory");
-}
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_mx_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,

@@ -49,6 +49,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Acquire load at GPU scope (a counter or flag another block releases).
+__device__ __forceinline__ int ld_acquire(const int* ptr) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 // ---- mbarrier ----
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
@@ -215,6 +222,31 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
           "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+// 32 lanes x one 32-bit column.
+__device__ __forceinline__ uint32_t tmem_ld_32x32b_x1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr)
+                 : "memory");
+    return r;
+}
+// 32 lanes x 4 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x4(uint32_t taddr, uint32_t (&r)[4]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr)
+                 : "memory");
+}
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
 }
@@ -393,6 +425,40 @@ struct DecodeFusedArgs {
     void* h_scales = nullptr;
 };
 cudaError_t launch_decode_fused(const DecodeFusedArgs& a, cudaStream_t s);
+
+// One-kernel MX decode layer on the block-scaled tensor cores (decode_mx_tc.cu), for
+// moe_forward_mx_tc: weights in the MX tensor-core layout, no shared expert, at most 16 tokens,
+// d <= 2048, I <= 4096. Its one counter sits in the workspace head at kDecodeMxTcCounterByte
+// (cleared with the status word before the launch); its partial sums take
+// decode_mx_tc_part_bytes.
+constexpr size_t kDecodeMxTcCounterByte = 128;
+bool decode_mx_tc_applies(int T, int d, int k, int I, int Is);
+size_t decode_mx_tc_part_bytes(int T, int d, int k, int I);
+struct DecodeMxTcArgs {
+    const void* x;          // [T, d] bf16
+    const float* logits;    // [T, E]
+    const void* w_gate_up;  // MX tensor-core layout (moe_quantize_weights_mx_tc)
+    const void* w_down;
+    int score_fn;
+    bool renorm;
+    bool scale_input;
+    int T, d, E, k, I;
+    int32_t* topk_ids;      // outputs: router and dispatch results
+    float* topk_weights;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* sorted_to_slot;
+    int32_t* slot_to_sorted;
+    void* x_codes;          // x and h rounded to MXFP8, written for the routed rows in the
+    void* x_sf;             // padded layout of moe_forward_mx_tc's workspace
+    void* h_codes;
+    void* h_sf;
+    void* partials;         // decode_mx_tc_part_bytes
+    void* out;              // [T, d] bf16
+    int* done;              // the counter (zero at launch)
+    int* status;
+};
+cudaError_t launch_decode_mx_tc(const DecodeMxTcArgs& a, cudaStream_t s);
 
 cudaError_t launch_combine(const float* y_sorted, const int32_t* slot_to_sorted,
                            const float* weights, const float* y_shared, int T, int d, int k,

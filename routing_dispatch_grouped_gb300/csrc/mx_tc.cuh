@@ -9,6 +9,17 @@ namespace rdg {
 
 constexpr int kAtom = 512;  // one scale atom: 32 rows of 16 bytes (see gemm_mx_tc.cu)
 
+// 1D bulk copy global -> shared, completing on an mbarrier (both addresses 16-byte aligned,
+// size a multiple of 16).
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Shared-memory descriptor without swizzle (a scale atom: 32 rows of 16 bytes, 8-row groups
 // 128 bytes apart).
 __device__ __forceinline__ uint64_t smem_desc_plain(uint32_t addr) {
@@ -37,6 +48,13 @@ __device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t adesc, uint64_
 // 17-22), E8M0 scales (bit 23), M >> 4 (bits 24-28), A scale-factor id (bits 29-30).
 __host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t sf_id) {
     return (sf_id << 4) | (5u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(M >> 4) << 24) | (sf_id << 29);
+}
+
+// The same with the roles of the formats swapped: A E2M1 (bits 7-9 = 5), B E4M3 (bits 10-12 = 0),
+// for products with the weights as the M side (the decode layer of decode_mx_tc.cu).
+__host__ __device__ constexpr uint32_t idesc_mx_w4a8(int M, int N, uint32_t sf_id) {
+    return (sf_id << 4) | (5u << 7) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
            ((uint32_t)(M >> 4) << 24) | (sf_id << 29);
 }
 

@@ -79,6 +79,7 @@ SIGNATURES = {
                                _P]),
     "moe_down_mx_tc": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _S, _P]),
     "moe_forward_mx_tc_workspace_size": (_S, [_I, _I, _I, _I, _I, _I]),
+    "moe_forward_mx_tc_kernel_count": (_I, [_I, _I, _I, _I, _I]),
     "moe_forward_mx_tc": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _U, _P, _P, _P, _P, _I, _P, _P,
                                _P, _P, _S, _P]),
     "moe_read_device_status": (_I, [_P, _P]),
@@ -793,6 +794,11 @@ def moe_forward_mx(x, logits, w_gate_up: MxWeights, w_down: MxWeights, k, score_
 
 def moe_forward_mx_tc_workspace_size(T, d, E, k, I, Is) -> int:
     return lib().moe_forward_mx_tc_workspace_size(T, d, E, k, I, Is)
+
+
+def moe_forward_mx_tc_kernel_count(T, d, k, I, Is=0) -> int:
+    """Kernels moe_forward_mx_tc launches for these sizes (1: the one-kernel decode layer)."""
+    return lib().moe_forward_mx_tc_kernel_count(T, d, k, I, Is)
 
 
 def moe_forward_mx_tc(x, logits, w_gate_up: MxWeights, w_down: MxWeights, k, score_fn=SOFTMAX,

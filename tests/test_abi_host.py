@@ -180,6 +180,17 @@ def test_kernel_count_and_strings(L):
     assert L.moe_forward_kernel_count(bf16, 10, 2, 128) == 7    # shared expert: no decode kernel
     assert L.moe_forward_kernel_count(bf16, 4096, 2, 0) == 8
     assert L.moe_forward_kernel_count(bf16, 16384, 1, 8192) == 10
+    # the MX tensor-core layer: (T, d, k, I, Is)
+    mc = L.moe_forward_mx_tc_kernel_count
+    assert mc(0, 2048, 8, 768, 0) == 0
+    assert mc(1, 2048, 8, 768, 0) == 1          # one-kernel decode layer
+    assert mc(16, 2048, 16, 768, 0) == 1
+    assert mc(17, 2048, 8, 768, 0) == 5         # route+dispatch, rows, gate_up, down, combine
+    assert mc(16, 2048, 17, 768, 0) == 5        # T*k above the decode limit
+    assert mc(8, 2176, 8, 768, 0) == 5          # d above the one-kernel layer's 2048
+    assert mc(8, 2048, 8, 4128, 0) == 5         # I above its 4096
+    assert mc(8, 2048, 8, 768, 256) == 7        # shared expert: no one-kernel layer
+    assert mc(4096, 4096, 2, 14336, 0) == 8     # dispatch in 3 kernels above 1024 slots
     for code in range(7):
         assert L.moe_status_string(code).decode().startswith(moe.STATUS[code])
 
