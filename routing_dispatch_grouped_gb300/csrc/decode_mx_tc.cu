@@ -130,16 +130,16 @@ __device__ __forceinline__ void owned_range(int NH, int G, int b, int* lo, int* 
         *lo = b;
         *hi = b < NH ? b + 1 : b;
     } else {
-        *lo = (int)((long long)b * NH / G);
-        *hi = (int)((long long)(b + 1) * NH / G);
+        *lo = b * NH / G;
+        *hi = (b + 1) * NH / G;
     }
 }
 // Whether h block hb of the q-th touched expert starts a run (an expert's first h block, or the
-// first h block of some block's range).
+// first h block of some block's range). NH * G stays far below 2^31.
 __device__ __forceinline__ bool run_start(int q, int hb, int nbh, int NH, int G) {
     if (hb == 0 || NH <= G) return true;
-    const long long g = (long long)q * nbh + hb;
-    const long long b = (g * G + NH - 1) / NH;  // first block whose range starts at or after g
+    const int g = q * nbh + hb;
+    const int b = (g * G + NH - 1) / NH;  // first block whose range starts at or after g
     return b * NH / G == g;
 }
 
@@ -249,7 +249,7 @@ __device__ void issue_mmas(const Params& p, uint8_t* smem, uint32_t tmem, const 
                 for (int j = 0; j < 4; ++j) {
                     // K-major, 128-byte swizzle, +32 bytes per K = 32 step on both sides
                     const uint64_t bd = smem_desc(xb + 32 * j, 16, 1024);
-                    const uint32_t id = idesc_mx_w4a8(128, kN, (uint32_t)j);
+                    const uint32_t id = idesc_mx_w4a8(128, kN, (uint32_t)j, (uint32_t)j);
                     const uint32_t acc = (kc | j) != 0 ? 1u : 0u;
                     umma_mx(dg, smem_desc(a0 + 32 * j, 16, 1024), bd, id, sfw, sfx, acc);
                     umma_mx(du, smem_desc(a1 + 32 * j, 16, 1024), bd, id, sfw + 4, sfx, acc);
@@ -285,7 +285,7 @@ __device__ void issue_mmas(const Params& p, uint8_t* smem, uint32_t tmem, const 
                     for (int j = 0; j < 4; ++j)
                         umma_mx(d, smem_desc(a0 + x * kBox + 32 * j, 16, 1024),
                                 smem_desc(hbase + 32 * j, 16, 1024),
-                                idesc_mx_w4a8(128, kN, (uint32_t)j), sfw + 4 * x, sfh,
+                                idesc_mx_w4a8(128, kN, (uint32_t)j, (uint32_t)j), sfw + 4 * x, sfh,
                                 (!first || j > 0) ? 1u : 0u);
                 }
                 release();
@@ -435,7 +435,7 @@ __device__ void epilogue(const Params& p, uint8_t* smem, uint32_t tmem, const Ba
         asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.done) : "memory");
 }
 
-// ================= x to MXFP8 (warps 1..5, beside the routing) =================
+// ================= x to MXFP8 (warps 1..5, beside the first weight copies) =================
 // Token n's 32-element block kb: codes into row n of the B tile of chunk kb / 4, the scale into
 // x's atom of that chunk (16 n + kb % 4). Rows past T and blocks past d are zero with scale 1.
 __device__ void quantize_x(const Params& p, uint8_t* smem) {

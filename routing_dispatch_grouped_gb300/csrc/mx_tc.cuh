@@ -52,10 +52,12 @@ __host__ __device__ constexpr uint32_t idesc_mx(int M, int N, uint32_t sf_id) {
 }
 
 // The same with the roles of the formats swapped: A E2M1 (bits 7-9 = 5), B E4M3 (bits 10-12 = 0),
-// for products with the weights as the M side (the decode layer of decode_mx_tc.cu).
-__host__ __device__ constexpr uint32_t idesc_mx_w4a8(int M, int N, uint32_t sf_id) {
-    return (sf_id << 4) | (5u << 7) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
-           ((uint32_t)(M >> 4) << 24) | (sf_id << 29);
+// for products with the weights as the M side (the decode layer of decode_mx_tc.cu); the A and
+// B scale-factor ids (which K block of their atoms' four) given separately.
+__host__ __device__ constexpr uint32_t idesc_mx_w4a8(int M, int N, uint32_t sfa_id,
+                                                     uint32_t sfb_id) {
+    return (sfb_id << 4) | (5u << 7) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(M >> 4) << 24) | (sfa_id << 29);
 }
 
 // One MX block of h (32 columns from col0) from its gate and up accumulators: SwiGLU in
