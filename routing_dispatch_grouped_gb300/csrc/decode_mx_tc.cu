@@ -43,8 +43,8 @@
 // end of a run the epilogue writes the routing-weighted sums of the expert's rows as fp32
 // partials part[first h block of the run][sorted row][d] and, when the block is done, bumps
 // a counter (release).
-// Summing step. Once every owner has bumped the counter, unit (token t, 64 output columns) is
-// the sum over t's rows (ascending sorted row: an expert appears once per token) and each
+// Summing step. Once every owner has bumped the counter, unit (token t, 128 output columns) is
+// the sum over t's slots (in slot order: an expert appears once per token) and each slot's
 // row's runs (ascending h block) of the partials, rounded once to bf16; units are dealt to the
 // blocks from the last one down, so blocks that own nothing take them first.
 // Every sum runs in an order fixed by the sizes, so repeated calls give the same bits. The
